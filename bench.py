@@ -1,0 +1,366 @@
+#!/usr/bin/env python
+"""Benchmark: fp64 PCG iterations/s and achieved HBM GB/s on the
+1024 x 1024 x 128 graded, variable-coefficient anisotropic workload.
+
+One step = one pass of the whole hot path on one right-hand side: the
+per-operator set-up (level tables, face values, per-cell diagonal and Thomas
+factors), the initial residual, the interleaved PCG loop to a 1e-10 relative
+residual (preconditioner sweep + SpMV sweep per iteration, reductions on the
+device) and the deferred solution update.  Inputs are resident in HBM before
+the timed region; every vector (1.07 GB) is larger than the 129 MB L2, so no
+flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  With --impl reference the CPU oracle (plain
+sequential C, 1 thread) is timed instead, on a bounded sample of the same
+workload: a fixed number of PCG iterations on the full grid per step.
+Under torchrun (N > 1) every rank solves its own copy of the workload
+(replicas, weak scaling); the path has no collective.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "PCG iters/s & achieved HBM GB/s (fp64, 1024x1024x128 grid) vs HBM roofline"
+UNIT = "iters/s"
+# fp64 pipe operations per cell (FMA, MUL and ADD each count one) of the two
+# sweeps in this implementation; see the kernel sources.
+OPS_SPMV = {True: 12, False: 11}     # keyed by "a_h varies per column"
+OPS_PRECOND = 6
+# Algorithmic bytes per cell: vectors read/written once per sweep.
+BYTES_SPMV = {True: 64, False: 56}   # u,p,z,q (+ per-cell diagonal) read; u,p,q written
+BYTES_PRECOND = {True: 48, False: 32}  # r,q (+ 2 per-cell Thomas factors) read; r,z written
+FP64_LANES_PER_SM_CLK = 2.0          # GB300 non-tensor fp64 rate: 2 FMA lanes per SM per clock
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=W.HEADLINE, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--cpu-iters", type=int, default=4,
+                    help="PCG iterations of the oracle sample (cpu_baseline / reference)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--grid", type=int, nargs=3, metavar=("NX", "NY", "NZ"),
+                    help="same coefficients on another grid size (profiling captures)")
+    return ap.parse_args()
+
+
+def rank_info():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def workload_inputs(w):
+    h, ah, vec = W.make_inputs(w)
+    if w.rhs == "manufactured":
+        raise SystemExit("bench.py times right-hand-side workloads only")
+    return h, ah, vec
+
+
+def cpu_oracle_sample(w, h, ah, b, iters):
+    """The oracle as it stands on the full grid, `iters` fixed iterations."""
+    import oracle
+    prob = oracle.Problem(w.nx, w.ny, w.nz, ah=ah, a_v=w.a_v, mass=w.mass, h=h)
+    t0 = time.perf_counter()
+    _, it, _, _ = oracle.pcg(prob, b, rtol=0.0, maxit=iters)
+    dt = time.perf_counter() - t0
+    return it, dt
+
+
+def run_reference(args, w):
+    rank, world, _ = rank_info()
+    if rank != 0:
+        return 0
+    h, ah, b = workload_inputs(w)
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, h, ah, b, args.cpu_iters)
+    tot_it, tot_t = 0, 0.0
+    for _ in range(args.steps):
+        it, dt = cpu_oracle_sample(w, h, ah, b, args.cpu_iters)
+        tot_it += it
+        tot_t += dt
+    value = tot_it / tot_t
+    sample = ("oracle_pcg on the full %dx%dx%d grid, %d fixed PCG iterations per step "
+              "(initial residual and first preconditioner solve included), sequential C, "
+              "1 thread" % (w.nx, w.ny, w.nz, args.cpu_iters))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "grid": [w.nx, w.ny, w.nz], "iters_per_step":
+                   args.cpu_iters, "l2": "inputs larger than L2"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    import torch
+    rank, world, local = rank_info()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import matrix_free_pcg_gb300 as mf
+
+    h, ah, b = workload_inputs(w)
+    varying = w.varying_ah
+    coeffs = dict(a_h=w.a_h, a_h_field=ah if varying else None, a_v=w.a_v, mass=w.mass, dz=h)
+    solver = mf.Solver(w.nx, w.ny, w.nz, **coeffs)
+    bd = torch.from_numpy(b).to(dev)
+    x = torch.zeros_like(bd)
+    stream = torch.cuda.current_stream(dev)
+    solver.set_stream(stream)
+
+    def step():
+        solver.update_coeffs(**coeffs)
+        x.zero_()
+        it, _, st = solver.solve(bd, x, rtol=w.rtol, maxit=w.maxit, history=False)
+        if st not in (mf.PCG_OK,):
+            raise RuntimeError("solve status %d: %s" % (st, mf.pcg_last_error(solver.ctx)))
+        return it
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    solver.enable_timing(True)
+    iters = []
+    launches = 0
+    setup_launches = 3 if varying else 0
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            iters.append(step())
+            launches += solver.launch_info()["last_solve_launches"] + setup_launches
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    ms = e0.elapsed_time(e1)
+    ktimes = solver.kernel_times()
+    solver.enable_timing(False)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms, float(sum(iters))], dtype=torch.float64, device=dev)
+        tmax = t[:1].clone()
+        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+        tsum = t[1:].clone()
+        dist.all_reduce(tsum, op=dist.ReduceOp.SUM)
+        ms_max, total_iters = float(tmax.item()), float(tsum.item())
+    else:
+        ms_max, total_iters = ms, float(sum(iters))
+    value = total_iters / (ms_max * 1e-3)
+
+    n = w.n
+    peaks, peak_src = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    clk = clocks.summary()
+    bytes_iter = (BYTES_SPMV[varying] + BYTES_PRECOND[varying]) * n
+    ops_iter = (OPS_SPMV[varying] + OPS_PRECOND) * n
+    hbm_gbs = bytes_iter * (total_iters / world) / (ms_max * 1e-3) / 1e9
+
+    # roofline of the dominant kernel, from its live CUDA-event times
+    kinds = {"spmv_fused": (OPS_SPMV[varying], BYTES_SPMV[varying]),
+             "precond_fused": (OPS_PRECOND, BYTES_PRECOND[varying])}
+    dom = max(kinds, key=lambda k: ktimes[k][0])
+    dom_ms, dom_n = ktimes[dom]
+    avg_s = dom_ms * 1e-3 / max(dom_n, 1)
+    ops_cell, bytes_cell = kinds[dom]
+    sm_mhz = (clk or {}).get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    alu_peak = FP64_LANES_PER_SM_CLK * nsm * sm_mhz * 1e6 / 1e9  # G fp64 ops / s
+    alu_ach = ops_cell * n / avg_s / 1e9
+    hbm_ach = bytes_cell * n / avg_s / 1e9
+    traffic = None
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            traffic = json.load(f).get(dom)
+    except (OSError, ValueError):
+        traffic = None
+    roofline = {
+        "bound": "alu", "kernel": dom, "achieved": alu_ach, "peak": alu_peak,
+        "unit": "G fp64 ops/s", "frac": alu_ach / alu_peak, "traffic": traffic,
+        "peak_source": "derived: %.0f fp64 lanes/SM/clk x %d SMs x %.0f MHz (median under load)"
+                       % (FP64_LANES_PER_SM_CLK, nsm, sm_mhz),
+        "ops_per_cell": ops_cell, "bytes_per_cell": bytes_cell,
+        "avg_launch_ms": avg_s * 1e3, "launches": dom_n,
+        "hbm_achieved_gbs": hbm_ach, "hbm_peak_gbs": hbm_peak,
+        "hbm_frac": hbm_ach / hbm_peak, "hbm_peak_source": peak_src,
+    }
+    kernels = {k: {"ms": v[0], "launches": v[1]} for k, v in ktimes.items() if v[1]}
+
+    # end to end through the host-buffer entry point: pinned b and x0 in, x out
+    e2e = None
+    if not args.no_e2e:
+        nbuf = args.steps + 1
+        bh = torch.from_numpy(b).pin_memory()
+        xs = [torch.zeros(n, dtype=torch.float64).pin_memory() for _ in range(nbuf)]
+        solver.update_coeffs(**coeffs)
+        solver.solve_host(bh, xs[0], rtol=w.rtol, maxit=w.maxit, history=False)  # warm-up
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e2e_it = 0
+        for i in range(1, nbuf):
+            solver.update_coeffs(**coeffs)
+            it, _, st = solver.solve_host(bh, xs[i], rtol=w.rtol, maxit=w.maxit, history=False)
+            e2e_it += it
+        torch.cuda.synchronize()
+        t_e2e = time.perf_counter() - t0
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            t_e2e = float(t.item())
+        e2e = {"value": e2e_it * world / t_e2e, "unit": UNIT,
+               "h2d_bytes_per_step": 2 * 8 * n, "d2h_bytes_per_step": 8 * n,
+               "api": "pcg_solve_host", "steps": nbuf - 1}
+        del xs, bh
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        it_c, dt_c = cpu_oracle_sample(w, h, ah, b, args.cpu_iters)
+        cpu = {"value": it_c / dt_c, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": "oracle_pcg on the full %dx%dx%d grid, %d fixed PCG iterations "
+                         "(initial residual and first preconditioner solve included), "
+                         "sequential C, 1 thread, %.1f s" % (w.nx, w.ny, w.nz, args.cpu_iters,
+                                                            dt_c)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": max(args.warmup, 3),
+            "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "grid": [w.nx, w.ny, w.nz], "cells": n,
+                       "rtol": w.rtol, "iters_per_step": iters[0], "a_v": w.a_v,
+                       "graded": w.graded, "varying_ah": varying,
+                       "l2": "inputs larger than L2 (1.07 GB per vector)",
+                       "parallelism": "replicas" if world > 1 else "single"},
+            "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / hbm_peak,
+            "bytes_per_cell_iter": bytes_iter / n, "fp64_ops_per_cell_iter": ops_iter / n,
+            "roofline": roofline, "kernels": kernels, "clocks": clk, "e2e": e2e,
+            "cpu_baseline": cpu, "gpu_launches": launches,
+            "time_to_solution_ms": ms_max / args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    solver.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    w = W.WORKLOADS[args.workload]
+    if args.grid:
+        import dataclasses
+        nx, ny, nz = args.grid
+        w = dataclasses.replace(w, name="%s_on_%dx%dx%d" % (w.name.rsplit("_", 1)[0], nx, ny, nz),
+                                nx=nx, ny=ny, nz=nz)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,165 @@
+/*
+ * pcg.h -- C ABI of libpcg: a matrix-free preconditioned conjugate gradient
+ * (PCG) solver, in fp64 on one GB300 GPU (sm_103a), for strongly vertically
+ * anisotropic 3D elliptic operators on flat tensor-product grids.
+ *
+ * The method is that of E. Mueller, X. Guo, R. Scheichl, S. Shi, "Matrix-free
+ * GPU implementation of a preconditioned conjugate gradient solver for
+ * anisotropic elliptic PDEs" (2013):
+ *   - the operator is applied matrix-free, the 7-point stencil recomputed from
+ *     a few per-level and per-column coefficients (section 4.2, eq. (18));
+ *   - the preconditioner solves one tridiagonal system exactly per vertical
+ *     column with the Thomas algorithm (section 4.1, eq. (19));
+ *   - the PCG iteration is loop-fused into two sweeps over the grid per
+ *     iteration, each carrying its own inner products (section 4.3,
+ *     Algorithm 1; Appendix A, Algorithms 2 and 3).
+ *
+ * Operator.  On an nx x ny x nz grid, periodic in the horizontal (i, j),
+ * homogeneous Neumann at the bottom (k = 0) and top (k = nz-1), with layer
+ * thicknesses h_k and unit horizontal cell area and spacing:
+ *   (A u)_{ijk} = mass*h_k*u_{ijk}
+ *               + h_k * sum_{4 faces f} a_f (u_{ijk} - u_{nbr(f),k})
+ *               + T_{k+1/2} (u_{ijk} - u_{ij,k+1})   [k < nz-1]
+ *               + T_{k-1/2} (u_{ijk} - u_{ij,k-1})   [k > 0]
+ * with T_{k+1/2} = a_v / (0.5*(h_k + h_{k+1})) and a_f the mean of a_h over
+ * the two cells of face f (section 3, eqs. (5)-(8)).  A is symmetric
+ * positive definite when mass > 0.  The preconditioner M keeps, per column,
+ * the vertical couplings and the full diagonal and drops every coupling to
+ * the horizontal neighbours (eq. (19)).
+ *
+ * Layout.  Every vector is nx*ny*nz fp64 values, vertical index fastest:
+ * cell (i, j, k) is at ((j*nx) + i)*nz + k (section 3, eq. (10)).
+ *
+ * Devices and streams.  A context lives on the CUDA device that is current
+ * when pcg_create is called; every later call must be made with that device
+ * current.  Device pointers must point to memory of that device.  All work
+ * is enqueued on the context's stream (pcg_set_stream; default: the legacy
+ * default stream).
+ *
+ * Errors.  Every function returns a status code (pcg_status) and never
+ * aborts, exits or prints.  On failure, pcg_last_error() gives a message.
+ * Argument errors are detected on the host before any work is enqueued.
+ */
+#ifndef PCG_H
+#define PCG_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PCG_OK = 0,          /* success */
+  PCG_EINVAL = 1,      /* invalid argument (sizes, NULL pointers, coefficients, rtol, maxit) */
+  PCG_ENOMEM = 2,      /* device or pinned-host allocation failed */
+  PCG_ECUDA = 3,       /* a CUDA runtime call failed (no device, launch error, ...) */
+  PCG_ENOTCONV = 4,    /* rtol > 0 and maxit iterations did not reach it */
+  PCG_EBREAKDOWN = 5,  /* <p,Ap> <= 0, <r,z> <= 0 or a non-finite residual (NaN/Inf input) */
+  PCG_ETIMEOUT = 6     /* reserved: a bounded device wait ran out */
+} pcg_status;
+
+typedef struct pcg_ctx pcg_ctx; /* opaque; owns every internal device buffer */
+
+/* Coefficients of the operator.  All host pointers are read during the call
+ * (pcg_create / pcg_update_coeffs) and copied; the caller keeps ownership. */
+typedef struct {
+  double a_h;              /* constant horizontal coefficient (>= 0), used when a_h_field == NULL */
+  const double* a_h_field; /* host, nx*ny values a_h(i,j) >= 0 at index j*nx+i, or NULL */
+  double a_v;              /* vertical coefficient (>= 0) */
+  double mass;             /* zero-order coefficient (> 0) */
+  const double* dz;        /* host, nz layer thicknesses h_k > 0 (k = 0 is the bottom), or NULL for all 1 */
+} pcg_coeffs;
+
+/* Create a solver context for an nx x ny x nz grid on the current device.
+ * Copies the coefficients, builds the per-level tables on the host and the
+ * per-column / per-cell tables (face coefficients, diagonal, Thomas factors)
+ * on the device (section 4.2: "four vectors ... copied to the device once"),
+ * and allocates the workspace r, z, p, q.  Synchronous.
+ * Sizes: nx, ny, nz >= 1, nx*ny*nz < 2^40.  *out receives the context, or
+ * NULL on failure.  Errors: PCG_EINVAL, PCG_ENOMEM, PCG_ECUDA. */
+int pcg_create(int nx, int ny, int nz, const pcg_coeffs* coeffs, pcg_ctx** out);
+
+/* Free every resource of the context.  NULL-safe.  Synchronises its stream. */
+void pcg_destroy(pcg_ctx* ctx);
+
+/* Replace the coefficients of an existing context without any allocation
+ * (same grid).  A context created with a constant a_h cannot switch to a
+ * field (PCG_EINVAL); the reverse is allowed.  Enqueued on the context's
+ * stream. */
+int pcg_update_coeffs(pcg_ctx* ctx, const pcg_coeffs* coeffs);
+
+/* Use `stream` (a cudaStream_t, or NULL for the legacy default stream) for
+ * all later work of this context. */
+int pcg_set_stream(pcg_ctx* ctx, void* stream);
+
+/* y = A x, the matrix-free 7-point stencil of eq. (18), standalone.
+ * x_dev, y_dev: device, N values each, must not overlap.  Asynchronous. */
+int pcg_apply_A(pcg_ctx* ctx, const double* x_dev, double* y_dev);
+
+/* z = M^{-1} r, one Thomas solve per column (eq. (19)), standalone.
+ * r_dev, z_dev: device, N values each, must not overlap.  Asynchronous. */
+int pcg_precond(pcg_ctx* ctx, const double* r_dev, double* z_dev);
+
+/* Solve A x = b by interleaved PCG (Algorithm 1 with the fused sweeps of
+ * Algorithms 2 and 3).
+ *   b_dev       device, N values (read only).
+ *   x_dev       device, N values: the initial guess on entry, the solution
+ *               on return (also on PCG_ENOTCONV / PCG_EBREAKDOWN: the last
+ *               iterate).  Must not overlap b_dev.
+ *   rtol        stop at the first k with ||r_k|| / ||r_0|| < rtol (2-norm of
+ *               the recursively updated residual); rtol = 0 runs exactly
+ *               maxit iterations.  An exactly zero residual also stops.
+ *   maxit       >= 0, at most this many products A p.
+ *   iters_out   (may be NULL) number of products A p performed.
+ *   res_hist    (host, may be NULL) maxit+1 values; entries 0..iters receive
+ *               ||r_k|| / ||r_0|| (0 when r_0 = 0).
+ * The whole iteration runs on the context's stream; the host only polls a
+ * completion flag between batches.  Returns after the result is in x_dev
+ * and res_hist (synchronous on the stream).
+ * Errors: PCG_EINVAL, PCG_ECUDA, PCG_ENOTCONV, PCG_EBREAKDOWN. */
+int pcg_solve(pcg_ctx* ctx, const double* b_dev, double* x_dev, double rtol, int maxit,
+              int* iters_out, double* res_hist);
+
+/* As pcg_solve, with b and x in HOST memory: copies b and x in, solves,
+ * copies x out (section 6: the host copies the initial solution and the
+ * right-hand side in and the solution out).  The device copies of b and x
+ * are allocated on the first call and kept by the context.  Page-locked
+ * host memory gives the fastest transfers; pageable memory also works. */
+int pcg_solve_host(pcg_ctx* ctx, const double* b_host, double* x_host, double rtol,
+                   int maxit, int* iters_out, double* res_hist);
+
+/* Message for the last failed call on this context (or of the last failed
+ * pcg_create when ctx is NULL).  Never NULL; owned by the library. */
+const char* pcg_last_error(const pcg_ctx* ctx);
+
+/* Per-kernel timing.  When enabled, pcg_solve records CUDA events around
+ * every kernel it launches on the context's stream; pcg_kernel_times then
+ * gives, per kernel kind, the summed device time in milliseconds and the
+ * number of launches since the last reset (disabled by default; enabling or
+ * disabling resets the counters). */
+typedef enum {
+  PCG_K_PRECOND_FUSED = 0, /* Algorithm 3 sweep: r -= alpha q; z = M^-1 r; <r,r>, <r,z> */
+  PCG_K_SPMV_FUSED = 1,    /* Algorithm 2 sweep: u += alpha p; p = z + beta p; q = Az + beta q; <p,q> */
+  PCG_K_RESIDUAL = 2,      /* r = b - A x0, p = q = 0, scalar state reset */
+  PCG_K_FINALIZE = 3,      /* deferred x += alpha p */
+  PCG_K_APPLY_A = 4,       /* standalone stencil */
+  PCG_K_PRECOND = 5,       /* standalone Thomas solve */
+  PCG_K_COUNT = 6
+} pcg_kernel_kind;
+
+int pcg_enable_timing(pcg_ctx* ctx, int enable);
+int pcg_kernel_times(pcg_ctx* ctx, double* ms_out /* PCG_K_COUNT */,
+                     long long* launches_out /* PCG_K_COUNT */);
+
+/* Geometry of the launches (for the roofline accounting of a caller):
+ * grid sizes of the fused kernels and the number of kernels pcg_solve
+ * launched in its last call. */
+int pcg_launch_info(const pcg_ctx* ctx, int* grid_precond, int* grid_spmv,
+                    long long* last_solve_launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PCG_H */

@@ -1,0 +1,289 @@
+"""Python binding of libpcg: matrix-free fp64 PCG for anisotropic 3D
+elliptic operators on GB300.
+
+Argument marshalling only.  Every step of the solver runs in the CUDA
+kernels of ``libpcg.so`` behind the C ABI of ``include/pcg.h``; PyTorch
+provides device memory and streams.  Importing this package loads the
+library and raises if it has not been built (``python -m
+matrix_free_pcg_gb300.build`` or ``__graft_entry__.build()``): there is no
+CPU fallback.
+
+The functions carry the C names (``pcg_create``, ``pcg_apply_A``,
+``pcg_precond``, ``pcg_solve``, ...); :class:`Solver` wraps a context.
+Vectors are fp64, nx*ny*nz long, vertical index fastest: cell (i, j, k) at
+((j*nx)+i)*nz + k, i.e. a contiguous tensor of shape (ny, nx, nz).
+"""
+import ctypes
+import os
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libpcg.so")
+
+PCG_OK, PCG_EINVAL, PCG_ENOMEM, PCG_ECUDA, PCG_ENOTCONV, PCG_EBREAKDOWN, PCG_ETIMEOUT = range(7)
+STATUS_NAMES = {0: "PCG_OK", 1: "PCG_EINVAL", 2: "PCG_ENOMEM", 3: "PCG_ECUDA",
+                4: "PCG_ENOTCONV", 5: "PCG_EBREAKDOWN", 6: "PCG_ETIMEOUT"}
+KERNEL_KINDS = ["precond_fused", "spmv_fused", "residual", "finalize", "apply_A", "precond"]
+PCG_K_COUNT = len(KERNEL_KINDS)
+
+EXPORTED = ["pcg_create", "pcg_destroy", "pcg_update_coeffs", "pcg_set_stream", "pcg_apply_A",
+            "pcg_precond", "pcg_solve", "pcg_solve_host", "pcg_last_error",
+            "pcg_enable_timing", "pcg_kernel_times", "pcg_launch_info"]
+
+
+class pcg_coeffs(ctypes.Structure):
+    _fields_ = [("a_h", ctypes.c_double), ("a_h_field", ctypes.POINTER(ctypes.c_double)),
+                ("a_v", ctypes.c_double), ("mass", ctypes.c_double),
+                ("dz", ctypes.POINTER(ctypes.c_double))]
+
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_vp = ctypes.c_void_p
+
+
+def _load(path=LIB_PATH):
+    if not os.path.exists(path):
+        raise ImportError("libpcg.so is not built (%s); run __graft_entry__.build()" % path)
+    lib = ctypes.CDLL(path)
+    sig = {
+        "pcg_create": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      ctypes.POINTER(pcg_coeffs), ctypes.POINTER(_vp)]),
+        "pcg_destroy": (None, [_vp]),
+        "pcg_update_coeffs": (ctypes.c_int, [_vp, ctypes.POINTER(pcg_coeffs)]),
+        "pcg_set_stream": (ctypes.c_int, [_vp, _vp]),
+        "pcg_apply_A": (ctypes.c_int, [_vp, _vp, _vp]),
+        "pcg_precond": (ctypes.c_int, [_vp, _vp, _vp]),
+        "pcg_solve": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_double, ctypes.c_int,
+                                     ctypes.POINTER(ctypes.c_int), _vp]),
+        "pcg_solve_host": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_double, ctypes.c_int,
+                                          ctypes.POINTER(ctypes.c_int), _vp]),
+        "pcg_last_error": (ctypes.c_char_p, [_vp]),
+        "pcg_enable_timing": (ctypes.c_int, [_vp, ctypes.c_int]),
+        "pcg_kernel_times": (ctypes.c_int, [_vp, _vp, _vp]),
+        "pcg_launch_info": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int),
+                                           ctypes.POINTER(ctypes.c_int),
+                                           ctypes.POINTER(ctypes.c_longlong)]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+class PCGError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__("%s: %s" % (STATUS_NAMES.get(status, status), msg))
+        self.status = status
+
+
+def _check(status, ctx=None):
+    if status != PCG_OK:
+        raise PCGError(status, pcg_last_error(ctx))
+    return status
+
+
+def _f64(a, n, what):
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    if a.size != n:
+        raise ValueError("%s: expected %d values, got %d" % (what, n, a.size))
+    return a
+
+
+def _dev_ptr(t, n, what):
+    """Device pointer of a contiguous fp64 CUDA tensor with n elements."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor on a CUDA device" % what)
+    if t.dtype != torch.float64 or not t.is_cuda or not t.is_contiguous() or t.numel() != n:
+        raise ValueError("%s must be a contiguous float64 CUDA tensor with %d elements "
+                         "(got %s %s %s)" % (what, n, t.dtype, t.device, tuple(t.shape)))
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _host_ptr(a, n, what, writable=False):
+    """Host pointer of a C-contiguous fp64 numpy array or CPU tensor with n elements."""
+    try:
+        import torch
+        if isinstance(a, torch.Tensor):
+            if a.is_cuda or a.dtype != torch.float64 or not a.is_contiguous() or a.numel() != n:
+                raise ValueError("%s must be a contiguous float64 CPU tensor with %d elements"
+                                 % (what, n))
+            return ctypes.c_void_p(a.data_ptr())
+    except ImportError:
+        pass
+    if not (isinstance(a, np.ndarray) and a.dtype == np.float64 and a.flags.c_contiguous
+            and a.size == n and (a.flags.writeable or not writable)):
+        raise ValueError("%s must be a C-contiguous float64 array with %d elements" % (what, n))
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def make_coeffs(nx, ny, nz, a_h=1.0, a_h_field=None, a_v=1.0, mass=1.0, dz=None):
+    """pcg_coeffs plus the numpy arrays it points into (keep both alive)."""
+    keep = []
+    c = pcg_coeffs()
+    c.a_h = float(a_h)
+    c.a_v = float(a_v)
+    c.mass = float(mass)
+    if a_h_field is not None:
+        f = _f64(a_h_field, nx * ny, "a_h_field")
+        keep.append(f)
+        c.a_h_field = f.ctypes.data_as(_dp)
+    if dz is not None:
+        d = _f64(dz, nz, "dz")
+        keep.append(d)
+        c.dz = d.ctypes.data_as(_dp)
+    return c, keep
+
+
+# ------------------------------------------------------------ C-named calls
+
+def pcg_last_error(ctx=None):
+    return _lib.pcg_last_error(ctx).decode()
+
+
+def pcg_create(nx, ny, nz, a_h=1.0, a_h_field=None, a_v=1.0, mass=1.0, dz=None):
+    c, keep = make_coeffs(nx, ny, nz, a_h, a_h_field, a_v, mass, dz)
+    ctx = ctypes.c_void_p()
+    _check(_lib.pcg_create(int(nx), int(ny), int(nz), ctypes.byref(c), ctypes.byref(ctx)))
+    return ctx
+
+
+def pcg_destroy(ctx):
+    _lib.pcg_destroy(ctx)
+
+
+def pcg_update_coeffs(ctx, nx, ny, nz, a_h=1.0, a_h_field=None, a_v=1.0, mass=1.0, dz=None):
+    c, keep = make_coeffs(nx, ny, nz, a_h, a_h_field, a_v, mass, dz)
+    return _check(_lib.pcg_update_coeffs(ctx, ctypes.byref(c)), ctx)
+
+
+def pcg_set_stream(ctx, stream):
+    """stream: a torch.cuda.Stream, a raw cudaStream_t integer, or None."""
+    handle = getattr(stream, "cuda_stream", stream)
+    return _check(_lib.pcg_set_stream(ctx, ctypes.c_void_p(handle or 0)), ctx)
+
+
+def pcg_apply_A(ctx, n, x, y):
+    return _check(_lib.pcg_apply_A(ctx, _dev_ptr(x, n, "x"), _dev_ptr(y, n, "y")), ctx)
+
+
+def pcg_precond(ctx, n, r, z):
+    return _check(_lib.pcg_precond(ctx, _dev_ptr(r, n, "r"), _dev_ptr(z, n, "z")), ctx)
+
+
+def pcg_solve(ctx, n, b, x, rtol, maxit, history=True):
+    """Returns (iters, hist or None, status); raises on EINVAL/ENOMEM/ECUDA."""
+    it = ctypes.c_int(-1)
+    hist = np.full(int(maxit) + 1, np.nan) if history else None
+    st = _lib.pcg_solve(ctx, _dev_ptr(b, n, "b"), _dev_ptr(x, n, "x"), float(rtol), int(maxit),
+                        ctypes.byref(it), hist.ctypes.data_as(_vp) if history else None)
+    if st not in (PCG_OK, PCG_ENOTCONV, PCG_EBREAKDOWN):
+        _check(st, ctx)
+    return it.value, (hist[: it.value + 1] if history else None), st
+
+
+def pcg_solve_host(ctx, n, b, x, rtol, maxit, history=True):
+    """b, x: host arrays (numpy or CPU tensors, pinned for full speed)."""
+    it = ctypes.c_int(-1)
+    hist = np.full(int(maxit) + 1, np.nan) if history else None
+    st = _lib.pcg_solve_host(ctx, _host_ptr(b, n, "b"), _host_ptr(x, n, "x", writable=True),
+                             float(rtol), int(maxit), ctypes.byref(it),
+                             hist.ctypes.data_as(_vp) if history else None)
+    if st not in (PCG_OK, PCG_ENOTCONV, PCG_EBREAKDOWN):
+        _check(st, ctx)
+    return it.value, (hist[: it.value + 1] if history else None), st
+
+
+def pcg_enable_timing(ctx, enable=True):
+    return _check(_lib.pcg_enable_timing(ctx, int(bool(enable))), ctx)
+
+
+def pcg_kernel_times(ctx):
+    ms = (ctypes.c_double * PCG_K_COUNT)()
+    cnt = (ctypes.c_longlong * PCG_K_COUNT)()
+    _check(_lib.pcg_kernel_times(ctx, ms, cnt), ctx)
+    return {k: (ms[i], cnt[i]) for i, k in enumerate(KERNEL_KINDS)}
+
+
+def pcg_launch_info(ctx):
+    gm, ga, nl = ctypes.c_int(), ctypes.c_int(), ctypes.c_longlong()
+    _check(_lib.pcg_launch_info(ctx, ctypes.byref(gm), ctypes.byref(ga), ctypes.byref(nl)), ctx)
+    return {"grid_precond": gm.value, "grid_spmv": ga.value, "last_solve_launches": nl.value}
+
+
+# ------------------------------------------------------------------- class
+
+class Solver:
+    """One solver context on the current CUDA device.
+
+    a_h: constant horizontal coefficient, or a_h_field: (ny, nx) array of
+    a_h(i, j); a_v: vertical coefficient; mass: zero-order coefficient;
+    dz: nz layer thicknesses (bottom first), default all ones.
+    """
+
+    def __init__(self, nx, ny, nz, a_h=1.0, a_h_field=None, a_v=1.0, mass=1.0, dz=None,
+                 stream=None):
+        self.nx, self.ny, self.nz = int(nx), int(ny), int(nz)
+        self.n = self.nx * self.ny * self.nz
+        self.ctx = pcg_create(nx, ny, nz, a_h, a_h_field, a_v, mass, dz)
+        if stream is not None:
+            pcg_set_stream(self.ctx, stream)
+
+    def close(self):
+        if self.ctx is not None:
+            pcg_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def update_coeffs(self, a_h=1.0, a_h_field=None, a_v=1.0, mass=1.0, dz=None):
+        pcg_update_coeffs(self.ctx, self.nx, self.ny, self.nz, a_h, a_h_field, a_v, mass, dz)
+
+    def set_stream(self, stream):
+        pcg_set_stream(self.ctx, stream)
+
+    def apply_A(self, x, y=None):
+        import torch
+        if y is None:
+            y = torch.empty_like(x)
+        pcg_apply_A(self.ctx, self.n, x, y)
+        return y
+
+    def precond(self, r, z=None):
+        import torch
+        if z is None:
+            z = torch.empty_like(r)
+        pcg_precond(self.ctx, self.n, r, z)
+        return z
+
+    def solve(self, b, x, rtol=1e-10, maxit=500, history=True):
+        """x (device tensor): initial guess in, solution out.
+        Returns (iters, residual history, status)."""
+        return pcg_solve(self.ctx, self.n, b, x, rtol, maxit, history)
+
+    def solve_host(self, b, x, rtol=1e-10, maxit=500, history=True):
+        return pcg_solve_host(self.ctx, self.n, b, x, rtol, maxit, history)
+
+    def enable_timing(self, enable=True):
+        pcg_enable_timing(self.ctx, enable)
+
+    def kernel_times(self):
+        return pcg_kernel_times(self.ctx)
+
+    def launch_info(self):
+        return pcg_launch_info(self.ctx)

@@ -1,0 +1,552 @@
+// Host driver and C ABI of libpcg (declared in include/pcg.h).
+//
+// Method: Mueller, Guo, Scheichl, Shi, "Matrix-free GPU implementation of a
+// preconditioned conjugate gradient solver for anisotropic elliptic PDEs":
+// the interleaved PCG loop of section 4.3, Algorithm 1, driven from the host
+// with all data and all scalars resident on the device (section 6: only the
+// initial solution and right-hand side go in, the solution comes out).
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <algorithm>
+#include <new>
+#include <string>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "../../include/pcg.h"
+#include "pcg_internal.h"
+
+using pcg::DevState;
+using pcg::Op;
+
+namespace {
+
+thread_local std::string g_create_error = "no error";
+
+struct KernelEvent {
+  int kind;
+  cudaEvent_t start, stop;
+};
+
+}  // namespace
+
+struct pcg_ctx {
+  int device = -1;
+  int num_sms = 0;
+  cudaStream_t stream = nullptr;
+  Op op{};
+  bool has_field_buffers = false;
+  // device buffers owned by the context
+  double *r = nullptr, *z = nullptr, *p = nullptr, *q = nullptr;
+  double *lev = nullptr, *ah = nullptr, *faceE = nullptr, *faceN = nullptr;
+  double *cdiag = nullptr, *tnphi = nullptr, *tinvd = nullptr;
+  double *partials = nullptr, *hist = nullptr;
+  int hist_cap = 0;
+  DevState* state = nullptr;
+  double *b_host_api = nullptr, *x_host_api = nullptr;  // device copies for pcg_solve_host
+  DevState* pinned = nullptr;                           // 3 host slots
+  int grid_m = 1, grid_a = 1;
+  long long last_launches = 0;
+  // timing
+  bool timing = false;
+  std::vector<KernelEvent> events;  // recorded during the current solve
+  std::vector<cudaEvent_t> event_pool;
+  size_t pool_used = 0;
+  double ms[PCG_K_COUNT] = {0};
+  long long launches[PCG_K_COUNT] = {0};
+  std::string err = "no error";
+};
+
+namespace {
+
+int fail(pcg_ctx* ctx, int status, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  if (ctx)
+    ctx->err = buf;
+  else
+    g_create_error = buf;
+  return status;
+}
+
+int cuda_fail(pcg_ctx* ctx, cudaError_t e, const char* what) {
+  const int st = (e == cudaErrorMemoryAllocation) ? PCG_ENOMEM : PCG_ECUDA;
+  return fail(ctx, st, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// Makes the context's device current for the duration of a call.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) return;
+    ok = (prev == dev) || (cudaSetDevice(dev) == cudaSuccess);
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (ok && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+bool finite_nonneg(double v) { return std::isfinite(v) && v >= 0.0; }
+
+int validate_coeffs(pcg_ctx* ctx, int nx, int ny, int nz, const pcg_coeffs* c) {
+  if (!c) return fail(ctx, PCG_EINVAL, "coeffs is NULL");
+  if (!finite_nonneg(c->a_v)) return fail(ctx, PCG_EINVAL, "a_v must be finite and >= 0");
+  if (!(std::isfinite(c->mass) && c->mass > 0.0))
+    return fail(ctx, PCG_EINVAL, "mass must be finite and > 0");
+  if (!c->a_h_field && !finite_nonneg(c->a_h))
+    return fail(ctx, PCG_EINVAL, "a_h must be finite and >= 0");
+  if (c->a_h_field) {
+    const long long nc = (long long)nx * ny;
+    for (long long i = 0; i < nc; ++i)
+      if (!finite_nonneg(c->a_h_field[i]))
+        return fail(ctx, PCG_EINVAL, "a_h_field[%lld] must be finite and >= 0", i);
+  }
+  if (c->dz)
+    for (int k = 0; k < nz; ++k)
+      if (!(std::isfinite(c->dz[k]) && c->dz[k] > 0.0))
+        return fail(ctx, PCG_EINVAL, "dz[%d] must be finite and > 0", k);
+  return PCG_OK;
+}
+
+// Per-level tables (eq. (17): the vertical discretisation is the same in
+// every column and only nz long).  For a constant a_h the Thomas factors are
+// identical in every column and are computed here once.
+int build_levels(pcg_ctx* ctx, int nz, const pcg_coeffs* c, bool varying,
+                 std::vector<double>& lev) {
+  using namespace pcg;
+  lev.assign((size_t)kLevCount * nz, 0.0);
+  std::vector<double> h(nz), tup(nz), tdn(nz);
+  for (int k = 0; k < nz; ++k) h[k] = c->dz ? c->dz[k] : 1.0;
+  for (int k = 0; k < nz; ++k) tup[k] = (k < nz - 1) ? c->a_v / (0.5 * (h[k] + h[k + 1])) : 0.0;
+  for (int k = 0; k < nz; ++k) tdn[k] = (k > 0) ? tup[k - 1] : 0.0;
+  double nphi_prev = 0.0;
+  for (int k = 0; k < nz; ++k) {
+    const double base = c->mass * h[k] + tup[k] + tdn[k];
+    lev[LV_UP * nz + k] = -tup[k];
+    lev[LV_DN * nz + k] = -tdn[k];
+    lev[LV_H * nz + k] = h[k];
+    lev[LV_TUP * nz + k] = tup[k];
+    lev[LV_TDN * nz + k] = tdn[k];
+    if (varying) {
+      lev[LV_DIAG * nz + k] = base;
+      lev[LV_HW * nz + k] = -h[k];
+    } else {
+      const double diag = base + h[k] * (4.0 * c->a_h);
+      lev[LV_DIAG * nz + k] = diag;
+      lev[LV_HW * nz + k] = -h[k] * c->a_h;
+      const double D = diag - tdn[k] * nphi_prev;
+      if (!(D > 0.0) || !std::isfinite(D))
+        return fail(ctx, PCG_EBREAKDOWN, "Thomas pivot D_%d = %g is not positive", k, D);
+      lev[LV_NPHI * nz + k] = tup[k] / D;
+      lev[LV_INVD * nz + k] = 1.0 / D;
+      nphi_prev = tup[k] / D;
+    }
+  }
+  return PCG_OK;
+}
+
+template <typename T>
+cudaError_t dalloc(T** p, size_t count) {
+  return cudaMalloc(reinterpret_cast<void**>(p), count * sizeof(T));
+}
+
+void free_all(pcg_ctx* ctx) {
+  double* bufs[] = {ctx->r,     ctx->z,     ctx->p,     ctx->q,        ctx->lev,
+                    ctx->ah,    ctx->faceE, ctx->faceN, ctx->cdiag,    ctx->tnphi,
+                    ctx->tinvd, ctx->partials, ctx->hist, ctx->b_host_api, ctx->x_host_api};
+  for (double* b : bufs)
+    if (b) cudaFree(b);
+  if (ctx->state) cudaFree(ctx->state);
+  if (ctx->pinned) cudaFreeHost(ctx->pinned);
+  for (cudaEvent_t e : ctx->event_pool) cudaEventDestroy(e);
+  ctx->event_pool.clear();
+}
+
+// Upload coefficients and (for a field) rebuild the per-column and per-cell
+// tables on the device.  Synchronous.
+int load_coeffs(pcg_ctx* ctx, const pcg_coeffs* c, bool varying) {
+  std::vector<double> lev;
+  int st = build_levels(ctx, ctx->op.nz, c, varying, lev);
+  if (st) return st;
+  cudaError_t e = cudaMemcpyAsync(ctx->lev, lev.data(), lev.size() * sizeof(double),
+                                  cudaMemcpyHostToDevice, ctx->stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "upload of the level table");
+  ctx->op.varying = varying ? 1 : 0;
+  if (varying) {
+    e = cudaMemcpyAsync(ctx->ah, c->a_h_field, ctx->op.ncols * sizeof(double),
+                        cudaMemcpyHostToDevice, ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "upload of a_h_field");
+    e = cudaMemsetAsync(&ctx->state->setup_error, 0, sizeof(int), ctx->stream);
+    if (e == cudaSuccess) e = pcg::launch_face_coeffs(ctx->op, ctx->faceE, ctx->faceN, ctx->stream);
+    if (e == cudaSuccess) e = pcg::launch_cell_diag(ctx->op, ctx->cdiag, ctx->stream);
+    if (e == cudaSuccess)
+      e = pcg::launch_thomas_factors(ctx->op, ctx->state, ctx->tnphi, ctx->tinvd, ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "coefficient set-up kernels");
+    int bad = 0;
+    e = cudaMemcpyAsync(&bad, &ctx->state->setup_error, sizeof(int), cudaMemcpyDeviceToHost,
+                        ctx->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "coefficient set-up");
+    if (bad) return fail(ctx, PCG_EBREAKDOWN, "a Thomas pivot of some column is not positive");
+  } else {
+    e = cudaStreamSynchronize(ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "coefficient upload");
+  }
+  return PCG_OK;
+}
+
+cudaEvent_t pool_event(pcg_ctx* ctx) {
+  if (ctx->pool_used == ctx->event_pool.size()) {
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    ctx->event_pool.push_back(e);
+  }
+  return ctx->event_pool[ctx->pool_used++];
+}
+
+// Launch helper: records start/stop events when timing is on.
+template <typename F>
+cudaError_t timed(pcg_ctx* ctx, int kind, F&& launch) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (ctx->timing) {
+    a = pool_event(ctx);
+    b = pool_event(ctx);
+    if (a && b) cudaEventRecord(a, ctx->stream);
+  }
+  cudaError_t e = launch();
+  ctx->last_launches++;
+  if (ctx->timing && a && b) {
+    cudaEventRecord(b, ctx->stream);
+    ctx->events.push_back({kind, a, b});
+  }
+  return e;
+}
+
+// After the stream has been synchronised: fold the recorded events into the
+// per-kernel totals.  Sweeps enqueued after the device set its completion
+// flag return at once; only the first `work_m` preconditioner sweeps and
+// `work_a` SpMV sweeps did work, and only those are counted.
+void collect_events(pcg_ctx* ctx, long long work_m, long long work_a) {
+  long long seen_m = 0, seen_a = 0;
+  for (const KernelEvent& ke : ctx->events) {
+    if (ke.kind == PCG_K_PRECOND_FUSED && seen_m++ >= work_m) continue;
+    if (ke.kind == PCG_K_SPMV_FUSED && seen_a++ >= work_a) continue;
+    float ms = 0.0f;
+    if (cudaEventElapsedTime(&ms, ke.start, ke.stop) == cudaSuccess) {
+      ctx->ms[ke.kind] += ms;
+      ctx->launches[ke.kind]++;
+    }
+  }
+  ctx->events.clear();
+  ctx->pool_used = 0;
+}
+
+bool overlap(const double* a, const double* b, long long n) {
+  return (a < b + n) && (b < a + n);
+}
+
+int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxit,
+                 int* iters_out, double* res_hist) {
+  cudaError_t e;
+  if (maxit + 1 > ctx->hist_cap) {
+    double* nh = nullptr;
+    e = dalloc(&nh, (size_t)maxit + 1);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "allocation of the residual history");
+    if (ctx->hist) cudaFree(ctx->hist);
+    ctx->hist = nh;
+    ctx->hist_cap = maxit + 1;
+  }
+  const Op& op = ctx->op;
+  cudaStream_t s = ctx->stream;
+  ctx->last_launches = 0;
+  ctx->events.clear();
+  ctx->pool_used = 0;
+  e = timed(ctx, PCG_K_RESIDUAL, [&] {
+    return pcg::launch_residual(op, ctx->state, b, x, ctx->r, ctx->p, ctx->q, rtol, maxit,
+                                ctx->grid_a, s);
+  });
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "residual kernel launch");
+
+  // Enqueue the loop in batches; poll the device's `done` flag one batch
+  // behind, so the GPU always has queued work and never waits for the host.
+  const int batch = (op.n >= (1LL << 24)) ? 4 : 16;
+  int enq = 0, slot = 0, pending = -1;
+  cudaEvent_t ev[2] = {pool_event(ctx), pool_event(ctx)};
+  if (!ev[0] || !ev[1]) return fail(ctx, PCG_ECUDA, "event creation failed");
+  bool stop = false;
+  while (enq <= maxit && !stop) {
+    const int nb = std::min(batch, maxit + 1 - enq);
+    for (int i = 0; i < nb; ++i) {
+      e = timed(ctx, PCG_K_PRECOND_FUSED, [&] {
+        return pcg::launch_precond_fused(op, ctx->state, ctx->r, ctx->q, ctx->z, ctx->partials,
+                                         ctx->hist, ctx->grid_m, s);
+      });
+      if (e != cudaSuccess) return cuda_fail(ctx, e, "preconditioner sweep launch");
+      if (enq + i < maxit) {
+        e = timed(ctx, PCG_K_SPMV_FUSED, [&] {
+          return pcg::launch_spmv_fused(op, ctx->state, ctx->z, x, ctx->p, ctx->q,
+                                        ctx->partials + 2 * ctx->grid_m, ctx->grid_a, s);
+        });
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "SpMV sweep launch");
+      }
+    }
+    enq += nb;
+    e = cudaMemcpyAsync(&ctx->pinned[slot], ctx->state, sizeof(DevState),
+                        cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[slot], s);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "state poll");
+    if (pending >= 0) {
+      e = cudaEventSynchronize(ev[pending]);
+      if (e != cudaSuccess) return cuda_fail(ctx, e, "solve loop");
+      if (ctx->pinned[pending].done) stop = true;
+    }
+    pending = slot;
+    slot ^= 1;
+  }
+  e = timed(ctx, PCG_K_FINALIZE,
+            [&] { return pcg::launch_finalize(op, ctx->state, x, ctx->p, ctx->grid_a, s); });
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "finalize launch");
+  e = cudaMemcpyAsync(&ctx->pinned[2], ctx->state, sizeof(DevState), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "solve");
+  const DevState fin = ctx->pinned[2];
+  if (!fin.done) return fail(ctx, PCG_ECUDA, "solve ended without the device completion flag");
+  if (res_hist && fin.iters >= 0) {
+    e = cudaMemcpyAsync(res_hist, ctx->hist, sizeof(double) * ((size_t)fin.iters + 1),
+                        cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "residual history copy");
+  }
+  if (ctx->timing) collect_events(ctx, fin.it, fin.it > 0 ? fin.it - 1 : 0);
+  if (iters_out) *iters_out = fin.iters;
+  if (fin.status == PCG_ENOTCONV)
+    return fail(ctx, PCG_ENOTCONV, "no convergence to rtol=%g in %d iterations (last ratio %g)",
+                rtol, maxit, fin.R0 > 0 ? std::sqrt(fin.last_R / fin.R0) : 0.0);
+  if (fin.status == PCG_EBREAKDOWN)
+    return fail(ctx, PCG_EBREAKDOWN,
+                "breakdown after %d iterations: ||r||^2=%g <r,z>=%g <p,Ap>=%g", fin.iters,
+                fin.last_R, fin.last_kappa, fin.last_sigma);
+  return fin.status;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pcg_create(int nx, int ny, int nz, const pcg_coeffs* coeffs, pcg_ctx** out) {
+  if (!out) return fail(nullptr, PCG_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (nx < 1 || ny < 1 || nz < 1)
+    return fail(nullptr, PCG_EINVAL, "grid %d x %d x %d: every size must be >= 1", nx, ny, nz);
+  const long long ncols = (long long)nx * ny;
+  const long long n = ncols * nz;
+  if (n >= (1LL << 40)) return fail(nullptr, PCG_EINVAL, "grid too large (%lld cells)", n);
+  int st = validate_coeffs(nullptr, nx, ny, nz, coeffs);
+  if (st) return st;
+
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) {
+    int count = 0;
+    e = cudaGetDeviceCount(&count);
+    if (e == cudaSuccess && count < 1) e = cudaErrorNoDevice;
+  }
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "no usable CUDA device");
+
+  pcg_ctx* ctx = new (std::nothrow) pcg_ctx();
+  if (!ctx) return fail(nullptr, PCG_ENOMEM, "host allocation failed");
+  ctx->device = dev;
+  cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, dev);
+  Op& op = ctx->op;
+  op.nx = nx;
+  op.ny = ny;
+  op.nz = nz;
+  op.pz = (nz + 15) / 16 * 16;
+  op.ncols = ncols;
+  op.n = n;
+  op.ntiles = (ncols + pcg::kTile - 1) / pcg::kTile;
+  const bool varying = coeffs->a_h_field != nullptr;
+  ctx->has_field_buffers = varying;
+
+  auto bail = [&](int status) {
+    std::string msg = ctx->err;
+    free_all(ctx);
+    delete ctx;
+    g_create_error = msg;
+    return status;
+  };
+  e = dalloc(&ctx->r, n);
+  if (e == cudaSuccess) e = dalloc(&ctx->z, n);
+  if (e == cudaSuccess) e = dalloc(&ctx->p, n);
+  if (e == cudaSuccess) e = dalloc(&ctx->q, n);
+  if (e == cudaSuccess) e = dalloc(&ctx->lev, (size_t)pcg::kLevCount * nz);
+  if (e == cudaSuccess) e = dalloc(&ctx->state, 1);
+  if (e == cudaSuccess) e = cudaMemset(ctx->state, 0, sizeof(DevState));
+  if (e == cudaSuccess && varying) {
+    const size_t tiled = (size_t)op.ntiles * pcg::kTile * nz;
+    e = dalloc(&ctx->ah, ncols);
+    if (e == cudaSuccess) e = dalloc(&ctx->faceE, ncols);
+    if (e == cudaSuccess) e = dalloc(&ctx->faceN, ncols);
+    if (e == cudaSuccess) e = dalloc(&ctx->cdiag, n);
+    if (e == cudaSuccess) e = dalloc(&ctx->tnphi, tiled);
+    if (e == cudaSuccess) e = dalloc(&ctx->tinvd, tiled);
+  }
+  if (e == cudaSuccess)
+    e = cudaHostAlloc(reinterpret_cast<void**>(&ctx->pinned), 3 * sizeof(DevState),
+                      cudaHostAllocDefault);
+  if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "workspace allocation"));
+  memset(ctx->pinned, 0, 3 * sizeof(DevState));
+  op.lev = ctx->lev;
+  op.ah = ctx->ah;
+  op.faceE = ctx->faceE;
+  op.faceN = ctx->faceN;
+  op.cdiag = ctx->cdiag;
+  op.tnphi = ctx->tnphi;
+  op.tinvd = ctx->tinvd;
+  op.varying = varying ? 1 : 0;
+
+  e = pcg::prepare_kernels(op);
+  if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "kernel attribute set-up"));
+  ctx->grid_m = pcg::grid_precond(op, ctx->num_sms);
+  ctx->grid_a = pcg::grid_spmv(op, ctx->num_sms);
+  e = dalloc(&ctx->partials, 2 * (size_t)(ctx->grid_m + ctx->grid_a));
+  if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "workspace allocation"));
+  st = load_coeffs(ctx, coeffs, varying);
+  if (st) return bail(st);
+  *out = ctx;
+  return PCG_OK;
+}
+
+void pcg_destroy(pcg_ctx* ctx) {
+  if (!ctx) return;
+  DeviceGuard g(ctx->device);
+  cudaStreamSynchronize(ctx->stream);
+  free_all(ctx);
+  delete ctx;
+}
+
+int pcg_update_coeffs(pcg_ctx* ctx, const pcg_coeffs* coeffs) {
+  if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
+  int st = validate_coeffs(ctx, ctx->op.nx, ctx->op.ny, ctx->op.nz, coeffs);
+  if (st) return st;
+  const bool varying = coeffs->a_h_field != nullptr;
+  if (varying && !ctx->has_field_buffers)
+    return fail(ctx, PCG_EINVAL,
+                "context was created with a constant a_h; it cannot take an a_h field");
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
+  return load_coeffs(ctx, coeffs, varying);
+}
+
+int pcg_set_stream(pcg_ctx* ctx, void* stream) {
+  if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
+  ctx->stream = static_cast<cudaStream_t>(stream);
+  return PCG_OK;
+}
+
+int pcg_apply_A(pcg_ctx* ctx, const double* x_dev, double* y_dev) {
+  if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
+  if (!x_dev || !y_dev) return fail(ctx, PCG_EINVAL, "x and y must be non-NULL device pointers");
+  if (overlap(x_dev, y_dev, ctx->op.n)) return fail(ctx, PCG_EINVAL, "x and y overlap");
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
+  cudaError_t e = pcg::launch_apply(ctx->op, x_dev, y_dev, ctx->grid_a, ctx->stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "apply_A launch");
+  return PCG_OK;
+}
+
+int pcg_precond(pcg_ctx* ctx, const double* r_dev, double* z_dev) {
+  if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
+  if (!r_dev || !z_dev) return fail(ctx, PCG_EINVAL, "r and z must be non-NULL device pointers");
+  if (overlap(r_dev, z_dev, ctx->op.n)) return fail(ctx, PCG_EINVAL, "r and z overlap");
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
+  cudaError_t e = pcg::launch_precond(ctx->op, r_dev, z_dev, ctx->grid_m, ctx->stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "precond launch");
+  return PCG_OK;
+}
+
+static int check_solve_args(pcg_ctx* ctx, const double* b, const double* x, double rtol,
+                            int maxit) {
+  if (!b || !x) return fail(ctx, PCG_EINVAL, "b and x must be non-NULL");
+  if (!(std::isfinite(rtol) && rtol >= 0.0)) return fail(ctx, PCG_EINVAL, "rtol must be >= 0");
+  if (maxit < 0) return fail(ctx, PCG_EINVAL, "maxit must be >= 0");
+  if (overlap(b, x, ctx->op.n)) return fail(ctx, PCG_EINVAL, "b and x overlap");
+  return PCG_OK;
+}
+
+int pcg_solve(pcg_ctx* ctx, const double* b_dev, double* x_dev, double rtol, int maxit,
+              int* iters_out, double* res_hist) {
+  if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
+  int st = check_solve_args(ctx, b_dev, x_dev, rtol, maxit);
+  if (st) return st;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
+  return solve_device(ctx, b_dev, x_dev, rtol, maxit, iters_out, res_hist);
+}
+
+int pcg_solve_host(pcg_ctx* ctx, const double* b_host, double* x_host, double rtol, int maxit,
+                   int* iters_out, double* res_hist) {
+  if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
+  int st = check_solve_args(ctx, b_host, x_host, rtol, maxit);
+  if (st) return st;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
+  cudaError_t e = cudaSuccess;
+  if (!ctx->b_host_api) e = dalloc(&ctx->b_host_api, ctx->op.n);
+  if (e == cudaSuccess && !ctx->x_host_api) e = dalloc(&ctx->x_host_api, ctx->op.n);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "device buffers for b and x");
+  const size_t bytes = sizeof(double) * (size_t)ctx->op.n;
+  e = cudaMemcpyAsync(ctx->b_host_api, b_host, bytes, cudaMemcpyHostToDevice, ctx->stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(ctx->x_host_api, x_host, bytes, cudaMemcpyHostToDevice, ctx->stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "host-to-device copy");
+  st = solve_device(ctx, ctx->b_host_api, ctx->x_host_api, rtol, maxit, iters_out, res_hist);
+  if (st != PCG_OK && st != PCG_ENOTCONV && st != PCG_EBREAKDOWN) return st;
+  e = cudaMemcpyAsync(x_host, ctx->x_host_api, bytes, cudaMemcpyDeviceToHost, ctx->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "device-to-host copy");
+  return st;
+}
+
+const char* pcg_last_error(const pcg_ctx* ctx) {
+  return ctx ? ctx->err.c_str() : g_create_error.c_str();
+}
+
+int pcg_enable_timing(pcg_ctx* ctx, int enable) {
+  if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
+  ctx->timing = enable != 0;
+  for (int i = 0; i < PCG_K_COUNT; ++i) {
+    ctx->ms[i] = 0.0;
+    ctx->launches[i] = 0;
+  }
+  return PCG_OK;
+}
+
+int pcg_kernel_times(pcg_ctx* ctx, double* ms_out, long long* launches_out) {
+  if (!ctx || !ms_out || !launches_out) return fail(ctx, PCG_EINVAL, "NULL argument");
+  for (int i = 0; i < PCG_K_COUNT; ++i) {
+    ms_out[i] = ctx->ms[i];
+    launches_out[i] = ctx->launches[i];
+  }
+  return PCG_OK;
+}
+
+int pcg_launch_info(const pcg_ctx* ctx, int* grid_precond, int* grid_spmv,
+                    long long* last_solve_launches) {
+  if (!ctx) return PCG_EINVAL;
+  if (grid_precond) *grid_precond = ctx->grid_m;
+  if (grid_spmv) *grid_spmv = ctx->grid_a;
+  if (last_solve_launches) *last_solve_launches = ctx->last_launches;
+  return PCG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,100 @@
+// Internal declarations shared by the host driver (pcg_api.cu) and the
+// kernels (pcg_kernels.cu).  Not part of the public ABI (include/pcg.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace pcg {
+
+// Columns per preconditioner tile: one warp, one thread per vertical column.
+constexpr int kTile = 32;
+// Threads per block of the stencil sweeps.
+constexpr int kSpmvThreads = 256;
+// Largest column height whose tile pair (r and q, 32 columns) fits in the
+// 227 KB of shared memory of one block; taller columns use the unstaged
+// preconditioner sweep.
+constexpr int kMaxStagedNz = 448;
+
+// Per-level coefficient table, kLevCount rows of nz doubles (row-major).
+enum LevRow {
+  LV_DIAG = 0,  // constant a_h: full diagonal; field: h_k*mass + T_{k+1/2} + T_{k-1/2}
+  LV_UP,        // -T_{k+1/2}  (0 at the top)
+  LV_DN,        // -T_{k-1/2}  (0 at the bottom)
+  LV_HW,        // constant a_h: -h_k*a_h ; field: -h_k
+  LV_NPHI,      // constant a_h: T_{k+1/2} / D_k  (minus the Thomas factor phi_k)
+  LV_INVD,      // constant a_h: 1 / D_k
+  LV_H,         // h_k
+  LV_TUP,       // T_{k+1/2}
+  LV_TDN,       // T_{k-1/2}
+  kLevCount
+};
+
+// Operator description handed to every kernel by value.
+struct Op {
+  int nx, ny, nz;
+  int pz;              // nz rounded up to a multiple of 16 (shared-memory column stride)
+  long long ncols;     // nx*ny
+  long long n;         // ncols*nz
+  long long ntiles;    // ceil(ncols / kTile)
+  int varying;         // 1: a_h given per column
+  const double* lev;   // kLevCount*nz
+  const double* ah;    // field: a_h per column
+  const double* faceE; // field: face value between (i,j) and (i+1,j), per column
+  const double* faceN; // field: face value between (i,j) and (i,j+1), per column
+  const double* cdiag; // field: diagonal per cell, vertical index fastest
+  const double* tnphi; // field: T_{k+1/2}/D_k per cell, tile-interleaved ((t*nz+k)*32+lane)
+  const double* tinvd; // field: 1/D_k per cell, tile-interleaved
+};
+
+// Scalars of the interleaved iteration, resident on the device.
+struct DevState {
+  double alpha;      // step length of the current direction (0 before the first sweep)
+  double beta;       // direction update factor for the next sweep
+  double kappa_old;  // <r,z> of the previous preconditioner sweep (1 initially)
+  double R0;         // ||r_0||^2
+  double rtol;
+  double last_sigma, last_kappa, last_R;  // diagnostics
+  int it;            // preconditioner sweeps completed
+  int done;          // 1: stop; every later sweep returns at once
+  int status;        // pcg_status of the solve
+  int iters;         // products A p performed when the solve stopped
+  int maxit;
+  unsigned int ticket_m;  // last-block tickets of the two grid reductions
+  unsigned int ticket_a;
+  int setup_error;   // a non-positive Thomas pivot was met in the setup kernel
+};
+
+// ---- launchers (pcg_kernels.cu); all enqueue on `s` and return the launch error
+
+cudaError_t launch_face_coeffs(const Op& op, double* faceE, double* faceN, cudaStream_t s);
+cudaError_t launch_cell_diag(const Op& op, double* cdiag, cudaStream_t s);
+cudaError_t launch_thomas_factors(const Op& op, DevState* st, double* tnphi, double* tinvd,
+                                  cudaStream_t s);
+
+// r = b - A x ; p = q = 0 ; scalar state reset for a new solve.
+cudaError_t launch_residual(const Op& op, DevState* st, const double* b, const double* x,
+                            double* r, double* p, double* q, double rtol, int maxit, int grid,
+                            cudaStream_t s);
+// y = A x
+cudaError_t launch_apply(const Op& op, const double* x, double* y, int grid, cudaStream_t s);
+// z = M^{-1} r
+cudaError_t launch_precond(const Op& op, const double* r, double* z, int grid, cudaStream_t s);
+// Algorithm 3 sweep
+cudaError_t launch_precond_fused(const Op& op, DevState* st, double* r, const double* q,
+                                 double* z, double* partials, double* hist, int grid,
+                                 cudaStream_t s);
+// Algorithm 2 sweep
+cudaError_t launch_spmv_fused(const Op& op, DevState* st, const double* z, double* u,
+                              double* p, double* q, double* partials, int grid, cudaStream_t s);
+// x += alpha p (the update deferred past the last sweep)
+cudaError_t launch_finalize(const Op& op, const DevState* st, double* x, const double* p,
+                            int grid, cudaStream_t s);
+
+// Occupancy-derived grid sizes (blocks) for the persistent sweeps.
+int grid_precond(const Op& op, int num_sms);
+int grid_spmv(const Op& op, int num_sms);
+// Shared-memory attribute set-up for the staged preconditioner (once per device).
+cudaError_t prepare_kernels(const Op& op);
+
+}  // namespace pcg

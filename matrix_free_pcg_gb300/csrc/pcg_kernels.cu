@@ -1,0 +1,798 @@
+// Device kernels of the matrix-free PCG solver (fp64, sm_103a).
+//
+// Method: Mueller, Guo, Scheichl, Shi, "Matrix-free GPU implementation of a
+// preconditioned conjugate gradient solver for anisotropic elliptic PDEs".
+//   - stencil: section 4.2, eq. (18), recomputed from per-level tables
+//     (eq. (17)) and per-column face values;
+//   - column preconditioner: section 4.1 and eq. (19), Thomas algorithm;
+//   - fused sweeps: section 4.3, Algorithm 1, with the two kernels of
+//     Appendix A (Algorithm 2: SpMV sweep, Algorithm 3: preconditioner sweep).
+//
+// Design for GB300.  The fp64 pipe of this part retires about 1.6 lane
+// operations per SM per clock, so at the 88-112 bytes per cell and iteration
+// that the fused sweeps move, the iteration is bound by fp64 arithmetic, not
+// by HBM.  The kernels therefore spend integer and load/store instructions
+// freely and keep the fp64 instruction count at the minimum of the
+// formulation: 6 per cell in the preconditioner sweep, 11 (constant a_h) or
+// 12 (a_h per column) in the stencil sweep.  Both sweeps are persistent grids
+// (a few blocks per SM), so the per-thread partial sums are folded into the
+// grid reduction only once per launch.
+//
+// Vectors use the column-contiguous layout: cell (i,j,k) at ((j*nx)+i)*nz+k.
+#include <cmath>
+#include <cstdint>
+
+#include "pcg_internal.h"
+
+namespace pcg {
+namespace {
+
+constexpr int kStOK = 0, kStNotConv = 4, kStBreakdown = 5;
+
+__device__ __forceinline__ double2 ld2(const double* p) {
+  return *reinterpret_cast<const double2*>(p);
+}
+__device__ __forceinline__ double2 ldg2(const double* p) {
+  return __ldg(reinterpret_cast<const double2*>(p));
+}
+__device__ __forceinline__ void st2(double* p, double2 v) {
+  *reinterpret_cast<double2*>(p) = v;
+}
+__device__ __forceinline__ int ld_done(const DevState* st) {
+  return *reinterpret_cast<const volatile int*>(&st->done);
+}
+
+// Horizontal neighbours of a column, periodic in i and j.
+struct Nbr {
+  long long e, w, n, s;
+};
+__device__ __forceinline__ Nbr neighbours(const Op& op, long long col) {
+  const long long j = col / op.nx;
+  const int i = (int)(col - j * op.nx);
+  Nbr nb;
+  nb.e = (i == op.nx - 1) ? col - (op.nx - 1) : col + 1;
+  nb.w = (i == 0) ? col + (op.nx - 1) : col - 1;
+  nb.n = (j == op.ny - 1) ? col - (long long)(op.ny - 1) * op.nx : col + op.nx;
+  nb.s = (j == 0) ? col + (long long)(op.ny - 1) * op.nx : col - op.nx;
+  return nb;
+}
+
+// acc + (A z) at the two cells l, l+1 of one column (k even, k+1 < nz),
+// eq. (18).  zc = (z[l], z[l+1]).  The vertical neighbours outside the column
+// enter with a zero coefficient (Neumann lid and floor).
+template <bool VARY>
+__device__ __forceinline__ double2 stencil2(const Op& op, const double* __restrict__ z,
+                                            long long l, long long col, int k, double2 acc,
+                                            double2 zc) {
+  const int nz = op.nz;
+  const double* __restrict__ lev = op.lev;
+  const Nbr nb = neighbours(op, col);
+  const double zd = (k > 0) ? z[l - 1] : 0.0;
+  const double zu = (k + 2 < nz) ? z[l + 2] : 0.0;
+  const double2 zE = ld2(z + nb.e * nz + k);
+  const double2 zW = ld2(z + nb.w * nz + k);
+  const double2 zN = ld2(z + nb.n * nz + k);
+  const double2 zS = ld2(z + nb.s * nz + k);
+  double h0, h1, d0, d1;
+  if (VARY) {
+    const double aE = __ldg(op.faceE + col), aW = __ldg(op.faceE + nb.w);
+    const double aN = __ldg(op.faceN + col), aS = __ldg(op.faceN + nb.s);
+    h0 = aE * zE.x;
+    h0 = fma(aW, zW.x, h0);
+    h0 = fma(aN, zN.x, h0);
+    h0 = fma(aS, zS.x, h0);
+    h1 = aE * zE.y;
+    h1 = fma(aW, zW.y, h1);
+    h1 = fma(aN, zN.y, h1);
+    h1 = fma(aS, zS.y, h1);
+    const double2 dg = ldg2(op.cdiag + l);
+    d0 = dg.x;
+    d1 = dg.y;
+  } else {
+    h0 = (zE.x + zW.x) + (zN.x + zS.x);
+    h1 = (zE.y + zW.y) + (zN.y + zS.y);
+    d0 = __ldg(lev + LV_DIAG * nz + k);
+    d1 = __ldg(lev + LV_DIAG * nz + k + 1);
+  }
+  double a0 = fma(d0, zc.x, acc.x);
+  a0 = fma(__ldg(lev + LV_UP * nz + k), zc.y, a0);
+  a0 = fma(__ldg(lev + LV_DN * nz + k), zd, a0);
+  a0 = fma(__ldg(lev + LV_HW * nz + k), h0, a0);
+  double a1 = fma(d1, zc.y, acc.y);
+  a1 = fma(__ldg(lev + LV_UP * nz + k + 1), zu, a1);
+  a1 = fma(__ldg(lev + LV_DN * nz + k + 1), zc.x, a1);
+  a1 = fma(__ldg(lev + LV_HW * nz + k + 1), h1, a1);
+  return make_double2(a0, a1);
+}
+
+// acc + (A z) at one cell l (any nz, any alignment).
+template <bool VARY>
+__device__ __forceinline__ double stencil1(const Op& op, const double* __restrict__ z,
+                                           long long l, long long col, int k, double acc,
+                                           double zc) {
+  const int nz = op.nz;
+  const double* __restrict__ lev = op.lev;
+  const Nbr nb = neighbours(op, col);
+  const double zd = (k > 0) ? z[l - 1] : 0.0;
+  const double zu = (k + 1 < nz) ? z[l + 1] : 0.0;
+  const double zE = z[nb.e * nz + k], zW = z[nb.w * nz + k];
+  const double zN = z[nb.n * nz + k], zS = z[nb.s * nz + k];
+  double hs, d;
+  if (VARY) {
+    hs = __ldg(op.faceE + col) * zE;
+    hs = fma(__ldg(op.faceE + nb.w), zW, hs);
+    hs = fma(__ldg(op.faceN + col), zN, hs);
+    hs = fma(__ldg(op.faceN + nb.s), zS, hs);
+    d = __ldg(op.cdiag + l);
+  } else {
+    hs = (zE + zW) + (zN + zS);
+    d = __ldg(lev + LV_DIAG * nz + k);
+  }
+  double a = fma(d, zc, acc);
+  a = fma(__ldg(lev + LV_UP * nz + k), zu, a);
+  a = fma(__ldg(lev + LV_DN * nz + k), zd, a);
+  return fma(__ldg(lev + LV_HW * nz + k), hs, a);
+}
+
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Deterministic grid reduction of two values: warp shuffle tree -> block
+// (fixed order) -> per-block partials -> the last block to take a ticket sums
+// the partials in block order.  No block ever waits on another.  Returns true
+// in thread 0 of the last block, with the totals in tot0/tot1.
+template <int NT>
+__device__ bool grid_sum2(double v0, double v1, double* __restrict__ partials,
+                          unsigned int* ticket, double& tot0, double& tot1) {
+  constexpr int NW = NT / 32;
+  __shared__ double sh0[NW], sh1[NW];
+  __shared__ bool am_last;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  v0 = warp_sum(v0);
+  v1 = warp_sum(v1);
+  if (NW > 1) {
+    if (lane == 0) {
+      sh0[w] = v0;
+      sh1[w] = v1;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    double a = v0, b = v1;
+    for (int i = 1; i < NW; ++i) {
+      a += sh0[i];
+      b += sh1[i];
+    }
+    partials[2 * blockIdx.x] = a;
+    partials[2 * blockIdx.x + 1] = b;
+    __threadfence();
+    const unsigned int t = atomicAdd(ticket, 1u);
+    am_last = (t == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!am_last) return false;
+  __threadfence();
+  double a = 0.0, b = 0.0;
+  for (int i = threadIdx.x; i < (int)gridDim.x; i += NT) {
+    a += __ldcg(partials + 2 * i);
+    b += __ldcg(partials + 2 * i + 1);
+  }
+  a = warp_sum(a);
+  b = warp_sum(b);
+  if (NW > 1) {
+    if (lane == 0) {
+      sh0[w] = a;
+      sh1[w] = b;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 1; i < NW; ++i) {
+      a += sh0[i];
+      b += sh1[i];
+    }
+    tot0 = a;
+    tot1 = b;
+    *ticket = 0u;
+  }
+  return threadIdx.x == 0;
+}
+
+// ------------------------------------------------------------------ setup
+
+__global__ void k_face_coeffs(Op op, double* __restrict__ faceE, double* __restrict__ faceN) {
+  for (long long c = blockIdx.x * (long long)blockDim.x + threadIdx.x; c < op.ncols;
+       c += (long long)gridDim.x * blockDim.x) {
+    const Nbr nb = neighbours(op, c);
+    faceE[c] = 0.5 * (op.ah[c] + op.ah[nb.e]);
+    faceN[c] = 0.5 * (op.ah[c] + op.ah[nb.n]);
+  }
+}
+
+// Diagonal per cell for a_h given per column: h_k*mass + T_{k+1/2} + T_{k-1/2}
+// + h_k * (sum of the four face values), eqs. (8) and (18).
+__global__ void k_cell_diag(Op op, double* __restrict__ cdiag) {
+  const int nz = op.nz;
+  for (long long l = blockIdx.x * (long long)blockDim.x + threadIdx.x; l < op.n;
+       l += (long long)gridDim.x * blockDim.x) {
+    const long long col = l / nz;
+    const int k = (int)(l - col * nz);
+    const Nbr nb = neighbours(op, col);
+    const double s = op.faceE[col] + op.faceE[nb.w] + op.faceN[col] + op.faceN[nb.s];
+    cdiag[l] = op.lev[LV_DIAG * nz + k] + op.lev[LV_H * nz + k] * s;
+  }
+}
+
+// Thomas factors per column (eq. (19)), in the LDL^T form used by the sweep:
+// D_k = diag_k - T_{k-1/2} * (T_{k-1/2} / D_{k-1}); stored are T_{k+1/2}/D_k
+// and 1/D_k, tile-interleaved so that a warp reads 32 columns' level k as one
+// contiguous 256-byte line.
+__global__ void k_thomas_factors(Op op, DevState* st, double* __restrict__ tnphi,
+                                 double* __restrict__ tinvd) {
+  const int nz = op.nz;
+  for (long long c = blockIdx.x * (long long)blockDim.x + threadIdx.x; c < op.ncols;
+       c += (long long)gridDim.x * blockDim.x) {
+    const long long t = c / kTile;
+    const int lane = (int)(c - t * kTile);
+    double nphi_prev = 0.0;
+    int bad = 0;
+    for (int k = 0; k < nz; ++k) {
+      const double D = op.cdiag[c * nz + k] - op.lev[LV_TDN * nz + k] * nphi_prev;
+      if (!(D > 0.0)) bad = 1;
+      const double invd = 1.0 / D;
+      const double nphi = op.lev[LV_TUP * nz + k] / D;
+      const long long o = (t * nz + k) * kTile + lane;
+      tnphi[o] = nphi;
+      tinvd[o] = invd;
+      nphi_prev = nphi;
+    }
+    if (bad) st->setup_error = 1;
+  }
+}
+
+// ------------------------------------------------- preconditioner sweep (K_M)
+
+// Shared-memory index of level k of a staged column: XOR swizzle of the low
+// four bits with the column's position in the tile, so that 16 threads that
+// read the same level of 16 different columns hit 16 distinct 8-byte bank
+// pairs (column stride pz is a multiple of 16 doubles).
+struct SwzIdx {
+  int sw;
+  __device__ __forceinline__ int operator()(int k) const { return k ^ sw; }
+};
+struct LinIdx {
+  __device__ __forceinline__ int operator()(int k) const { return k; }
+};
+
+// Copy cnt = nc*nz consecutive doubles (nc whole columns) from global memory
+// into the swizzled tile, cooperatively by the 32 lanes of the warp.
+template <bool VEC2>
+__device__ __forceinline__ void tile_load(const double* __restrict__ g, double* s, int cnt,
+                                          int nz, int pz, int lane) {
+  if (VEC2) {  // nz even: a pair never straddles two columns
+    int e = 2 * lane, c = e / nz, k = e - c * nz;
+    for (; e < cnt; e += 64) {
+      const double2 v = ld2(g + e);
+      const int sw = c & 15;
+      s[c * pz + (k ^ sw)] = v.x;
+      s[c * pz + ((k + 1) ^ sw)] = v.y;
+      k += 64;
+      while (k >= nz) {
+        k -= nz;
+        ++c;
+      }
+    }
+  } else {
+    int e = lane, c = e / nz, k = e - c * nz;
+    for (; e < cnt; e += 32) {
+      s[c * pz + (k ^ (c & 15))] = g[e];
+      k += 32;
+      while (k >= nz) {
+        k -= nz;
+        ++c;
+      }
+    }
+  }
+}
+
+template <bool VEC2>
+__device__ __forceinline__ void tile_store(const double* s, double* __restrict__ g, int cnt,
+                                           int nz, int pz, int lane) {
+  if (VEC2) {
+    int e = 2 * lane, c = e / nz, k = e - c * nz;
+    for (; e < cnt; e += 64) {
+      const int sw = c & 15;
+      st2(g + e, make_double2(s[c * pz + (k ^ sw)], s[c * pz + ((k + 1) ^ sw)]));
+      k += 64;
+      while (k >= nz) {
+        k -= nz;
+        ++c;
+      }
+    }
+  } else {
+    int e = lane, c = e / nz, k = e - c * nz;
+    for (; e < cnt; e += 32) {
+      g[e] = s[c * pz + (k ^ (c & 15))];
+      k += 32;
+      while (k >= nz) {
+        k -= nz;
+        ++c;
+      }
+    }
+  }
+}
+
+// One column of Algorithm 3 (FUSED) or of the plain solve M z = r.
+//   rp: r on entry; with FUSED r* = r - alpha q on exit.
+//   qp: q (FUSED only).  wp: receives z (may alias qp: q_k is read before
+//   w_k overwrites it).
+// Forward: y_k = r*_k + (T_{k-1/2}/D_{k-1}) y_{k-1},  w_k = y_k / D_k;
+// backward: z_k = w_k + (T_{k+1/2}/D_k) z_{k+1}.  fp64 operations per level:
+// 4 forward (r*, ||r||^2, y, w), 2 backward (z, <r,z>).
+template <bool VARY, bool FUSED, typename IDX>
+__device__ __forceinline__ void column_solve(const Op& op, long long tile, int lane, IDX idx,
+                                             double* rp, const double* qp, double* wp,
+                                             double nalpha, double& accR, double& accK) {
+  const int nz = op.nz;
+  const double* __restrict__ lev = op.lev;
+  const double* fn = VARY ? op.tnphi + tile * nz * kTile + lane : lev + LV_NPHI * nz;
+  const double* fi = VARY ? op.tinvd + tile * nz * kTile + lane : lev + LV_INVD * nz;
+  const int fs = VARY ? kTile : 1;
+  int o = idx(0);
+  double rk = rp[o];
+  if (FUSED) {
+    rk = fma(nalpha, qp[o], rk);
+    accR = fma(rk, rk, accR);
+    rp[o] = rk;
+  }
+  double y = rk;
+  wp[o] = y * __ldg(fi);
+  for (int k = 1; k < nz; ++k) {
+    o = idx(k);
+    rk = rp[o];
+    if (FUSED) {
+      rk = fma(nalpha, qp[o], rk);
+      accR = fma(rk, rk, accR);
+      rp[o] = rk;
+    }
+    y = fma(__ldg(fn + (k - 1) * fs), y, rk);
+    wp[o] = y * __ldg(fi + k * fs);
+  }
+  o = idx(nz - 1);
+  double zz = wp[o];
+  if (FUSED) accK = fma(zz, rp[o], accK);
+  for (int k = nz - 2; k >= 0; --k) {
+    o = idx(k);
+    zz = fma(__ldg(fn + k * fs), zz, wp[o]);
+    wp[o] = zz;
+    if (FUSED) accK = fma(zz, rp[o], accK);
+  }
+}
+
+// Last-block bookkeeping of Algorithm 1 after the preconditioner sweep of
+// iteration it: ||r||, stopping test, beta = kappa/kappa_old.
+__device__ void finish_precond_sweep(DevState* st, double R, double K, double* hist) {
+  const int it = st->it;
+  if (it == 0) st->R0 = R;
+  const double R0 = st->R0;
+  st->last_R = R;
+  st->last_kappa = K;
+  const double ratio = (R0 > 0.0) ? sqrt(R / R0) : 0.0;
+  hist[it] = ratio;
+  int done = 0, status = kStOK;
+  if (R0 == 0.0) {
+    done = 1;  // r_0 = 0: the initial guess solves the system
+  } else if (!(R < INFINITY) || !(R0 < INFINITY)) {
+    done = 1;
+    status = kStBreakdown;  // NaN or Inf in the residual
+  } else if (ratio < st->rtol || R == 0.0) {
+    done = 1;
+  } else if (it >= st->maxit) {
+    done = 1;
+    status = (st->rtol > 0.0) ? kStNotConv : kStOK;
+  } else if (!(K > 0.0)) {
+    done = 1;
+    status = kStBreakdown;
+  } else {
+    st->beta = K / st->kappa_old;
+    st->kappa_old = K;
+  }
+  if (done) {
+    st->iters = it;
+    st->status = status;
+    __threadfence();
+    st->done = 1;
+  }
+  st->it = it + 1;
+}
+
+template <bool VARY, bool FUSED, bool VEC2>
+__global__ void __launch_bounds__(kTile) k_precond_staged(Op op, DevState* st,
+                                                          double* __restrict__ r,
+                                                          const double* __restrict__ q,
+                                                          double* __restrict__ z,
+                                                          double* __restrict__ partials,
+                                                          double* __restrict__ hist) {
+  extern __shared__ double smem[];
+  if (FUSED && ld_done(st)) return;
+  const int lane = threadIdx.x;
+  const int nz = op.nz, pz = op.pz;
+  double* sr = smem;
+  double* sq = smem + kTile * pz;
+  const double nalpha = FUSED ? -st->alpha : 0.0;
+  double accR = 0.0, accK = 0.0;
+  const SwzIdx idx{lane & 15};
+  for (long long t = blockIdx.x; t < op.ntiles; t += gridDim.x) {
+    const long long col0 = t * kTile;
+    const int nc = (int)min((long long)kTile, op.ncols - col0);
+    const long long base = col0 * nz;
+    const int cnt = nc * nz;
+    tile_load<VEC2>(r + base, sr, cnt, nz, pz, lane);
+    if (FUSED) tile_load<VEC2>(q + base, sq, cnt, nz, pz, lane);
+    __syncwarp();
+    if (lane < nc)
+      column_solve<VARY, FUSED>(op, t, lane, idx, sr + lane * pz, sq + lane * pz,
+                                sq + lane * pz, nalpha, accR, accK);
+    __syncwarp();
+    if (FUSED) tile_store<VEC2>(sr, r + base, cnt, nz, pz, lane);
+    tile_store<VEC2>(sq, z + base, cnt, nz, pz, lane);
+    __syncwarp();
+  }
+  if (FUSED) {
+    double R, K;
+    if (grid_sum2<kTile>(accR, accK, partials, &st->ticket_m, R, K))
+      finish_precond_sweep(st, R, K, hist);
+  }
+}
+
+// Unstaged variant for columns too tall for the shared-memory tile: each
+// thread walks its column in global memory (correct for any nz; the
+// reduction and bookkeeping are those of the staged kernel).
+template <bool VARY, bool FUSED>
+__global__ void __launch_bounds__(kTile) k_precond_direct(Op op, DevState* st,
+                                                          double* __restrict__ r,
+                                                          const double* __restrict__ q,
+                                                          double* __restrict__ z,
+                                                          double* __restrict__ partials,
+                                                          double* __restrict__ hist) {
+  if (FUSED && ld_done(st)) return;
+  const int lane = threadIdx.x;
+  const int nz = op.nz;
+  const double nalpha = FUSED ? -st->alpha : 0.0;
+  double accR = 0.0, accK = 0.0;
+  for (long long t = blockIdx.x; t < op.ntiles; t += gridDim.x) {
+    const long long col = t * kTile + lane;
+    if (col < op.ncols)
+      column_solve<VARY, FUSED>(op, t, lane, LinIdx{}, r + col * nz, FUSED ? q + col * nz : nullptr,
+                                z + col * nz, nalpha, accR, accK);
+  }
+  if (FUSED) {
+    double R, K;
+    if (grid_sum2<kTile>(accR, accK, partials, &st->ticket_m, R, K))
+      finish_precond_sweep(st, R, K, hist);
+  }
+}
+
+// ----------------------------------------------------- stencil sweeps (K_A)
+
+// Algorithm 2: u += alpha p; p = z + beta p; q = A z + beta q; sigma = <p,q>;
+// then alpha = kappa_old / sigma in the last block.
+template <bool VARY, bool VEC2>
+__global__ void __launch_bounds__(kSpmvThreads) k_spmv_fused(Op op, DevState* st,
+                                                             const double* __restrict__ z,
+                                                             double* __restrict__ u,
+                                                             double* __restrict__ p,
+                                                             double* __restrict__ q,
+                                                             double* __restrict__ partials) {
+  if (ld_done(st)) return;
+  const double alpha = st->alpha, beta = st->beta;
+  const int nz = op.nz;
+  double sig = 0.0;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  if (VEC2) {
+    const long long np = op.n >> 1;
+    for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x; g < np; g += stride) {
+      const long long l = g << 1;
+      const long long col = l / nz;
+      const int k = (int)(l - col * nz);
+      const double2 zc = ld2(z + l);
+      double2 pc = ld2(p + l);
+      const double2 qc = ld2(q + l);
+      double2 uc = ld2(u + l);
+      uc.x = fma(alpha, pc.x, uc.x);
+      uc.y = fma(alpha, pc.y, uc.y);
+      pc.x = fma(beta, pc.x, zc.x);
+      pc.y = fma(beta, pc.y, zc.y);
+      const double2 qn =
+          stencil2<VARY>(op, z, l, col, k, make_double2(beta * qc.x, beta * qc.y), zc);
+      sig = fma(pc.x, qn.x, sig);
+      sig = fma(pc.y, qn.y, sig);
+      st2(u + l, uc);
+      st2(p + l, pc);
+      st2(q + l, qn);
+    }
+  } else {
+    for (long long l = blockIdx.x * (long long)blockDim.x + threadIdx.x; l < op.n; l += stride) {
+      const long long col = l / nz;
+      const int k = (int)(l - col * nz);
+      const double zc = z[l];
+      const double pc = fma(beta, p[l], zc);
+      u[l] = fma(alpha, p[l], u[l]);
+      const double qn = stencil1<VARY>(op, z, l, col, k, beta * q[l], zc);
+      sig = fma(pc, qn, sig);
+      p[l] = pc;
+      q[l] = qn;
+    }
+  }
+  double S, unused;
+  if (grid_sum2<kSpmvThreads>(sig, 0.0, partials, &st->ticket_a, S, unused)) {
+    st->last_sigma = S;
+    if (!(S > 0.0) || !(S < INFINITY)) {
+      st->alpha = 0.0;  // x keeps the iterate before this direction
+      st->iters = st->it - 1;
+      st->status = kStBreakdown;
+      __threadfence();
+      st->done = 1;
+    } else {
+      st->alpha = st->kappa_old / S;
+    }
+  }
+}
+
+// MODE 0: y = A x.  MODE 1: r = b - A x, p = q = 0, and the scalar state of
+// a new solve (alpha = 0, kappa_old = 1: the first sweeps then give p = z_0,
+// q = A z_0).
+template <bool VARY, bool VEC2, int MODE>
+__global__ void __launch_bounds__(kSpmvThreads) k_stencil(Op op, DevState* st,
+                                                          const double* __restrict__ x,
+                                                          const double* __restrict__ b,
+                                                          double* __restrict__ y,
+                                                          double* __restrict__ p,
+                                                          double* __restrict__ q, double rtol,
+                                                          int maxit) {
+  if (MODE == 1 && blockIdx.x == 0 && threadIdx.x == 0) {
+    st->alpha = 0.0;
+    st->beta = 0.0;
+    st->kappa_old = 1.0;
+    st->R0 = 0.0;
+    st->rtol = rtol;
+    st->last_sigma = st->last_kappa = st->last_R = 0.0;
+    st->it = 0;
+    st->status = kStOK;
+    st->iters = 0;
+    st->maxit = maxit;
+    st->ticket_m = 0u;
+    st->ticket_a = 0u;
+    st->done = 0;
+  }
+  const int nz = op.nz;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  if (VEC2) {
+    const long long np = op.n >> 1;
+    for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x; g < np; g += stride) {
+      const long long l = g << 1;
+      const long long col = l / nz;
+      const int k = (int)(l - col * nz);
+      const double2 ax = stencil2<VARY>(op, x, l, col, k, make_double2(0.0, 0.0), ld2(x + l));
+      if (MODE == 0) {
+        st2(y + l, ax);
+      } else {
+        const double2 bv = ld2(b + l);
+        st2(y + l, make_double2(bv.x - ax.x, bv.y - ax.y));
+        st2(p + l, make_double2(0.0, 0.0));
+        st2(q + l, make_double2(0.0, 0.0));
+      }
+    }
+  } else {
+    for (long long l = blockIdx.x * (long long)blockDim.x + threadIdx.x; l < op.n; l += stride) {
+      const long long col = l / nz;
+      const int k = (int)(l - col * nz);
+      const double ax = stencil1<VARY>(op, x, l, col, k, 0.0, x[l]);
+      if (MODE == 0) {
+        y[l] = ax;
+      } else {
+        y[l] = b[l] - ax;
+        p[l] = 0.0;
+        q[l] = 0.0;
+      }
+    }
+  }
+}
+
+template <bool VEC2>
+__global__ void __launch_bounds__(kSpmvThreads) k_finalize(Op op, const DevState* st,
+                                                           double* __restrict__ x,
+                                                           const double* __restrict__ p) {
+  const double alpha = st->alpha;
+  if (alpha == 0.0) return;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  if (VEC2) {
+    const long long np = op.n >> 1;
+    for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x; g < np; g += stride) {
+      double2 xv = ld2(x + 2 * g);
+      const double2 pv = ld2(p + 2 * g);
+      xv.x = fma(alpha, pv.x, xv.x);
+      xv.y = fma(alpha, pv.y, xv.y);
+      st2(x + 2 * g, xv);
+    }
+  } else {
+    for (long long l = blockIdx.x * (long long)blockDim.x + threadIdx.x; l < op.n; l += stride)
+      x[l] = fma(alpha, p[l], x[l]);
+  }
+}
+
+// ------------------------------------------------------------- dispatch
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline bool staged(const Op& op) { return op.nz <= kMaxStagedNz; }
+inline size_t staged_smem(const Op& op) { return 2u * kTile * (size_t)op.pz * sizeof(double); }
+
+template <bool VARY, bool FUSED, bool VEC2>
+cudaError_t run_precond(const Op& op, DevState* st, double* r, const double* q, double* z,
+                        double* partials, double* hist, int grid, cudaStream_t s) {
+  if (staged(op))
+    k_precond_staged<VARY, FUSED, VEC2>
+        <<<grid, kTile, staged_smem(op), s>>>(op, st, r, q, z, partials, hist);
+  else
+    k_precond_direct<VARY, FUSED><<<grid, kTile, 0, s>>>(op, st, r, q, z, partials, hist);
+  return cudaGetLastError();
+}
+
+template <bool VARY, bool FUSED>
+cudaError_t run_precond_v(const Op& op, DevState* st, double* r, const double* q, double* z,
+                          double* partials, double* hist, int grid, cudaStream_t s, bool v2) {
+  return v2 ? run_precond<VARY, FUSED, true>(op, st, r, q, z, partials, hist, grid, s)
+            : run_precond<VARY, FUSED, false>(op, st, r, q, z, partials, hist, grid, s);
+}
+
+template <bool FUSED>
+cudaError_t run_precond_any(const Op& op, DevState* st, double* r, const double* q, double* z,
+                            double* partials, double* hist, int grid, cudaStream_t s) {
+  const bool v2 = (op.nz % 2 == 0) && aligned16(r) && aligned16(z) && (!q || aligned16(q));
+  return op.varying ? run_precond_v<true, FUSED>(op, st, r, q, z, partials, hist, grid, s, v2)
+                    : run_precond_v<false, FUSED>(op, st, r, q, z, partials, hist, grid, s, v2);
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, size_t bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+}  // namespace
+
+// ------------------------------------------------------------- launchers
+
+cudaError_t prepare_kernels(const Op& op) {
+  if (!staged(op)) return cudaSuccess;
+  const size_t b = staged_smem(op);
+  cudaError_t e = cudaSuccess;
+  cudaError_t r;
+#define PCG_SET(V, F, W)                                          \
+  r = set_smem(k_precond_staged<V, F, W>, b);                     \
+  if (r != cudaSuccess) e = r;
+  PCG_SET(false, false, false) PCG_SET(false, false, true) PCG_SET(false, true, false)
+  PCG_SET(false, true, true) PCG_SET(true, false, false) PCG_SET(true, false, true)
+  PCG_SET(true, true, false) PCG_SET(true, true, true)
+#undef PCG_SET
+  return e;
+}
+
+int grid_precond(const Op& op, int num_sms) {
+  int per_sm = 0;
+  cudaError_t e;
+  if (staged(op))
+    e = op.varying ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                         &per_sm, k_precond_staged<true, true, true>, kTile, staged_smem(op))
+                   : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                         &per_sm, k_precond_staged<false, true, true>, kTile, staged_smem(op));
+  else
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_precond_direct<false, true>,
+                                                      kTile, 0);
+  if (e != cudaSuccess || per_sm < 1) per_sm = 1;
+  long long g = (long long)per_sm * num_sms;
+  if (g > op.ntiles) g = op.ntiles;
+  return (int)(g < 1 ? 1 : g);
+}
+
+int grid_spmv(const Op& op, int num_sms) {
+  int per_sm = 0;
+  cudaError_t e = op.varying ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                                   &per_sm, k_spmv_fused<true, true>, kSpmvThreads, 0)
+                             : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                                   &per_sm, k_spmv_fused<false, true>, kSpmvThreads, 0);
+  if (e != cudaSuccess || per_sm < 1) per_sm = 1;
+  long long g = (long long)per_sm * num_sms;
+  const long long work = (op.n + 2 * kSpmvThreads - 1) / (2 * kSpmvThreads);
+  if (g > work) g = work;
+  return (int)(g < 1 ? 1 : g);
+}
+
+cudaError_t launch_face_coeffs(const Op& op, double* faceE, double* faceN, cudaStream_t s) {
+  long long g = (op.ncols + 255) / 256;
+  if (g > 65536) g = 65536;
+  k_face_coeffs<<<(int)g, 256, 0, s>>>(op, faceE, faceN);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cell_diag(const Op& op, double* cdiag, cudaStream_t s) {
+  long long g = (op.n + 255) / 256;
+  if (g > 65536) g = 65536;
+  k_cell_diag<<<(int)g, 256, 0, s>>>(op, cdiag);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_thomas_factors(const Op& op, DevState* st, double* tnphi, double* tinvd,
+                                  cudaStream_t s) {
+  long long g = (op.ncols + 127) / 128;
+  if (g > 65536) g = 65536;
+  k_thomas_factors<<<(int)g, 128, 0, s>>>(op, st, tnphi, tinvd);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_residual(const Op& op, DevState* st, const double* b, const double* x,
+                            double* r, double* p, double* q, double rtol, int maxit, int grid,
+                            cudaStream_t s) {
+  const bool v2 = (op.nz % 2 == 0) && aligned16(b) && aligned16(x) && aligned16(r) &&
+                  aligned16(p) && aligned16(q);
+  if (op.varying) {
+    if (v2) k_stencil<true, true, 1><<<grid, kSpmvThreads, 0, s>>>(op, st, x, b, r, p, q, rtol, maxit);
+    else k_stencil<true, false, 1><<<grid, kSpmvThreads, 0, s>>>(op, st, x, b, r, p, q, rtol, maxit);
+  } else {
+    if (v2) k_stencil<false, true, 1><<<grid, kSpmvThreads, 0, s>>>(op, st, x, b, r, p, q, rtol, maxit);
+    else k_stencil<false, false, 1><<<grid, kSpmvThreads, 0, s>>>(op, st, x, b, r, p, q, rtol, maxit);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_apply(const Op& op, const double* x, double* y, int grid, cudaStream_t s) {
+  const bool v2 = (op.nz % 2 == 0) && aligned16(x) && aligned16(y);
+  if (op.varying) {
+    if (v2) k_stencil<true, true, 0><<<grid, kSpmvThreads, 0, s>>>(op, nullptr, x, nullptr, y, nullptr, nullptr, 0.0, 0);
+    else k_stencil<true, false, 0><<<grid, kSpmvThreads, 0, s>>>(op, nullptr, x, nullptr, y, nullptr, nullptr, 0.0, 0);
+  } else {
+    if (v2) k_stencil<false, true, 0><<<grid, kSpmvThreads, 0, s>>>(op, nullptr, x, nullptr, y, nullptr, nullptr, 0.0, 0);
+    else k_stencil<false, false, 0><<<grid, kSpmvThreads, 0, s>>>(op, nullptr, x, nullptr, y, nullptr, nullptr, 0.0, 0);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_precond(const Op& op, const double* r, double* z, int grid, cudaStream_t s) {
+  return run_precond_any<false>(op, nullptr, const_cast<double*>(r), nullptr, z, nullptr,
+                                nullptr, grid, s);
+}
+
+cudaError_t launch_precond_fused(const Op& op, DevState* st, double* r, const double* q,
+                                 double* z, double* partials, double* hist, int grid,
+                                 cudaStream_t s) {
+  return run_precond_any<true>(op, st, r, q, z, partials, hist, grid, s);
+}
+
+cudaError_t launch_spmv_fused(const Op& op, DevState* st, const double* z, double* u,
+                              double* p, double* q, double* partials, int grid,
+                              cudaStream_t s) {
+  const bool v2 = (op.nz % 2 == 0) && aligned16(z) && aligned16(u) && aligned16(p) &&
+                  aligned16(q);
+  if (op.varying) {
+    if (v2) k_spmv_fused<true, true><<<grid, kSpmvThreads, 0, s>>>(op, st, z, u, p, q, partials);
+    else k_spmv_fused<true, false><<<grid, kSpmvThreads, 0, s>>>(op, st, z, u, p, q, partials);
+  } else {
+    if (v2) k_spmv_fused<false, true><<<grid, kSpmvThreads, 0, s>>>(op, st, z, u, p, q, partials);
+    else k_spmv_fused<false, false><<<grid, kSpmvThreads, 0, s>>>(op, st, z, u, p, q, partials);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const Op& op, const DevState* st, double* x, const double* p,
+                            int grid, cudaStream_t s) {
+  if (aligned16(x) && aligned16(p) && (op.n % 2 == 0))
+    k_finalize<true><<<grid, kSpmvThreads, 0, s>>>(op, st, x, p);
+  else
+    k_finalize<false><<<grid, kSpmvThreads, 0, s>>>(op, st, x, p);
+  return cudaGetLastError();
+}
+
+}  // namespace pcg

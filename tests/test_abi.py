@@ -1,0 +1,88 @@
+"""The C ABI library: it loads, exports every entry point include/pcg.h
+declares, and rejects bad arguments on the host before touching a GPU."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pcg.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from matrix_free_pcg_gb300 import build
+    build.build()
+    import matrix_free_pcg_gb300 as mf
+    return mf
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(pcg_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ["pcg_create", "pcg_destroy", "pcg_apply_A", "pcg_precond", "pcg_solve",
+                     "pcg_solve_host", "pcg_last_error"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    so = ctypes.CDLL(lib.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(so, n)]
+    assert not missing, missing
+    assert sorted(lib.EXPORTED) == declared_functions()
+
+
+def test_symbols_have_c_linkage(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", lib.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if " T " in line)
+    for n in declared_functions():
+        assert n in exported
+
+
+@pytest.mark.parametrize("dims", [(0, 4, 4), (4, -1, 4), (4, 4, 0)])
+def test_create_rejects_bad_sizes(lib, dims):
+    with pytest.raises(lib.PCGError) as e:
+        lib.pcg_create(*dims)
+    assert e.value.status == lib.PCG_EINVAL
+    assert "must be >= 1" in lib.pcg_last_error()
+
+
+@pytest.mark.parametrize("kw,msg", [({"mass": 0.0}, "mass"), ({"mass": float("nan")}, "mass"),
+                                    ({"a_v": -1.0}, "a_v"), ({"a_h": -0.5}, "a_h"),
+                                    ({"dz": [1.0, 0.0, 1.0]}, "dz[1]"),
+                                    ({"a_h_field": [1.0] * 3 + [float("inf")]}, "a_h_field[3]")])
+def test_create_rejects_bad_coefficients(lib, kw, msg):
+    args = dict(a_h=1.0, a_v=10.0, mass=1.0)
+    args.update(kw)
+    with pytest.raises(lib.PCGError) as e:
+        lib.pcg_create(2, 2, 3, **args)
+    assert e.value.status == lib.PCG_EINVAL
+    assert msg in lib.pcg_last_error()
+
+
+def test_null_context_calls_fail_cleanly(lib):
+    assert lib._lib.pcg_apply_A(None, None, None) == lib.PCG_EINVAL
+    assert lib._lib.pcg_precond(None, None, None) == lib.PCG_EINVAL
+    assert lib._lib.pcg_solve(None, None, None, 1e-10, 10, None, None) == lib.PCG_EINVAL
+    assert lib._lib.pcg_set_stream(None, None) == lib.PCG_EINVAL
+    lib._lib.pcg_destroy(None)  # NULL-safe
+    assert isinstance(lib.pcg_last_error(None), str)
+
+
+def test_create_without_gpu_reports_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(lib.PCGError) as e:
+        lib.pcg_create(4, 4, 4, a_h=1.0, a_v=10.0)
+    assert e.value.status == lib.PCG_ECUDA
+    assert "no usable CUDA device" in lib.pcg_last_error()

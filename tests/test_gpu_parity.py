@@ -1,0 +1,229 @@
+"""GPU path vs the CPU oracle, through the C ABI, on seeded inputs.
+
+Tolerances: apply_A and precond within 1e-12 relative max-norm; the PCG
+solution within 1e-8 relative 2-norm at equal iteration count; iteration
+counts to the 1e-10 residual within +-1.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import matrix_free_pcg_gb300 as mf  # noqa: E402
+
+DEV = torch.device("cuda:0")
+OP_TOL = 1e-12
+SOL_TOL = 1e-8
+
+
+def rel_maxdiff(a, b):
+    return np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300)
+
+
+def case(nx, ny, nz, varying, graded, a_v=1e3, seed=0):
+    h = W.layer_thickness(nz, graded)
+    ah = W.horizontal_coefficient(nx, ny, varying)
+    prob = oracle.Problem(nx, ny, nz, ah=ah, a_v=a_v, mass=1.0, h=h)
+    kw = dict(a_h_field=ah if varying else None, a_h=1.0, a_v=a_v, mass=1.0, dz=h)
+    return prob, kw, np.random.default_rng(seed).uniform(-1, 1, nx * ny * nz)
+
+
+SHAPES = [
+    (37, 29, 16, True, True),     # 1073 columns: 33 full tiles + a ragged one
+    (37, 29, 16, False, False),
+    (33, 5, 7, True, True),       # odd nz: scalar path
+    (64, 48, 64, False, True),
+    (17, 19, 130, True, True),    # nz not a multiple of 16
+    (5, 3, 1, False, False),      # single level
+    (1, 1, 3, True, True),        # one column, self-neighbour in i and j
+    (3, 1, 2, False, True),
+    (2, 2, 4, True, False),
+    (7, 5, 500, True, True),      # too tall for the staged tile: direct path
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s[:3])) +
+                         ("v" if s[3] else "c") + ("g" if s[4] else "u"))
+def test_apply_A_matches_oracle(shape):
+    prob, kw, x = case(*shape)
+    with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        y = s.apply_A(torch.from_numpy(x).to(DEV)).cpu().numpy()
+    assert rel_maxdiff(y, oracle.apply_A(prob, x)) <= OP_TOL
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s[:3])) +
+                         ("v" if s[3] else "c") + ("g" if s[4] else "u"))
+def test_precond_matches_oracle(shape):
+    prob, kw, r = case(*shape)
+    with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        z = s.precond(torch.from_numpy(r).to(DEV)).cpu().numpy()
+    assert rel_maxdiff(z, oracle.precond(prob, r)) <= OP_TOL
+
+
+def test_unaligned_pointers_take_the_scalar_path():
+    prob, kw, x = case(16, 12, 8, True, True)
+    n = prob.n
+    buf_x = torch.zeros(n + 1, dtype=torch.float64, device=DEV)
+    buf_y = torch.zeros(n + 1, dtype=torch.float64, device=DEV)
+    xv, yv = buf_x[1:], buf_y[1:]          # 8-byte aligned views
+    xv.copy_(torch.from_numpy(x))
+    with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        s.apply_A(xv, yv)
+        z = s.precond(xv, buf_y[1:]).cpu().numpy()
+        y2 = s.apply_A(xv).cpu().numpy()
+    assert rel_maxdiff(y2, oracle.apply_A(prob, x)) <= OP_TOL
+    assert rel_maxdiff(z, oracle.precond(prob, x)) <= OP_TOL
+
+
+SOLVE_CASES = [
+    (37, 29, 16, True, True, 1e3),
+    (33, 5, 7, True, True, 1e2),
+    (40, 36, 64, False, True, 1e4),
+    (17, 19, 130, True, True, 1e5),
+    (6, 5, 500, False, True, 1e3),
+]
+
+
+@pytest.mark.parametrize("cfg", SOLVE_CASES, ids=lambda c: "x".join(map(str, c[:3])))
+def test_solve_matches_oracle(cfg):
+    nx, ny, nz, varying, graded, a_v = cfg
+    prob, kw, b = case(nx, ny, nz, varying, graded, a_v=a_v, seed=3)
+    x_ref, it_ref, hist_ref, st_ref = oracle.pcg(prob, b, rtol=1e-10, maxit=500)
+    assert st_ref == oracle.OK
+    with mf.Solver(nx, ny, nz, **kw) as s:
+        bd = torch.from_numpy(b).to(DEV)
+        x = torch.zeros_like(bd)
+        iters, hist, st = s.solve(bd, x, rtol=1e-10, maxit=500)
+        assert st == mf.PCG_OK
+        assert abs(iters - it_ref) <= 1
+        np.testing.assert_allclose(hist[: min(iters, it_ref) + 1],
+                                   hist_ref[: min(iters, it_ref) + 1], rtol=1e-6, atol=1e-13)
+        # compare the iterates at the oracle's iteration count
+        x.zero_()
+        it2, _, st2 = s.solve(bd, x, rtol=0.0, maxit=it_ref)
+        assert (it2, st2) == (it_ref, mf.PCG_OK)
+        xs = x.cpu().numpy()
+    assert np.linalg.norm(xs - x_ref) <= SOL_TOL * np.linalg.norm(x_ref)
+
+
+def test_solve_is_bitwise_repeatable():
+    prob, kw, b = case(40, 36, 64, True, True, a_v=1e4, seed=5)
+    with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        bd = torch.from_numpy(b).to(DEV)
+        x1, x2 = torch.zeros_like(bd), torch.zeros_like(bd)
+        i1, h1, _ = s.solve(bd, x1, rtol=1e-10)
+        i2, h2, _ = s.solve(bd, x2, rtol=1e-10)
+    assert i1 == i2
+    assert np.array_equal(h1, h2)
+    assert torch.equal(x1, x2)
+
+
+def test_solve_host_equals_solve_device():
+    prob, kw, b = case(30, 20, 32, True, True, a_v=1e3, seed=6)
+    with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        bd = torch.from_numpy(b).to(DEV)
+        xd = torch.zeros_like(bd)
+        i1, h1, st1 = s.solve(bd, xd, rtol=1e-10)
+        bh = torch.from_numpy(b).pin_memory()
+        xh = torch.zeros(prob.n, dtype=torch.float64).pin_memory()
+        i2, h2, st2 = s.solve_host(bh, xh, rtol=1e-10)
+        xn = np.zeros(prob.n)                       # pageable host memory works too
+        i3, _, _ = s.solve_host(b, xn, rtol=1e-10)
+    assert (i1, st1) == (i2, st2) == (i3, mf.PCG_OK)
+    assert np.array_equal(xd.cpu().numpy(), xh.numpy())
+    assert np.array_equal(xh.numpy(), xn)
+
+
+def test_status_semantics_match_oracle():
+    prob, kw, b = case(20, 18, 16, True, True, a_v=1e3, seed=7)
+    with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        bd = torch.from_numpy(b).to(DEV)
+        _, it_ref, _, _ = oracle.pcg(prob, b, rtol=1e-8)
+        x = torch.zeros_like(bd)
+        it, hist, st = s.solve(bd, x, rtol=1e-8, maxit=it_ref - 2)
+        assert (it, st) == (it_ref - 2, mf.PCG_ENOTCONV)
+        x.zero_()
+        it, hist, st = s.solve(bd, x, rtol=0.0, maxit=3)
+        assert (it, st, len(hist)) == (3, mf.PCG_OK, 4)
+        x.zero_()
+        it, hist, st = s.solve(torch.zeros_like(bd), x, rtol=1e-10)
+        assert (it, st) == (0, mf.PCG_OK) and hist[0] == 0.0 and float(x.abs().max()) == 0.0
+        x.zero_()
+        it, hist, st = s.solve(bd, x, rtol=1e-10, maxit=0)
+        assert (it, st) == (0, mf.PCG_ENOTCONV)
+        bad = bd.clone()
+        bad[123] = float("nan")
+        x.zero_()
+        it, hist, st = s.solve(bad, x, rtol=1e-10)
+        assert st == mf.PCG_EBREAKDOWN
+        assert "breakdown" in mf.pcg_last_error(s.ctx)
+        # restart from a non-zero iterate: x carries the state, as in the oracle
+        x0 = np.random.default_rng(11).standard_normal(prob.n)
+        x.copy_(torch.from_numpy(x0))
+        it, hist, st = s.solve(bd, x, rtol=1e-8)
+        x_ref, it_ref, _, st_ref = oracle.pcg(prob, b, x0=x0, rtol=1e-8)
+        assert st == mf.PCG_OK and abs(it - it_ref) <= 1
+        assert np.linalg.norm(x.cpu().numpy() - x_ref) <= 1e-6 * np.linalg.norm(x_ref)
+        with pytest.raises(mf.PCGError) as e:
+            s.solve(bd, bd, rtol=1e-10)
+        assert e.value.status == mf.PCG_EINVAL
+
+
+def test_zero_horizontal_coupling_converges_in_one_iteration():
+    nx, ny, nz = 12, 10, 24
+    h = W.layer_thickness(nz, True)
+    b = np.random.default_rng(9).uniform(-1, 1, nx * ny * nz)
+    with mf.Solver(nx, ny, nz, a_h=0.0, a_v=1e3, mass=1.0, dz=h) as s:
+        x = torch.zeros(nx * ny * nz, dtype=torch.float64, device=DEV)
+        it, hist, st = s.solve(torch.from_numpy(b).to(DEV), x, rtol=1e-10)
+    assert (it, st) == (1, mf.PCG_OK)
+
+
+def test_update_coeffs_and_streams():
+    prob, kw, x = case(24, 20, 32, True, True, a_v=1e3, seed=8)
+    prob2 = oracle.Problem(prob.nx, prob.ny, prob.nz, ah=prob.ah * 2.0, a_v=5e4, mass=0.5,
+                           h=prob.h)
+    stream = torch.cuda.Stream()
+    with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        s.update_coeffs(a_h_field=prob2.ah, a_v=5e4, mass=0.5, dz=prob.h)
+        s.set_stream(stream)
+        xd = torch.from_numpy(x).to(DEV)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            y = torch.empty_like(xd)
+            s.apply_A(xd, y)
+        stream.synchronize()
+        assert rel_maxdiff(y.cpu().numpy(), oracle.apply_A(prob2, x)) <= OP_TOL
+        # a field context may drop back to a constant a_h
+        s.update_coeffs(a_h=0.7, a_v=5e4, mass=0.5, dz=prob.h)
+        prob3 = oracle.Problem(prob.nx, prob.ny, prob.nz, ah=0.7, a_v=5e4, mass=0.5, h=prob.h)
+        with torch.cuda.stream(stream):
+            z = s.precond(xd)
+        stream.synchronize()
+        assert rel_maxdiff(z.cpu().numpy(), oracle.precond(prob3, x)) <= OP_TOL
+    with mf.Solver(8, 8, 8, a_h=1.0, a_v=10.0) as s:
+        with pytest.raises(mf.PCGError) as e:
+            s.update_coeffs(a_h_field=np.ones(64), a_v=10.0)
+        assert e.value.status == mf.PCG_EINVAL
+
+
+def test_kernel_timing_counts_launches():
+    prob, kw, b = case(40, 40, 64, True, True, a_v=1e4, seed=10)
+    with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        s.enable_timing(True)
+        bd = torch.from_numpy(b).to(DEV)
+        x = torch.zeros_like(bd)
+        it, _, _ = s.solve(bd, x, rtol=1e-10)
+        t = s.kernel_times()
+        info = s.launch_info()
+    assert t["residual"][1] == 1 and t["finalize"][1] == 1
+    assert t["precond_fused"][1] >= it + 1 and t["spmv_fused"][1] >= it
+    assert info["last_solve_launches"] == sum(v[1] for v in t.values())
+    assert all(v[0] >= 0 for v in t.values())
