@@ -56,7 +56,7 @@ typedef enum {
   PCG_ECUDA = 3,       /* a CUDA runtime call failed (no device, launch error, ...) */
   PCG_ENOTCONV = 4,    /* rtol > 0 and maxit iterations did not reach it */
   PCG_EBREAKDOWN = 5,  /* <p,Ap> <= 0, <r,z> <= 0 or a non-finite residual (NaN/Inf input) */
-  PCG_ETIMEOUT = 6     /* reserved: a bounded device wait ran out */
+  PCG_ETIMEOUT = 6     /* a bounded device wait (bulk-copy completion) ran out; reported by pcg_solve */
 } pcg_status;
 
 typedef struct pcg_ctx pcg_ctx; /* opaque; owns every internal device buffer */

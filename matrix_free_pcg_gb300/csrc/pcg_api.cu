@@ -330,6 +330,9 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
   if (fin.status == PCG_ENOTCONV)
     return fail(ctx, PCG_ENOTCONV, "no convergence to rtol=%g in %d iterations (last ratio %g)",
                 rtol, maxit, fin.R0 > 0 ? std::sqrt(fin.last_R / fin.R0) : 0.0);
+  if (fin.status == PCG_ETIMEOUT || fin.dev_error)
+    return fail(ctx, PCG_ETIMEOUT, "a bounded device wait ran out after %d iterations",
+                fin.iters);
   if (fin.status == PCG_EBREAKDOWN)
     return fail(ctx, PCG_EBREAKDOWN,
                 "breakdown after %d iterations: ||r||^2=%g <r,z>=%g <p,Ap>=%g", fin.iters,
@@ -370,6 +373,7 @@ int pcg_create(int nx, int ny, int nz, const pcg_coeffs* coeffs, pcg_ctx** out) 
   op.ny = ny;
   op.nz = nz;
   op.pz = (nz + 15) / 16 * 16;
+  op.pt = (nz % 4 == 0) ? nz + 2 : (nz % 2 == 0 ? nz : nz + 1);
   op.ncols = ncols;
   op.n = n;
   op.ntiles = (ncols + pcg::kTile - 1) / pcg::kTile;
@@ -415,7 +419,7 @@ int pcg_create(int nx, int ny, int nz, const pcg_coeffs* coeffs, pcg_ctx** out) 
 
   e = pcg::prepare_kernels(op);
   if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "kernel attribute set-up"));
-  ctx->grid_m = pcg::grid_precond(op, ctx->num_sms);
+  ctx->grid_m = pcg::grid_precond(op, ctx->num_sms);  // also sets op.stream_smem
   ctx->grid_a = pcg::grid_spmv(op, ctx->num_sms);
   e = dalloc(&ctx->partials, 2 * (size_t)(ctx->grid_m + ctx->grid_a));
   if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "workspace allocation"));
@@ -469,7 +473,8 @@ int pcg_precond(pcg_ctx* ctx, const double* r_dev, double* z_dev) {
   if (overlap(r_dev, z_dev, ctx->op.n)) return fail(ctx, PCG_EINVAL, "r and z overlap");
   DeviceGuard g(ctx->device);
   if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
-  cudaError_t e = pcg::launch_precond(ctx->op, r_dev, z_dev, ctx->grid_m, ctx->stream);
+  cudaError_t e = pcg::launch_precond(ctx->op, ctx->state, r_dev, z_dev, ctx->grid_m,
+                                      ctx->stream);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "precond launch");
   return PCG_OK;
 }

@@ -11,9 +11,8 @@ namespace pcg {
 constexpr int kTile = 32;
 // Threads per block of the stencil sweeps.
 constexpr int kSpmvThreads = 256;
-// Largest column height whose tile pair (r and q, 32 columns) fits in the
-// 227 KB of shared memory of one block; taller columns use the unstaged
-// preconditioner sweep.
+// Largest column height whose staged tiles (32 columns) fit in the 227 KB of
+// shared memory of one block; taller columns use the unstaged sweep.
 constexpr int kMaxStagedNz = 448;
 
 // Per-level coefficient table, kLevCount rows of nz doubles (row-major).
@@ -33,7 +32,9 @@ enum LevRow {
 // Operator description handed to every kernel by value.
 struct Op {
   int nx, ny, nz;
-  int pz;              // nz rounded up to a multiple of 16 (shared-memory column stride)
+  int pz;              // nz rounded up to a multiple of 16 (swizzled tile column stride)
+  int pt;              // column stride of the bulk-copied tile: >= nz, even, 2 mod 4
+  int stream_smem;     // dynamic shared memory of the streaming preconditioner launch
   long long ncols;     // nx*ny
   long long n;         // ncols*nz
   long long ntiles;    // ceil(ncols / kTile)
@@ -63,6 +64,7 @@ struct DevState {
   unsigned int ticket_m;  // last-block tickets of the two grid reductions
   unsigned int ticket_a;
   int setup_error;   // a non-positive Thomas pivot was met in the setup kernel
+  int dev_error;     // a bounded device wait ran out (pcg_status PCG_ETIMEOUT)
 };
 
 // ---- launchers (pcg_kernels.cu); all enqueue on `s` and return the launch error
@@ -78,8 +80,9 @@ cudaError_t launch_residual(const Op& op, DevState* st, const double* b, const d
                             cudaStream_t s);
 // y = A x
 cudaError_t launch_apply(const Op& op, const double* x, double* y, int grid, cudaStream_t s);
-// z = M^{-1} r
-cudaError_t launch_precond(const Op& op, const double* r, double* z, int grid, cudaStream_t s);
+// z = M^{-1} r  (st receives dev_error if a bounded wait runs out)
+cudaError_t launch_precond(const Op& op, DevState* st, const double* r, double* z, int grid,
+                           cudaStream_t s);
 // Algorithm 3 sweep
 cudaError_t launch_precond_fused(const Op& op, DevState* st, double* r, const double* q,
                                  double* z, double* partials, double* hist, int grid,
@@ -91,8 +94,9 @@ cudaError_t launch_spmv_fused(const Op& op, DevState* st, const double* z, doubl
 cudaError_t launch_finalize(const Op& op, const DevState* st, double* x, const double* p,
                             int grid, cudaStream_t s);
 
-// Occupancy-derived grid sizes (blocks) for the persistent sweeps.
-int grid_precond(const Op& op, int num_sms);
+// Occupancy-derived grid sizes (blocks) for the persistent sweeps.  The
+// preconditioner's also fixes op.stream_smem (see pcg_kernels.cu).
+int grid_precond(Op& op, int num_sms);
 int grid_spmv(const Op& op, int num_sms);
 // Shared-memory attribute set-up for the staged preconditioner (once per device).
 cudaError_t prepare_kernels(const Op& op);

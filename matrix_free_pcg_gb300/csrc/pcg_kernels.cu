@@ -19,6 +19,7 @@
 // grid reduction only once per launch.
 //
 // Vectors use the column-contiguous layout: cell (i,j,k) at ((j*nx)+i)*nz+k.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -27,7 +28,7 @@
 namespace pcg {
 namespace {
 
-constexpr int kStOK = 0, kStNotConv = 4, kStBreakdown = 5;
+constexpr int kStOK = 0, kStNotConv = 4, kStBreakdown = 5, kStTimeout = 6;
 
 __device__ __forceinline__ double2 ld2(const double* p) {
   return *reinterpret_cast<const double2*>(p);
@@ -40,6 +41,10 @@ __device__ __forceinline__ void st2(double* p, double2 v) {
 }
 __device__ __forceinline__ int ld_done(const DevState* st) {
   return *reinterpret_cast<const volatile int*>(&st->done);
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
 // Horizontal neighbours of a column, periodic in i and j.
@@ -268,59 +273,30 @@ struct LinIdx {
 };
 
 // Copy cnt = nc*nz consecutive doubles (nc whole columns) from global memory
-// into the swizzled tile, cooperatively by the 32 lanes of the warp.
-template <bool VEC2>
+// into the swizzled tile, cooperatively by the 32 lanes of the warp (used for
+// odd nz or 8-byte aligned vectors, where the bulk-copy engine cannot be).
 __device__ __forceinline__ void tile_load(const double* __restrict__ g, double* s, int cnt,
                                           int nz, int pz, int lane) {
-  if (VEC2) {  // nz even: a pair never straddles two columns
-    int e = 2 * lane, c = e / nz, k = e - c * nz;
-    for (; e < cnt; e += 64) {
-      const double2 v = ld2(g + e);
-      const int sw = c & 15;
-      s[c * pz + (k ^ sw)] = v.x;
-      s[c * pz + ((k + 1) ^ sw)] = v.y;
-      k += 64;
-      while (k >= nz) {
-        k -= nz;
-        ++c;
-      }
-    }
-  } else {
-    int e = lane, c = e / nz, k = e - c * nz;
-    for (; e < cnt; e += 32) {
-      s[c * pz + (k ^ (c & 15))] = g[e];
-      k += 32;
-      while (k >= nz) {
-        k -= nz;
-        ++c;
-      }
+  int e = lane, c = e / nz, k = e - c * nz;
+  for (; e < cnt; e += 32) {
+    s[c * pz + (k ^ (c & 15))] = g[e];
+    k += 32;
+    while (k >= nz) {
+      k -= nz;
+      ++c;
     }
   }
 }
 
-template <bool VEC2>
 __device__ __forceinline__ void tile_store(const double* s, double* __restrict__ g, int cnt,
                                            int nz, int pz, int lane) {
-  if (VEC2) {
-    int e = 2 * lane, c = e / nz, k = e - c * nz;
-    for (; e < cnt; e += 64) {
-      const int sw = c & 15;
-      st2(g + e, make_double2(s[c * pz + (k ^ sw)], s[c * pz + ((k + 1) ^ sw)]));
-      k += 64;
-      while (k >= nz) {
-        k -= nz;
-        ++c;
-      }
-    }
-  } else {
-    int e = lane, c = e / nz, k = e - c * nz;
-    for (; e < cnt; e += 32) {
-      g[e] = s[c * pz + (k ^ (c & 15))];
-      k += 32;
-      while (k >= nz) {
-        k -= nz;
-        ++c;
-      }
+  int e = lane, c = e / nz, k = e - c * nz;
+  for (; e < cnt; e += 32) {
+    g[e] = s[c * pz + (k ^ (c & 15))];
+    k += 32;
+    while (k >= nz) {
+      k -= nz;
+      ++c;
     }
   }
 }
@@ -332,43 +308,86 @@ __device__ __forceinline__ void tile_store(const double* s, double* __restrict__
 // Forward: y_k = r*_k + (T_{k-1/2}/D_{k-1}) y_{k-1},  w_k = y_k / D_k;
 // backward: z_k = w_k + (T_{k+1/2}/D_k) z_{k+1}.  fp64 operations per level:
 // 4 forward (r*, ||r||^2, y, w), 2 backward (z, <r,z>).
+//
+// The two Thomas factors of every level are loaded kPre levels ahead of their
+// use into registers, so their global-memory latency overlaps the serial
+// recurrence instead of sitting inside it.
+constexpr int kPre = 16;
+
 template <bool VARY, bool FUSED, typename IDX>
 __device__ __forceinline__ void column_solve(const Op& op, long long tile, int lane, IDX idx,
                                              double* rp, const double* qp, double* wp,
                                              double nalpha, double& accR, double& accK) {
   const int nz = op.nz;
   const double* __restrict__ lev = op.lev;
-  const double* fn = VARY ? op.tnphi + tile * nz * kTile + lane : lev + LV_NPHI * nz;
-  const double* fi = VARY ? op.tinvd + tile * nz * kTile + lane : lev + LV_INVD * nz;
+  const double* __restrict__ fn = VARY ? op.tnphi + tile * nz * kTile + lane : lev + LV_NPHI * nz;
+  const double* __restrict__ fi = VARY ? op.tinvd + tile * nz * kTile + lane : lev + LV_INVD * nz;
   const int fs = VARY ? kTile : 1;
-  int o = idx(0);
-  double rk = rp[o];
-  if (FUSED) {
-    rk = fma(nalpha, qp[o], rk);
-    accR = fma(rk, rk, accR);
-    rp[o] = rk;
+  // ---- forward elimination; level k uses nphi_{k-1} (0 at k = 0) and invd_k
+  double cn[kPre], ci[kPre];
+#pragma unroll
+  for (int j = 0; j < kPre; ++j) {
+    cn[j] = (j >= 1 && j - 1 < nz) ? __ldg(fn + (j - 1) * fs) : 0.0;
+    ci[j] = (j < nz) ? __ldg(fi + j * fs) : 0.0;
   }
-  double y = rk;
-  wp[o] = y * __ldg(fi);
-  for (int k = 1; k < nz; ++k) {
-    o = idx(k);
-    rk = rp[o];
-    if (FUSED) {
-      rk = fma(nalpha, qp[o], rk);
-      accR = fma(rk, rk, accR);
-      rp[o] = rk;
+  double y = 0.0;
+  for (int kc = 0; kc < nz; kc += kPre) {
+    double nn[kPre], ni[kPre];
+#pragma unroll
+    for (int j = 0; j < kPre; ++j) {
+      const int k = kc + kPre + j;
+      nn[j] = (k - 1 < nz) ? __ldg(fn + (k - 1) * fs) : 0.0;
+      ni[j] = (k < nz) ? __ldg(fi + k * fs) : 0.0;
     }
-    y = fma(__ldg(fn + (k - 1) * fs), y, rk);
-    wp[o] = y * __ldg(fi + k * fs);
+#pragma unroll
+    for (int j = 0; j < kPre; ++j) {
+      const int k = kc + j;
+      if (k < nz) {
+        const int o = idx(k);
+        double rk = rp[o];
+        if (FUSED) {
+          rk = fma(nalpha, qp[o], rk);
+          accR = fma(rk, rk, accR);
+          rp[o] = rk;
+        }
+        y = fma(cn[j], y, rk);
+        wp[o] = y * ci[j];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kPre; ++j) {
+      cn[j] = nn[j];
+      ci[j] = ni[j];
+    }
   }
-  o = idx(nz - 1);
+  // ---- back substitution; level k uses nphi_k
+  int o = idx(nz - 1);
   double zz = wp[o];
   if (FUSED) accK = fma(zz, rp[o], accK);
-  for (int k = nz - 2; k >= 0; --k) {
-    o = idx(k);
-    zz = fma(__ldg(fn + k * fs), zz, wp[o]);
-    wp[o] = zz;
-    if (FUSED) accK = fma(zz, rp[o], accK);
+#pragma unroll
+  for (int j = 0; j < kPre; ++j) {
+    const int k = nz - 2 - j;
+    cn[j] = (k >= 0) ? __ldg(fn + k * fs) : 0.0;
+  }
+  for (int kb = nz - 2; kb >= 0; kb -= kPre) {
+    double nn[kPre];
+#pragma unroll
+    for (int j = 0; j < kPre; ++j) {
+      const int k = kb - kPre - j;
+      nn[j] = (k >= 0) ? __ldg(fn + k * fs) : 0.0;
+    }
+#pragma unroll
+    for (int j = 0; j < kPre; ++j) {
+      const int k = kb - j;
+      if (k >= 0) {
+        o = idx(k);
+        zz = fma(cn[j], zz, wp[o]);
+        wp[o] = zz;
+        if (FUSED) accK = fma(zz, rp[o], accK);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kPre; ++j) cn[j] = nn[j];
   }
 }
 
@@ -383,7 +402,10 @@ __device__ void finish_precond_sweep(DevState* st, double R, double K, double* h
   const double ratio = (R0 > 0.0) ? sqrt(R / R0) : 0.0;
   hist[it] = ratio;
   int done = 0, status = kStOK;
-  if (R0 == 0.0) {
+  if (st->dev_error) {
+    done = 1;
+    status = kStTimeout;
+  } else if (R0 == 0.0) {
     done = 1;  // r_0 = 0: the initial guess solves the system
   } else if (!(R < INFINITY) || !(R0 < INFINITY)) {
     done = 1;
@@ -409,7 +431,7 @@ __device__ void finish_precond_sweep(DevState* st, double R, double K, double* h
   st->it = it + 1;
 }
 
-template <bool VARY, bool FUSED, bool VEC2>
+template <bool VARY, bool FUSED>
 __global__ void __launch_bounds__(kTile) k_precond_staged(Op op, DevState* st,
                                                           double* __restrict__ r,
                                                           const double* __restrict__ q,
@@ -430,17 +452,230 @@ __global__ void __launch_bounds__(kTile) k_precond_staged(Op op, DevState* st,
     const int nc = (int)min((long long)kTile, op.ncols - col0);
     const long long base = col0 * nz;
     const int cnt = nc * nz;
-    tile_load<VEC2>(r + base, sr, cnt, nz, pz, lane);
-    if (FUSED) tile_load<VEC2>(q + base, sq, cnt, nz, pz, lane);
+    tile_load(r + base, sr, cnt, nz, pz, lane);
+    if (FUSED) tile_load(q + base, sq, cnt, nz, pz, lane);
     __syncwarp();
     if (lane < nc)
       column_solve<VARY, FUSED>(op, t, lane, idx, sr + lane * pz, sq + lane * pz,
                                 sq + lane * pz, nalpha, accR, accK);
     __syncwarp();
-    if (FUSED) tile_store<VEC2>(sr, r + base, cnt, nz, pz, lane);
-    tile_store<VEC2>(sq, z + base, cnt, nz, pz, lane);
+    if (FUSED) tile_store(sr, r + base, cnt, nz, pz, lane);
+    tile_store(sq, z + base, cnt, nz, pz, lane);
     __syncwarp();
   }
+  if (FUSED) {
+    double R, K;
+    if (grid_sum2<kTile>(accR, accK, partials, &st->ticket_m, R, K))
+      finish_precond_sweep(st, R, K, hist);
+  }
+}
+
+// Streaming variant (nz even, 16-byte aligned vectors), the main path.
+//
+// Only w, the result of the forward sweep that the backward sweep consumes in
+// reverse, stays in shared memory for a whole column (tile W, 32 columns at
+// an even stride pt = 2 (mod 4) doubles, at most 2-way bank conflicts).  r
+// and q stream through rings of kStages slots of kChunk levels, filled two
+// chunks ahead by 16-byte asynchronous copies (cp.async) in a transposed
+// lane mapping: four lanes cover the 64 bytes of one column's chunk, so one
+// instruction moves 8 columns x 64 contiguous bytes.  r* = r - alpha q is
+// written back into its ring slot and then to global memory, and z from W at
+// the end of the column, with the same coalesced mapping.  At nz = 128 this
+// is 48.7 KB of shared memory per warp: four warps per SM, the number the
+// SM's fp64 unit needs to run at full rate (a single warp issues one fp64
+// instruction about every 68 clocks).  The launch sizes its shared-memory
+// request so that the warps per SM are a multiple of four.
+//
+// <r,z> is accumulated in the forward sweep as sum_k y_k w_k: with
+// y = L^{-1} r* and w = D^{-1} y this is r*^T L^{-T} D^{-1} L^{-1} r* =
+// <r*, M^{-1} r*>, the same number Algorithm 3 sums in its backward loop.
+constexpr int kChunk = 8;
+constexpr int kStages = 3;
+constexpr int kCS = kChunk + 2;  // ring column stride (doubles)
+// Dynamic shared memory the streaming kernels may request: the per-block
+// opt-in limit minus their static shared memory (set in prepare_kernels).
+static int g_max_stream_smem = 0;
+
+template <bool FUSED>
+__host__ __device__ inline size_t stream_smem_bytes(int pt) {
+  return sizeof(double) * ((size_t)kTile * pt + (FUSED ? 2 : 1) * (size_t)kStages * kTile * kCS);
+}
+
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ double2 lds2(const double* p) {
+  return *reinterpret_cast<const double2*>(p);
+}
+
+template <bool VARY, bool FUSED>
+__global__ void __launch_bounds__(kTile) k_precond_stream(Op op, DevState* st,
+                                                          double* __restrict__ r,
+                                                          const double* __restrict__ q,
+                                                          double* __restrict__ z,
+                                                          double* __restrict__ partials,
+                                                          double* __restrict__ hist) {
+  extern __shared__ __align__(16) double smem[];
+  if (FUSED && ld_done(st)) return;
+  const int lane = threadIdx.x;
+  const int nz = op.nz, pt = op.pt;
+  const int nch = (nz + kChunk - 1) / kChunk;
+  double* W = smem;
+  double* Rg = W + kTile * pt;
+  double* Qg = Rg + kStages * kTile * kCS;
+  const double nalpha = FUSED ? -st->alpha : 0.0;
+  const double* __restrict__ lev = op.lev;
+  // transposed roles for the coalesced copies: columns cq + 8i, 16-byte piece pp
+  const int cq = lane >> 2, pp = 2 * (lane & 3);
+  double accR = 0.0, accK = 0.0;
+  // Static tile assignment (block b takes tiles b, b+G, ...): the per-block
+  // partial sums, and with them the reductions, are the same on every run.
+  const long long G = gridDim.x;
+  long long p_tile = blockIdx.x;
+  int p_m = 0, p_sl = 0;
+  // Producer: the copies of the next chunk in (tile, chunk) order, one
+  // commit group per chunk (possibly empty past the last tile).
+  auto issue = [&]() {
+    if (p_tile < op.ntiles) {
+      const long long col0 = p_tile * kTile;
+      const int nc = (int)min((long long)kTile, op.ncols - col0);
+      const int k0 = p_m * kChunk;
+      const int clen = min(kChunk, nz - k0);
+      if (pp < clen) {
+#pragma unroll
+        for (int i = 0; i < kTile / 8; ++i) {
+          const int c = cq + 8 * i;
+          if (c < nc) {
+            const long long g = (col0 + c) * nz + k0 + pp;
+            cp_async16(Rg + (p_sl * kTile + c) * kCS + pp, r + g);
+            if (FUSED) cp_async16(Qg + (p_sl * kTile + c) * kCS + pp, q + g);
+          }
+        }
+      }
+    }
+    cp_async_commit();
+    if (++p_m == nch) {
+      p_m = 0;
+      p_tile += G;
+    }
+    if (++p_sl == kStages) p_sl = 0;
+  };
+  for (int i = 0; i < kStages - 1; ++i) issue();  // prologue: chunks 0 and 1
+  int c_sl = 0;
+  for (long long t = blockIdx.x; t < op.ntiles; t += G) {
+    const long long col0 = t * kTile;
+    const int nc = (int)min((long long)kTile, op.ncols - col0);
+    double* wcol = W + lane * pt;
+    const double* fi = VARY ? op.tinvd + t * nz * kTile + lane : lev + LV_INVD * nz;
+    const double* fn = VARY ? op.tnphi + t * nz * kTile + lane : lev + LV_NPHI * nz;
+    const int fs = VARY ? kTile : 1;
+    double y = 0.0, nprev = 0.0;
+    // factors of chunk 0; those of chunk m+1 are loaded while chunk m runs
+    double fiv[kChunk], fnv[kChunk];
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      fiv[j] = (j < nz) ? __ldg(fi + j * fs) : 0.0;
+      fnv[j] = (j < nz) ? __ldg(fn + j * fs) : 0.0;
+    }
+    // ---- forward sweep, chunk by chunk
+    for (int m = 0; m < nch; ++m) {
+      const int k0 = m * kChunk;
+      const int clen = min(kChunk, nz - k0);
+      issue();                         // chunk seq+2 into the slot of chunk seq-1
+      cp_async_wait<kStages - 1>();    // this lane's copies of chunk seq have landed
+      __syncwarp();                    // ... and everyone else's
+      double fin[kChunk], fnn[kChunk];
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j) {
+        const int k = k0 + kChunk + j;
+        fin[j] = (k < nz) ? __ldg(fi + k * fs) : 0.0;
+        fnn[j] = (k < nz) ? __ldg(fn + k * fs) : 0.0;
+      }
+      if (lane < nc) {
+        double* rs = Rg + (c_sl * kTile + lane) * kCS;
+        const double* qs = Qg + (c_sl * kTile + lane) * kCS;
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+          if (j < clen) {
+            double rk = rs[j];
+            if (FUSED) {
+              rk = fma(nalpha, qs[j], rk);
+              accR = fma(rk, rk, accR);
+              rs[j] = rk;
+            }
+            y = fma(nprev, y, rk);
+            const double w = y * fiv[j];
+            if (FUSED) accK = fma(y, w, accK);
+            wcol[k0 + j] = w;
+            nprev = fnv[j];
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j) {
+        fiv[j] = fin[j];
+        fnv[j] = fnn[j];
+      }
+      __syncwarp();
+      if (FUSED && pp < clen) {  // r* of this chunk back to global memory
+#pragma unroll
+        for (int i = 0; i < kTile / 8; ++i) {
+          const int c = cq + 8 * i;
+          if (c < nc)
+            st2(r + (col0 + c) * nz + k0 + pp, lds2(Rg + (c_sl * kTile + c) * kCS + pp));
+        }
+      }
+      __syncwarp();  // the slot is refilled by the next issue()
+      if (++c_sl == kStages) c_sl = 0;
+    }
+    // ---- backward sweep over W
+    if (lane < nc) {
+      double zz = wcol[nz - 1];
+      double cn[kPre];
+#pragma unroll
+      for (int j = 0; j < kPre; ++j) {
+        const int k = nz - 2 - j;
+        cn[j] = (k >= 0) ? __ldg(fn + k * fs) : 0.0;
+      }
+      for (int kb = nz - 2; kb >= 0; kb -= kPre) {
+        double nn[kPre];
+#pragma unroll
+        for (int j = 0; j < kPre; ++j) {
+          const int k = kb - kPre - j;
+          nn[j] = (k >= 0) ? __ldg(fn + k * fs) : 0.0;
+        }
+#pragma unroll
+        for (int j = 0; j < kPre; ++j) {
+          const int k = kb - j;
+          if (k >= 0) {
+            zz = fma(cn[j], zz, wcol[k]);
+            wcol[k] = zz;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kPre; ++j) cn[j] = nn[j];
+      }
+    }
+    __syncwarp();
+    // z of the whole tile to global memory, 8 columns x 64 bytes per store
+#pragma unroll
+    for (int i = 0; i < kTile / 8; ++i) {
+      const int c = cq + 8 * i;
+      if (c < nc)
+        for (int k = pp; k < nz; k += kChunk)
+          st2(z + (col0 + c) * nz + k, lds2(W + c * pt + k));
+    }
+    __syncwarp();  // W is rewritten by the next tile
+  }
+  cp_async_wait<0>();
   if (FUSED) {
     double R, K;
     if (grid_sum2<kTile>(accR, accK, partials, &st->ticket_m, R, K))
@@ -566,6 +801,7 @@ __global__ void __launch_bounds__(kSpmvThreads) k_stencil(Op op, DevState* st,
     st->maxit = maxit;
     st->ticket_m = 0u;
     st->ticket_a = 0u;
+    st->dev_error = 0;
     st->done = 0;
   }
   const int nz = op.nz;
@@ -631,30 +867,38 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline bool staged(const Op& op) { return op.nz <= kMaxStagedNz; }
 inline size_t staged_smem(const Op& op) { return 2u * kTile * (size_t)op.pz * sizeof(double); }
 
-template <bool VARY, bool FUSED, bool VEC2>
-cudaError_t run_precond(const Op& op, DevState* st, double* r, const double* q, double* z,
-                        double* partials, double* hist, int grid, cudaStream_t s) {
-  if (staged(op))
-    k_precond_staged<VARY, FUSED, VEC2>
-        <<<grid, kTile, staged_smem(op), s>>>(op, st, r, q, z, partials, hist);
-  else
-    k_precond_direct<VARY, FUSED><<<grid, kTile, 0, s>>>(op, st, r, q, z, partials, hist);
-  return cudaGetLastError();
+// Which preconditioner sweep a launch takes: 0 bulk-copy tile (nz even,
+// 16-byte aligned vectors), 1 swizzled tile filled by scalar loads (odd nz or
+// 8-byte aligned vectors), 2 unstaged (columns taller than the tile).
+inline int precond_path(const Op& op, const double* r, const double* q, const double* z) {
+  if (!staged(op)) return 2;
+  const bool al = aligned16(r) && aligned16(z) && (!q || aligned16(q));
+  return (op.nz % 2 == 0 && al) ? 0 : 1;
 }
 
 template <bool VARY, bool FUSED>
-cudaError_t run_precond_v(const Op& op, DevState* st, double* r, const double* q, double* z,
-                          double* partials, double* hist, int grid, cudaStream_t s, bool v2) {
-  return v2 ? run_precond<VARY, FUSED, true>(op, st, r, q, z, partials, hist, grid, s)
-            : run_precond<VARY, FUSED, false>(op, st, r, q, z, partials, hist, grid, s);
+cudaError_t run_precond(const Op& op, DevState* st, double* r, const double* q, double* z,
+                        double* partials, double* hist, int grid, cudaStream_t s) {
+  switch (precond_path(op, r, q, z)) {
+    case 0:
+      k_precond_stream<VARY, FUSED><<<grid, kTile, op.stream_smem, s>>>(op, st, r, q, z,
+                                                                       partials, hist);
+      break;
+    case 1:
+      k_precond_staged<VARY, FUSED><<<grid, kTile, staged_smem(op), s>>>(op, st, r, q, z,
+                                                                         partials, hist);
+      break;
+    default:
+      k_precond_direct<VARY, FUSED><<<grid, kTile, 0, s>>>(op, st, r, q, z, partials, hist);
+  }
+  return cudaGetLastError();
 }
 
 template <bool FUSED>
 cudaError_t run_precond_any(const Op& op, DevState* st, double* r, const double* q, double* z,
                             double* partials, double* hist, int grid, cudaStream_t s) {
-  const bool v2 = (op.nz % 2 == 0) && aligned16(r) && aligned16(z) && (!q || aligned16(q));
-  return op.varying ? run_precond_v<true, FUSED>(op, st, r, q, z, partials, hist, grid, s, v2)
-                    : run_precond_v<false, FUSED>(op, st, r, q, z, partials, hist, grid, s, v2);
+  return op.varying ? run_precond<true, FUSED>(op, st, r, q, z, partials, hist, grid, s)
+                    : run_precond<false, FUSED>(op, st, r, q, z, partials, hist, grid, s);
 }
 
 template <typename K>
@@ -668,30 +912,68 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 
 cudaError_t prepare_kernels(const Op& op) {
   if (!staged(op)) return cudaSuccess;
+  {
+    int dev = 0, optin = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    size_t stat = 0;
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, k_precond_stream<true, true>) == cudaSuccess)
+      stat = std::max(stat, fa.sharedSizeBytes);
+    if (cudaFuncGetAttributes(&fa, k_precond_stream<false, true>) == cudaSuccess)
+      stat = std::max(stat, fa.sharedSizeBytes);
+    g_max_stream_smem = optin - (int)stat;
+  }
+  const int kMaxStreamSmem = g_max_stream_smem;
   const size_t b = staged_smem(op);
   cudaError_t e = cudaSuccess;
   cudaError_t r;
-#define PCG_SET(V, F, W)                                          \
-  r = set_smem(k_precond_staged<V, F, W>, b);                     \
+#define PCG_SET(V, F)                                             \
+  r = set_smem(k_precond_staged<V, F>, b);                        \
+  if (r != cudaSuccess) e = r;                                    \
+  r = set_smem(k_precond_stream<V, F>, kMaxStreamSmem);           \
   if (r != cudaSuccess) e = r;
-  PCG_SET(false, false, false) PCG_SET(false, false, true) PCG_SET(false, true, false)
-  PCG_SET(false, true, true) PCG_SET(true, false, false) PCG_SET(true, false, true)
-  PCG_SET(true, true, false) PCG_SET(true, true, true)
+  PCG_SET(false, false) PCG_SET(false, true) PCG_SET(true, false) PCG_SET(true, true)
 #undef PCG_SET
   return e;
 }
 
-int grid_precond(const Op& op, int num_sms) {
+// The streaming sweep runs one warp per block.  Each of the four
+// sub-partitions of an SM has its own fp64 unit, so the launch asks for
+// enough shared memory that the resident warps per SM are a multiple of four
+// (4 at nz = 128, 8 for short columns): a fifth warp would share a
+// sub-partition with another and, under the static tile assignment, set the
+// pace for the whole grid.
+int grid_precond(Op& op, int num_sms) {
   int per_sm = 0;
-  cudaError_t e;
-  if (staged(op))
-    e = op.varying ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                         &per_sm, k_precond_staged<true, true, true>, kTile, staged_smem(op))
-                   : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                         &per_sm, k_precond_staged<false, true, true>, kTile, staged_smem(op));
-  else
+  cudaError_t e = cudaSuccess;
+  op.stream_smem = (int)stream_smem_bytes<true>(op.pt);
+  if (staged(op)) {
+    int dev = 0, smem_sm = 0, reserved = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    auto occ = [&](int bytes) {
+      int b = 0;
+      cudaError_t r = op.varying ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                                       &b, k_precond_stream<true, true>, kTile, bytes)
+                                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                                       &b, k_precond_stream<false, true>, kTile, bytes);
+      return r == cudaSuccess ? b : 0;
+    };
+    per_sm = occ(op.stream_smem);
+    if (per_sm > 4 && per_sm % 4 != 0) {
+      const int target = per_sm / 4 * 4;
+      const int padded = smem_sm / target - reserved - 256;
+      if (padded > op.stream_smem && padded <= g_max_stream_smem && occ(padded) == target) {
+        op.stream_smem = padded;
+        per_sm = target;
+      }
+    }
+  } else {
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_precond_direct<false, true>,
                                                       kTile, 0);
+  }
   if (e != cudaSuccess || per_sm < 1) per_sm = 1;
   long long g = (long long)per_sm * num_sms;
   if (g > op.ntiles) g = op.ntiles;
@@ -760,9 +1042,10 @@ cudaError_t launch_apply(const Op& op, const double* x, double* y, int grid, cud
   return cudaGetLastError();
 }
 
-cudaError_t launch_precond(const Op& op, const double* r, double* z, int grid, cudaStream_t s) {
-  return run_precond_any<false>(op, nullptr, const_cast<double*>(r), nullptr, z, nullptr,
-                                nullptr, grid, s);
+cudaError_t launch_precond(const Op& op, DevState* st, const double* r, double* z, int grid,
+                           cudaStream_t s) {
+  return run_precond_any<false>(op, st, const_cast<double*>(r), nullptr, z, nullptr, nullptr,
+                                grid, s);
 }
 
 cudaError_t launch_precond_fused(const Op& op, DevState* st, double* r, const double* q,

@@ -13,8 +13,8 @@ HEADER = os.path.join(ROOT, "include", "pcg.h")
 
 @pytest.fixture(scope="module")
 def lib():
-    from matrix_free_pcg_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import matrix_free_pcg_gb300 as mf
     return mf
 
