@@ -129,6 +129,27 @@ int pcg_solve(pcg_ctx* ctx, const double* b_dev, double* x_dev, double rtol, int
 int pcg_solve_host(pcg_ctx* ctx, const double* b_host, double* x_host, double rtol,
                    int maxit, int* iters_out, double* res_hist);
 
+/* z = M^{-1} r and *rz_dev = <r, z>, without allocating anything.
+ * The paper has no counterpart: this entry point exists for callers that
+ * must not allocate device memory while they run -- for instance code that
+ * must not synchronise the device (cudaFree does, cudaMalloc may), code
+ * running while a stream is captured into a CUDA graph, or applications
+ * that hand all device memory to their own pool at start-up.  The context
+ * (made earlier with pcg_create) supplies the operator tables; the only
+ * scratch, one partial sum per tile of 32 columns, comes from a fixed array
+ * of 65,536 doubles (512 KB) compiled into the library, which every GPU that
+ * loads the library holds until the process exits.
+ *   r_dev, z_dev  device, N values each, must not overlap.
+ *   rz_dev        device, 1 value: receives <r, z>.
+ * Grids of more than 65,536 x 32 = 2,097,152 columns are rejected with
+ * PCG_EINVAL.  The first call on a device looks up the device address of the
+ * scratch array (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  All calls share the one array: calls that overlap on the
+ * GPU (from two streams or two host threads) race and give wrong results.
+ * Asynchronous on the context's stream; calls no cudaMalloc, cudaFree or
+ * other allocating routine. */
+int pcg_precond_dot_noalloc(pcg_ctx* ctx, const double* r_dev, double* z_dev, double* rz_dev);
+
 /* Message for the last failed call on this context (or of the last failed
  * pcg_create when ctx is NULL).  Never NULL; owned by the library. */
 const char* pcg_last_error(const pcg_ctx* ctx);

@@ -29,7 +29,8 @@ PCG_K_COUNT = len(KERNEL_KINDS)
 
 EXPORTED = ["pcg_create", "pcg_destroy", "pcg_update_coeffs", "pcg_set_stream", "pcg_apply_A",
             "pcg_precond", "pcg_solve", "pcg_solve_host", "pcg_last_error",
-            "pcg_enable_timing", "pcg_kernel_times", "pcg_launch_info"]
+            "pcg_enable_timing", "pcg_kernel_times", "pcg_launch_info",
+            "pcg_precond_dot_noalloc"]
 
 
 class pcg_coeffs(ctypes.Structure):
@@ -64,6 +65,7 @@ def _load(path=LIB_PATH):
         "pcg_launch_info": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int),
                                            ctypes.POINTER(ctypes.c_int),
                                            ctypes.POINTER(ctypes.c_longlong)]),
+        "pcg_precond_dot_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -197,6 +199,20 @@ def pcg_solve_host(ctx, n, b, x, rtol, maxit, history=True):
     if st not in (PCG_OK, PCG_ENOTCONV, PCG_EBREAKDOWN):
         _check(st, ctx)
     return it.value, (hist[: it.value + 1] if history else None), st
+
+
+def pcg_precond_dot_noalloc(ctx, n, r, z, rz):
+    """z = M^{-1} r and rz[0] = <r, z>, with no device allocation.
+
+    For callers that must not allocate device memory while they run (no
+    synchronising cudaFree, stream capture in progress, a pre-reserved memory
+    pool).  r, z: contiguous float64 CUDA tensors of n values; rz: a float64
+    CUDA tensor of one value.  Scratch comes from a fixed array inside the
+    library, shared by every call: calls that overlap on the GPU race.  Grids
+    above 2,097,152 columns are rejected.
+    """
+    return _check(_lib.pcg_precond_dot_noalloc(ctx, _dev_ptr(r, n, "r"), _dev_ptr(z, n, "z"),
+                                               _dev_ptr(rz, 1, "rz")), ctx)
 
 
 def pcg_enable_timing(ctx, enable=True):

@@ -522,6 +522,24 @@ int pcg_solve_host(pcg_ctx* ctx, const double* b_host, double* x_host, double rt
   return st;
 }
 
+int pcg_precond_dot_noalloc(pcg_ctx* ctx, const double* r_dev, double* z_dev, double* rz_dev) {
+  if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
+  if (!r_dev || !z_dev || !rz_dev)
+    return fail(ctx, PCG_EINVAL, "r, z and rz must be non-NULL device pointers");
+  if (overlap(r_dev, z_dev, ctx->op.n)) return fail(ctx, PCG_EINVAL, "r and z overlap");
+  if (ctx->op.ntiles > pcg::kNoallocMaxTiles)
+    return fail(ctx, PCG_EINVAL,
+                "grid has %lld columns; the no-allocation scratch holds at most %lld "
+                "(%lld tiles of 32 columns)",
+                ctx->op.ncols, pcg::kNoallocMaxTiles * pcg::kTile, pcg::kNoallocMaxTiles);
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
+  cudaError_t e = pcg::launch_precond_dot_noalloc(ctx->op, r_dev, z_dev, rz_dev, ctx->num_sms,
+                                                  ctx->stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "precond_dot_noalloc");
+  return PCG_OK;
+}
+
 const char* pcg_last_error(const pcg_ctx* ctx) {
   return ctx ? ctx->err.c_str() : g_create_error.c_str();
 }

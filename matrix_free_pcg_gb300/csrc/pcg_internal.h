@@ -94,6 +94,12 @@ cudaError_t launch_spmv_fused(const Op& op, DevState* st, const double* z, doubl
 cudaError_t launch_finalize(const Op& op, const DevState* st, double* x, const double* p,
                             int grid, cudaStream_t s);
 
+// z = M^{-1} r and *rz = <r, z> with scratch from a fixed device array in
+// pcg_noalloc.cu (no allocation); at most kNoallocMaxTiles tiles of 32 columns.
+constexpr long long kNoallocMaxTiles = 65536;
+cudaError_t launch_precond_dot_noalloc(const Op& op, const double* r, double* z, double* rz,
+                                       int num_sms, cudaStream_t s);
+
 // Occupancy-derived grid sizes (blocks) for the persistent sweeps.  The
 // preconditioner's also fixes op.stream_smem (see pcg_kernels.cu).
 int grid_precond(Op& op, int num_sms);

@@ -1,0 +1,72 @@
+"""The preconditioner solve that allocates nothing, checked against pcg_precond.
+
+pcg_precond_dot_noalloc is for callers that must not allocate device memory
+while they run -- code that must not synchronise the device (as cudaFree
+does), code running during a CUDA-graph stream capture, applications that
+reserve all device memory for their own pool.  It returns z = M^{-1} r and
+<r, z>, taking its scratch from a fixed array inside the library that every
+call reuses.  So it must agree with pcg_precond (and with <r, z> computed on
+the host) on every call, not only the first.  This file sorts last so that a
+run stopping at the first failure has already run every other test.
+"""
+import numpy as np
+import pytest
+
+import oracle  # noqa: F401  (same import order as the other GPU tests)
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import matrix_free_pcg_gb300 as mf  # noqa: E402
+
+DEV = torch.device("cuda:0")
+TOL = 1e-12
+
+
+def rel_maxdiff(a, b):
+    return np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300)
+
+
+@pytest.mark.parametrize("shape", [(37, 29, 16, True), (64, 48, 64, False), (33, 5, 7, True)])
+def test_noalloc_matches_precond_on_two_calls_in_a_row(shape):
+    nx, ny, nz, varying = shape
+    n = nx * ny * nz
+    h = W.layer_thickness(nz, graded=True)
+    ah = W.horizontal_coefficient(nx, ny, varying)
+    kw = dict(a_h_field=ah if varying else None, a_h=1.0, a_v=1e3, mass=1.0, dz=h)
+    rng = np.random.default_rng(nz)
+    with mf.Solver(nx, ny, nz, **kw) as s:
+        for call, r_host in enumerate([rng.uniform(-1, 1, n), rng.standard_normal(n)]):
+            r = torch.from_numpy(r_host).to(DEV)
+            z_ref = s.precond(r).cpu().numpy()
+            rz_ref = float(np.dot(r_host, z_ref))
+            z = torch.full_like(r, float("nan"))
+            rz = torch.full((1,), float("nan"), dtype=torch.float64, device=DEV)
+            mf.pcg_precond_dot_noalloc(s.ctx, n, r, z, rz)
+            torch.cuda.synchronize()
+            zn = z.cpu().numpy()
+            assert rel_maxdiff(zn, z_ref) <= TOL, "call %d: z" % call
+            assert abs(float(rz.item()) - rz_ref) <= TOL * abs(rz_ref), "call %d: <r,z>" % call
+        # the same input again gives the same bits: nothing left over in the scratch
+        z2 = torch.empty_like(r)
+        rz2 = torch.empty((1,), dtype=torch.float64, device=DEV)
+        mf.pcg_precond_dot_noalloc(s.ctx, n, r, z2, rz2)
+        torch.cuda.synchronize()
+        assert torch.equal(z2, z) and torch.equal(rz2, rz)
+
+
+def test_noalloc_rejects_grids_beyond_its_scratch():
+    nx, ny, nz = 2048, 1025, 2          # 2,099,200 columns > 65,536 tiles of 32
+    with mf.Solver(nx, ny, nz, a_h=1.0, a_v=10.0, mass=1.0) as s:
+        n = nx * ny * nz
+        r = torch.zeros(n, dtype=torch.float64, device=DEV)
+        z = torch.empty_like(r)
+        rz = torch.empty((1,), dtype=torch.float64, device=DEV)
+        with pytest.raises(mf.PCGError) as e:
+            mf.pcg_precond_dot_noalloc(s.ctx, n, r, z, rz)
+        assert e.value.status == mf.PCG_EINVAL
+        assert "no-allocation scratch" in mf.pcg_last_error(s.ctx)
