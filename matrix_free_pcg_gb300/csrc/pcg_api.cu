@@ -43,7 +43,7 @@ struct pcg_ctx {
   double *r = nullptr, *z = nullptr, *p = nullptr, *q = nullptr;
   double *lev = nullptr, *ah = nullptr, *faceE = nullptr, *faceN = nullptr;
   double *cdiag = nullptr, *tnphi = nullptr, *tinvd = nullptr;
-  double *partials = nullptr, *hist = nullptr;
+  double *partials = nullptr, *hist = nullptr, *wscratch = nullptr;
   int hist_cap = 0;
   DevState* state = nullptr;
   double *b_host_api = nullptr, *x_host_api = nullptr;  // device copies for pcg_solve_host
@@ -161,7 +161,8 @@ cudaError_t dalloc(T** p, size_t count) {
 void free_all(pcg_ctx* ctx) {
   double* bufs[] = {ctx->r,     ctx->z,     ctx->p,     ctx->q,        ctx->lev,
                     ctx->ah,    ctx->faceE, ctx->faceN, ctx->cdiag,    ctx->tnphi,
-                    ctx->tinvd, ctx->partials, ctx->hist, ctx->b_host_api, ctx->x_host_api};
+                    ctx->tinvd, ctx->partials, ctx->hist, ctx->b_host_api, ctx->x_host_api,
+                    ctx->wscratch};
   for (double* b : bufs)
     if (b) cudaFree(b);
   if (ctx->state) cudaFree(ctx->state);
@@ -374,6 +375,7 @@ int pcg_create(int nx, int ny, int nz, const pcg_coeffs* coeffs, pcg_ctx** out) 
   op.nz = nz;
   op.pz = (nz + 15) / 16 * 16;
   op.pt = (nz % 4 == 0) ? nz + 2 : (nz % 2 == 0 ? nz : nz + 1);
+  op.fixed = (nz == 32 || nz == 64 || nz == 128) ? 1 : 0;
   op.ncols = ncols;
   op.n = n;
   op.ntiles = (ncols + pcg::kTile - 1) / pcg::kTile;
@@ -422,7 +424,10 @@ int pcg_create(int nx, int ny, int nz, const pcg_coeffs* coeffs, pcg_ctx** out) 
   ctx->grid_m = pcg::grid_precond(op, ctx->num_sms);  // also sets op.stream_smem
   ctx->grid_a = pcg::grid_spmv(op, ctx->num_sms);
   e = dalloc(&ctx->partials, 2 * (size_t)(ctx->grid_m + ctx->grid_a));
+  if (e == cudaSuccess && op.fixed)
+    e = dalloc(&ctx->wscratch, (size_t)ctx->grid_m * pcg::kTile * nz);
   if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "workspace allocation"));
+  op.wscratch = ctx->wscratch;
   st = load_coeffs(ctx, coeffs, varying);
   if (st) return bail(st);
   *out = ctx;

@@ -35,6 +35,9 @@ struct Op {
   int pz;              // nz rounded up to a multiple of 16 (swizzled tile column stride)
   int pt;              // column stride of the bulk-copied tile: >= nz, even, 2 mod 4
   int stream_smem;     // dynamic shared memory of the streaming preconditioner launch
+  int fixed;           // 1: nz is 32, 64 or 128 and the height-specialised sweep is used
+  int fixed_smem;      // dynamic shared memory of the height-specialised sweep
+  double* wscratch;    // height-specialised sweep: 32*nz doubles per block (grid_precond blocks)
   long long ncols;     // nx*ny
   long long n;         // ncols*nz
   long long ntiles;    // ceil(ncols / kTile)

@@ -489,9 +489,9 @@ __global__ void __launch_bounds__(kTile) k_precond_staged(Op op, DevState* st,
 // <r,z> is accumulated in the forward sweep as sum_k y_k w_k: with
 // y = L^{-1} r* and w = D^{-1} y this is r*^T L^{-T} D^{-1} L^{-1} r* =
 // <r*, M^{-1} r*>, the same number Algorithm 3 sums in its backward loop.
-constexpr int kChunk = 8;
-constexpr int kStages = 3;
-constexpr int kCS = kChunk + 2;  // ring column stride (doubles)
+constexpr int kChunk = 16;
+constexpr int kStages = 2;
+constexpr int kCS = kChunk + 2;  // ring row (doubles): 144 B, 16-byte aligned, no 16-byte conflicts
 // Dynamic shared memory the streaming kernels may request: the per-block
 // opt-in limit minus their static shared memory (set in prepare_kernels).
 static int g_max_stream_smem = 0;
@@ -515,8 +515,12 @@ __device__ __forceinline__ void cp_async_wait() {
 __device__ __forceinline__ double2 lds2(const double* p) {
   return *reinterpret_cast<const double2*>(p);
 }
+__device__ __forceinline__ void sts2(double* p, double a, double b) {
+  *reinterpret_cast<double2*>(p) = make_double2(a, b);
+}
 
-template <bool VARY, bool FUSED>
+// FULL: nz is a multiple of kChunk (no partial chunk, no guards).
+template <bool VARY, bool FUSED, bool FULL>
 __global__ void __launch_bounds__(kTile) k_precond_stream(Op op, DevState* st,
                                                           double* __restrict__ r,
                                                           const double* __restrict__ q,
@@ -533,9 +537,11 @@ __global__ void __launch_bounds__(kTile) k_precond_stream(Op op, DevState* st,
   double* Qg = Rg + kStages * kTile * kCS;
   const double nalpha = FUSED ? -st->alpha : 0.0;
   const double* __restrict__ lev = op.lev;
-  // transposed roles for the coalesced copies: columns cq + 8i, 16-byte piece pp
-  const int cq = lane >> 2, pp = 2 * (lane & 3);
-  double accR = 0.0, accK = 0.0;
+  // Transposed roles for the coalesced copies: eight lanes cover the 128
+  // bytes of one column's chunk, so one instruction moves 4 columns x 128
+  // contiguous bytes.  Lane handles columns cq + 4i, 16-byte piece pp.
+  const int cq = lane >> 3, pp = 2 * (lane & 7);
+  double accR0 = 0.0, accR1 = 0.0, accK0 = 0.0, accK1 = 0.0;
   // Static tile assignment (block b takes tiles b, b+G, ...): the per-block
   // partial sums, and with them the reductions, are the same on every run.
   const long long G = gridDim.x;
@@ -548,15 +554,17 @@ __global__ void __launch_bounds__(kTile) k_precond_stream(Op op, DevState* st,
       const long long col0 = p_tile * kTile;
       const int nc = (int)min((long long)kTile, op.ncols - col0);
       const int k0 = p_m * kChunk;
-      const int clen = min(kChunk, nz - k0);
-      if (pp < clen) {
+      const int clen = FULL ? kChunk : min(kChunk, nz - k0);
+      if (FULL || pp < clen) {
+        const double* rsrc = r + (col0 + cq) * nz + k0 + pp;
+        const double* qsrc = FUSED ? q + (col0 + cq) * nz + k0 + pp : nullptr;
+        double* rdst = Rg + (p_sl * kTile + cq) * kCS + pp;
+        double* qdst = Qg + (p_sl * kTile + cq) * kCS + pp;
 #pragma unroll
-        for (int i = 0; i < kTile / 8; ++i) {
-          const int c = cq + 8 * i;
-          if (c < nc) {
-            const long long g = (col0 + c) * nz + k0 + pp;
-            cp_async16(Rg + (p_sl * kTile + c) * kCS + pp, r + g);
-            if (FUSED) cp_async16(Qg + (p_sl * kTile + c) * kCS + pp, q + g);
+        for (int i = 0; i < kTile / 4; ++i) {
+          if (cq + 4 * i < nc) {
+            cp_async16(rdst + 4 * i * kCS, rsrc + (long long)4 * i * nz);
+            if (FUSED) cp_async16(qdst + 4 * i * kCS, qsrc + (long long)4 * i * nz);
           }
         }
       }
@@ -566,9 +574,9 @@ __global__ void __launch_bounds__(kTile) k_precond_stream(Op op, DevState* st,
       p_m = 0;
       p_tile += G;
     }
-    if (++p_sl == kStages) p_sl = 0;
+    p_sl ^= 1;
   };
-  for (int i = 0; i < kStages - 1; ++i) issue();  // prologue: chunks 0 and 1
+  issue();  // prologue: chunk 0
   int c_sl = 0;
   for (long long t = blockIdx.x; t < op.ntiles; t += G) {
     const long long col0 = t * kTile;
@@ -578,86 +586,102 @@ __global__ void __launch_bounds__(kTile) k_precond_stream(Op op, DevState* st,
     const double* fn = VARY ? op.tnphi + t * nz * kTile + lane : lev + LV_NPHI * nz;
     const int fs = VARY ? kTile : 1;
     double y = 0.0, nprev = 0.0;
-    // factors of chunk 0; those of chunk m+1 are loaded while chunk m runs
-    double fiv[kChunk], fnv[kChunk];
+    double cfi[kChunk], cfn[kChunk];
 #pragma unroll
     for (int j = 0; j < kChunk; ++j) {
-      fiv[j] = (j < nz) ? __ldg(fi + j * fs) : 0.0;
-      fnv[j] = (j < nz) ? __ldg(fn + j * fs) : 0.0;
+      cfi[j] = (FULL || j < nz) ? __ldg(fi + j * fs) : 0.0;
+      cfn[j] = (FULL || j < nz) ? __ldg(fn + j * fs) : 0.0;
     }
     // ---- forward sweep, chunk by chunk
+#pragma unroll 1
     for (int m = 0; m < nch; ++m) {
       const int k0 = m * kChunk;
-      const int clen = min(kChunk, nz - k0);
-      issue();                         // chunk seq+2 into the slot of chunk seq-1
-      cp_async_wait<kStages - 1>();    // this lane's copies of chunk seq have landed
-      __syncwarp();                    // ... and everyone else's
-      double fin[kChunk], fnn[kChunk];
+      const int clen = FULL ? kChunk : min(kChunk, nz - k0);
+      issue();                 // chunk seq+1 into the slot of chunk seq-1
+      double nfi[kChunk], nfn[kChunk];
 #pragma unroll
       for (int j = 0; j < kChunk; ++j) {
         const int k = k0 + kChunk + j;
-        fin[j] = (k < nz) ? __ldg(fi + k * fs) : 0.0;
-        fnn[j] = (k < nz) ? __ldg(fn + k * fs) : 0.0;
+        nfi[j] = (k < nz) ? __ldg(fi + k * fs) : 0.0;
+        nfn[j] = (k < nz) ? __ldg(fn + k * fs) : 0.0;
       }
+      cp_async_wait<1>();      // this lane's copies of chunk seq have landed
+      __syncwarp();            // ... and everyone else's
       if (lane < nc) {
         double* rs = Rg + (c_sl * kTile + lane) * kCS;
         const double* qs = Qg + (c_sl * kTile + lane) * kCS;
 #pragma unroll
-        for (int j = 0; j < kChunk; ++j) {
-          if (j < clen) {
-            double rk = rs[j];
+        for (int j = 0; j < kChunk; j += 2) {
+          if (FULL || j < clen) {
+            const double2 rv = lds2(rs + j);
+            double r0 = rv.x, r1 = rv.y;
             if (FUSED) {
-              rk = fma(nalpha, qs[j], rk);
-              accR = fma(rk, rk, accR);
-              rs[j] = rk;
+              const double2 qv = lds2(qs + j);
+              r0 = fma(nalpha, qv.x, r0);
+              r1 = fma(nalpha, qv.y, r1);
+              accR0 = fma(r0, r0, accR0);
+              accR1 = fma(r1, r1, accR1);
+              sts2(rs + j, r0, r1);
             }
-            y = fma(nprev, y, rk);
-            const double w = y * fiv[j];
-            if (FUSED) accK = fma(y, w, accK);
-            wcol[k0 + j] = w;
-            nprev = fnv[j];
+            y = fma(nprev, y, r0);
+            const double w0 = y * cfi[j];
+            if (FUSED) accK0 = fma(y, w0, accK0);
+            y = fma(cfn[j], y, r1);
+            const double w1 = y * cfi[j + 1];
+            if (FUSED) accK1 = fma(y, w1, accK1);
+            nprev = cfn[j + 1];
+            sts2(wcol + k0 + j, w0, w1);
           }
         }
       }
 #pragma unroll
       for (int j = 0; j < kChunk; ++j) {
-        fiv[j] = fin[j];
-        fnv[j] = fnn[j];
+        cfi[j] = nfi[j];
+        cfn[j] = nfn[j];
       }
       __syncwarp();
-      if (FUSED && pp < clen) {  // r* of this chunk back to global memory
+      if (FUSED && (FULL || pp < clen)) {  // r* of this chunk back to global memory
+        double* rdst = r + (col0 + cq) * nz + k0 + pp;
+        const double* rsrc = Rg + (c_sl * kTile + cq) * kCS + pp;
 #pragma unroll
-        for (int i = 0; i < kTile / 8; ++i) {
-          const int c = cq + 8 * i;
-          if (c < nc)
-            st2(r + (col0 + c) * nz + k0 + pp, lds2(Rg + (c_sl * kTile + c) * kCS + pp));
-        }
+        for (int i = 0; i < kTile / 4; ++i)
+          if (cq + 4 * i < nc) st2(rdst + (long long)4 * i * nz, lds2(rsrc + 4 * i * kCS));
       }
       __syncwarp();  // the slot is refilled by the next issue()
-      if (++c_sl == kStages) c_sl = 0;
+      c_sl ^= 1;
     }
-    // ---- backward sweep over W
+    // ---- backward sweep over W (nz is even here).  Level nz-1 is final;
+    // level nz-2 alone; then pairs (kh-1, kh), kh = nz-3, nz-5, ..., 1, each
+    // read and written as one 16-byte pair.  Factor s of the pair sequence
+    // belongs to level nz-3-s and is loaded kPre levels ahead.
     if (lane < nc) {
       double zz = wcol[nz - 1];
+      if (nz >= 2) {
+        zz = fma(__ldg(fn + (nz - 2) * fs), zz, wcol[nz - 2]);
+        wcol[nz - 2] = zz;
+      }
       double cn[kPre];
 #pragma unroll
       for (int j = 0; j < kPre; ++j) {
-        const int k = nz - 2 - j;
+        const int k = nz - 3 - j;
         cn[j] = (k >= 0) ? __ldg(fn + k * fs) : 0.0;
       }
-      for (int kb = nz - 2; kb >= 0; kb -= kPre) {
+#pragma unroll 1
+      for (int sb = 0; sb < nz - 2; sb += kPre) {
         double nn[kPre];
 #pragma unroll
         for (int j = 0; j < kPre; ++j) {
-          const int k = kb - kPre - j;
+          const int k = nz - 3 - (sb + kPre + j);
           nn[j] = (k >= 0) ? __ldg(fn + k * fs) : 0.0;
         }
 #pragma unroll
-        for (int j = 0; j < kPre; ++j) {
-          const int k = kb - j;
-          if (k >= 0) {
-            zz = fma(cn[j], zz, wcol[k]);
-            wcol[k] = zz;
+        for (int j = 0; j < kPre; j += 2) {
+          const int kh = nz - 3 - (sb + j);  // odd
+          if (kh >= 1) {
+            const double2 wv = lds2(wcol + kh - 1);
+            const double zh = fma(cn[j], zz, wv.y);
+            zz = fma(cn[j + 1], zh, wv.x);
+            sts2(wcol + kh - 1, zz, zh);
           }
         }
 #pragma unroll
@@ -665,22 +689,220 @@ __global__ void __launch_bounds__(kTile) k_precond_stream(Op op, DevState* st,
       }
     }
     __syncwarp();
-    // z of the whole tile to global memory, 8 columns x 64 bytes per store
+    // z of the whole tile to global memory, 4 columns x 128 bytes per store
+    {
+      double* zdst = z + (col0 + cq) * nz + pp;
+      const double* wsrc = W + cq * pt + pp;
 #pragma unroll
-    for (int i = 0; i < kTile / 8; ++i) {
-      const int c = cq + 8 * i;
-      if (c < nc)
-        for (int k = pp; k < nz; k += kChunk)
-          st2(z + (col0 + c) * nz + k, lds2(W + c * pt + k));
+      for (int i = 0; i < kTile / 4; ++i) {
+        if (cq + 4 * i < nc) {
+          for (int k = 0; k < nz; k += kChunk)
+            if (FULL || pp + k < nz)
+              st2(zdst + (long long)4 * i * nz + k, lds2(wsrc + 4 * i * pt + k));
+        }
+      }
     }
     __syncwarp();  // W is rewritten by the next tile
   }
   cp_async_wait<0>();
   if (FUSED) {
     double R, K;
-    if (grid_sum2<kTile>(accR, accK, partials, &st->ticket_m, R, K))
+    if (grid_sum2<kTile>(accR0 + accR1, accK0 + accK1, partials, &st->ticket_m, R, K))
       finish_precond_sweep(st, R, K, hist);
   }
+}
+
+// Column-height-specialised variant of the streaming sweep (nz = 32, 64,
+// 128: the heights of the workloads), the main path for those heights.
+//
+// It keeps the data flow of k_precond_stream for r, q and r*, with every
+// level loop unrolled at compile time.  w, the forward result the backward
+// sweep consumes in reverse, does not stay in shared memory: each block owns
+// a private scratch region in global memory (32 x NZ doubles, level-major,
+// so that one level of the 32 columns is one 256-byte line), written in the
+// forward sweep and read back, still resident in L2, in the backward sweep.
+// Shared memory then holds only the two r/q rings (18.4 KB), so eight warps
+// -- two per SM sub-partition -- fit on an SM and hide each other's
+// latencies; with one warp per sub-partition every dependent instruction
+// waits out a full fp64 latency.  z leaves through the ring slot that is
+// free during the backward sweep, transposed for coalesced stores.
+template <int NZ, bool VARY, bool FUSED>
+__global__ void __launch_bounds__(kTile) k_precond_fixed(Op op, DevState* st,
+                                                         double* __restrict__ r,
+                                                         const double* __restrict__ q,
+                                                         double* __restrict__ z,
+                                                         double* __restrict__ partials,
+                                                         double* __restrict__ hist) {
+  constexpr int NCH = NZ / kChunk;
+  constexpr int FS = VARY ? kTile : 1;  // factor stride between levels
+  static_assert(NZ % (2 * kChunk) == 0, "an even number of whole chunks");
+  extern __shared__ __align__(16) double smem[];
+  if (FUSED && ld_done(st)) return;
+  const int lane = threadIdx.x;
+  double* Rg = smem;
+  double* Qg = Rg + kStages * kTile * kCS;
+  double* wsb = op.wscratch + (long long)blockIdx.x * NZ * kTile + lane;  // level k at wsb[k*32]
+  const double nalpha = FUSED ? -st->alpha : 0.0;
+  const int cq = lane >> 3, pp = 2 * (lane & 7);
+  double accR0 = 0.0, accR1 = 0.0, accK0 = 0.0, accK1 = 0.0;
+  const long long G = gridDim.x;
+  // copies of chunk m of tile t into ring slot sl (whole warp), one group
+  auto issue = [&](long long t, int m, int sl) {
+    if (t < op.ntiles) {
+      const long long col0 = t * kTile;
+      const int nc = (int)min((long long)kTile, op.ncols - col0);
+      const double* rsrc = r + (col0 + cq) * NZ + m * kChunk + pp;
+      const double* qsrc = FUSED ? q + (col0 + cq) * NZ + m * kChunk + pp : nullptr;
+      double* rdst = Rg + (sl * kTile + cq) * kCS + pp;
+      double* qdst = Qg + (sl * kTile + cq) * kCS + pp;
+#pragma unroll
+      for (int i = 0; i < kTile / 4; ++i) {
+        if (cq + 4 * i < nc) {
+          cp_async16(rdst + 4 * i * kCS, rsrc + 4 * i * NZ);
+          if (FUSED) cp_async16(qdst + 4 * i * kCS, qsrc + 4 * i * NZ);
+        }
+      }
+    }
+    cp_async_commit();
+  };
+  issue(blockIdx.x, 0, 0);
+  for (long long t = blockIdx.x; t < op.ntiles; t += G) {
+    const long long col0 = t * kTile;
+    const int nc = (int)min((long long)kTile, op.ncols - col0);
+    const double* __restrict__ fi =
+        VARY ? op.tinvd + t * NZ * kTile + lane : op.lev + LV_INVD * NZ;
+    const double* __restrict__ fn =
+        VARY ? op.tnphi + t * NZ * kTile + lane : op.lev + LV_NPHI * NZ;
+    double y = 0.0, nprev = 0.0;
+    double ci[kChunk], cn[kChunk], ww[kChunk];
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      ci[j] = __ldg(fi + j * FS);
+      cn[j] = __ldg(fn + j * FS);
+    }
+    // ---- forward sweep
+#pragma unroll 1
+    for (int m = 0; m < NCH; ++m) {
+      const int sl = m & 1;
+      if (m + 1 < NCH)
+        issue(t, m + 1, (m + 1) & 1);
+      else
+        issue(t + G, 0, 0);
+      double ni[kChunk], nn[kChunk];
+      if (m + 1 < NCH) {
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+          ni[j] = __ldg(fi + ((m + 1) * kChunk + j) * FS);
+          nn[j] = __ldg(fn + ((m + 1) * kChunk + j) * FS);
+        }
+      }
+      cp_async_wait<1>();
+      __syncwarp();
+      if (lane < nc) {
+        double* rs = Rg + (sl * kTile + lane) * kCS;
+        const double* qs = Qg + (sl * kTile + lane) * kCS;
+#pragma unroll
+        for (int j = 0; j < kChunk; j += 2) {
+          const double2 rv = lds2(rs + j);
+          double r0 = rv.x, r1 = rv.y;
+          if (FUSED) {
+            const double2 qv = lds2(qs + j);
+            r0 = fma(nalpha, qv.x, r0);
+            r1 = fma(nalpha, qv.y, r1);
+            accR0 = fma(r0, r0, accR0);
+            accR1 = fma(r1, r1, accR1);
+            sts2(rs + j, r0, r1);
+          }
+          y = fma(nprev, y, r0);
+          ww[j] = y * ci[j];
+          if (FUSED) accK0 = fma(y, ww[j], accK0);
+          y = fma(cn[j], y, r1);
+          ww[j + 1] = y * ci[j + 1];
+          if (FUSED) accK1 = fma(y, ww[j + 1], accK1);
+          nprev = cn[j + 1];
+        }
+        if (m + 1 < NCH) {  // the last chunk's w stays in registers for the backward sweep
+#pragma unroll
+          for (int j = 0; j < kChunk; ++j) wsb[(m * kChunk + j) * kTile] = ww[j];
+        }
+      }
+      __syncwarp();
+      if (FUSED) {
+        double* rdst = r + (col0 + cq) * NZ + m * kChunk + pp;
+        const double* rsrc = Rg + (sl * kTile + cq) * kCS + pp;
+#pragma unroll
+        for (int i = 0; i < kTile / 4; ++i)
+          if (cq + 4 * i < nc) st2(rdst + 4 * i * NZ, lds2(rsrc + 4 * i * kCS));
+      }
+      __syncwarp();
+      if (m + 1 < NCH) {
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+          ci[j] = ni[j];
+          cn[j] = nn[j];
+        }
+      }
+    }
+    // ---- backward sweep, chunk by chunk from the top; w of the top chunk is
+    // in registers, the others come back from the scratch region.  Each
+    // finished chunk of z is staged in ring slot 1 (free now: the producer's
+    // next copy went to slot 0) and stored transposed.
+    double* zs = Rg + (kTile + lane) * kCS;
+    double bw[kChunk], bn[kChunk];
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      bw[j] = ww[j];
+      bn[j] = __ldg(fn + ((NCH - 1) * kChunk + j) * FS);
+    }
+    double zz = 0.0;
+#pragma unroll 1
+    for (int c = NCH - 1; c >= 0; --c) {
+      double nw[kChunk], nb[kChunk];
+      if (c > 0 && lane < nc) {
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+          nw[j] = wsb[((c - 1) * kChunk + j) * kTile];
+          nb[j] = __ldg(fn + ((c - 1) * kChunk + j) * FS);
+        }
+      }
+      if (lane < nc) {
+#pragma unroll
+        for (int j = kChunk - 1; j >= 1; j -= 2) {
+          const int k = c * kChunk + j;
+          const double zh = (k == NZ - 1) ? bw[j] : fma(bn[j], zz, bw[j]);
+          zz = fma(bn[j - 1], zh, bw[j - 1]);
+          sts2(zs + j - 1, zz, zh);
+        }
+      }
+      __syncwarp();
+      {
+        double* zdst = z + (col0 + cq) * NZ + c * kChunk + pp;
+        const double* zsrc = Rg + (kTile + cq) * kCS + pp;
+#pragma unroll
+        for (int i = 0; i < kTile / 4; ++i)
+          if (cq + 4 * i < nc) st2(zdst + 4 * i * NZ, lds2(zsrc + 4 * i * kCS));
+      }
+      __syncwarp();
+      if (c > 0) {
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+          bw[j] = nw[j];
+          bn[j] = nb[j];
+        }
+      }
+    }
+  }
+  cp_async_wait<0>();
+  if (FUSED) {
+    double R, K;
+    if (grid_sum2<kTile>(accR0 + accR1, accK0 + accK1, partials, &st->ticket_m, R, K))
+      finish_precond_sweep(st, R, K, hist);
+  }
+}
+
+template <bool FUSED>
+__host__ __device__ inline size_t fixed_smem_bytes() {
+  return sizeof(double) * (FUSED ? 2 : 1) * (size_t)kStages * kTile * kCS;
 }
 
 // Unstaged variant for columns too tall for the shared-memory tile: each
@@ -881,8 +1103,21 @@ cudaError_t run_precond(const Op& op, DevState* st, double* r, const double* q, 
                         double* partials, double* hist, int grid, cudaStream_t s) {
   switch (precond_path(op, r, q, z)) {
     case 0:
-      k_precond_stream<VARY, FUSED><<<grid, kTile, op.stream_smem, s>>>(op, st, r, q, z,
-                                                                       partials, hist);
+      if (op.fixed && op.nz == 128)
+        k_precond_fixed<128, VARY, FUSED><<<grid, kTile, op.fixed_smem, s>>>(
+            op, st, r, q, z, partials, hist);
+      else if (op.fixed && op.nz == 64)
+        k_precond_fixed<64, VARY, FUSED><<<grid, kTile, op.fixed_smem, s>>>(
+            op, st, r, q, z, partials, hist);
+      else if (op.fixed && op.nz == 32)
+        k_precond_fixed<32, VARY, FUSED><<<grid, kTile, op.fixed_smem, s>>>(
+            op, st, r, q, z, partials, hist);
+      else if (op.nz % kChunk == 0)
+        k_precond_stream<VARY, FUSED, true><<<grid, kTile, op.stream_smem, s>>>(
+            op, st, r, q, z, partials, hist);
+      else
+        k_precond_stream<VARY, FUSED, false><<<grid, kTile, op.stream_smem, s>>>(
+            op, st, r, q, z, partials, hist);
       break;
     case 1:
       k_precond_staged<VARY, FUSED><<<grid, kTile, staged_smem(op), s>>>(op, st, r, q, z,
@@ -918,9 +1153,9 @@ cudaError_t prepare_kernels(const Op& op) {
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     size_t stat = 0;
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, k_precond_stream<true, true>) == cudaSuccess)
+    if (cudaFuncGetAttributes(&fa, k_precond_stream<true, true, true>) == cudaSuccess)
       stat = std::max(stat, fa.sharedSizeBytes);
-    if (cudaFuncGetAttributes(&fa, k_precond_stream<false, true>) == cudaSuccess)
+    if (cudaFuncGetAttributes(&fa, k_precond_stream<false, true, false>) == cudaSuccess)
       stat = std::max(stat, fa.sharedSizeBytes);
     g_max_stream_smem = optin - (int)stat;
   }
@@ -931,7 +1166,15 @@ cudaError_t prepare_kernels(const Op& op) {
 #define PCG_SET(V, F)                                             \
   r = set_smem(k_precond_staged<V, F>, b);                        \
   if (r != cudaSuccess) e = r;                                    \
-  r = set_smem(k_precond_stream<V, F>, kMaxStreamSmem);           \
+  r = set_smem(k_precond_fixed<128, V, F>, kMaxStreamSmem);       \
+  if (r != cudaSuccess) e = r;                                    \
+  r = set_smem(k_precond_fixed<64, V, F>, kMaxStreamSmem);        \
+  if (r != cudaSuccess) e = r;                                    \
+  r = set_smem(k_precond_fixed<32, V, F>, kMaxStreamSmem);        \
+  if (r != cudaSuccess) e = r;                                    \
+  r = set_smem(k_precond_stream<V, F, true>, kMaxStreamSmem);     \
+  if (r != cudaSuccess) e = r;                                    \
+  r = set_smem(k_precond_stream<V, F, false>, kMaxStreamSmem);    \
   if (r != cudaSuccess) e = r;
   PCG_SET(false, false) PCG_SET(false, true) PCG_SET(true, false) PCG_SET(true, true)
 #undef PCG_SET
@@ -948,7 +1191,38 @@ int grid_precond(Op& op, int num_sms) {
   int per_sm = 0;
   cudaError_t e = cudaSuccess;
   op.stream_smem = (int)stream_smem_bytes<true>(op.pt);
-  if (staged(op)) {
+  op.fixed_smem = (int)fixed_smem_bytes<true>();
+  if (op.fixed) {
+    // Two warps per sub-partition: eight per SM (the register file allows up
+    // to ten); the shared-memory request is padded so that no ninth fits.
+    int dev = 0, smem_sm = 0, reserved = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    auto occ = [&](int bytes) {
+      int b = 0;
+      cudaError_t r = cudaErrorInvalidValue;
+#define PCG_OCC(NZ)                                                                         \
+  if (op.nz == NZ)                                                                          \
+    r = op.varying                                                                          \
+            ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_precond_fixed<NZ, true, true>, \
+                                                            kTile, bytes)                   \
+            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(                                \
+                  &b, k_precond_fixed<NZ, false, true>, kTile, bytes);
+      PCG_OCC(128) PCG_OCC(64) PCG_OCC(32)
+#undef PCG_OCC
+      return r == cudaSuccess ? b : 0;
+    };
+    per_sm = occ(op.fixed_smem);
+    if (per_sm > 4 && per_sm % 4 != 0) {
+      const int target = per_sm / 4 * 4;
+      const int padded = smem_sm / target - reserved - 256;
+      if (padded > op.fixed_smem && padded <= g_max_stream_smem && occ(padded) == target) {
+        op.fixed_smem = padded;
+        per_sm = target;
+      }
+    }
+  } else if (staged(op)) {
     int dev = 0, smem_sm = 0, reserved = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
@@ -956,9 +1230,9 @@ int grid_precond(Op& op, int num_sms) {
     auto occ = [&](int bytes) {
       int b = 0;
       cudaError_t r = op.varying ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                                       &b, k_precond_stream<true, true>, kTile, bytes)
+                                       &b, k_precond_stream<true, true, true>, kTile, bytes)
                                  : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                                       &b, k_precond_stream<false, true>, kTile, bytes);
+                                       &b, k_precond_stream<false, true, true>, kTile, bytes);
       return r == cudaSuccess ? b : 0;
     };
     per_sm = occ(op.stream_smem);
