@@ -154,8 +154,10 @@ int pcg_precond_dot_noalloc(pcg_ctx* ctx, const double* r_dev, double* z_dev, do
  * pcg_create when ctx is NULL).  Never NULL; owned by the library. */
 const char* pcg_last_error(const pcg_ctx* ctx);
 
-/* Per-kernel timing.  When enabled, pcg_solve records CUDA events around
- * every kernel it launches on the context's stream; pcg_kernel_times then
+/* Per-kernel timing.  When enabled, pcg_solve and pcg_update_coeffs record
+ * CUDA events around the kernels they launch on the context's stream (the
+ * sweeps enqueued after convergence, which return at once, are not counted);
+ * pcg_kernel_times then
  * gives, per kernel kind, the summed device time in milliseconds and the
  * number of launches since the last reset (disabled by default; enabling or
  * disabling resets the counters). */
@@ -166,7 +168,9 @@ typedef enum {
   PCG_K_FINALIZE = 3,      /* deferred x += alpha p */
   PCG_K_APPLY_A = 4,       /* standalone stencil */
   PCG_K_PRECOND = 5,       /* standalone Thomas solve */
-  PCG_K_COUNT = 6
+  PCG_K_SETUP = 6,         /* coefficient set-up kernels of pcg_update_coeffs (face values,
+                              per-cell diagonal and Thomas factors), timed together */
+  PCG_K_COUNT = 7
 } pcg_kernel_kind;
 
 int pcg_enable_timing(pcg_ctx* ctx, int enable);

@@ -15,8 +15,10 @@ LIB = os.path.join(OUT_DIR, "libpcg.so")
 SOURCES = ["pcg_kernels.cu", "pcg_api.cu", "pcg_noalloc.cu"]
 HEADERS = [os.path.join(CSRC, "pcg_internal.h"), os.path.join(ROOT, "include", "pcg.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+# Host code (the per-level tables) is compiled without floating-point
+# contraction, so it rounds like its plain definition on every host.
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
-         "--expt-relaxed-constexpr"]
+         "-Xcompiler", "-ffp-contract=off", "--expt-relaxed-constexpr"]
 
 
 def _nvcc():

@@ -186,15 +186,31 @@ int load_coeffs(pcg_ctx* ctx, const pcg_coeffs* c, bool varying) {
                         cudaMemcpyHostToDevice, ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "upload of a_h_field");
     e = cudaMemsetAsync(&ctx->state->setup_error, 0, sizeof(int), ctx->stream);
+    cudaEvent_t t0 = nullptr, t1 = nullptr;
+    if (ctx->timing) {
+      cudaEventCreate(&t0);
+      cudaEventCreate(&t1);
+      if (t0) cudaEventRecord(t0, ctx->stream);
+    }
     if (e == cudaSuccess) e = pcg::launch_face_coeffs(ctx->op, ctx->faceE, ctx->faceN, ctx->stream);
     if (e == cudaSuccess) e = pcg::launch_cell_diag(ctx->op, ctx->cdiag, ctx->stream);
     if (e == cudaSuccess)
       e = pcg::launch_thomas_factors(ctx->op, ctx->state, ctx->tnphi, ctx->tinvd, ctx->stream);
+    if (t1) cudaEventRecord(t1, ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "coefficient set-up kernels");
     int bad = 0;
     e = cudaMemcpyAsync(&bad, &ctx->state->setup_error, sizeof(int), cudaMemcpyDeviceToHost,
                         ctx->stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+    if (t0 && t1) {
+      float ms = 0.0f;
+      if (e == cudaSuccess && cudaEventElapsedTime(&ms, t0, t1) == cudaSuccess) {
+        ctx->ms[PCG_K_SETUP] += ms;
+        ctx->launches[PCG_K_SETUP] += 3;
+      }
+    }
+    if (t0) cudaEventDestroy(t0);
+    if (t1) cudaEventDestroy(t1);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "coefficient set-up");
     if (bad) return fail(ctx, PCG_EBREAKDOWN, "a Thomas pivot of some column is not positive");
   } else {

@@ -219,6 +219,13 @@ __global__ void k_face_coeffs(Op op, double* __restrict__ faceE, double* __restr
 
 // Diagonal per cell for a_h given per column: h_k*mass + T_{k+1/2} + T_{k-1/2}
 // + h_k * (sum of the four face values), eqs. (8) and (18).
+//
+// The set-up arithmetic is written with explicitly rounded operations (no
+// fused multiply-add): the column systems of strongly graded, strongly
+// anisotropic grids amplify a one-ulp change of a pivot by up to ~1e5 in the
+// solution, so the diagonal and the Thomas pivots are formed exactly as
+// their definition rounds them (product rounded, then sum), the same numbers
+// any plain fp64 evaluation of eq. (19) produces.
 __global__ void k_cell_diag(Op op, double* __restrict__ cdiag) {
   const int nz = op.nz;
   for (long long l = blockIdx.x * (long long)blockDim.x + threadIdx.x; l < op.n;
@@ -227,7 +234,7 @@ __global__ void k_cell_diag(Op op, double* __restrict__ cdiag) {
     const int k = (int)(l - col * nz);
     const Nbr nb = neighbours(op, col);
     const double s = op.faceE[col] + op.faceE[nb.w] + op.faceN[col] + op.faceN[nb.s];
-    cdiag[l] = op.lev[LV_DIAG * nz + k] + op.lev[LV_H * nz + k] * s;
+    cdiag[l] = __dadd_rn(op.lev[LV_DIAG * nz + k], __dmul_rn(op.lev[LV_H * nz + k], s));
   }
 }
 
@@ -245,7 +252,7 @@ __global__ void k_thomas_factors(Op op, DevState* st, double* __restrict__ tnphi
     double nphi_prev = 0.0;
     int bad = 0;
     for (int k = 0; k < nz; ++k) {
-      const double D = op.cdiag[c * nz + k] - op.lev[LV_TDN * nz + k] * nphi_prev;
+      const double D = __dsub_rn(op.cdiag[c * nz + k], __dmul_rn(op.lev[LV_TDN * nz + k], nphi_prev));
       if (!(D > 0.0)) bad = 1;
       const double invd = 1.0 / D;
       const double nphi = op.lev[LV_TUP * nz + k] / D;
@@ -512,6 +519,41 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
+// L2 eviction-priority hints: data read again soon (the w scratch, the
+// Thomas factors the backward sweep reads a second time) is kept, data that
+// streams through once is let go first.
+__device__ __forceinline__ uint64_t l2_keep() {
+  uint64_t p;
+  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_stream() {
+  uint64_t p;
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void cp_async16_hint(void* dst_smem, const void* src, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(
+                   smem_addr(dst_smem)),
+               "l"(src), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void st_hint(double* a, double v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.f64 [%0], %1, %2;" ::"l"(a), "d"(v), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void st2_hint(double* a, double2 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v2.f64 [%0], {%1, %2}, %3;" ::"l"(a), "d"(v.x),
+               "d"(v.y), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ double ld_hint(const double* a, uint64_t pol) {
+  double v;
+  asm volatile("ld.global.L2::cache_hint.f64 %0, [%1], %2;" : "=d"(v) : "l"(a), "l"(pol)
+               : "memory");
+  return v;
+}
+
 __device__ __forceinline__ double2 lds2(const double* p) {
   return *reinterpret_cast<const double2*>(p);
 }
@@ -744,7 +786,11 @@ __global__ void __launch_bounds__(kTile) k_precond_fixed(Op op, DevState* st,
   double* wsb = op.wscratch + (long long)blockIdx.x * NZ * kTile + lane;  // level k at wsb[k*32]
   const double nalpha = FUSED ? -st->alpha : 0.0;
   const int cq = lane >> 3, pp = 2 * (lane & 7);
+  const uint64_t keep = l2_keep(), stream = l2_stream();
   double accR0 = 0.0, accR1 = 0.0, accK0 = 0.0, accK1 = 0.0;
+  // factor loads: per-cell arrays stream through L2 (nphi is read twice);
+  // the per-level table of a constant a_h stays in L1
+  auto ldf = [&](const double* a, uint64_t pol) { return VARY ? ld_hint(a, pol) : __ldg(a); };
   const long long G = gridDim.x;
   // copies of chunk m of tile t into ring slot sl (whole warp), one group
   auto issue = [&](long long t, int m, int sl) {
@@ -758,8 +804,8 @@ __global__ void __launch_bounds__(kTile) k_precond_fixed(Op op, DevState* st,
 #pragma unroll
       for (int i = 0; i < kTile / 4; ++i) {
         if (cq + 4 * i < nc) {
-          cp_async16(rdst + 4 * i * kCS, rsrc + 4 * i * NZ);
-          if (FUSED) cp_async16(qdst + 4 * i * kCS, qsrc + 4 * i * NZ);
+          cp_async16_hint(rdst + 4 * i * kCS, rsrc + 4 * i * NZ, stream);
+          if (FUSED) cp_async16_hint(qdst + 4 * i * kCS, qsrc + 4 * i * NZ, stream);
         }
       }
     }
@@ -777,8 +823,8 @@ __global__ void __launch_bounds__(kTile) k_precond_fixed(Op op, DevState* st,
     double ci[kChunk], cn[kChunk], ww[kChunk];
 #pragma unroll
     for (int j = 0; j < kChunk; ++j) {
-      ci[j] = __ldg(fi + j * FS);
-      cn[j] = __ldg(fn + j * FS);
+      ci[j] = ldf(fi + j * FS, stream);
+      cn[j] = ldf(fn + j * FS, keep);
     }
     // ---- forward sweep
 #pragma unroll 1
@@ -792,8 +838,8 @@ __global__ void __launch_bounds__(kTile) k_precond_fixed(Op op, DevState* st,
       if (m + 1 < NCH) {
 #pragma unroll
         for (int j = 0; j < kChunk; ++j) {
-          ni[j] = __ldg(fi + ((m + 1) * kChunk + j) * FS);
-          nn[j] = __ldg(fn + ((m + 1) * kChunk + j) * FS);
+          ni[j] = ldf(fi + ((m + 1) * kChunk + j) * FS, stream);
+          nn[j] = ldf(fn + ((m + 1) * kChunk + j) * FS, keep);
         }
       }
       cp_async_wait<1>();
@@ -823,7 +869,7 @@ __global__ void __launch_bounds__(kTile) k_precond_fixed(Op op, DevState* st,
         }
         if (m + 1 < NCH) {  // the last chunk's w stays in registers for the backward sweep
 #pragma unroll
-          for (int j = 0; j < kChunk; ++j) wsb[(m * kChunk + j) * kTile] = ww[j];
+          for (int j = 0; j < kChunk; ++j) st_hint(wsb + (m * kChunk + j) * kTile, ww[j], keep);
         }
       }
       __syncwarp();
@@ -832,7 +878,7 @@ __global__ void __launch_bounds__(kTile) k_precond_fixed(Op op, DevState* st,
         const double* rsrc = Rg + (sl * kTile + cq) * kCS + pp;
 #pragma unroll
         for (int i = 0; i < kTile / 4; ++i)
-          if (cq + 4 * i < nc) st2(rdst + 4 * i * NZ, lds2(rsrc + 4 * i * kCS));
+          if (cq + 4 * i < nc) st2_hint(rdst + 4 * i * NZ, lds2(rsrc + 4 * i * kCS), stream);
       }
       __syncwarp();
       if (m + 1 < NCH) {
@@ -852,7 +898,7 @@ __global__ void __launch_bounds__(kTile) k_precond_fixed(Op op, DevState* st,
 #pragma unroll
     for (int j = 0; j < kChunk; ++j) {
       bw[j] = ww[j];
-      bn[j] = __ldg(fn + ((NCH - 1) * kChunk + j) * FS);
+      bn[j] = ldf(fn + ((NCH - 1) * kChunk + j) * FS, stream);
     }
     double zz = 0.0;
 #pragma unroll 1
@@ -861,8 +907,8 @@ __global__ void __launch_bounds__(kTile) k_precond_fixed(Op op, DevState* st,
       if (c > 0 && lane < nc) {
 #pragma unroll
         for (int j = 0; j < kChunk; ++j) {
-          nw[j] = wsb[((c - 1) * kChunk + j) * kTile];
-          nb[j] = __ldg(fn + ((c - 1) * kChunk + j) * FS);
+          nw[j] = ld_hint(wsb + ((c - 1) * kChunk + j) * kTile, stream);
+          nb[j] = ldf(fn + ((c - 1) * kChunk + j) * FS, stream);
         }
       }
       if (lane < nc) {
@@ -880,7 +926,7 @@ __global__ void __launch_bounds__(kTile) k_precond_fixed(Op op, DevState* st,
         const double* zsrc = Rg + (kTile + cq) * kCS + pp;
 #pragma unroll
         for (int i = 0; i < kTile / 4; ++i)
-          if (cq + 4 * i < nc) st2(zdst + 4 * i * NZ, lds2(zsrc + 4 * i * kCS));
+          if (cq + 4 * i < nc) st2_hint(zdst + 4 * i * NZ, lds2(zsrc + 4 * i * kCS), stream);
       }
       __syncwarp();
       if (c > 0) {
@@ -999,6 +1045,23 @@ __global__ void __launch_bounds__(kSpmvThreads) k_spmv_fused(Op op, DevState* st
   }
 }
 
+// True when x is +0.0 (all bits zero) at the cell pair and at every point
+// its stencil reads, so that A x is exactly zero there.
+__device__ __forceinline__ bool x_is_zero2(const Op& op, const double* __restrict__ x,
+                                           long long l, long long col, int k, double2 xc) {
+  const int nz = op.nz;
+  const Nbr nb = neighbours(op, col);
+  unsigned long long bits = __double_as_longlong(xc.x) | __double_as_longlong(xc.y);
+  if (k > 0) bits |= __double_as_longlong(x[l - 1]);
+  if (k + 2 < nz) bits |= __double_as_longlong(x[l + 2]);
+  const double2 e = ld2(x + nb.e * nz + k), w = ld2(x + nb.w * nz + k);
+  const double2 n = ld2(x + nb.n * nz + k), s = ld2(x + nb.s * nz + k);
+  bits |= __double_as_longlong(e.x) | __double_as_longlong(e.y) | __double_as_longlong(w.x) |
+          __double_as_longlong(w.y) | __double_as_longlong(n.x) | __double_as_longlong(n.y) |
+          __double_as_longlong(s.x) | __double_as_longlong(s.y);
+  return bits == 0ull;
+}
+
 // MODE 0: y = A x.  MODE 1: r = b - A x, p = q = 0, and the scalar state of
 // a new solve (alpha = 0, kappa_old = 1: the first sweeps then give p = z_0,
 // q = A z_0).
@@ -1034,7 +1097,13 @@ __global__ void __launch_bounds__(kSpmvThreads) k_stencil(Op op, DevState* st,
       const long long l = g << 1;
       const long long col = l / nz;
       const int k = (int)(l - col * nz);
-      const double2 ax = stencil2<VARY>(op, x, l, col, k, make_double2(0.0, 0.0), ld2(x + l));
+      const double2 xc = ld2(x + l);
+      double2 ax;
+      if (MODE == 1 && x_is_zero2(op, x, l, col, k, xc)) {
+        ax = make_double2(0.0, 0.0);  // A 0 = 0: the common zero initial guess costs no fp64
+      } else {
+        ax = stencil2<VARY>(op, x, l, col, k, make_double2(0.0, 0.0), xc);
+      }
       if (MODE == 0) {
         st2(y + l, ax);
       } else {
