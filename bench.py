@@ -53,8 +53,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=W.HEADLINE, choices=sorted(W.WORKLOADS))
-    ap.add_argument("--cpu-iters", type=int, default=4,
-                    help="PCG iterations of the oracle sample (cpu_baseline / reference)")
+    ap.add_argument("--cpu-iters", type=int, default=None,
+                    help="PCG iterations of one oracle sample (default: 4 for cpu_baseline, "
+                         "2 per step for --impl reference)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--grid", type=int, nargs=3, metavar=("NX", "NY", "NZ"),
@@ -132,6 +133,23 @@ class ClockSampler:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_traffic(kernel, cells):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    when the kernel source has changed since the capture or the size differs."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        src = os.path.join(ROOT, "matrix_free_pcg_gb300", "csrc", "pcg_kernels.cu")
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+    except (OSError, ValueError):
+        return None
+    if t.get("kernel_source_sha256") != sha or t.get("full_cells") != cells or kernel not in t:
+        return None
+    return t[kernel]["bytes_per_launch"]
 
 
 def workload_inputs(w):
@@ -269,12 +287,7 @@ def run_ours(args, w):
     alu_peak = FP64_LANES_PER_SM_CLK * nsm * sm_mhz * 1e6 / 1e9  # G fp64 ops / s
     alu_ach = ops_cell * n / avg_s / 1e9
     hbm_ach = bytes_cell * n / avg_s / 1e9
-    traffic = None
-    try:
-        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            traffic = json.load(f).get(dom)
-    except (OSError, ValueError):
-        traffic = None
+    traffic = measured_traffic(dom, n)
     roofline = {
         "bound": "alu", "kernel": dom, "achieved": alu_ach, "peak": alu_peak,
         "unit": "G fp64 ops/s", "frac": alu_ach / alu_peak, "traffic": traffic,
@@ -351,6 +364,8 @@ def run_ours(args, w):
 
 def main():
     args = parse()
+    if args.cpu_iters is None:
+        args.cpu_iters = 2 if args.impl == "reference" else 4
     w = W.WORKLOADS[args.workload]
     if args.grid:
         import dataclasses
