@@ -135,6 +135,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def reduce_over_ranks(ms, iters, device):
+    """(max over ranks of the timed milliseconds, sum over ranks of the
+    iterations).  Every rank solves its own copy of the workload (replicas),
+    so the job's throughput is the summed work over the slowest rank's time."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(ms), float(iters)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    n = torch.tensor([float(iters)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(n.item())
+
+
 def measured_traffic(kernel, cells):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
     when the kernel source has changed since the capture or the size differs."""
@@ -255,16 +270,7 @@ def run_ours(args, w):
     ms = e0.elapsed_time(e1)
     ktimes = solver.kernel_times()
     solver.enable_timing(False)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms, float(sum(iters))], dtype=torch.float64, device=dev)
-        tmax = t[:1].clone()
-        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
-        tsum = t[1:].clone()
-        dist.all_reduce(tsum, op=dist.ReduceOp.SUM)
-        ms_max, total_iters = float(tmax.item()), float(tsum.item())
-    else:
-        ms_max, total_iters = ms, float(sum(iters))
+    ms_max, total_iters = reduce_over_ranks(ms, sum(iters), dev)
     value = total_iters / (ms_max * 1e-3)
 
     n = w.n
@@ -318,12 +324,8 @@ def run_ours(args, w):
             e2e_it += it
         torch.cuda.synchronize()
         t_e2e = time.perf_counter() - t0
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            t_e2e = float(t.item())
-        e2e = {"value": e2e_it * world / t_e2e, "unit": UNIT,
+        t_e2e_ms, e2e_iters = reduce_over_ranks(1e3 * t_e2e, e2e_it, dev)
+        e2e = {"value": e2e_iters / (1e-3 * t_e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": 2 * 8 * n, "d2h_bytes_per_step": 8 * n,
                "api": "pcg_solve_host", "steps": nbuf - 1}
         del xs, bh
