@@ -58,6 +58,8 @@ def parse():
                          "2 per step for --impl reference)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layout", choices=["column", "tiled"], default="column",
+                    help="layout of the solver's internal vectors")
     ap.add_argument("--grid", type=int, nargs=3, metavar=("NX", "NY", "NZ"),
                     help="same coefficients on another grid size (profiling captures)")
     return ap.parse_args()
@@ -234,6 +236,7 @@ def run_ours(args, w):
     x = torch.zeros_like(bd)
     stream = torch.cuda.current_stream(dev)
     solver.set_stream(stream)
+    solver.set_layout(args.layout)
 
     def step():
         solver.update_coeffs(**coeffs)
@@ -349,6 +352,7 @@ def run_ours(args, w):
                        "rtol": w.rtol, "iters_per_step": iters[0], "a_v": w.a_v,
                        "graded": w.graded, "varying_ah": varying,
                        "l2": "inputs larger than L2 (1.07 GB per vector)",
+                       "layout": args.layout,
                        "parallelism": "replicas" if world > 1 else "single"},
             "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / hbm_peak,
             "bytes_per_cell_iter": bytes_iter / n, "fp64_ops_per_cell_iter": ops_iter / n,

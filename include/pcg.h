@@ -93,6 +93,22 @@ int pcg_update_coeffs(pcg_ctx* ctx, const pcg_coeffs* coeffs);
  * all later work of this context. */
 int pcg_set_stream(pcg_ctx* ctx, void* stream);
 
+/* Layout of the solver's internal vectors (r, z, p, q and a copy of the
+ * iterate) during pcg_solve.  The caller's vectors always keep the
+ * column-contiguous layout of this header.
+ *   PCG_LAYOUT_COLUMN  vertical index fastest, like the caller's vectors
+ *                      (default; section 3 eq. (10)).
+ *   PCG_LAYOUT_TILED   horizontal index fastest within tiles of 32
+ *                      consecutive columns: cell (column c, level k) at
+ *                      (c/32*nz + k)*32 + c%32, the GPU layout of the paper
+ *                      (section 6.1, eq. (22)) in blocked form.  b and x are
+ *                      converted at the start and the end of each solve; the
+ *                      context then holds two more vectors (one if a_h is
+ *                      constant).
+ * Synchronous.  Errors: PCG_EINVAL (unknown layout), PCG_ENOMEM, PCG_ECUDA. */
+enum { PCG_LAYOUT_COLUMN = 0, PCG_LAYOUT_TILED = 1 };
+int pcg_set_layout(pcg_ctx* ctx, int layout);
+
 /* y = A x, the matrix-free 7-point stencil of eq. (18), standalone.
  * x_dev, y_dev: device, N values each, must not overlap.  Asynchronous. */
 int pcg_apply_A(pcg_ctx* ctx, const double* x_dev, double* y_dev);

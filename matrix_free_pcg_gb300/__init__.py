@@ -31,7 +31,8 @@ PCG_K_COUNT = len(KERNEL_KINDS)
 EXPORTED = ["pcg_create", "pcg_destroy", "pcg_update_coeffs", "pcg_set_stream", "pcg_apply_A",
             "pcg_precond", "pcg_solve", "pcg_solve_host", "pcg_last_error",
             "pcg_enable_timing", "pcg_kernel_times", "pcg_launch_info",
-            "pcg_precond_dot_noalloc"]
+            "pcg_precond_dot_noalloc", "pcg_set_layout"]
+PCG_LAYOUT_COLUMN, PCG_LAYOUT_TILED = 0, 1
 
 
 class pcg_coeffs(ctypes.Structure):
@@ -67,6 +68,7 @@ def _load(path=LIB_PATH):
                                            ctypes.POINTER(ctypes.c_int),
                                            ctypes.POINTER(ctypes.c_longlong)]),
         "pcg_precond_dot_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
+        "pcg_set_layout": (ctypes.c_int, [_vp, ctypes.c_int]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -171,6 +173,11 @@ def pcg_set_stream(ctx, stream):
     return _check(_lib.pcg_set_stream(ctx, ctypes.c_void_p(handle or 0)), ctx)
 
 
+def pcg_set_layout(ctx, layout):
+    """PCG_LAYOUT_COLUMN (default) or PCG_LAYOUT_TILED for the solver's internal vectors."""
+    return _check(_lib.pcg_set_layout(ctx, int(layout)), ctx)
+
+
 def pcg_apply_A(ctx, n, x, y):
     return _check(_lib.pcg_apply_A(ctx, _dev_ptr(x, n, "x"), _dev_ptr(y, n, "y")), ctx)
 
@@ -273,6 +280,12 @@ class Solver:
 
     def set_stream(self, stream):
         pcg_set_stream(self.ctx, stream)
+
+    def set_layout(self, layout):
+        """"column" / PCG_LAYOUT_COLUMN or "tiled" / PCG_LAYOUT_TILED."""
+        if isinstance(layout, str):
+            layout = {"column": PCG_LAYOUT_COLUMN, "tiled": PCG_LAYOUT_TILED}[layout]
+        pcg_set_layout(self.ctx, layout)
 
     def apply_A(self, x, y=None):
         import torch

@@ -44,6 +44,9 @@ struct pcg_ctx {
   double *lev = nullptr, *ah = nullptr, *faceE = nullptr, *faceN = nullptr;
   double *cdiag = nullptr, *tnphi = nullptr, *tinvd = nullptr;
   double *partials = nullptr, *hist = nullptr, *wscratch = nullptr;
+  int layout = PCG_LAYOUT_COLUMN;       // layout of the solver's internal vectors
+  double *u_t = nullptr, *cdiag_t = nullptr;  // row-tiled layout: iterate, diagonal
+  int grid_t = 1;
   int hist_cap = 0;
   DevState* state = nullptr;
   double *b_host_api = nullptr, *x_host_api = nullptr;  // device copies for pcg_solve_host
@@ -162,7 +165,7 @@ void free_all(pcg_ctx* ctx) {
   double* bufs[] = {ctx->r,     ctx->z,     ctx->p,     ctx->q,        ctx->lev,
                     ctx->ah,    ctx->faceE, ctx->faceN, ctx->cdiag,    ctx->tnphi,
                     ctx->tinvd, ctx->partials, ctx->hist, ctx->b_host_api, ctx->x_host_api,
-                    ctx->wscratch};
+                    ctx->wscratch, ctx->u_t, ctx->cdiag_t};
   for (double* b : bufs)
     if (b) cudaFree(b);
   if (ctx->state) cudaFree(ctx->state);
@@ -196,6 +199,8 @@ int load_coeffs(pcg_ctx* ctx, const pcg_coeffs* c, bool varying) {
     if (e == cudaSuccess) e = pcg::launch_cell_diag(ctx->op, ctx->cdiag, ctx->stream);
     if (e == cudaSuccess)
       e = pcg::launch_thomas_factors(ctx->op, ctx->state, ctx->tnphi, ctx->tinvd, ctx->stream);
+    if (e == cudaSuccess && ctx->cdiag_t)
+      e = pcg::launch_to_tiled(ctx->op, ctx->cdiag, ctx->cdiag_t, ctx->stream);
     if (t1) cudaEventRecord(t1, ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "coefficient set-up kernels");
     int bad = 0;
@@ -286,10 +291,19 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
   ctx->last_launches = 0;
   ctx->events.clear();
   ctx->pool_used = 0;
+  const bool tiled = ctx->layout == PCG_LAYOUT_TILED;
+  // The row-tiled layout forms r = b - A x0 column-contiguously in z, then
+  // converts r and x0 into the solver's layout.
   e = timed(ctx, PCG_K_RESIDUAL, [&] {
-    return pcg::launch_residual(op, ctx->state, b, x, ctx->r, ctx->p, ctx->q, rtol, maxit,
-                                ctx->grid_a, s);
+    return pcg::launch_residual(op, ctx->state, b, x, tiled ? ctx->z : ctx->r, ctx->p, ctx->q,
+                                rtol, maxit, ctx->grid_a, s);
   });
+  if (e == cudaSuccess && tiled) {
+    e = timed(ctx, PCG_K_RESIDUAL, [&] { return pcg::launch_to_tiled(op, ctx->z, ctx->r, s); });
+    if (e == cudaSuccess)  // x0 -> u, and p = q = 0 at the row-tiled positions
+      e = timed(ctx, PCG_K_RESIDUAL,
+                [&] { return pcg::launch_to_tiled(op, x, ctx->u_t, s, ctx->p, ctx->q); });
+  }
   if (e != cudaSuccess) return cuda_fail(ctx, e, "residual kernel launch");
 
   // Enqueue the loop in batches; poll the device's `done` flag one batch
@@ -303,14 +317,18 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
     const int nb = std::min(batch, maxit + 1 - enq);
     for (int i = 0; i < nb; ++i) {
       e = timed(ctx, PCG_K_PRECOND_FUSED, [&] {
-        return pcg::launch_precond_fused(op, ctx->state, ctx->r, ctx->q, ctx->z, ctx->partials,
-                                         ctx->hist, ctx->grid_m, s);
+        return tiled ? pcg::launch_precond_tiled(op, ctx->state, ctx->r, ctx->q, ctx->z,
+                                                 ctx->partials, ctx->hist, ctx->grid_t, s)
+                     : pcg::launch_precond_fused(op, ctx->state, ctx->r, ctx->q, ctx->z,
+                                                 ctx->partials, ctx->hist, ctx->grid_m, s);
       });
       if (e != cudaSuccess) return cuda_fail(ctx, e, "preconditioner sweep launch");
       if (enq + i < maxit) {
         e = timed(ctx, PCG_K_SPMV_FUSED, [&] {
-          return pcg::launch_spmv_fused(op, ctx->state, ctx->z, x, ctx->p, ctx->q,
-                                        ctx->partials + 2 * ctx->grid_m, ctx->grid_a, s);
+          return tiled ? pcg::launch_spmv_tiled(op, ctx->state, ctx->z, ctx->u_t, ctx->p, ctx->q,
+                                                ctx->partials + 2 * ctx->grid_t, ctx->grid_t, s)
+                       : pcg::launch_spmv_fused(op, ctx->state, ctx->z, x, ctx->p, ctx->q,
+                                                ctx->partials + 2 * ctx->grid_m, ctx->grid_a, s);
         });
         if (e != cudaSuccess) return cuda_fail(ctx, e, "SpMV sweep launch");
       }
@@ -328,8 +346,10 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
     pending = slot;
     slot ^= 1;
   }
-  e = timed(ctx, PCG_K_FINALIZE,
-            [&] { return pcg::launch_finalize(op, ctx->state, x, ctx->p, ctx->grid_a, s); });
+  e = timed(ctx, PCG_K_FINALIZE, [&] {
+    return tiled ? pcg::launch_from_tiled(op, ctx->state, ctx->u_t, ctx->p, x, s)
+                 : pcg::launch_finalize(op, ctx->state, x, ctx->p, ctx->grid_a, s);
+  });
   if (e != cudaSuccess) return cuda_fail(ctx, e, "finalize launch");
   e = cudaMemcpyAsync(&ctx->pinned[2], ctx->state, sizeof(DevState), cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
@@ -405,10 +425,12 @@ int pcg_create(int nx, int ny, int nz, const pcg_coeffs* coeffs, pcg_ctx** out) 
     g_create_error = msg;
     return status;
   };
-  e = dalloc(&ctx->r, n);
-  if (e == cudaSuccess) e = dalloc(&ctx->z, n);
-  if (e == cudaSuccess) e = dalloc(&ctx->p, n);
-  if (e == cudaSuccess) e = dalloc(&ctx->q, n);
+  // internal vectors are sized for the row-tiled layout too (last tile padded)
+  const long long npad = op.ntiles * pcg::kTile * nz;
+  e = dalloc(&ctx->r, npad);
+  if (e == cudaSuccess) e = dalloc(&ctx->z, npad);
+  if (e == cudaSuccess) e = dalloc(&ctx->p, npad);
+  if (e == cudaSuccess) e = dalloc(&ctx->q, npad);
   if (e == cudaSuccess) e = dalloc(&ctx->lev, (size_t)pcg::kLevCount * nz);
   if (e == cudaSuccess) e = dalloc(&ctx->state, 1);
   if (e == cudaSuccess) e = cudaMemset(ctx->state, 0, sizeof(DevState));
@@ -439,7 +461,9 @@ int pcg_create(int nx, int ny, int nz, const pcg_coeffs* coeffs, pcg_ctx** out) 
   if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "kernel attribute set-up"));
   ctx->grid_m = pcg::grid_precond(op, ctx->num_sms);  // also sets op.stream_smem
   ctx->grid_a = pcg::grid_spmv(op, ctx->num_sms);
-  e = dalloc(&ctx->partials, 2 * (size_t)(ctx->grid_m + ctx->grid_a));
+  ctx->grid_t = pcg::grid_tiled(op, ctx->num_sms);
+  e = dalloc(&ctx->partials,
+             2 * (size_t)std::max(ctx->grid_m + ctx->grid_a, 2 * ctx->grid_t));
   if (e == cudaSuccess && op.fixed)
     e = dalloc(&ctx->wscratch, (size_t)ctx->grid_m * pcg::kTile * nz);
   if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "workspace allocation"));
@@ -469,6 +493,27 @@ int pcg_update_coeffs(pcg_ctx* ctx, const pcg_coeffs* coeffs) {
   DeviceGuard g(ctx->device);
   if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
   return load_coeffs(ctx, coeffs, varying);
+}
+
+int pcg_set_layout(pcg_ctx* ctx, int layout) {
+  if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
+  if (layout != PCG_LAYOUT_COLUMN && layout != PCG_LAYOUT_TILED)
+    return fail(ctx, PCG_EINVAL, "unknown layout %d", layout);
+  if (layout == ctx->layout) return PCG_OK;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
+  cudaError_t e = cudaStreamSynchronize(ctx->stream);
+  const long long npad = ctx->op.ntiles * pcg::kTile * ctx->op.nz;
+  if (e == cudaSuccess && layout == PCG_LAYOUT_TILED && !ctx->u_t) e = dalloc(&ctx->u_t, npad);
+  if (e == cudaSuccess && layout == PCG_LAYOUT_TILED && ctx->has_field_buffers && !ctx->cdiag_t) {
+    e = dalloc(&ctx->cdiag_t, npad);
+    ctx->op.cdiag_t = ctx->cdiag_t;
+    if (e == cudaSuccess) e = pcg::launch_to_tiled(ctx->op, ctx->cdiag, ctx->cdiag_t, ctx->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+  }
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "layout change");
+  ctx->layout = layout;
+  return PCG_OK;
 }
 
 int pcg_set_stream(pcg_ctx* ctx, void* stream) {

@@ -38,6 +38,7 @@ struct Op {
   int fixed;           // 1: nz is 32, 64 or 128 and the height-specialised sweep is used
   int fixed_smem;      // dynamic shared memory of the height-specialised sweep
   double* wscratch;    // height-specialised sweep: 32*nz doubles per block (grid_precond blocks)
+  const double* cdiag_t; // field, row-tiled solver layout: diagonal per cell, row-tiled
   long long ncols;     // nx*ny
   long long n;         // ncols*nz
   long long ntiles;    // ceil(ncols / kTile)
@@ -102,6 +103,21 @@ cudaError_t launch_finalize(const Op& op, const DevState* st, double* x, const d
 constexpr long long kNoallocMaxTiles = 65536;
 cudaError_t launch_precond_dot_noalloc(const Op& op, const double* r, double* z, double* rz,
                                        int num_sms, cudaStream_t s);
+
+// Row-tiled solver layout (cell (c,k) at (c/32*nz + k)*32 + c%32).
+// zero1/zero2 (optional) are cleared at the same row-tiled positions.  Row-tiled
+// vectors hold ntiles*32*nz values (the last tile padded to 32 columns).
+cudaError_t launch_to_tiled(const Op& op, const double* src_k, double* dst_t, cudaStream_t s,
+                            double* zero1 = nullptr, double* zero2 = nullptr);
+// dst_k = src_t + alpha p_t (alpha from the device state), or a copy when p_t is NULL.
+cudaError_t launch_from_tiled(const Op& op, const DevState* st, const double* src_t,
+                              const double* p_t, double* dst_k, cudaStream_t s);
+cudaError_t launch_precond_tiled(const Op& op, DevState* st, double* r, const double* q,
+                                 double* z, double* partials, double* hist, int grid,
+                                 cudaStream_t s);
+cudaError_t launch_spmv_tiled(const Op& op, DevState* st, const double* z, double* u, double* p,
+                              double* q, double* partials, int grid, cudaStream_t s);
+int grid_tiled(const Op& op, int num_sms);
 
 // Occupancy-derived grid sizes (blocks) for the persistent sweeps.  The
 // preconditioner's also fixes op.stream_smem (see pcg_kernels.cu).

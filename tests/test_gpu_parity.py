@@ -91,13 +91,15 @@ SOLVE_CASES = [
 ]
 
 
+@pytest.mark.parametrize("layout", ["column", "tiled"])
 @pytest.mark.parametrize("cfg", SOLVE_CASES, ids=lambda c: "x".join(map(str, c[:3])))
-def test_solve_matches_oracle(cfg):
+def test_solve_matches_oracle(cfg, layout):
     nx, ny, nz, varying, graded, a_v = cfg
     prob, kw, b = case(nx, ny, nz, varying, graded, a_v=a_v, seed=3)
     x_ref, it_ref, hist_ref, st_ref = oracle.pcg(prob, b, rtol=1e-10, maxit=500)
     assert st_ref == oracle.OK
     with mf.Solver(nx, ny, nz, **kw) as s:
+        s.set_layout(layout)
         bd = torch.from_numpy(b).to(DEV)
         x = torch.zeros_like(bd)
         iters, hist, st = s.solve(bd, x, rtol=1e-10, maxit=500)
@@ -113,9 +115,11 @@ def test_solve_matches_oracle(cfg):
     assert np.linalg.norm(xs - x_ref) <= SOL_TOL * np.linalg.norm(x_ref)
 
 
-def test_solve_is_bitwise_repeatable():
+@pytest.mark.parametrize("layout", ["column", "tiled"])
+def test_solve_is_bitwise_repeatable(layout):
     prob, kw, b = case(40, 36, 64, True, True, a_v=1e4, seed=5)
     with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        s.set_layout(layout)
         bd = torch.from_numpy(b).to(DEV)
         x1, x2 = torch.zeros_like(bd), torch.zeros_like(bd)
         i1, h1, _ = s.solve(bd, x1, rtol=1e-10)
@@ -141,9 +145,11 @@ def test_solve_host_equals_solve_device():
     assert np.array_equal(xh.numpy(), xn)
 
 
-def test_status_semantics_match_oracle():
+@pytest.mark.parametrize("layout", ["column", "tiled"])
+def test_status_semantics_match_oracle(layout):
     prob, kw, b = case(20, 18, 16, True, True, a_v=1e3, seed=7)
     with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        s.set_layout(layout)
         bd = torch.from_numpy(b).to(DEV)
         _, it_ref, _, _ = oracle.pcg(prob, b, rtol=1e-8)
         x = torch.zeros_like(bd)
@@ -230,3 +236,21 @@ def test_kernel_timing_counts_launches():
     worked = sum(v[1] for v in t.values())
     assert worked <= info["last_solve_launches"] <= worked + 2 * 2 * 16
     assert all(v[0] >= 0 for v in t.values())
+
+
+def test_layouts_agree_and_switch_back_and_forth():
+    prob, kw, b = case(45, 33, 64, True, True, a_v=1e4, seed=12)
+    with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        bd = torch.from_numpy(b).to(DEV)
+        xs = {}
+        for layout in ["tiled", "column", "tiled"]:
+            s.set_layout(layout)
+            x = torch.zeros_like(bd)
+            it, hist, st = s.solve(bd, x, rtol=0.0, maxit=12)
+            assert (it, st) == (12, mf.PCG_OK)
+            xs.setdefault(layout, []).append(x.cpu().numpy())
+        with pytest.raises(mf.PCGError):
+            mf.pcg_set_layout(s.ctx, 7)
+    assert np.array_equal(xs["tiled"][0], xs["tiled"][1])
+    xc, xt = xs["column"][0], xs["tiled"][0]
+    assert np.linalg.norm(xt - xc) <= 1e-12 * np.linalg.norm(xc)

@@ -59,14 +59,17 @@ def test_workload_full_solve_parity(name):
     assert st_ref == oracle.OK
     with mf.Solver(w.nx, w.ny, w.nz, **kw) as s:
         bd = sampled_operator_checks(w, prob, s, b)
-        x = torch.zeros_like(bd)
-        iters, hist, st = s.solve(bd, x, rtol=w.rtol, maxit=w.maxit)
-        assert st == mf.PCG_OK and abs(iters - it_ref) <= 1, (iters, it_ref)
-        x.zero_()
-        it2, _, st2 = s.solve(bd, x, rtol=0.0, maxit=it_ref)
-        assert (it2, st2) == (it_ref, mf.PCG_OK)
-        xs = x.cpu().numpy()
-    assert np.linalg.norm(xs - x_ref) <= 1e-8 * np.linalg.norm(x_ref)
+        for layout in ["column", "tiled"]:
+            s.set_layout(layout)
+            x = torch.zeros_like(bd)
+            iters, hist, st = s.solve(bd, x, rtol=w.rtol, maxit=w.maxit)
+            assert st == mf.PCG_OK and abs(iters - it_ref) <= 1, (layout, iters, it_ref)
+            x.zero_()
+            it2, _, st2 = s.solve(bd, x, rtol=0.0, maxit=it_ref)
+            assert (it2, st2) == (it_ref, mf.PCG_OK)
+            xs = x.cpu().numpy()
+            assert np.linalg.norm(xs - x_ref) <= 1e-8 * np.linalg.norm(x_ref), layout
+        s.set_layout("column")
     if w.rhs == "manufactured":
         # the manufactured solution comes back to 1e-9 with a tight tolerance
         with mf.Solver(w.nx, w.ny, w.nz, **kw) as s:
@@ -86,10 +89,13 @@ def test_workload_large_parity(name, fixed_iters):
     with mf.Solver(w.nx, w.ny, w.nz, **kw) as s:
         bd = sampled_operator_checks(w, prob, s, b)
         x = torch.zeros_like(bd)
-        it, _, st = s.solve(bd, x, rtol=0.0, maxit=fixed_iters)
-        assert (it, st) == (fixed_iters, mf.PCG_OK)
-        xs = x.cpu().numpy()
-        assert np.linalg.norm(xs - x_ref) <= 1e-8 * np.linalg.norm(x_ref)
+        for layout in ["tiled", "column"]:
+            s.set_layout(layout)
+            x.zero_()
+            it, _, st = s.solve(bd, x, rtol=0.0, maxit=fixed_iters)
+            assert (it, st) == (fixed_iters, mf.PCG_OK)
+            xs = x.cpu().numpy()
+            assert np.linalg.norm(xs - x_ref) <= 1e-8 * np.linalg.norm(x_ref), layout
         del xs, x_ref
         # the workload's own stopping rule, then the true residual on the CPU
         x.zero_()
