@@ -12,8 +12,9 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libpcg.so")
-SOURCES = ["pcg_kernels.cu", "pcg_api.cu", "pcg_noalloc.cu"]
-HEADERS = [os.path.join(CSRC, "pcg_internal.h"), os.path.join(ROOT, "include", "pcg.h")]
+SOURCES = ["pcg_kernels.cu", "pcg_tiled.cu", "pcg_api.cu", "pcg_noalloc.cu"]
+HEADERS = [os.path.join(CSRC, "pcg_internal.h"), os.path.join(CSRC, "pcg_device.cuh"),
+           os.path.join(ROOT, "include", "pcg.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # Host code (the per-level tables) is compiled without floating-point
 # contraction, so it rounds like its plain definition on every host.

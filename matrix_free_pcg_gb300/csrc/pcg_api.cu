@@ -46,7 +46,7 @@ struct pcg_ctx {
   double *partials = nullptr, *hist = nullptr, *wscratch = nullptr;
   int layout = PCG_LAYOUT_COLUMN;       // layout of the solver's internal vectors
   double *u_t = nullptr, *cdiag_t = nullptr;  // row-tiled layout: iterate, diagonal
-  int grid_t = 1;
+  int grid_tm = 1, grid_ta = 1;  // row-tiled preconditioner / stencil sweeps
   int hist_cap = 0;
   DevState* state = nullptr;
   double *b_host_api = nullptr, *x_host_api = nullptr;  // device copies for pcg_solve_host
@@ -318,7 +318,7 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
     for (int i = 0; i < nb; ++i) {
       e = timed(ctx, PCG_K_PRECOND_FUSED, [&] {
         return tiled ? pcg::launch_precond_tiled(op, ctx->state, ctx->r, ctx->q, ctx->z,
-                                                 ctx->partials, ctx->hist, ctx->grid_t, s)
+                                                 ctx->partials, ctx->hist, ctx->grid_tm, s)
                      : pcg::launch_precond_fused(op, ctx->state, ctx->r, ctx->q, ctx->z,
                                                  ctx->partials, ctx->hist, ctx->grid_m, s);
       });
@@ -326,7 +326,7 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
       if (enq + i < maxit) {
         e = timed(ctx, PCG_K_SPMV_FUSED, [&] {
           return tiled ? pcg::launch_spmv_tiled(op, ctx->state, ctx->z, ctx->u_t, ctx->p, ctx->q,
-                                                ctx->partials + 2 * ctx->grid_t, ctx->grid_t, s)
+                                                ctx->partials + 2 * ctx->grid_tm, ctx->grid_ta, s)
                        : pcg::launch_spmv_fused(op, ctx->state, ctx->z, x, ctx->p, ctx->q,
                                                 ctx->partials + 2 * ctx->grid_m, ctx->grid_a, s);
         });
@@ -461,9 +461,10 @@ int pcg_create(int nx, int ny, int nz, const pcg_coeffs* coeffs, pcg_ctx** out) 
   if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "kernel attribute set-up"));
   ctx->grid_m = pcg::grid_precond(op, ctx->num_sms);  // also sets op.stream_smem
   ctx->grid_a = pcg::grid_spmv(op, ctx->num_sms);
-  ctx->grid_t = pcg::grid_tiled(op, ctx->num_sms);
+  ctx->grid_tm = pcg::grid_tiled_precond(op, ctx->num_sms);
+  ctx->grid_ta = pcg::grid_tiled_spmv(op, ctx->num_sms);
   e = dalloc(&ctx->partials,
-             2 * (size_t)std::max(ctx->grid_m + ctx->grid_a, 2 * ctx->grid_t));
+             2 * (size_t)std::max(ctx->grid_m + ctx->grid_a, ctx->grid_tm + ctx->grid_ta));
   if (e == cudaSuccess && op.fixed)
     e = dalloc(&ctx->wscratch, (size_t)ctx->grid_m * pcg::kTile * nz);
   if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "workspace allocation"));
@@ -632,8 +633,9 @@ int pcg_kernel_times(pcg_ctx* ctx, double* ms_out, long long* launches_out) {
 int pcg_launch_info(const pcg_ctx* ctx, int* grid_precond, int* grid_spmv,
                     long long* last_solve_launches) {
   if (!ctx) return PCG_EINVAL;
-  if (grid_precond) *grid_precond = ctx->grid_m;
-  if (grid_spmv) *grid_spmv = ctx->grid_a;
+  const bool tiled = ctx->layout == PCG_LAYOUT_TILED;
+  if (grid_precond) *grid_precond = tiled ? ctx->grid_tm : ctx->grid_m;
+  if (grid_spmv) *grid_spmv = tiled ? ctx->grid_ta : ctx->grid_a;
   if (last_solve_launches) *last_solve_launches = ctx->last_launches;
   return PCG_OK;
 }

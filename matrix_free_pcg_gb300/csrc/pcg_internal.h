@@ -1,5 +1,5 @@
 // Internal declarations shared by the host driver (pcg_api.cu) and the
-// kernels (pcg_kernels.cu).  Not part of the public ABI (include/pcg.h).
+// kernel files (pcg_kernels.cu, pcg_tiled.cu, pcg_noalloc.cu).  Not part of the public ABI (include/pcg.h).
 #pragma once
 
 #include <cstdint>
@@ -104,7 +104,7 @@ constexpr long long kNoallocMaxTiles = 65536;
 cudaError_t launch_precond_dot_noalloc(const Op& op, const double* r, double* z, double* rz,
                                        int num_sms, cudaStream_t s);
 
-// Row-tiled solver layout (cell (c,k) at (c/32*nz + k)*32 + c%32).
+// Row-tiled solver layout (pcg_tiled.cu): cell (c,k) at (c/32*nz + k)*32 + c%32.
 // zero1/zero2 (optional) are cleared at the same row-tiled positions.  Row-tiled
 // vectors hold ntiles*32*nz values (the last tile padded to 32 columns).
 cudaError_t launch_to_tiled(const Op& op, const double* src_k, double* dst_t, cudaStream_t s,
@@ -117,7 +117,9 @@ cudaError_t launch_precond_tiled(const Op& op, DevState* st, double* r, const do
                                  cudaStream_t s);
 cudaError_t launch_spmv_tiled(const Op& op, DevState* st, const double* z, double* u, double* p,
                               double* q, double* partials, int grid, cudaStream_t s);
-int grid_tiled(const Op& op, int num_sms);
+// Grid sizes (blocks) of the two row-tiled sweeps.
+int grid_tiled_precond(const Op& op, int num_sms);
+int grid_tiled_spmv(const Op& op, int num_sms);
 
 // Occupancy-derived grid sizes (blocks) for the persistent sweeps.  The
 // preconditioner's also fixes op.stream_smem (see pcg_kernels.cu).

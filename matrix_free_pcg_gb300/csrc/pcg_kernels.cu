@@ -24,43 +24,10 @@
 #include <cstdint>
 
 #include "pcg_internal.h"
+#include "pcg_device.cuh"
 
 namespace pcg {
 namespace {
-
-constexpr int kStOK = 0, kStNotConv = 4, kStBreakdown = 5, kStTimeout = 6;
-
-__device__ __forceinline__ double2 ld2(const double* p) {
-  return *reinterpret_cast<const double2*>(p);
-}
-__device__ __forceinline__ double2 ldg2(const double* p) {
-  return __ldg(reinterpret_cast<const double2*>(p));
-}
-__device__ __forceinline__ void st2(double* p, double2 v) {
-  *reinterpret_cast<double2*>(p) = v;
-}
-__device__ __forceinline__ int ld_done(const DevState* st) {
-  return *reinterpret_cast<const volatile int*>(&st->done);
-}
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// Horizontal neighbours of a column, periodic in i and j.
-struct Nbr {
-  long long e, w, n, s;
-};
-__device__ __forceinline__ Nbr neighbours(const Op& op, long long col) {
-  const long long j = col / op.nx;
-  const int i = (int)(col - j * op.nx);
-  Nbr nb;
-  nb.e = (i == op.nx - 1) ? col - (op.nx - 1) : col + 1;
-  nb.w = (i == 0) ? col + (op.nx - 1) : col - 1;
-  nb.n = (j == op.ny - 1) ? col - (long long)(op.ny - 1) * op.nx : col + op.nx;
-  nb.s = (j == 0) ? col + (long long)(op.ny - 1) * op.nx : col - op.nx;
-  return nb;
-}
 
 // acc + (A z) at the two cells l, l+1 of one column (k even, k+1 < nz),
 // eq. (18).  zc = (z[l], z[l+1]).  The vertical neighbours outside the column
@@ -137,73 +104,6 @@ __device__ __forceinline__ double stencil1(const Op& op, const double* __restric
   a = fma(__ldg(lev + LV_UP * nz + k), zu, a);
   a = fma(__ldg(lev + LV_DN * nz + k), zd, a);
   return fma(__ldg(lev + LV_HW * nz + k), hs, a);
-}
-
-__device__ __forceinline__ double warp_sum(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// Deterministic grid reduction of two values: warp shuffle tree -> block
-// (fixed order) -> per-block partials -> the last block to take a ticket sums
-// the partials in block order.  No block ever waits on another.  Returns true
-// in thread 0 of the last block, with the totals in tot0/tot1.
-template <int NT>
-__device__ bool grid_sum2(double v0, double v1, double* __restrict__ partials,
-                          unsigned int* ticket, double& tot0, double& tot1) {
-  constexpr int NW = NT / 32;
-  __shared__ double sh0[NW], sh1[NW];
-  __shared__ bool am_last;
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  v0 = warp_sum(v0);
-  v1 = warp_sum(v1);
-  if (NW > 1) {
-    if (lane == 0) {
-      sh0[w] = v0;
-      sh1[w] = v1;
-    }
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) {
-    double a = v0, b = v1;
-    for (int i = 1; i < NW; ++i) {
-      a += sh0[i];
-      b += sh1[i];
-    }
-    partials[2 * blockIdx.x] = a;
-    partials[2 * blockIdx.x + 1] = b;
-    __threadfence();
-    const unsigned int t = atomicAdd(ticket, 1u);
-    am_last = (t == gridDim.x - 1);
-  }
-  __syncthreads();
-  if (!am_last) return false;
-  __threadfence();
-  double a = 0.0, b = 0.0;
-  for (int i = threadIdx.x; i < (int)gridDim.x; i += NT) {
-    a += __ldcg(partials + 2 * i);
-    b += __ldcg(partials + 2 * i + 1);
-  }
-  a = warp_sum(a);
-  b = warp_sum(b);
-  if (NW > 1) {
-    if (lane == 0) {
-      sh0[w] = a;
-      sh1[w] = b;
-    }
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) {
-    for (int i = 1; i < NW; ++i) {
-      a += sh0[i];
-      b += sh1[i];
-    }
-    tot0 = a;
-    tot1 = b;
-    *ticket = 0u;
-  }
-  return threadIdx.x == 0;
 }
 
 // ------------------------------------------------------------------ setup
@@ -398,46 +298,6 @@ __device__ __forceinline__ void column_solve(const Op& op, long long tile, int l
   }
 }
 
-// Last-block bookkeeping of Algorithm 1 after the preconditioner sweep of
-// iteration it: ||r||, stopping test, beta = kappa/kappa_old.
-__device__ void finish_precond_sweep(DevState* st, double R, double K, double* hist) {
-  const int it = st->it;
-  if (it == 0) st->R0 = R;
-  const double R0 = st->R0;
-  st->last_R = R;
-  st->last_kappa = K;
-  const double ratio = (R0 > 0.0) ? sqrt(R / R0) : 0.0;
-  hist[it] = ratio;
-  int done = 0, status = kStOK;
-  if (st->dev_error) {
-    done = 1;
-    status = kStTimeout;
-  } else if (R0 == 0.0) {
-    done = 1;  // r_0 = 0: the initial guess solves the system
-  } else if (!(R < INFINITY) || !(R0 < INFINITY)) {
-    done = 1;
-    status = kStBreakdown;  // NaN or Inf in the residual
-  } else if (ratio < st->rtol || R == 0.0) {
-    done = 1;
-  } else if (it >= st->maxit) {
-    done = 1;
-    status = (st->rtol > 0.0) ? kStNotConv : kStOK;
-  } else if (!(K > 0.0)) {
-    done = 1;
-    status = kStBreakdown;
-  } else {
-    st->beta = K / st->kappa_old;
-    st->kappa_old = K;
-  }
-  if (done) {
-    st->iters = it;
-    st->status = status;
-    __threadfence();
-    st->done = 1;
-  }
-  st->it = it + 1;
-}
-
 template <bool VARY, bool FUSED>
 __global__ void __launch_bounds__(kTile) k_precond_staged(Op op, DevState* st,
                                                           double* __restrict__ r,
@@ -506,59 +366,6 @@ static int g_max_stream_smem = 0;
 template <bool FUSED>
 __host__ __device__ inline size_t stream_smem_bytes(int pt) {
   return sizeof(double) * ((size_t)kTile * pt + (FUSED ? 2 : 1) * (size_t)kStages * kTile * kCS);
-}
-
-__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-// L2 eviction-priority hints: data read again soon (the w scratch, the
-// Thomas factors the backward sweep reads a second time) is kept, data that
-// streams through once is let go first.
-__device__ __forceinline__ uint64_t l2_keep() {
-  uint64_t p;
-  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint64_t l2_stream() {
-  uint64_t p;
-  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ void cp_async16_hint(void* dst_smem, const void* src, uint64_t pol) {
-  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(
-                   smem_addr(dst_smem)),
-               "l"(src), "l"(pol)
-               : "memory");
-}
-__device__ __forceinline__ void st_hint(double* a, double v, uint64_t pol) {
-  asm volatile("st.global.L2::cache_hint.f64 [%0], %1, %2;" ::"l"(a), "d"(v), "l"(pol)
-               : "memory");
-}
-__device__ __forceinline__ void st2_hint(double* a, double2 v, uint64_t pol) {
-  asm volatile("st.global.L2::cache_hint.v2.f64 [%0], {%1, %2}, %3;" ::"l"(a), "d"(v.x),
-               "d"(v.y), "l"(pol)
-               : "memory");
-}
-__device__ __forceinline__ double ld_hint(const double* a, uint64_t pol) {
-  double v;
-  asm volatile("ld.global.L2::cache_hint.f64 %0, [%1], %2;" : "=d"(v) : "l"(a), "l"(pol)
-               : "memory");
-  return v;
-}
-
-__device__ __forceinline__ double2 lds2(const double* p) {
-  return *reinterpret_cast<const double2*>(p);
-}
-__device__ __forceinline__ void sts2(double* p, double a, double b) {
-  *reinterpret_cast<double2*>(p) = make_double2(a, b);
 }
 
 // FULL: nz is a multiple of kChunk (no partial chunk, no guards).
@@ -1151,208 +958,6 @@ __global__ void __launch_bounds__(kSpmvThreads) k_finalize(Op op, const DevState
   }
 }
 
-// ----------------------------------------------- row-tiled layout (eq. (22))
-//
-// The solver's internal vectors may instead use the layout of the paper's
-// GPU code, eq. (22): horizontal index fastest.  Here in blocked form, so
-// that it works for any nx: cell (column c, level k) at
-//     (c/32 * nz + k) * 32 + c%32,
-// i.e. level-major within tiles of 32 consecutive columns.  A warp owns a
-// tile, one lane per column, and every level of the tile is one 256-byte
-// line: the preconditioner needs no shared memory at all and keeps w in z,
-// and the stencil walks its column with a register window along k.  The
-// caller's b and x stay column-contiguous; they are converted at the start
-// and the end of a solve.
-
-__device__ __forceinline__ long long tiled_base(long long col, int nz) {
-  return (col >> 5) * (long long)nz * kTile + (col & 31);
-}
-
-// Column-contiguous <-> row-tiled conversion, 32 columns x 32 levels per
-// block through a padded shared tile (coalesced on both sides).
-// TO_TILED: dst_t = src_k.  Otherwise dst_k = src_t + alpha * p_t (AXPY,
-// alpha from the device state: the deferred x += alpha p of Algorithm 1), or
-// a plain copy.
-// With TO_TILED, zero1/zero2 (may be NULL) are cleared at the same row-tiled
-// positions (p and q at the start of a solve).
-template <bool TO_TILED, bool AXPY>
-__global__ void __launch_bounds__(256) k_retile(Op op, const DevState* st,
-                                                const double* __restrict__ src,
-                                                const double* __restrict__ pt,
-                                                double* __restrict__ dst,
-                                                double* __restrict__ zero1,
-                                                double* __restrict__ zero2) {
-  __shared__ double tile[kTile][kTile + 1];
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  const int nz = op.nz;
-  const long long t = blockIdx.x;
-  const int k0 = blockIdx.y * kTile;
-  const long long col0 = t * kTile;
-  const int nc = (int)min((long long)kTile, op.ncols - col0);
-  const int nk = min(kTile, nz - k0);
-  const double alpha = AXPY ? st->alpha : 0.0;
-  if (TO_TILED) {
-    for (int c = ty; c < nc; c += 8)
-      if (tx < nk) tile[c][tx] = src[(col0 + c) * nz + k0 + tx];
-    __syncthreads();
-    for (int k = ty; k < nk; k += 8)
-      if (tx < nc) {
-        const long long o = (t * nz + k0 + k) * kTile + tx;
-        dst[o] = tile[tx][k];
-        if (zero1) zero1[o] = 0.0;
-        if (zero2) zero2[o] = 0.0;
-      }
-  } else {
-    for (int k = ty; k < nk; k += 8)
-      if (tx < nc) {
-        const long long o = (t * nz + k0 + k) * kTile + tx;
-        tile[tx][k] = AXPY ? fma(alpha, pt[o], src[o]) : src[o];
-      }
-    __syncthreads();
-    for (int c = ty; c < nc; c += 8)
-      if (tx < nk) dst[(col0 + c) * nz + k0 + tx] = tile[c][tx];
-  }
-}
-
-// Algorithm 3 sweep (FUSED) or z = M^{-1} r on row-tiled vectors.  w is
-// written into z on the way up (normal caching, so it tends to stay in L2)
-// and replaced by z on the way down; streamed data is loaded and stored with
-// the evict-first hint.
-template <bool VARY, bool FUSED>
-__global__ void __launch_bounds__(256) k_precond_tiled(Op op, DevState* st,
-                                                       double* __restrict__ r,
-                                                       const double* __restrict__ q,
-                                                       double* __restrict__ z,
-                                                       double* __restrict__ partials,
-                                                       double* __restrict__ hist) {
-  if (FUSED && ld_done(st)) return;
-  const int lane = threadIdx.x & 31;
-  const long long warp0 = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
-  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
-  const int nz = op.nz;
-  const double nalpha = FUSED ? -st->alpha : 0.0;
-  double accR = 0.0, accK = 0.0;
-  for (long long t = warp0; t < op.ntiles; t += nwarps) {
-    const long long col = t * kTile + lane;
-    if (col >= op.ncols) continue;
-    const long long base = t * nz * kTile + lane;
-    const double* __restrict__ fi = VARY ? op.tinvd + base : op.lev + LV_INVD * nz;
-    const double* __restrict__ fn = VARY ? op.tnphi + base : op.lev + LV_NPHI * nz;
-    const int fs = VARY ? kTile : 1;
-    double y = 0.0, nprev = 0.0, w = 0.0;
-#pragma unroll 8
-    for (int k = 0; k < nz; ++k) {
-      const long long o = base + (long long)k * kTile;
-      double rk = __ldcs(r + o);
-      if (FUSED) {
-        rk = fma(nalpha, __ldcs(q + o), rk);
-        accR = fma(rk, rk, accR);
-        __stcs(r + o, rk);
-      }
-      y = fma(nprev, y, rk);
-      w = y * __ldg(fi + k * fs);
-      if (FUSED) accK = fma(y, w, accK);
-      z[o] = w;
-      nprev = __ldg(fn + k * fs);
-    }
-    double zz = w;  // z_{nz-1} = w_{nz-1}, already in place
-#pragma unroll 8
-    for (int k = nz - 2; k >= 0; --k) {
-      const long long o = base + (long long)k * kTile;
-      zz = fma(__ldg(fn + k * fs), zz, __ldcs(z + o));
-      __stcs(z + o, zz);
-    }
-  }
-  if (FUSED) {
-    double R, K;
-    if (grid_sum2<256>(accR, accK, partials, &st->ticket_m, R, K))
-      finish_precond_sweep(st, R, K, hist);
-  }
-}
-
-// Algorithm 2 sweep on row-tiled vectors: u += alpha p; p = z + beta p;
-// q = A z + beta q; <p,q>.  One thread per column walking up the levels
-// with z_{k-1}, z_k, z_{k+1} in registers; the horizontal neighbours are
-// fixed offsets from the column's own.
-template <bool VARY>
-__global__ void __launch_bounds__(256) k_spmv_tiled(Op op, DevState* st,
-                                                    const double* __restrict__ z,
-                                                    double* __restrict__ u,
-                                                    double* __restrict__ p,
-                                                    double* __restrict__ q,
-                                                    double* __restrict__ partials) {
-  if (ld_done(st)) return;
-  const double alpha = st->alpha, beta = st->beta;
-  const int lane = threadIdx.x & 31;
-  const long long warp0 = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
-  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
-  const int nz = op.nz;
-  const double* __restrict__ lev = op.lev;
-  double sig = 0.0;
-  for (long long t = warp0; t < op.ntiles; t += nwarps) {
-    const long long col = t * kTile + lane;
-    if (col >= op.ncols) continue;
-    const long long base = t * nz * kTile + lane;
-    const Nbr nb = neighbours(op, col);
-    const long long bE = tiled_base(nb.e, nz), bW = tiled_base(nb.w, nz);
-    const long long bN = tiled_base(nb.n, nz), bS = tiled_base(nb.s, nz);
-    double aE = 0.0, aW = 0.0, aN = 0.0, aS = 0.0;
-    if (VARY) {
-      aE = __ldg(op.faceE + col);
-      aW = __ldg(op.faceE + nb.w);
-      aN = __ldg(op.faceN + col);
-      aS = __ldg(op.faceN + nb.s);
-    }
-    double zd = 0.0, zc = z[base];
-#pragma unroll 4
-    for (int k = 0; k < nz; ++k) {
-      const long long o = base + (long long)k * kTile;
-      const long long ko = (long long)k * kTile;
-      const double zu = (k + 1 < nz) ? z[o + kTile] : 0.0;
-      const double zE = z[bE + ko], zW = z[bW + ko], zN = z[bN + ko], zS = z[bS + ko];
-      double uc = __ldcs(u + o);
-      double pc = __ldcs(p + o);
-      const double qc = __ldcs(q + o);
-      uc = fma(alpha, pc, uc);
-      pc = fma(beta, pc, zc);
-      double hs, d;
-      if (VARY) {
-        hs = aE * zE;
-        hs = fma(aW, zW, hs);
-        hs = fma(aN, zN, hs);
-        hs = fma(aS, zS, hs);
-        d = __ldcs(op.cdiag_t + o);
-      } else {
-        hs = (zE + zW) + (zN + zS);
-        d = __ldg(lev + LV_DIAG * nz + k);
-      }
-      double a = fma(d, zc, beta * qc);
-      a = fma(__ldg(lev + LV_UP * nz + k), zu, a);
-      a = fma(__ldg(lev + LV_DN * nz + k), zd, a);
-      a = fma(__ldg(lev + LV_HW * nz + k), hs, a);
-      sig = fma(pc, a, sig);
-      __stcs(u + o, uc);
-      __stcs(p + o, pc);
-      __stcs(q + o, a);
-      zd = zc;
-      zc = zu;
-    }
-  }
-  double S, unused;
-  if (grid_sum2<256>(sig, 0.0, partials, &st->ticket_a, S, unused)) {
-    st->last_sigma = S;
-    if (!(S > 0.0) || !(S < INFINITY)) {
-      st->alpha = 0.0;
-      st->iters = st->it - 1;
-      st->status = kStBreakdown;
-      __threadfence();
-      st->done = 1;
-    } else {
-      st->alpha = st->kappa_old / S;
-    }
-  }
-}
-
 // ------------------------------------------------------------- dispatch
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -1612,58 +1217,6 @@ cudaError_t launch_spmv_fused(const Op& op, DevState* st, const double* z, doubl
     else k_spmv_fused<false, false><<<grid, kSpmvThreads, 0, s>>>(op, st, z, u, p, q, partials);
   }
   return cudaGetLastError();
-}
-
-cudaError_t launch_to_tiled(const Op& op, const double* src_k, double* dst_t, cudaStream_t s,
-                            double* zero1, double* zero2) {
-  dim3 g((unsigned)op.ntiles, (unsigned)((op.nz + kTile - 1) / kTile));
-  k_retile<true, false><<<g, 256, 0, s>>>(op, nullptr, src_k, nullptr, dst_t, zero1, zero2);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_from_tiled(const Op& op, const DevState* st, const double* src_t,
-                              const double* p_t, double* dst_k, cudaStream_t s) {
-  dim3 g((unsigned)op.ntiles, (unsigned)((op.nz + kTile - 1) / kTile));
-  if (p_t)
-    k_retile<false, true><<<g, 256, 0, s>>>(op, st, src_t, p_t, dst_k, nullptr, nullptr);
-  else
-    k_retile<false, false><<<g, 256, 0, s>>>(op, st, src_t, nullptr, dst_k, nullptr, nullptr);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_precond_tiled(const Op& op, DevState* st, double* r, const double* q,
-                                 double* z, double* partials, double* hist, int grid,
-                                 cudaStream_t s) {
-  if (op.varying)
-    k_precond_tiled<true, true><<<grid, 256, 0, s>>>(op, st, r, q, z, partials, hist);
-  else
-    k_precond_tiled<false, true><<<grid, 256, 0, s>>>(op, st, r, q, z, partials, hist);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_spmv_tiled(const Op& op, DevState* st, const double* z, double* u, double* p,
-                              double* q, double* partials, int grid, cudaStream_t s) {
-  if (op.varying)
-    k_spmv_tiled<true><<<grid, 256, 0, s>>>(op, st, z, u, p, q, partials);
-  else
-    k_spmv_tiled<false><<<grid, 256, 0, s>>>(op, st, z, u, p, q, partials);
-  return cudaGetLastError();
-}
-
-int grid_tiled(const Op& op, int num_sms) {
-  int a = 0, b = 0;
-  if (op.varying) {
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, k_precond_tiled<true, true>, 256, 0);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_spmv_tiled<true>, 256, 0);
-  } else {
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, k_precond_tiled<false, true>, 256, 0);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_spmv_tiled<false>, 256, 0);
-  }
-  int per_sm = std::max(1, std::min(a, b));
-  long long g = (long long)per_sm * num_sms;
-  const long long work = (op.ntiles + 7) / 8;  // 8 tiles (warps) per block
-  if (g > work) g = work;
-  return (int)(g < 1 ? 1 : g);
 }
 
 cudaError_t launch_finalize(const Op& op, const DevState* st, double* x, const double* p,

@@ -1,0 +1,354 @@
+// Row-tiled solver layout: the paper's eq. (22) ordering (horizontal index
+// fastest) in blocked form, with its two fused sweeps.
+//
+// Method: Mueller, Guo, Scheichl, Shi, "Matrix-free GPU implementation of a
+// preconditioned conjugate gradient solver for anisotropic elliptic PDEs",
+// section 4.4, eq. (22) (layout), Appendix A Algorithms 2 and 3 (sweeps).
+//
+// Cell (column c, level k) sits at (c/32 * nz + k) * 32 + c%32: level-major
+// within tiles of 32 consecutive columns, so it works for any nx.  A warp
+// owns a tile, one lane per column, and every level of the tile is one
+// 256-byte line: the preconditioner needs no shared memory at all and keeps
+// w in z, and the stencil walks its column with a register window along k.
+// The caller's b and x stay column-contiguous; they are converted at the
+// start and the end of a solve.  Vectors in this layout hold ntiles*32*nz
+// values (the last tile padded to 32 columns; padded lanes never compute).
+#include <algorithm>
+#include <cstdint>
+
+#include "pcg_device.cuh"
+#include "pcg_internal.h"
+
+namespace pcg {
+namespace {
+
+// Preconditioner sweep: threads per block and levels per register chunk.
+constexpr int kTmThreads = 128;
+constexpr int kTmChunk = 8;
+// Resident warps per SM of the preconditioner sweep.  Each warp keeps the w
+// of its tile (32 x nz doubles) and the factors the backward pass reads a
+// second time live in L2 between the two passes; 12 warps per SM keep this
+// within L2 at nz = 128 while leaving three warps per sub-partition to hide
+// the fp64 latency of the serial recurrences.
+constexpr int kTmWarpsPerSm = 12;
+
+__device__ __forceinline__ long long tiled_base(long long col, int nz) {
+  return (col >> 5) * (long long)nz * kTile + (col & 31);
+}
+
+// Column-contiguous <-> row-tiled conversion, 32 columns x 32 levels per
+// block through a padded shared tile (coalesced on both sides).
+// TO_TILED: dst_t = src_k.  Otherwise dst_k = src_t + alpha * p_t (AXPY,
+// alpha from the device state: the deferred x += alpha p of Algorithm 1), or
+// a plain copy.
+// With TO_TILED, zero1/zero2 (may be NULL) are cleared at the same row-tiled
+// positions (p and q at the start of a solve).
+template <bool TO_TILED, bool AXPY>
+__global__ void __launch_bounds__(256) k_retile(Op op, const DevState* st,
+                                                const double* __restrict__ src,
+                                                const double* __restrict__ pt,
+                                                double* __restrict__ dst,
+                                                double* __restrict__ zero1,
+                                                double* __restrict__ zero2) {
+  __shared__ double tile[kTile][kTile + 1];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int nz = op.nz;
+  const long long t = blockIdx.x;
+  const int k0 = blockIdx.y * kTile;
+  const long long col0 = t * kTile;
+  const int nc = (int)min((long long)kTile, op.ncols - col0);
+  const int nk = min(kTile, nz - k0);
+  const double alpha = AXPY ? st->alpha : 0.0;
+  if (TO_TILED) {
+    for (int c = ty; c < nc; c += 8)
+      if (tx < nk) tile[c][tx] = src[(col0 + c) * nz + k0 + tx];
+    __syncthreads();
+    for (int k = ty; k < nk; k += 8)
+      if (tx < nc) {
+        const long long o = (t * nz + k0 + k) * kTile + tx;
+        dst[o] = tile[tx][k];
+        if (zero1) zero1[o] = 0.0;
+        if (zero2) zero2[o] = 0.0;
+      }
+  } else {
+    for (int k = ty; k < nk; k += 8)
+      if (tx < nc) {
+        const long long o = (t * nz + k0 + k) * kTile + tx;
+        tile[tx][k] = AXPY ? fma(alpha, pt[o], src[o]) : src[o];
+      }
+    __syncthreads();
+    for (int c = ty; c < nc; c += 8)
+      if (tx < nk) dst[(col0 + c) * nz + k0 + tx] = tile[c][tx];
+  }
+}
+
+// Algorithm 3 sweep (FUSED: r* = r - alpha q, then z = M^{-1} r*, with the
+// partial sums of r*.r* and <r*, z>) or plain z = M^{-1} r, on row-tiled
+// vectors.  One warp per tile, one lane per column.
+//
+// Every load is independent of the recurrences, so the sweep fetches the
+// operands of kTmChunk levels (r, q and the two Thomas factors forward; w and
+// nphi backward) one chunk ahead into registers: the loads of chunk c+1 are
+// in flight while chunk c computes.  w is written into z on the way up with
+// the L2 evict-last hint and replaced by z on the way down; streamed data
+// carries evict-first.
+template <bool VARY, bool FUSED>
+__global__ void __launch_bounds__(kTmThreads) k_precond_tiled(Op op, DevState* st,
+                                                              double* __restrict__ r,
+                                                              const double* __restrict__ q,
+                                                              double* __restrict__ z,
+                                                              double* __restrict__ partials,
+                                                              double* __restrict__ hist) {
+  if (FUSED && ld_done(st)) return;
+  const int lane = threadIdx.x & 31;
+  const long long warp0 = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  const int nz = op.nz;
+  const int fs = VARY ? kTile : 1;  // factor stride between levels
+  const double nalpha = FUSED ? -st->alpha : 0.0;
+  const uint64_t keep = l2_keep(), stream = l2_stream();
+  double accR = 0.0, accK = 0.0;
+  for (long long t = warp0; t < op.ntiles; t += nwarps) {
+    if (t * kTile + lane >= op.ncols) continue;
+    const long long base = t * nz * kTile + lane;
+    double* __restrict__ rt = r + base;
+    const double* __restrict__ qt = FUSED ? q + base : nullptr;
+    double* __restrict__ zt = z + base;
+    const double* __restrict__ fi = VARY ? op.tinvd + base : op.lev + LV_INVD * nz;
+    const double* __restrict__ fn = VARY ? op.tnphi + base : op.lev + LV_NPHI * nz;
+    // ---- forward: level k uses nphi_{k-1} (0 at k = 0) and 1/D_k
+    double cr[kTmChunk], cq[kTmChunk], ci[kTmChunk], cn[kTmChunk];
+#pragma unroll
+    for (int j = 0; j < kTmChunk; ++j) {
+      const bool in = j < nz;
+      cr[j] = in ? ld_hint(rt + j * kTile, stream) : 0.0;
+      cq[j] = (FUSED && in) ? ld_hint(qt + j * kTile, stream) : 0.0;
+      ci[j] = in ? (VARY ? ld_hint(fi + j * fs, stream) : __ldg(fi + j)) : 0.0;
+      cn[j] = in ? (VARY ? ld_hint(fn + j * fs, keep) : __ldg(fn + j)) : 0.0;
+    }
+    double y = 0.0, nprev = 0.0, w = 0.0;
+#pragma unroll 1
+    for (int k0 = 0; k0 < nz; k0 += kTmChunk) {
+      double nr[kTmChunk], nq[kTmChunk], ni[kTmChunk], nn[kTmChunk];
+#pragma unroll
+      for (int j = 0; j < kTmChunk; ++j) {
+        const int k = k0 + kTmChunk + j;
+        const bool in = k < nz;
+        nr[j] = in ? ld_hint(rt + k * kTile, stream) : 0.0;
+        nq[j] = (FUSED && in) ? ld_hint(qt + k * kTile, stream) : 0.0;
+        ni[j] = in ? (VARY ? ld_hint(fi + k * fs, stream) : __ldg(fi + k)) : 0.0;
+        nn[j] = in ? (VARY ? ld_hint(fn + k * fs, keep) : __ldg(fn + k)) : 0.0;
+      }
+#pragma unroll
+      for (int j = 0; j < kTmChunk; ++j) {
+        const int k = k0 + j;
+        if (k < nz) {
+          double rk = cr[j];
+          if (FUSED) {
+            rk = fma(nalpha, cq[j], rk);
+            accR = fma(rk, rk, accR);
+            st_hint(rt + k * kTile, rk, stream);
+          }
+          y = fma(nprev, y, rk);
+          w = y * ci[j];
+          if (FUSED) accK = fma(y, w, accK);
+          st_hint(zt + k * kTile, w, keep);
+          nprev = cn[j];
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kTmChunk; ++j) {
+        cr[j] = nr[j];
+        cq[j] = nq[j];
+        ci[j] = ni[j];
+        cn[j] = nn[j];
+      }
+    }
+    // ---- backward: z_{nz-1} = w_{nz-1} (in place); level k uses nphi_k.
+    // Chunk b holds levels kb, kb-1, ..., kb-kTmChunk+1 with kb = nz-2-b*kTmChunk.
+    double zz = w;
+    double bw[kTmChunk], bn[kTmChunk];
+#pragma unroll
+    for (int j = 0; j < kTmChunk; ++j) {
+      const int k = nz - 2 - j;
+      bw[j] = (k >= 0) ? ld_hint(zt + k * kTile, stream) : 0.0;
+      bn[j] = (k >= 0) ? (VARY ? ld_hint(fn + k * fs, stream) : __ldg(fn + k)) : 0.0;
+    }
+#pragma unroll 1
+    for (int kb = nz - 2; kb >= 0; kb -= kTmChunk) {
+      double nw[kTmChunk], nb[kTmChunk];
+#pragma unroll
+      for (int j = 0; j < kTmChunk; ++j) {
+        const int k = kb - kTmChunk - j;
+        nw[j] = (k >= 0) ? ld_hint(zt + k * kTile, stream) : 0.0;
+        nb[j] = (k >= 0) ? (VARY ? ld_hint(fn + k * fs, stream) : __ldg(fn + k)) : 0.0;
+      }
+#pragma unroll
+      for (int j = 0; j < kTmChunk; ++j) {
+        const int k = kb - j;
+        if (k >= 0) {
+          zz = fma(bn[j], zz, bw[j]);
+          st_hint(zt + k * kTile, zz, stream);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kTmChunk; ++j) {
+        bw[j] = nw[j];
+        bn[j] = nb[j];
+      }
+    }
+  }
+  if (FUSED) {
+    double R, K;
+    if (grid_sum2<kTmThreads>(accR, accK, partials, &st->ticket_m, R, K))
+      finish_precond_sweep(st, R, K, hist);
+  }
+}
+
+// Algorithm 2 sweep on row-tiled vectors: u += alpha p; p = z + beta p;
+// q = A z + beta q; <p,q>.  One thread per column walking up the levels
+// with z_{k-1}, z_k, z_{k+1} in registers; the horizontal neighbours are
+// fixed offsets from the column's own.
+template <bool VARY>
+__global__ void __launch_bounds__(256) k_spmv_tiled(Op op, DevState* st,
+                                                    const double* __restrict__ z,
+                                                    double* __restrict__ u,
+                                                    double* __restrict__ p,
+                                                    double* __restrict__ q,
+                                                    double* __restrict__ partials) {
+  if (ld_done(st)) return;
+  const double alpha = st->alpha, beta = st->beta;
+  const int lane = threadIdx.x & 31;
+  const long long warp0 = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  const int nz = op.nz;
+  const double* __restrict__ lev = op.lev;
+  double sig = 0.0;
+  for (long long t = warp0; t < op.ntiles; t += nwarps) {
+    const long long col = t * kTile + lane;
+    if (col >= op.ncols) continue;
+    const long long base = t * nz * kTile + lane;
+    const Nbr nb = neighbours(op, col);
+    const long long bE = tiled_base(nb.e, nz), bW = tiled_base(nb.w, nz);
+    const long long bN = tiled_base(nb.n, nz), bS = tiled_base(nb.s, nz);
+    double aE = 0.0, aW = 0.0, aN = 0.0, aS = 0.0;
+    if (VARY) {
+      aE = __ldg(op.faceE + col);
+      aW = __ldg(op.faceE + nb.w);
+      aN = __ldg(op.faceN + col);
+      aS = __ldg(op.faceN + nb.s);
+    }
+    double zd = 0.0, zc = z[base];
+#pragma unroll 4
+    for (int k = 0; k < nz; ++k) {
+      const long long o = base + (long long)k * kTile;
+      const long long ko = (long long)k * kTile;
+      const double zu = (k + 1 < nz) ? z[o + kTile] : 0.0;
+      const double zE = z[bE + ko], zW = z[bW + ko], zN = z[bN + ko], zS = z[bS + ko];
+      double uc = __ldcs(u + o);
+      double pc = __ldcs(p + o);
+      const double qc = __ldcs(q + o);
+      uc = fma(alpha, pc, uc);
+      pc = fma(beta, pc, zc);
+      double hs, d;
+      if (VARY) {
+        hs = aE * zE;
+        hs = fma(aW, zW, hs);
+        hs = fma(aN, zN, hs);
+        hs = fma(aS, zS, hs);
+        d = __ldcs(op.cdiag_t + o);
+      } else {
+        hs = (zE + zW) + (zN + zS);
+        d = __ldg(lev + LV_DIAG * nz + k);
+      }
+      double a = fma(d, zc, beta * qc);
+      a = fma(__ldg(lev + LV_UP * nz + k), zu, a);
+      a = fma(__ldg(lev + LV_DN * nz + k), zd, a);
+      a = fma(__ldg(lev + LV_HW * nz + k), hs, a);
+      sig = fma(pc, a, sig);
+      __stcs(u + o, uc);
+      __stcs(p + o, pc);
+      __stcs(q + o, a);
+      zd = zc;
+      zc = zu;
+    }
+  }
+  double S, unused;
+  if (grid_sum2<256>(sig, 0.0, partials, &st->ticket_a, S, unused)) {
+    st->last_sigma = S;
+    if (!(S > 0.0) || !(S < INFINITY)) {
+      st->alpha = 0.0;
+      st->iters = st->it - 1;
+      st->status = kStBreakdown;
+      __threadfence();
+      st->done = 1;
+    } else {
+      st->alpha = st->kappa_old / S;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_to_tiled(const Op& op, const double* src_k, double* dst_t, cudaStream_t s,
+                            double* zero1, double* zero2) {
+  dim3 g((unsigned)op.ntiles, (unsigned)((op.nz + kTile - 1) / kTile));
+  k_retile<true, false><<<g, 256, 0, s>>>(op, nullptr, src_k, nullptr, dst_t, zero1, zero2);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_from_tiled(const Op& op, const DevState* st, const double* src_t,
+                              const double* p_t, double* dst_k, cudaStream_t s) {
+  dim3 g((unsigned)op.ntiles, (unsigned)((op.nz + kTile - 1) / kTile));
+  if (p_t)
+    k_retile<false, true><<<g, 256, 0, s>>>(op, st, src_t, p_t, dst_k, nullptr, nullptr);
+  else
+    k_retile<false, false><<<g, 256, 0, s>>>(op, st, src_t, nullptr, dst_k, nullptr, nullptr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_precond_tiled(const Op& op, DevState* st, double* r, const double* q,
+                                 double* z, double* partials, double* hist, int grid,
+                                 cudaStream_t s) {
+  if (op.varying)
+    k_precond_tiled<true, true><<<grid, kTmThreads, 0, s>>>(op, st, r, q, z, partials, hist);
+  else
+    k_precond_tiled<false, true><<<grid, kTmThreads, 0, s>>>(op, st, r, q, z, partials, hist);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_spmv_tiled(const Op& op, DevState* st, const double* z, double* u, double* p,
+                              double* q, double* partials, int grid, cudaStream_t s) {
+  if (op.varying)
+    k_spmv_tiled<true><<<grid, 256, 0, s>>>(op, st, z, u, p, q, partials);
+  else
+    k_spmv_tiled<false><<<grid, 256, 0, s>>>(op, st, z, u, p, q, partials);
+  return cudaGetLastError();
+}
+
+int grid_tiled_precond(const Op& op, int num_sms) {
+  int a = 0;
+  if (op.varying)
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, k_precond_tiled<true, true>, kTmThreads, 0);
+  else
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, k_precond_tiled<false, true>, kTmThreads, 0);
+  const int per_sm = std::max(1, std::min(a, kTmWarpsPerSm / (kTmThreads / 32)));
+  long long g = (long long)per_sm * num_sms;
+  const long long work = (op.ntiles + kTmThreads / 32 - 1) / (kTmThreads / 32);
+  if (g > work) g = work;
+  return (int)(g < 1 ? 1 : g);
+}
+
+int grid_tiled_spmv(const Op& op, int num_sms) {
+  int b = 0;
+  if (op.varying)
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_spmv_tiled<true>, 256, 0);
+  else
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_spmv_tiled<false>, 256, 0);
+  long long g = (long long)std::max(1, b) * num_sms;
+  const long long work = (op.ntiles + 7) / 8;  // 8 tiles (warps) per block
+  if (g > work) g = work;
+  return (int)(g < 1 ? 1 : g);
+}
+
+}  // namespace pcg
