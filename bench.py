@@ -58,7 +58,7 @@ def parse():
                          "2 per step for --impl reference)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--layout", choices=["column", "tiled"], default="column",
+    ap.add_argument("--layout", choices=["column", "tiled"], default="tiled",
                     help="layout of the solver's internal vectors")
     ap.add_argument("--grid", type=int, nargs=3, metavar=("NX", "NY", "NZ"),
                     help="same coefficients on another grid size (profiling captures)")

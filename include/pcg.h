@@ -96,15 +96,15 @@ int pcg_set_stream(pcg_ctx* ctx, void* stream);
 /* Layout of the solver's internal vectors (r, z, p, q and a copy of the
  * iterate) during pcg_solve.  The caller's vectors always keep the
  * column-contiguous layout of this header.
- *   PCG_LAYOUT_COLUMN  vertical index fastest, like the caller's vectors
- *                      (default; section 3 eq. (10)).
- *   PCG_LAYOUT_TILED   horizontal index fastest within tiles of 32
- *                      consecutive columns: cell (column c, level k) at
+ *   PCG_LAYOUT_TILED   (default) horizontal index fastest within tiles of
+ *                      32 consecutive columns: cell (column c, level k) at
  *                      (c/32*nz + k)*32 + c%32, the GPU layout of the paper
  *                      (section 6.1, eq. (22)) in blocked form.  b and x are
  *                      converted at the start and the end of each solve; the
- *                      context then holds two more vectors (one if a_h is
+ *                      context holds two more vectors for it (one if a_h is
  *                      constant).
+ *   PCG_LAYOUT_COLUMN  vertical index fastest, like the caller's vectors
+ *                      (section 3 eq. (10)); no conversions.
  * Synchronous.  Errors: PCG_EINVAL (unknown layout), PCG_ENOMEM, PCG_ECUDA. */
 enum { PCG_LAYOUT_COLUMN = 0, PCG_LAYOUT_TILED = 1 };
 int pcg_set_layout(pcg_ctx* ctx, int layout);

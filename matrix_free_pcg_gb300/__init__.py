@@ -174,7 +174,7 @@ def pcg_set_stream(ctx, stream):
 
 
 def pcg_set_layout(ctx, layout):
-    """PCG_LAYOUT_COLUMN (default) or PCG_LAYOUT_TILED for the solver's internal vectors."""
+    """PCG_LAYOUT_TILED (default) or PCG_LAYOUT_COLUMN for the solver's internal vectors."""
     return _check(_lib.pcg_set_layout(ctx, int(layout)), ctx)
 
 

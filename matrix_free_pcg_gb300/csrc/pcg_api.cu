@@ -471,6 +471,8 @@ int pcg_create(int nx, int ny, int nz, const pcg_coeffs* coeffs, pcg_ctx** out) 
   op.wscratch = ctx->wscratch;
   st = load_coeffs(ctx, coeffs, varying);
   if (st) return bail(st);
+  st = pcg_set_layout(ctx, PCG_LAYOUT_TILED);  // the default solver layout
+  if (st) return bail(st);
   *out = ctx;
   return PCG_OK;
 }

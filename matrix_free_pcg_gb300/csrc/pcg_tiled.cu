@@ -3,7 +3,7 @@
 //
 // Method: Mueller, Guo, Scheichl, Shi, "Matrix-free GPU implementation of a
 // preconditioned conjugate gradient solver for anisotropic elliptic PDEs",
-// section 4.4, eq. (22) (layout), Appendix A Algorithms 2 and 3 (sweeps).
+// section 6.1, eq. (22) (layout), Appendix A Algorithms 2 and 3 (sweeps).
 //
 // Cell (column c, level k) sits at (c/32 * nz + k) * 32 + c%32: level-major
 // within tiles of 32 consecutive columns, so it works for any nx.  A warp
@@ -208,14 +208,19 @@ __global__ void __launch_bounds__(kTmThreads) k_precond_tiled(Op op, DevState* s
 // Algorithm 2 sweep on row-tiled vectors: u += alpha p; p = z + beta p;
 // q = A z + beta q; <p,q>.  One thread per column walking up the levels
 // with z_{k-1}, z_k, z_{k+1} in registers; the horizontal neighbours are
-// fixed offsets from the column's own.
+// fixed offsets from the column's own.  The unit of work is a segment of
+// seglen levels of one tile (the stencil has no recurrence along k), so that
+// grids with few tiles still give every warp several units; units are
+// assigned statically (segment-major), which keeps the sum bitwise
+// repeatable.
 template <bool VARY>
 __global__ void __launch_bounds__(256) k_spmv_tiled(Op op, DevState* st,
                                                     const double* __restrict__ z,
                                                     double* __restrict__ u,
                                                     double* __restrict__ p,
                                                     double* __restrict__ q,
-                                                    double* __restrict__ partials) {
+                                                    double* __restrict__ partials,
+                                                    int seglen) {
   if (ld_done(st)) return;
   const double alpha = st->alpha, beta = st->beta;
   const int lane = threadIdx.x & 31;
@@ -224,7 +229,11 @@ __global__ void __launch_bounds__(256) k_spmv_tiled(Op op, DevState* st,
   const int nz = op.nz;
   const double* __restrict__ lev = op.lev;
   double sig = 0.0;
-  for (long long t = warp0; t < op.ntiles; t += nwarps) {
+  const long long nunits = op.ntiles * ((nz + seglen - 1) / seglen);
+  for (long long unit = warp0; unit < nunits; unit += nwarps) {
+    const long long t = unit % op.ntiles;
+    const int k0 = (int)(unit / op.ntiles) * seglen;
+    const int k1 = min(nz, k0 + seglen);
     const long long col = t * kTile + lane;
     if (col >= op.ncols) continue;
     const long long base = t * nz * kTile + lane;
@@ -238,9 +247,10 @@ __global__ void __launch_bounds__(256) k_spmv_tiled(Op op, DevState* st,
       aN = __ldg(op.faceN + col);
       aS = __ldg(op.faceN + nb.s);
     }
-    double zd = 0.0, zc = z[base];
+    double zd = (k0 > 0) ? z[base + (long long)(k0 - 1) * kTile] : 0.0;
+    double zc = z[base + (long long)k0 * kTile];
 #pragma unroll 4
-    for (int k = 0; k < nz; ++k) {
+    for (int k = k0; k < k1; ++k) {
       const long long o = base + (long long)k * kTile;
       const long long ko = (long long)k * kTile;
       const double zu = (k + 1 < nz) ? z[o + kTile] : 0.0;
@@ -288,6 +298,18 @@ __global__ void __launch_bounds__(256) k_spmv_tiled(Op op, DevState* st,
   }
 }
 
+// Levels per work unit of the tiled stencil sweep: whole columns when there
+// are at least 8 tiles per resident warp, else segments short enough to give
+// every warp about 8 units (at least 4 levels each).
+int tiled_spmv_seglen(const Op& op, int grid) {
+  const long long warps = (long long)grid * 8;
+  const long long want = 8 * warps;
+  if (op.ntiles >= want || op.nz <= 4) return op.nz;
+  long long nseg = (want + op.ntiles - 1) / op.ntiles;
+  nseg = std::min<long long>(nseg, op.nz / 4);
+  return (int)((op.nz + nseg - 1) / nseg);
+}
+
 }  // namespace
 
 cudaError_t launch_to_tiled(const Op& op, const double* src_k, double* dst_t, cudaStream_t s,
@@ -319,10 +341,11 @@ cudaError_t launch_precond_tiled(const Op& op, DevState* st, double* r, const do
 
 cudaError_t launch_spmv_tiled(const Op& op, DevState* st, const double* z, double* u, double* p,
                               double* q, double* partials, int grid, cudaStream_t s) {
+  const int seglen = tiled_spmv_seglen(op, grid);
   if (op.varying)
-    k_spmv_tiled<true><<<grid, 256, 0, s>>>(op, st, z, u, p, q, partials);
+    k_spmv_tiled<true><<<grid, 256, 0, s>>>(op, st, z, u, p, q, partials, seglen);
   else
-    k_spmv_tiled<false><<<grid, 256, 0, s>>>(op, st, z, u, p, q, partials);
+    k_spmv_tiled<false><<<grid, 256, 0, s>>>(op, st, z, u, p, q, partials, seglen);
   return cudaGetLastError();
 }
 
@@ -346,7 +369,9 @@ int grid_tiled_spmv(const Op& op, int num_sms) {
   else
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_spmv_tiled<false>, 256, 0);
   long long g = (long long)std::max(1, b) * num_sms;
-  const long long work = (op.ntiles + 7) / 8;  // 8 tiles (warps) per block
+  // enough blocks for one unit per warp at the shortest segments
+  const long long units = op.ntiles * std::max(1, op.nz / 4);
+  const long long work = (units + 7) / 8;  // 8 warps per block
   if (g > work) g = work;
   return (int)(g < 1 ? 1 : g);
 }
