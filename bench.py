@@ -43,6 +43,13 @@ OPS_PRECOND = 6
 # Algorithmic bytes per cell: vectors read/written once per sweep.
 BYTES_SPMV = {True: 64, False: 56}   # u,p,z,q (+ per-cell diagonal) read; u,p,q written
 BYTES_PRECOND = {True: 48, False: 32}  # r,q (+ 2 per-cell Thomas factors) read; r,z written
+# With the factors of an a_h field rebuilt in every sweep (--factors recompute):
+# the stencil sweep forms the diagonal (a product and a sum), the
+# preconditioner sweep the diagonal, the pivot and the two quotients (the
+# reciprocal and the division counted as one operation each: a lower bound),
+# and neither reads per-cell coefficients.
+OPS_SPMV_RECOMPUTE, BYTES_SPMV_RECOMPUTE = 14, 56
+OPS_PRECOND_RECOMPUTE, BYTES_PRECOND_RECOMPUTE = 12, 32
 FP64_LANES_PER_SM_CLK = 2.0          # GB300 non-tensor fp64 rate: 2 FMA lanes per SM per clock
 
 
@@ -60,6 +67,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layout", choices=["column", "tiled"], default="tiled",
                     help="layout of the solver's internal vectors")
+    ap.add_argument("--factors", choices=["stored", "recompute"], default="stored",
+                    help="per-cell factors of an a_h field read from arrays or rebuilt in "
+                         "every sweep (row-tiled layout)")
     ap.add_argument("--grid", type=int, nargs=3, metavar=("NX", "NY", "NZ"),
                     help="same coefficients on another grid size (profiling captures)")
     return ap.parse_args()
@@ -152,21 +162,32 @@ def reduce_over_ranks(ms, iters, device):
     return float(t.item()), float(n.item())
 
 
-def measured_traffic(kernel, cells):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
-    when the kernel source has changed since the capture or the size differs."""
+def sources_sha256(names):
+    """sha256 over the named kernel sources (csrc/), concatenated in order."""
     import hashlib
+    hsh = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "matrix_free_pcg_gb300", "csrc", name), "rb") as f:
+            hsh.update(f.read())
+    return hsh.hexdigest()
+
+
+def measured_traffic(kernel, cells, layout, factors):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary
+    (profiles/traffic.json), or None when no capture matches the layout, the
+    factor mode and the size, or the kernel sources changed since."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             t = json.load(f)
-        src = os.path.join(ROOT, "matrix_free_pcg_gb300", "csrc", "pcg_kernels.cu")
-        with open(src, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
-    except (OSError, ValueError):
+        for c in t["captures"]:
+            if (c["layout"], c["factors"], c["full_cells"]) != (layout, factors, cells):
+                continue
+            if c["sha256"] != sources_sha256(c["sources"]) or kernel not in c["kernels"]:
+                return None
+            return c["kernels"][kernel]["bytes_per_launch"]
+    except (OSError, ValueError, KeyError):
         return None
-    if t.get("kernel_source_sha256") != sha or t.get("full_cells") != cells or kernel not in t:
-        return None
-    return t[kernel]["bytes_per_launch"]
+    return None
 
 
 def workload_inputs(w):
@@ -237,6 +258,8 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream(dev)
     solver.set_stream(stream)
     solver.set_layout(args.layout)
+    solver.set_factors(args.factors)
+    recompute = args.factors == "recompute" and varying and args.layout == "tiled"
 
     def step():
         solver.update_coeffs(**coeffs)
@@ -257,7 +280,8 @@ def run_ours(args, w):
     solver.enable_timing(True)
     iters = []
     launches = 0
-    setup_launches = 3 if varying else 0
+    # face values, diagonal, Thomas factors (+ the row-tiled copy of the diagonal)
+    setup_launches = (4 if args.layout == "tiled" else 3) if varying else 0
     with ClockSampler(local) as clocks:
         barrier()
         torch.cuda.synchronize()
@@ -280,13 +304,16 @@ def run_ours(args, w):
     peaks, peak_src = measured_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
     clk = clocks.summary()
-    bytes_iter = (BYTES_SPMV[varying] + BYTES_PRECOND[varying]) * n
-    ops_iter = (OPS_SPMV[varying] + OPS_PRECOND) * n
+    ops_a, bytes_a = ((OPS_SPMV_RECOMPUTE, BYTES_SPMV_RECOMPUTE) if recompute
+                      else (OPS_SPMV[varying], BYTES_SPMV[varying]))
+    ops_m, bytes_m = ((OPS_PRECOND_RECOMPUTE, BYTES_PRECOND_RECOMPUTE) if recompute
+                      else (OPS_PRECOND, BYTES_PRECOND[varying]))
+    bytes_iter = (bytes_a + bytes_m) * n
+    ops_iter = (ops_a + ops_m) * n
     hbm_gbs = bytes_iter * (total_iters / world) / (ms_max * 1e-3) / 1e9
 
     # roofline of the dominant kernel, from its live CUDA-event times
-    kinds = {"spmv_fused": (OPS_SPMV[varying], BYTES_SPMV[varying]),
-             "precond_fused": (OPS_PRECOND, BYTES_PRECOND[varying])}
+    kinds = {"spmv_fused": (ops_a, bytes_a), "precond_fused": (ops_m, bytes_m)}
     dom = max(kinds, key=lambda k: ktimes[k][0])
     dom_ms, dom_n = ktimes[dom]
     avg_s = dom_ms * 1e-3 / max(dom_n, 1)
@@ -296,7 +323,7 @@ def run_ours(args, w):
     alu_peak = FP64_LANES_PER_SM_CLK * nsm * sm_mhz * 1e6 / 1e9  # G fp64 ops / s
     alu_ach = ops_cell * n / avg_s / 1e9
     hbm_ach = bytes_cell * n / avg_s / 1e9
-    traffic = measured_traffic(dom, n)
+    traffic = measured_traffic(dom, n, args.layout, args.factors)
     roofline = {
         "bound": "alu", "kernel": dom, "achieved": alu_ach, "peak": alu_peak,
         "unit": "G fp64 ops/s", "frac": alu_ach / alu_peak, "traffic": traffic,
@@ -352,7 +379,7 @@ def run_ours(args, w):
                        "rtol": w.rtol, "iters_per_step": iters[0], "a_v": w.a_v,
                        "graded": w.graded, "varying_ah": varying,
                        "l2": "inputs larger than L2 (1.07 GB per vector)",
-                       "layout": args.layout,
+                       "layout": args.layout, "factors": args.factors,
                        "parallelism": "replicas" if world > 1 else "single"},
             "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / hbm_peak,
             "bytes_per_cell_iter": bytes_iter / n, "fp64_ops_per_cell_iter": ops_iter / n,

@@ -109,6 +109,25 @@ int pcg_set_stream(pcg_ctx* ctx, void* stream);
 enum { PCG_LAYOUT_COLUMN = 0, PCG_LAYOUT_TILED = 1 };
 int pcg_set_layout(pcg_ctx* ctx, int layout);
 
+/* Where the sweeps of pcg_solve take the per-cell diagonal and the Thomas
+ * factors T_{k+1/2}/D_k and 1/D_k of an a_h field (eqs. (18)-(19)) from:
+ *   PCG_FACTORS_STORED     (default) the per-cell arrays that pcg_create and
+ *                          pcg_update_coeffs compute once: 24 bytes per cell
+ *                          read in every iteration;
+ *   PCG_FACTORS_RECOMPUTE  rebuilt in every sweep from the per-level table and
+ *                          the face values, as the paper's Algorithm 3 does:
+ *                          no per-cell reads, but a division, a reciprocal and
+ *                          about six more fp64 operations per cell.
+ * Both give bit for bit the same iterates (the rebuilt numbers are rounded
+ * like the set-up rounds them).  RECOMPUTE applies to the row-tiled layout
+ * with an a_h field; in the column layout, or with a constant a_h (whose
+ * factors are per level), the stored path runs.  The first switch to
+ * RECOMPUTE allocates a scratch of 32*nz doubles per resident warp of the
+ * preconditioner sweep.  Synchronous with the host only through that
+ * allocation.  Errors: PCG_EINVAL (unknown mode), PCG_ENOMEM, PCG_ECUDA. */
+enum { PCG_FACTORS_STORED = 0, PCG_FACTORS_RECOMPUTE = 1 };
+int pcg_set_factors(pcg_ctx* ctx, int mode);
+
 /* y = A x, the matrix-free 7-point stencil of eq. (18), standalone.
  * x_dev, y_dev: device, N values each, must not overlap.  Asynchronous. */
 int pcg_apply_A(pcg_ctx* ctx, const double* x_dev, double* y_dev);

@@ -31,8 +31,9 @@ PCG_K_COUNT = len(KERNEL_KINDS)
 EXPORTED = ["pcg_create", "pcg_destroy", "pcg_update_coeffs", "pcg_set_stream", "pcg_apply_A",
             "pcg_precond", "pcg_solve", "pcg_solve_host", "pcg_last_error",
             "pcg_enable_timing", "pcg_kernel_times", "pcg_launch_info",
-            "pcg_precond_dot_noalloc", "pcg_set_layout"]
+            "pcg_precond_dot_noalloc", "pcg_set_layout", "pcg_set_factors"]
 PCG_LAYOUT_COLUMN, PCG_LAYOUT_TILED = 0, 1
+PCG_FACTORS_STORED, PCG_FACTORS_RECOMPUTE = 0, 1
 
 
 class pcg_coeffs(ctypes.Structure):
@@ -69,6 +70,7 @@ def _load(path=LIB_PATH):
                                            ctypes.POINTER(ctypes.c_longlong)]),
         "pcg_precond_dot_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
         "pcg_set_layout": (ctypes.c_int, [_vp, ctypes.c_int]),
+        "pcg_set_factors": (ctypes.c_int, [_vp, ctypes.c_int]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -176,6 +178,12 @@ def pcg_set_stream(ctx, stream):
 def pcg_set_layout(ctx, layout):
     """PCG_LAYOUT_TILED (default) or PCG_LAYOUT_COLUMN for the solver's internal vectors."""
     return _check(_lib.pcg_set_layout(ctx, int(layout)), ctx)
+
+
+def pcg_set_factors(ctx, mode):
+    """PCG_FACTORS_STORED (default) or PCG_FACTORS_RECOMPUTE: per-cell factors of an
+    a_h field read from arrays, or rebuilt in every sweep (row-tiled layout)."""
+    return _check(_lib.pcg_set_factors(ctx, int(mode)), ctx)
 
 
 def pcg_apply_A(ctx, n, x, y):
@@ -286,6 +294,12 @@ class Solver:
         if isinstance(layout, str):
             layout = {"column": PCG_LAYOUT_COLUMN, "tiled": PCG_LAYOUT_TILED}[layout]
         pcg_set_layout(self.ctx, layout)
+
+    def set_factors(self, mode):
+        """"stored" / PCG_FACTORS_STORED or "recompute" / PCG_FACTORS_RECOMPUTE."""
+        if isinstance(mode, str):
+            mode = {"stored": PCG_FACTORS_STORED, "recompute": PCG_FACTORS_RECOMPUTE}[mode]
+        pcg_set_factors(self.ctx, mode)
 
     def apply_A(self, x, y=None):
         import torch

@@ -47,6 +47,8 @@ struct pcg_ctx {
   int layout = PCG_LAYOUT_COLUMN;       // layout of the solver's internal vectors
   double *u_t = nullptr, *cdiag_t = nullptr;  // row-tiled layout: iterate, diagonal
   int grid_tm = 1, grid_ta = 1;  // row-tiled preconditioner / stencil sweeps
+  int factors = PCG_FACTORS_STORED;  // per-cell factors read (stored) or rebuilt per sweep
+  double* nscratch = nullptr;        // recompute: per-warp T_{k+1/2}/D_k scratch
   int hist_cap = 0;
   DevState* state = nullptr;
   double *b_host_api = nullptr, *x_host_api = nullptr;  // device copies for pcg_solve_host
@@ -165,7 +167,7 @@ void free_all(pcg_ctx* ctx) {
   double* bufs[] = {ctx->r,     ctx->z,     ctx->p,     ctx->q,        ctx->lev,
                     ctx->ah,    ctx->faceE, ctx->faceN, ctx->cdiag,    ctx->tnphi,
                     ctx->tinvd, ctx->partials, ctx->hist, ctx->b_host_api, ctx->x_host_api,
-                    ctx->wscratch, ctx->u_t, ctx->cdiag_t};
+                    ctx->wscratch, ctx->u_t, ctx->cdiag_t, ctx->nscratch};
   for (double* b : bufs)
     if (b) cudaFree(b);
   if (ctx->state) cudaFree(ctx->state);
@@ -211,7 +213,7 @@ int load_coeffs(pcg_ctx* ctx, const pcg_coeffs* c, bool varying) {
       float ms = 0.0f;
       if (e == cudaSuccess && cudaEventElapsedTime(&ms, t0, t1) == cudaSuccess) {
         ctx->ms[PCG_K_SETUP] += ms;
-        ctx->launches[PCG_K_SETUP] += 3;
+        ctx->launches[PCG_K_SETUP] += ctx->cdiag_t ? 4 : 3;
       }
     }
     if (t0) cudaEventDestroy(t0);
@@ -286,12 +288,14 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
     ctx->hist = nh;
     ctx->hist_cap = maxit + 1;
   }
-  const Op& op = ctx->op;
+  Op op = ctx->op;
   cudaStream_t s = ctx->stream;
   ctx->last_launches = 0;
   ctx->events.clear();
   ctx->pool_used = 0;
   const bool tiled = ctx->layout == PCG_LAYOUT_TILED;
+  op.recompute = (tiled && op.varying && ctx->factors == PCG_FACTORS_RECOMPUTE) ? 1 : 0;
+  op.nscratch = ctx->nscratch;
   // The row-tiled layout forms r = b - A x0 column-contiguously in z, then
   // converts r and x0 into the solver's layout.
   e = timed(ctx, PCG_K_RESIDUAL, [&] {
@@ -516,6 +520,24 @@ int pcg_set_layout(pcg_ctx* ctx, int layout) {
   }
   if (e != cudaSuccess) return cuda_fail(ctx, e, "layout change");
   ctx->layout = layout;
+  return PCG_OK;
+}
+
+int pcg_set_factors(pcg_ctx* ctx, int mode) {
+  if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
+  if (mode != PCG_FACTORS_STORED && mode != PCG_FACTORS_RECOMPUTE)
+    return fail(ctx, PCG_EINVAL, "unknown factor mode %d", mode);
+  if (mode == PCG_FACTORS_RECOMPUTE && !ctx->nscratch) {
+    DeviceGuard g(ctx->device);
+    if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
+    const size_t count = (size_t)ctx->grid_tm * pcg::kTmWarpsPerBlock * pcg::kTile * ctx->op.nz;
+    cudaError_t e = dalloc(&ctx->nscratch, count);
+    if (e != cudaSuccess) {
+      ctx->nscratch = nullptr;
+      return cuda_fail(ctx, e, "allocation of the factor scratch");
+    }
+  }
+  ctx->factors = mode;
   return PCG_OK;
 }
 

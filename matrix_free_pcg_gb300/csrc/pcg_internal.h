@@ -39,6 +39,10 @@ struct Op {
   int fixed_smem;      // dynamic shared memory of the height-specialised sweep
   double* wscratch;    // height-specialised sweep: 32*nz doubles per block (grid_precond blocks)
   const double* cdiag_t; // field, row-tiled solver layout: diagonal per cell, row-tiled
+  int recompute;       // field, row-tiled layout: rebuild the diagonal and the Thomas
+                       // factors in every sweep instead of reading them per cell
+  double* nscratch;    // recompute: T_{k+1/2}/D_k of the tiles in flight, 32*nz doubles
+                       // per warp of the preconditioner grid
   long long ncols;     // nx*ny
   long long n;         // ncols*nz
   long long ntiles;    // ceil(ncols / kTile)
@@ -112,11 +116,16 @@ cudaError_t launch_to_tiled(const Op& op, const double* src_k, double* dst_t, cu
 // dst_k = src_t + alpha p_t (alpha from the device state), or a copy when p_t is NULL.
 cudaError_t launch_from_tiled(const Op& op, const DevState* st, const double* src_t,
                               const double* p_t, double* dst_k, cudaStream_t s);
+// Algorithm 3 / Algorithm 2 sweeps on row-tiled vectors; with op.recompute the
+// per-cell diagonal and Thomas factors are rebuilt on the fly (op.nscratch must
+// then hold kTmWarpsPerBlock*32*nz doubles per block of grid_tiled_precond).
 cudaError_t launch_precond_tiled(const Op& op, DevState* st, double* r, const double* q,
                                  double* z, double* partials, double* hist, int grid,
                                  cudaStream_t s);
 cudaError_t launch_spmv_tiled(const Op& op, DevState* st, const double* z, double* u, double* p,
                               double* q, double* partials, int grid, cudaStream_t s);
+// Warps per block of the row-tiled preconditioner sweep.
+constexpr int kTmWarpsPerBlock = 4;
 // Grid sizes (blocks) of the two row-tiled sweeps.
 int grid_tiled_precond(const Op& op, int num_sms);
 int grid_tiled_spmv(const Op& op, int num_sms);

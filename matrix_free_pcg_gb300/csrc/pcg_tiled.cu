@@ -23,7 +23,7 @@ namespace pcg {
 namespace {
 
 // Preconditioner sweep: threads per block and levels per register chunk.
-constexpr int kTmThreads = 128;
+constexpr int kTmThreads = kTmWarpsPerBlock * 32;
 constexpr int kTmChunk = 8;
 // Resident warps per SM of the preconditioner sweep.  Each warp keeps the w
 // of its tile (32 x nz doubles) and the factors the backward pass reads a
@@ -205,6 +205,130 @@ __global__ void __launch_bounds__(kTmThreads) k_precond_tiled(Op op, DevState* s
   }
 }
 
+// Algorithm 3 sweep with the factors rebuilt in the sweep (a_h per column),
+// as the paper's Algorithm 3 does, instead of read from per-cell arrays:
+//   diag_k = (h_k mass + T_{k+1/2} + T_{k-1/2}) + h_k * (sum of the four faces)
+//   D_k = diag_k - T_{k-1/2} * (T_{k-1/2}/D_{k-1}),   1/D_k,   T_{k+1/2}/D_k,
+// each rounded like the set-up kernels round them (no contraction), so the
+// sweep gives bit for bit the result of the stored-factor sweep.  This
+// trades 16 bytes per cell of factor reads for a division, a reciprocal and
+// four more fp64 operations per cell.  T_{k+1/2}/D_k, needed again by the
+// back substitution, goes to a per-warp scratch region (32 x nz doubles,
+// level-major) that stays in L2 like w.
+template <bool FUSED>
+__global__ void __launch_bounds__(kTmThreads) k_precond_tiled_rc(Op op, DevState* st,
+                                                                 double* __restrict__ r,
+                                                                 const double* __restrict__ q,
+                                                                 double* __restrict__ z,
+                                                                 double* __restrict__ partials,
+                                                                 double* __restrict__ hist) {
+  if (FUSED && ld_done(st)) return;
+  const int lane = threadIdx.x & 31;
+  const long long warp0 = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  const int nz = op.nz;
+  const double* __restrict__ lev = op.lev;
+  double* __restrict__ ns = op.nscratch + warp0 * nz * kTile + lane;  // level k at ns[k*32]
+  const double nalpha = FUSED ? -st->alpha : 0.0;
+  const uint64_t keep = l2_keep(), stream = l2_stream();
+  double accR = 0.0, accK = 0.0;
+  for (long long t = warp0; t < op.ntiles; t += nwarps) {
+    const long long col = t * kTile + lane;
+    if (col >= op.ncols) continue;
+    const long long base = t * nz * kTile + lane;
+    double* __restrict__ rt = r + base;
+    const double* __restrict__ qt = FUSED ? q + base : nullptr;
+    double* __restrict__ zt = z + base;
+    const Nbr nb = neighbours(op, col);
+    const double sf = op.faceE[col] + op.faceE[nb.w] + op.faceN[col] + op.faceN[nb.s];
+    // ---- forward
+    double cr[kTmChunk], cq[kTmChunk];
+#pragma unroll
+    for (int j = 0; j < kTmChunk; ++j) {
+      const bool in = j < nz;
+      cr[j] = in ? ld_hint(rt + j * kTile, stream) : 0.0;
+      cq[j] = (FUSED && in) ? ld_hint(qt + j * kTile, stream) : 0.0;
+    }
+    double y = 0.0, nprev = 0.0, w = 0.0;
+#pragma unroll 1
+    for (int k0 = 0; k0 < nz; k0 += kTmChunk) {
+      double nr[kTmChunk], nq[kTmChunk];
+#pragma unroll
+      for (int j = 0; j < kTmChunk; ++j) {
+        const int k = k0 + kTmChunk + j;
+        const bool in = k < nz;
+        nr[j] = in ? ld_hint(rt + k * kTile, stream) : 0.0;
+        nq[j] = (FUSED && in) ? ld_hint(qt + k * kTile, stream) : 0.0;
+      }
+#pragma unroll
+      for (int j = 0; j < kTmChunk; ++j) {
+        const int k = k0 + j;
+        if (k < nz) {
+          const double diag = __dadd_rn(__ldg(lev + LV_DIAG * nz + k),
+                                        __dmul_rn(__ldg(lev + LV_H * nz + k), sf));
+          const double D = __dsub_rn(diag, __dmul_rn(__ldg(lev + LV_TDN * nz + k), nprev));
+          const double invd = 1.0 / D;
+          const double nphi = __ldg(lev + LV_TUP * nz + k) / D;
+          double rk = cr[j];
+          if (FUSED) {
+            rk = fma(nalpha, cq[j], rk);
+            accR = fma(rk, rk, accR);
+            st_hint(rt + k * kTile, rk, stream);
+          }
+          y = fma(nprev, y, rk);
+          w = y * invd;
+          if (FUSED) accK = fma(y, w, accK);
+          st_hint(zt + k * kTile, w, keep);
+          st_hint(ns + k * kTile, nphi, keep);
+          nprev = nphi;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kTmChunk; ++j) {
+        cr[j] = nr[j];
+        cq[j] = nq[j];
+      }
+    }
+    // ---- backward, as in the stored-factor sweep with nphi from the scratch
+    double zz = w;
+    double bw[kTmChunk], bn[kTmChunk];
+#pragma unroll
+    for (int j = 0; j < kTmChunk; ++j) {
+      const int k = nz - 2 - j;
+      bw[j] = (k >= 0) ? ld_hint(zt + k * kTile, stream) : 0.0;
+      bn[j] = (k >= 0) ? ld_hint(ns + k * kTile, stream) : 0.0;
+    }
+#pragma unroll 1
+    for (int kb = nz - 2; kb >= 0; kb -= kTmChunk) {
+      double nw[kTmChunk], nb2[kTmChunk];
+#pragma unroll
+      for (int j = 0; j < kTmChunk; ++j) {
+        const int k = kb - kTmChunk - j;
+        nw[j] = (k >= 0) ? ld_hint(zt + k * kTile, stream) : 0.0;
+        nb2[j] = (k >= 0) ? ld_hint(ns + k * kTile, stream) : 0.0;
+      }
+#pragma unroll
+      for (int j = 0; j < kTmChunk; ++j) {
+        const int k = kb - j;
+        if (k >= 0) {
+          zz = fma(bn[j], zz, bw[j]);
+          st_hint(zt + k * kTile, zz, stream);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kTmChunk; ++j) {
+        bw[j] = nw[j];
+        bn[j] = nb2[j];
+      }
+    }
+  }
+  if (FUSED) {
+    double R, K;
+    if (grid_sum2<kTmThreads>(accR, accK, partials, &st->ticket_m, R, K))
+      finish_precond_sweep(st, R, K, hist);
+  }
+}
+
 // Algorithm 2 sweep on row-tiled vectors: u += alpha p; p = z + beta p;
 // q = A z + beta q; <p,q>.  One thread per column walking up the levels
 // with z_{k-1}, z_k, z_{k+1} in registers; the horizontal neighbours are
@@ -213,7 +337,7 @@ __global__ void __launch_bounds__(kTmThreads) k_precond_tiled(Op op, DevState* s
 // grids with few tiles still give every warp several units; units are
 // assigned statically (segment-major), which keeps the sum bitwise
 // repeatable.
-template <bool VARY>
+template <bool VARY, bool RECOMP>
 __global__ void __launch_bounds__(256) k_spmv_tiled(Op op, DevState* st,
                                                     const double* __restrict__ z,
                                                     double* __restrict__ u,
@@ -247,6 +371,8 @@ __global__ void __launch_bounds__(256) k_spmv_tiled(Op op, DevState* st,
       aN = __ldg(op.faceN + col);
       aS = __ldg(op.faceN + nb.s);
     }
+    // RECOMP: the diagonal rebuilt as the set-up kernel rounds it
+    const double sf = RECOMP ? aE + aW + aN + aS : 0.0;
     double zd = (k0 > 0) ? z[base + (long long)(k0 - 1) * kTile] : 0.0;
     double zc = z[base + (long long)k0 * kTile];
 #pragma unroll 4
@@ -266,7 +392,8 @@ __global__ void __launch_bounds__(256) k_spmv_tiled(Op op, DevState* st,
         hs = fma(aW, zW, hs);
         hs = fma(aN, zN, hs);
         hs = fma(aS, zS, hs);
-        d = __ldcs(op.cdiag_t + o);
+        d = RECOMP ? __dadd_rn(__ldg(lev + LV_DIAG * nz + k), __dmul_rn(__ldg(lev + LV_H * nz + k), sf))
+                   : __ldcs(op.cdiag_t + o);
       } else {
         hs = (zE + zW) + (zN + zS);
         d = __ldg(lev + LV_DIAG * nz + k);
@@ -332,7 +459,9 @@ cudaError_t launch_from_tiled(const Op& op, const DevState* st, const double* sr
 cudaError_t launch_precond_tiled(const Op& op, DevState* st, double* r, const double* q,
                                  double* z, double* partials, double* hist, int grid,
                                  cudaStream_t s) {
-  if (op.varying)
+  if (op.varying && op.recompute)
+    k_precond_tiled_rc<true><<<grid, kTmThreads, 0, s>>>(op, st, r, q, z, partials, hist);
+  else if (op.varying)
     k_precond_tiled<true, true><<<grid, kTmThreads, 0, s>>>(op, st, r, q, z, partials, hist);
   else
     k_precond_tiled<false, true><<<grid, kTmThreads, 0, s>>>(op, st, r, q, z, partials, hist);
@@ -342,10 +471,12 @@ cudaError_t launch_precond_tiled(const Op& op, DevState* st, double* r, const do
 cudaError_t launch_spmv_tiled(const Op& op, DevState* st, const double* z, double* u, double* p,
                               double* q, double* partials, int grid, cudaStream_t s) {
   const int seglen = tiled_spmv_seglen(op, grid);
-  if (op.varying)
-    k_spmv_tiled<true><<<grid, 256, 0, s>>>(op, st, z, u, p, q, partials, seglen);
+  if (op.varying && op.recompute)
+    k_spmv_tiled<true, true><<<grid, 256, 0, s>>>(op, st, z, u, p, q, partials, seglen);
+  else if (op.varying)
+    k_spmv_tiled<true, false><<<grid, 256, 0, s>>>(op, st, z, u, p, q, partials, seglen);
   else
-    k_spmv_tiled<false><<<grid, 256, 0, s>>>(op, st, z, u, p, q, partials, seglen);
+    k_spmv_tiled<false, false><<<grid, 256, 0, s>>>(op, st, z, u, p, q, partials, seglen);
   return cudaGetLastError();
 }
 
@@ -365,9 +496,9 @@ int grid_tiled_precond(const Op& op, int num_sms) {
 int grid_tiled_spmv(const Op& op, int num_sms) {
   int b = 0;
   if (op.varying)
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_spmv_tiled<true>, 256, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_spmv_tiled<true, false>, 256, 0);
   else
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_spmv_tiled<false>, 256, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_spmv_tiled<false, false>, 256, 0);
   long long g = (long long)std::max(1, b) * num_sms;
   // enough blocks for one unit per warp at the shortest segments
   const long long units = op.ntiles * std::max(1, op.nz / 4);

@@ -91,7 +91,13 @@ SOLVE_CASES = [
 ]
 
 
-@pytest.mark.parametrize("layout", ["column", "tiled"])
+def configure(s, mode):
+    """mode: "column", "tiled" (stored factors) or "tiled_recompute"."""
+    s.set_layout("column" if mode == "column" else "tiled")
+    s.set_factors("recompute" if mode == "tiled_recompute" else "stored")
+
+
+@pytest.mark.parametrize("layout", ["column", "tiled", "tiled_recompute"])
 @pytest.mark.parametrize("cfg", SOLVE_CASES, ids=lambda c: "x".join(map(str, c[:3])))
 def test_solve_matches_oracle(cfg, layout):
     nx, ny, nz, varying, graded, a_v = cfg
@@ -99,7 +105,7 @@ def test_solve_matches_oracle(cfg, layout):
     x_ref, it_ref, hist_ref, st_ref = oracle.pcg(prob, b, rtol=1e-10, maxit=500)
     assert st_ref == oracle.OK
     with mf.Solver(nx, ny, nz, **kw) as s:
-        s.set_layout(layout)
+        configure(s, layout)
         bd = torch.from_numpy(b).to(DEV)
         x = torch.zeros_like(bd)
         iters, hist, st = s.solve(bd, x, rtol=1e-10, maxit=500)
@@ -115,11 +121,11 @@ def test_solve_matches_oracle(cfg, layout):
     assert np.linalg.norm(xs - x_ref) <= SOL_TOL * np.linalg.norm(x_ref)
 
 
-@pytest.mark.parametrize("layout", ["column", "tiled"])
+@pytest.mark.parametrize("layout", ["column", "tiled", "tiled_recompute"])
 def test_solve_is_bitwise_repeatable(layout):
     prob, kw, b = case(40, 36, 64, True, True, a_v=1e4, seed=5)
     with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
-        s.set_layout(layout)
+        configure(s, layout)
         bd = torch.from_numpy(b).to(DEV)
         x1, x2 = torch.zeros_like(bd), torch.zeros_like(bd)
         i1, h1, _ = s.solve(bd, x1, rtol=1e-10)
@@ -257,3 +263,42 @@ def test_layouts_agree_and_switch_back_and_forth():
     assert np.array_equal(xs["tiled"][0], xs["tiled"][1])
     xc, xt = xs["column"][0], xs["tiled"][0]
     assert np.linalg.norm(xt - xc) <= 1e-12 * np.linalg.norm(xc)
+
+
+@pytest.mark.parametrize("cfg", [c for c in SOLVE_CASES if c[3]], ids=lambda c: "x".join(map(str, c[:3])))
+def test_recomputed_factors_give_the_stored_iterates_bit_for_bit(cfg):
+    # the sweeps rebuild the diagonal and the Thomas factors with the set-up's
+    # rounding, so nothing but the data source differs
+    nx, ny, nz, varying, graded, a_v = cfg
+    prob, kw, b = case(nx, ny, nz, varying, graded, a_v=a_v, seed=7)
+    with mf.Solver(nx, ny, nz, **kw) as s:
+        bd = torch.from_numpy(b).to(DEV)
+        out = {}
+        for mode in ["stored", "recompute", "stored"]:
+            s.set_factors(mode)
+            x = torch.zeros_like(bd)
+            it, hist, st = s.solve(bd, x, rtol=1e-10, maxit=500)
+            assert st == mf.PCG_OK
+            out.setdefault(mode, []).append((it, hist, x.cpu().numpy()))
+    (i0, h0, x0), (i2, h2, x2) = out["stored"]
+    (i1, h1, x1), = out["recompute"]
+    assert i0 == i1 == i2
+    assert np.array_equal(h0, h1) and np.array_equal(h0, h2)
+    assert np.array_equal(x0, x1) and np.array_equal(x0, x2)
+
+
+def test_factor_mode_arguments_and_column_layout():
+    prob, kw, b = case(20, 12, 16, True, True, a_v=1e3, seed=8)
+    with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        with pytest.raises(mf.PCGError) as e:
+            mf.pcg_set_factors(s.ctx, 2)
+        assert e.value.status == mf.PCG_EINVAL
+        bd = torch.from_numpy(b).to(DEV)
+        xs = []
+        s.set_layout("column")
+        for mode in ["stored", "recompute"]:   # the column layout always reads stored factors
+            s.set_factors(mode)
+            x = torch.zeros_like(bd)
+            s.solve(bd, x, rtol=1e-10)
+            xs.append(x.cpu().numpy())
+    assert np.array_equal(xs[0], xs[1])

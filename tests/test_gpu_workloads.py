@@ -89,14 +89,16 @@ def test_workload_large_parity(name, fixed_iters):
     with mf.Solver(w.nx, w.ny, w.nz, **kw) as s:
         bd = sampled_operator_checks(w, prob, s, b)
         x = torch.zeros_like(bd)
-        for layout in ["tiled", "column"]:
+        for layout, factors in [("tiled", "recompute"), ("tiled", "stored"), ("column", "stored")]:
             s.set_layout(layout)
+            s.set_factors(factors)
             x.zero_()
             it, _, st = s.solve(bd, x, rtol=0.0, maxit=fixed_iters)
             assert (it, st) == (fixed_iters, mf.PCG_OK)
             xs = x.cpu().numpy()
-            assert np.linalg.norm(xs - x_ref) <= 1e-8 * np.linalg.norm(x_ref), layout
+            assert np.linalg.norm(xs - x_ref) <= 1e-8 * np.linalg.norm(x_ref), (layout, factors)
         del xs, x_ref
+        s.set_layout("tiled")
         # the workload's own stopping rule, then the true residual on the CPU
         x.zero_()
         it, hist, st = s.solve(bd, x, rtol=w.rtol, maxit=w.maxit)
