@@ -70,6 +70,9 @@ def parse():
     ap.add_argument("--factors", choices=["stored", "recompute"], default="stored",
                     help="per-cell factors of an a_h field read from arrays or rebuilt in "
                          "every sweep (row-tiled layout)")
+    ap.add_argument("--substructuring", type=int, default=0,
+                    help="blocks per column of the substructured preconditioner solve "
+                         "(0 automatic, 1 off, 2/4/8/16)")
     ap.add_argument("--grid", type=int, nargs=3, metavar=("NX", "NY", "NZ"),
                     help="same coefficients on another grid size (profiling captures)")
     return ap.parse_args()
@@ -191,10 +194,19 @@ def measured_traffic(kernel, cells, layout, factors):
 
 
 def workload_inputs(w):
-    h, ah, vec = W.make_inputs(w)
-    if w.rhs == "manufactured":
-        raise SystemExit("bench.py times right-hand-side workloads only")
-    return h, ah, vec
+    """(h, a_h field, vector): the right-hand side, or for a manufactured
+    workload the solution u* whose image b = A u* the caller forms."""
+    return W.make_inputs(w)
+
+
+def oracle_rhs(w, h, ah, vec):
+    """b on the host for the oracle legs (b = A u* by the oracle's own operator
+    for a manufactured workload)."""
+    if w.rhs != "manufactured":
+        return vec
+    import oracle
+    prob = oracle.Problem(w.nx, w.ny, w.nz, ah=ah, a_v=w.a_v, mass=w.mass, h=h)
+    return oracle.apply_A(prob, vec)
 
 
 def cpu_oracle_sample(w, h, ah, b, iters):
@@ -211,7 +223,8 @@ def run_reference(args, w):
     rank, world, _ = rank_info()
     if rank != 0:
         return 0
-    h, ah, b = workload_inputs(w)
+    h, ah, vec = workload_inputs(w)
+    b = oracle_rhs(w, h, ah, vec)
     for _ in range(args.warmup):
         cpu_oracle_sample(w, h, ah, b, args.cpu_iters)
     tot_it, tot_t = 0, 0.0
@@ -249,16 +262,20 @@ def run_ours(args, w):
     dev = torch.device("cuda", local)
     import matrix_free_pcg_gb300 as mf
 
-    h, ah, b = workload_inputs(w)
+    h, ah, vec = workload_inputs(w)
     varying = w.varying_ah
     coeffs = dict(a_h=w.a_h, a_h_field=ah if varying else None, a_v=w.a_v, mass=w.mass, dz=h)
     solver = mf.Solver(w.nx, w.ny, w.nz, **coeffs)
-    bd = torch.from_numpy(b).to(dev)
-    x = torch.zeros_like(bd)
     stream = torch.cuda.current_stream(dev)
     solver.set_stream(stream)
+    bd = torch.from_numpy(vec).to(dev)
+    if w.rhs == "manufactured":  # b = A u*, formed by the library's own operator
+        bd = solver.apply_A(bd)
+    b = bd.cpu().numpy()
+    x = torch.zeros_like(bd)
     solver.set_layout(args.layout)
     solver.set_factors(args.factors)
+    solver.set_substructuring(args.substructuring)
     recompute = args.factors == "recompute" and varying and args.layout == "tiled"
 
     def step():
@@ -362,7 +379,7 @@ def run_ours(args, w):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        it_c, dt_c = cpu_oracle_sample(w, h, ah, b, args.cpu_iters)
+        it_c, dt_c = cpu_oracle_sample(w, h, ah, oracle_rhs(w, h, ah, vec), args.cpu_iters)
         cpu = {"value": it_c / dt_c, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": "oracle_pcg on the full %dx%dx%d grid, %d fixed PCG iterations "
                          "(initial residual and first preconditioner solve included), "
@@ -380,6 +397,7 @@ def run_ours(args, w):
                        "graded": w.graded, "varying_ah": varying,
                        "l2": "inputs larger than L2 (1.07 GB per vector)",
                        "layout": args.layout, "factors": args.factors,
+                       "substructuring": solver.substructuring,
                        "parallelism": "replicas" if world > 1 else "single"},
             "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / hbm_peak,
             "bytes_per_cell_iter": bytes_iter / n, "fp64_ops_per_cell_iter": ops_iter / n,

@@ -128,6 +128,35 @@ int pcg_set_layout(pcg_ctx* ctx, int layout);
 enum { PCG_FACTORS_STORED = 0, PCG_FACTORS_RECOMPUTE = 1 };
 int pcg_set_factors(pcg_ctx* ctx, int mode);
 
+/* How the preconditioner sweep of the row-tiled layout solves each column
+ * system of M (eq. (19)):
+ *   nblocks = 1        one thread walks the whole column (Thomas algorithm);
+ *   nblocks = 2,4,8,16 substructuring (section 6.1): the column is cut into
+ *                      nblocks blocks by nblocks-1 interface levels; the
+ *                      blocks are solved independently by different warps,
+ *                      then the interface (Schur complement) system, then
+ *                      the blocks are corrected.  Same M^{-1} r up to
+ *                      rounding (a few units of cond(T) * eps); more
+ *                      parallelism for grids with few columns.  Needs
+ *                      nz >= 2*nblocks-1 and 256*(2*nz+4*nblocks+1) bytes
+ *                      of shared memory per block of nblocks warps;
+ *   nblocks = 0        (default) automatic: 4 (or 2) blocks only for grids
+ *                      with fewer tiles of 32 columns than half the SMs,
+ *                      where the sweep is latency-bound; else 1.  (The
+ *                      substructured sweep does 8 fp64 operations per cell
+ *                      against 6, and the fp64 rate bounds larger grids.)
+ * The substructured sweep keeps its own per-cell tables (four doubles per
+ * cell, rebuilt by pcg_update_coeffs); it takes precedence over
+ * PCG_FACTORS_RECOMPUTE.  The column layout always uses Thomas.  Synchronous.
+ * Errors: PCG_EINVAL (bad nblocks, columns too tall), PCG_ENOMEM, PCG_ECUDA,
+ * PCG_EBREAKDOWN (a pivot of the block or interface system is not
+ * positive). */
+int pcg_set_substructuring(pcg_ctx* ctx, int nblocks);
+
+/* Blocks per column the row-tiled preconditioner sweep currently uses
+ * (1: Thomas), after the automatic choice.  Errors: PCG_EINVAL (NULL). */
+int pcg_get_substructuring(const pcg_ctx* ctx, int* nblocks_out);
+
 /* y = A x, the matrix-free 7-point stencil of eq. (18), standalone.
  * x_dev, y_dev: device, N values each, must not overlap.  Asynchronous. */
 int pcg_apply_A(pcg_ctx* ctx, const double* x_dev, double* y_dev);

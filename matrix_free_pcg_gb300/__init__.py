@@ -31,7 +31,8 @@ PCG_K_COUNT = len(KERNEL_KINDS)
 EXPORTED = ["pcg_create", "pcg_destroy", "pcg_update_coeffs", "pcg_set_stream", "pcg_apply_A",
             "pcg_precond", "pcg_solve", "pcg_solve_host", "pcg_last_error",
             "pcg_enable_timing", "pcg_kernel_times", "pcg_launch_info",
-            "pcg_precond_dot_noalloc", "pcg_set_layout", "pcg_set_factors"]
+            "pcg_precond_dot_noalloc", "pcg_set_layout", "pcg_set_factors",
+            "pcg_set_substructuring", "pcg_get_substructuring"]
 PCG_LAYOUT_COLUMN, PCG_LAYOUT_TILED = 0, 1
 PCG_FACTORS_STORED, PCG_FACTORS_RECOMPUTE = 0, 1
 
@@ -71,6 +72,8 @@ def _load(path=LIB_PATH):
         "pcg_precond_dot_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
         "pcg_set_layout": (ctypes.c_int, [_vp, ctypes.c_int]),
         "pcg_set_factors": (ctypes.c_int, [_vp, ctypes.c_int]),
+        "pcg_set_substructuring": (ctypes.c_int, [_vp, ctypes.c_int]),
+        "pcg_get_substructuring": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -186,6 +189,19 @@ def pcg_set_factors(ctx, mode):
     return _check(_lib.pcg_set_factors(ctx, int(mode)), ctx)
 
 
+def pcg_set_substructuring(ctx, nblocks):
+    """Blocks per column of the substructured preconditioner solve (row-tiled
+    layout): 0 automatic (default), 1 off (Thomas), 2, 4, 8 or 16."""
+    return _check(_lib.pcg_set_substructuring(ctx, int(nblocks)), ctx)
+
+
+def pcg_get_substructuring(ctx):
+    """Blocks per column in use by the row-tiled preconditioner sweep (1: Thomas)."""
+    v = ctypes.c_int(0)
+    _check(_lib.pcg_get_substructuring(ctx, ctypes.byref(v)), ctx)
+    return v.value
+
+
 def pcg_apply_A(ctx, n, x, y):
     return _check(_lib.pcg_apply_A(ctx, _dev_ptr(x, n, "x"), _dev_ptr(y, n, "y")), ctx)
 
@@ -294,6 +310,15 @@ class Solver:
         if isinstance(layout, str):
             layout = {"column": PCG_LAYOUT_COLUMN, "tiled": PCG_LAYOUT_TILED}[layout]
         pcg_set_layout(self.ctx, layout)
+
+    def set_substructuring(self, nblocks):
+        """0 automatic, 1 off, or 2/4/8/16 blocks per column."""
+        pcg_set_substructuring(self.ctx, nblocks)
+
+    @property
+    def substructuring(self):
+        """Blocks per column in use (after the automatic choice)."""
+        return pcg_get_substructuring(self.ctx)
 
     def set_factors(self, mode):
         """"stored" / PCG_FACTORS_STORED or "recompute" / PCG_FACTORS_RECOMPUTE."""

@@ -49,6 +49,9 @@ struct pcg_ctx {
   int grid_tm = 1, grid_ta = 1;  // row-tiled preconditioner / stencil sweeps
   int factors = PCG_FACTORS_STORED;  // per-cell factors read (stored) or rebuilt per sweep
   double* nscratch = nullptr;        // recompute: per-warp T_{k+1/2}/D_k scratch
+  // substructured column solve: requested blocks (0 automatic), blocks in use, grid
+  int split_req = 0, split_p = 1, grid_sp = 0;
+  size_t partials_cap = 0;           // doubles in `partials`
   int hist_cap = 0;
   DevState* state = nullptr;
   double *b_host_api = nullptr, *x_host_api = nullptr;  // device copies for pcg_solve_host
@@ -167,7 +170,9 @@ void free_all(pcg_ctx* ctx) {
   double* bufs[] = {ctx->r,     ctx->z,     ctx->p,     ctx->q,        ctx->lev,
                     ctx->ah,    ctx->faceE, ctx->faceN, ctx->cdiag,    ctx->tnphi,
                     ctx->tinvd, ctx->partials, ctx->hist, ctx->b_host_api, ctx->x_host_api,
-                    ctx->wscratch, ctx->u_t, ctx->cdiag_t, ctx->nscratch};
+                    ctx->wscratch, ctx->u_t, ctx->cdiag_t, ctx->nscratch,
+                    ctx->op.sp_nphi, ctx->op.sp_invd, ctx->op.sp_ta, ctx->op.sp_tb,
+                    ctx->op.sp_corners, ctx->op.sp_invdS, ctx->op.sp_nphiS};
   for (double* b : bufs)
     if (b) cudaFree(b);
   if (ctx->state) cudaFree(ctx->state);
@@ -178,6 +183,37 @@ void free_all(pcg_ctx* ctx) {
 
 // Upload coefficients and (for a field) rebuild the per-column and per-cell
 // tables on the device.  Synchronous.
+// Tables of the substructured column solve for the current coefficients.
+// Synchronous.
+int run_split_setup(pcg_ctx* ctx) {
+  cudaError_t e = cudaMemsetAsync(&ctx->state->setup_error, 0, sizeof(int), ctx->stream);
+  cudaEvent_t t0 = nullptr, t1 = nullptr;
+  if (ctx->timing) {
+    cudaEventCreate(&t0);
+    cudaEventCreate(&t1);
+    if (t0) cudaEventRecord(t0, ctx->stream);
+  }
+  if (e == cudaSuccess) e = pcg::launch_split_setup(ctx->op, ctx->split_p, ctx->state, ctx->stream);
+  if (t1) cudaEventRecord(t1, ctx->stream);
+  int bad = 0;
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(&bad, &ctx->state->setup_error, sizeof(int), cudaMemcpyDeviceToHost,
+                        ctx->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+  if (t0 && t1) {
+    float ms = 0.0f;
+    if (e == cudaSuccess && cudaEventElapsedTime(&ms, t0, t1) == cudaSuccess) {
+      ctx->ms[PCG_K_SETUP] += ms;
+      ctx->launches[PCG_K_SETUP] += 2;
+    }
+  }
+  if (t0) cudaEventDestroy(t0);
+  if (t1) cudaEventDestroy(t1);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "substructuring set-up");
+  if (bad) return fail(ctx, PCG_EBREAKDOWN, "a pivot of the substructured column solve is not positive");
+  return PCG_OK;
+}
+
 int load_coeffs(pcg_ctx* ctx, const pcg_coeffs* c, bool varying) {
   std::vector<double> lev;
   int st = build_levels(ctx, ctx->op.nz, c, varying, lev);
@@ -224,6 +260,7 @@ int load_coeffs(pcg_ctx* ctx, const pcg_coeffs* c, bool varying) {
     e = cudaStreamSynchronize(ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "coefficient upload");
   }
+  if (ctx->split_p > 1) return run_split_setup(ctx);
   return PCG_OK;
 }
 
@@ -295,6 +332,8 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
   ctx->pool_used = 0;
   const bool tiled = ctx->layout == PCG_LAYOUT_TILED;
   op.recompute = (tiled && op.varying && ctx->factors == PCG_FACTORS_RECOMPUTE) ? 1 : 0;
+  const bool split = tiled && ctx->split_p > 1;
+  const int grid_pm = split ? ctx->grid_sp : ctx->grid_tm;  // preconditioner sweep blocks
   op.nscratch = ctx->nscratch;
   // The row-tiled layout forms r = b - A x0 column-contiguously in z, then
   // converts r and x0 into the solver's layout.
@@ -321,6 +360,9 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
     const int nb = std::min(batch, maxit + 1 - enq);
     for (int i = 0; i < nb; ++i) {
       e = timed(ctx, PCG_K_PRECOND_FUSED, [&] {
+        if (split)
+          return pcg::launch_precond_split(op, ctx->split_p, ctx->state, ctx->r, ctx->q, ctx->z,
+                                           ctx->partials, ctx->hist, ctx->grid_sp, s);
         return tiled ? pcg::launch_precond_tiled(op, ctx->state, ctx->r, ctx->q, ctx->z,
                                                  ctx->partials, ctx->hist, ctx->grid_tm, s)
                      : pcg::launch_precond_fused(op, ctx->state, ctx->r, ctx->q, ctx->z,
@@ -330,7 +372,7 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
       if (enq + i < maxit) {
         e = timed(ctx, PCG_K_SPMV_FUSED, [&] {
           return tiled ? pcg::launch_spmv_tiled(op, ctx->state, ctx->z, ctx->u_t, ctx->p, ctx->q,
-                                                ctx->partials + 2 * ctx->grid_tm, ctx->grid_ta, s)
+                                                ctx->partials + 2 * grid_pm, ctx->grid_ta, s)
                        : pcg::launch_spmv_fused(op, ctx->state, ctx->z, x, ctx->p, ctx->q,
                                                 ctx->partials + 2 * ctx->grid_m, ctx->grid_a, s);
         });
@@ -467,8 +509,8 @@ int pcg_create(int nx, int ny, int nz, const pcg_coeffs* coeffs, pcg_ctx** out) 
   ctx->grid_a = pcg::grid_spmv(op, ctx->num_sms);
   ctx->grid_tm = pcg::grid_tiled_precond(op, ctx->num_sms);
   ctx->grid_ta = pcg::grid_tiled_spmv(op, ctx->num_sms);
-  e = dalloc(&ctx->partials,
-             2 * (size_t)std::max(ctx->grid_m + ctx->grid_a, ctx->grid_tm + ctx->grid_ta));
+  ctx->partials_cap = 2 * (size_t)std::max(ctx->grid_m + ctx->grid_a, ctx->grid_tm + ctx->grid_ta);
+  e = dalloc(&ctx->partials, ctx->partials_cap);
   if (e == cudaSuccess && op.fixed)
     e = dalloc(&ctx->wscratch, (size_t)ctx->grid_m * pcg::kTile * nz);
   if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "workspace allocation"));
@@ -476,6 +518,8 @@ int pcg_create(int nx, int ny, int nz, const pcg_coeffs* coeffs, pcg_ctx** out) 
   st = load_coeffs(ctx, coeffs, varying);
   if (st) return bail(st);
   st = pcg_set_layout(ctx, PCG_LAYOUT_TILED);  // the default solver layout
+  if (st) return bail(st);
+  st = pcg_set_substructuring(ctx, 0);  // automatic: only grids with few tiles
   if (st) return bail(st);
   *out = ctx;
   return PCG_OK;
@@ -538,6 +582,81 @@ int pcg_set_factors(pcg_ctx* ctx, int mode) {
     }
   }
   ctx->factors = mode;
+  return PCG_OK;
+}
+
+// Automatic blocks per column.  Substructuring adds two fp64 operations per
+// cell (the spike correction) to the six of the sweep, and on this part the
+// sweep is fp64-bound as soon as the grid has a few hundred tiles of 32
+// columns (measured: 128x128x64, 512 tiles, Thomas 31 us against 33 us with
+// 2 or 4 blocks).  Only grids with fewer tiles than half the SMs, where the
+// sweep is latency-bound, take 4 blocks (32x32x16: 14.1 us against 16.0 us),
+// or fewer if the column is too short.
+int auto_split(pcg_ctx* ctx) {
+  if (ctx->op.ntiles * 2 >= ctx->num_sms) return 1;
+  for (int P = 4; P >= 2; P /= 2)
+    if (pcg::split_valid(ctx->op.nz, P) && pcg::split_grid(ctx->op, P, ctx->num_sms) > 0) return P;
+  return 1;
+}
+
+int pcg_set_substructuring(pcg_ctx* ctx, int nblocks) {
+  if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
+  const int nz = ctx->op.nz;
+  if (nblocks != 0 && nblocks != 1 && !pcg::split_valid(nz, nblocks))
+    return fail(ctx, PCG_EINVAL,
+                "nblocks %d: must be 0, 1, 2, 4, 8 or 16, with nz (%d) >= 2*nblocks-1", nblocks,
+                nz);
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
+  int P = (nblocks == 0) ? auto_split(ctx) : nblocks;
+  int grid = 0;
+  if (P > 1) {
+    grid = pcg::split_grid(ctx->op, P, ctx->num_sms);
+    if (grid == 0)
+      return fail(ctx, PCG_EINVAL, "columns of %d levels do not fit the substructured sweep", nz);
+  }
+  cudaError_t e = cudaStreamSynchronize(ctx->stream);
+  Op& op = ctx->op;
+  if (e == cudaSuccess && P != ctx->split_p) {
+    double** tabs[] = {&op.sp_nphi, &op.sp_invd, &op.sp_ta,    &op.sp_tb,
+                       &op.sp_corners, &op.sp_invdS, &op.sp_nphiS};
+    for (double** t : tabs) {
+      if (*t) cudaFree(*t);
+      *t = nullptr;
+    }
+    ctx->split_p = 1;
+    if (P > 1) {
+      const size_t npad = (size_t)op.ntiles * pcg::kTile * nz;
+      const size_t per_col = (size_t)op.ntiles * pcg::kTile;
+      e = dalloc(&op.sp_nphi, npad);
+      if (e == cudaSuccess) e = dalloc(&op.sp_invd, npad);
+      if (e == cudaSuccess) e = dalloc(&op.sp_ta, npad);
+      if (e == cudaSuccess) e = dalloc(&op.sp_tb, npad);
+      if (e == cudaSuccess) e = dalloc(&op.sp_corners, per_col * 4 * P);
+      if (e == cudaSuccess) e = dalloc(&op.sp_invdS, per_col * (P - 1));
+      if (e == cudaSuccess) e = dalloc(&op.sp_nphiS, per_col * (P - 1));
+    }
+  }
+  const size_t need = 2 * (size_t)(grid + ctx->grid_ta);
+  if (e == cudaSuccess && need > ctx->partials_cap) {
+    double* np = nullptr;
+    e = dalloc(&np, need);
+    if (e == cudaSuccess) {
+      cudaFree(ctx->partials);
+      ctx->partials = np;
+      ctx->partials_cap = need;
+    }
+  }
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "substructuring tables");
+  ctx->split_req = nblocks;
+  ctx->split_p = P;
+  ctx->grid_sp = grid;
+  return (P > 1) ? run_split_setup(ctx) : PCG_OK;
+}
+
+int pcg_get_substructuring(const pcg_ctx* ctx, int* nblocks_out) {
+  if (!ctx || !nblocks_out) return fail(nullptr, PCG_EINVAL, "NULL argument");
+  *nblocks_out = ctx->split_p;
   return PCG_OK;
 }
 
@@ -658,7 +777,8 @@ int pcg_launch_info(const pcg_ctx* ctx, int* grid_precond, int* grid_spmv,
                     long long* last_solve_launches) {
   if (!ctx) return PCG_EINVAL;
   const bool tiled = ctx->layout == PCG_LAYOUT_TILED;
-  if (grid_precond) *grid_precond = tiled ? ctx->grid_tm : ctx->grid_m;
+  if (grid_precond)
+    *grid_precond = tiled ? (ctx->split_p > 1 ? ctx->grid_sp : ctx->grid_tm) : ctx->grid_m;
   if (grid_spmv) *grid_spmv = tiled ? ctx->grid_ta : ctx->grid_a;
   if (last_solve_launches) *last_solve_launches = ctx->last_launches;
   return PCG_OK;

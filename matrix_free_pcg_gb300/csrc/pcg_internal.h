@@ -43,6 +43,14 @@ struct Op {
                        // factors in every sweep instead of reading them per cell
   double* nscratch;    // recompute: T_{k+1/2}/D_k of the tiles in flight, 32*nz doubles
                        // per warp of the preconditioner grid
+  // substructured column solve (pcg_split.cu), row-tiled tables
+  double* sp_nphi;     // per cell: T_{k+1/2}/D_k of the block's own LDL^T (0 at its top)
+  double* sp_invd;     // per cell: 1/D_k of the block's LDL^T
+  double* sp_ta;       // per cell: T_{s-1/2} (T_i^{-1} e_first)_k
+  double* sp_tb;       // per cell: T_{s+m-1/2} (T_i^{-1} e_last)_k
+  double* sp_corners;  // per column and block: corners of T_i^{-1} (set-up only)
+  double* sp_invdS;    // per column and interface: 1/D of the interface system's LDL^T
+  double* sp_nphiS;    // per column and interface: its -S_{j,j+1}/D_j
   long long ncols;     // nx*ny
   long long n;         // ncols*nz
   long long ntiles;    // ceil(ncols / kTile)
@@ -124,11 +132,26 @@ cudaError_t launch_precond_tiled(const Op& op, DevState* st, double* r, const do
                                  cudaStream_t s);
 cudaError_t launch_spmv_tiled(const Op& op, DevState* st, const double* z, double* u, double* p,
                               double* q, double* partials, int grid, cudaStream_t s);
-// Warps per block of the row-tiled preconditioner sweep.
+// Warps per block of the row-tiled preconditioner sweep, and its resident
+// warps per SM (each warp keeps the w of its tile and the factors the
+// backward pass reads again live in L2; 12 per SM keep this within L2 at
+// nz = 128 and leave three warps per sub-partition to hide fp64 latency).
 constexpr int kTmWarpsPerBlock = 4;
+constexpr int kTmWarpsPerSm = 12;
 // Grid sizes (blocks) of the two row-tiled sweeps.
 int grid_tiled_precond(const Op& op, int num_sms);
 int grid_tiled_spmv(const Op& op, int num_sms);
+
+// Substructured column solve (pcg_split.cu): P blocks per column, P in
+// {2, 4, 8, 16}, nz >= 2P-1.  Tables in op.sp_*; set-up after every
+// coefficient change; sweep = Algorithm 3 with a block of P warps per tile.
+bool split_valid(int nz, int P);
+size_t split_smem_bytes(int nz, int P);
+int split_grid(const Op& op, int P, int num_sms);  // 0: not launchable
+cudaError_t launch_split_setup(const Op& op, int P, DevState* st, cudaStream_t s);
+cudaError_t launch_precond_split(const Op& op, int P, DevState* st, double* r, const double* q,
+                                 double* z, double* partials, double* hist, int grid,
+                                 cudaStream_t s);
 
 // Occupancy-derived grid sizes (blocks) for the persistent sweeps.  The
 // preconditioner's also fixes op.stream_smem (see pcg_kernels.cu).

@@ -25,12 +25,6 @@ namespace {
 // Preconditioner sweep: threads per block and levels per register chunk.
 constexpr int kTmThreads = kTmWarpsPerBlock * 32;
 constexpr int kTmChunk = 8;
-// Resident warps per SM of the preconditioner sweep.  Each warp keeps the w
-// of its tile (32 x nz doubles) and the factors the backward pass reads a
-// second time live in L2 between the two passes; 12 warps per SM keep this
-// within L2 at nz = 128 while leaving three warps per sub-partition to hide
-// the fp64 latency of the serial recurrences.
-constexpr int kTmWarpsPerSm = 12;
 
 __device__ __forceinline__ long long tiled_base(long long col, int nz) {
   return (col >> 5) * (long long)nz * kTile + (col & 31);

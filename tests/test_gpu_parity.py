@@ -92,12 +92,18 @@ SOLVE_CASES = [
 
 
 def configure(s, mode):
-    """mode: "column", "tiled" (stored factors) or "tiled_recompute"."""
+    """mode: "column"; "tiled" (Thomas column solves, stored factors);
+    "tiled_recompute" (Thomas, factors rebuilt per sweep); "tiled_split"
+    (substructured column solves, blocks chosen automatically)."""
     s.set_layout("column" if mode == "column" else "tiled")
     s.set_factors("recompute" if mode == "tiled_recompute" else "stored")
+    s.set_substructuring(0 if mode == "tiled_split" else 1)
 
 
-@pytest.mark.parametrize("layout", ["column", "tiled", "tiled_recompute"])
+MODES = ["column", "tiled", "tiled_recompute", "tiled_split"]
+
+
+@pytest.mark.parametrize("layout", MODES)
 @pytest.mark.parametrize("cfg", SOLVE_CASES, ids=lambda c: "x".join(map(str, c[:3])))
 def test_solve_matches_oracle(cfg, layout):
     nx, ny, nz, varying, graded, a_v = cfg
@@ -121,7 +127,7 @@ def test_solve_matches_oracle(cfg, layout):
     assert np.linalg.norm(xs - x_ref) <= SOL_TOL * np.linalg.norm(x_ref)
 
 
-@pytest.mark.parametrize("layout", ["column", "tiled", "tiled_recompute"])
+@pytest.mark.parametrize("layout", MODES)
 def test_solve_is_bitwise_repeatable(layout):
     prob, kw, b = case(40, 36, 64, True, True, a_v=1e4, seed=5)
     with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
@@ -250,6 +256,7 @@ def test_kernel_timing_counts_launches(layout):
 def test_layouts_agree_and_switch_back_and_forth():
     prob, kw, b = case(45, 33, 64, True, True, a_v=1e4, seed=12)
     with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        s.set_substructuring(1)  # Thomas column solves in both layouts
         bd = torch.from_numpy(b).to(DEV)
         xs = {}
         for layout in ["tiled", "column", "tiled"]:
@@ -272,6 +279,7 @@ def test_recomputed_factors_give_the_stored_iterates_bit_for_bit(cfg):
     nx, ny, nz, varying, graded, a_v = cfg
     prob, kw, b = case(nx, ny, nz, varying, graded, a_v=a_v, seed=7)
     with mf.Solver(nx, ny, nz, **kw) as s:
+        s.set_substructuring(1)
         bd = torch.from_numpy(b).to(DEV)
         out = {}
         for mode in ["stored", "recompute", "stored"]:
@@ -302,3 +310,100 @@ def test_factor_mode_arguments_and_column_layout():
             s.solve(bd, x, rtol=1e-10)
             xs.append(x.cpu().numpy())
     assert np.array_equal(xs[0], xs[1])
+
+
+# ---- substructured column solves (parallel in k)
+
+SPLIT_CASES = [  # nx, ny, nz, varying, graded, a_v, blocks per column
+    (32, 32, 16, False, False, 1e2, 8),    # the 32x32x16 operator
+    (37, 29, 16, True, True, 1e3, 4),      # ragged last tile
+    (33, 5, 7, True, True, 1e2, 4),        # odd nz: blocks of one level
+    (40, 36, 64, False, True, 1e4, 2),
+    (17, 19, 130, True, True, 1e5, 16),
+    (7, 5, 400, True, False, 1e3, 16),     # blocks of about 24 levels, 221 KB of shared tiles
+]
+
+
+def column_cond(prob):
+    """Largest 2-norm condition number of the column blocks of M (eq. (19)),
+    over the smallest and the largest horizontal face sum of the grid."""
+    nz, h = prob.nz, np.asarray(prob.h)
+    ah = np.asarray(prob.ah).reshape(prob.ny, prob.nx)
+    faces = 0.5 * (ah + np.roll(ah, -1, 1)) + 0.5 * (ah + np.roll(ah, 1, 1)) \
+        + 0.5 * (ah + np.roll(ah, -1, 0)) + 0.5 * (ah + np.roll(ah, 1, 0))
+    t = np.array([prob.a_v / (0.5 * (h[k] + h[k + 1])) for k in range(nz - 1)])
+    conds = []
+    for sf in (faces.min(), faces.max()):
+        d = h * (prob.mass + sf)
+        d[:-1] += t
+        d[1:] += t
+        T = np.diag(d) - np.diag(t, 1) - np.diag(t, -1)
+        conds.append(np.linalg.cond(T))
+    return max(conds)
+
+
+@pytest.mark.parametrize("cfg", SPLIT_CASES, ids=lambda c: "x".join(map(str, c[:3])) + "P%d" % c[6])
+def test_substructured_solve_matches_oracle(cfg):
+    nx, ny, nz, varying, graded, a_v, nb = cfg
+    prob, kw, b = case(nx, ny, nz, varying, graded, a_v=a_v, seed=11)
+    # one iteration: x_1 = alpha M^{-1} b, so x_1 carries the preconditioner's
+    # error, which for a different elimination order is bounded by a few units
+    # of cond(T) * eps of the column blocks T
+    tol1 = max(OP_TOL, column_cond(prob) * np.finfo(float).eps)
+    x1_ref, _, _, _ = oracle.pcg(prob, b, rtol=0.0, maxit=1)
+    x_ref, it_ref, hist_ref, st_ref = oracle.pcg(prob, b, rtol=1e-10, maxit=500)
+    assert st_ref == oracle.OK
+    with mf.Solver(nx, ny, nz, **kw) as s:
+        s.set_substructuring(nb)
+        bd = torch.from_numpy(b).to(DEV)
+        x = torch.zeros_like(bd)
+        assert s.solve(bd, x, rtol=0.0, maxit=1)[0] == 1
+        x1 = x.cpu().numpy()
+        x.zero_()
+        iters, hist, st = s.solve(bd, x, rtol=1e-10, maxit=500)
+        assert st == mf.PCG_OK and abs(iters - it_ref) <= 1
+        np.testing.assert_allclose(hist[: min(iters, it_ref) + 1],
+                                   hist_ref[: min(iters, it_ref) + 1], rtol=1e-6, atol=1e-13)
+        x.zero_()
+        assert s.solve(bd, x, rtol=0.0, maxit=it_ref)[:1] == (it_ref,)
+        xs = x.cpu().numpy()
+    assert rel_maxdiff(x1, x1_ref) <= tol1, (rel_maxdiff(x1, x1_ref), tol1)
+    assert np.linalg.norm(xs - x_ref) <= SOL_TOL * np.linalg.norm(x_ref)
+
+
+def test_substructuring_arguments():
+    prob, kw, b = case(20, 12, 7, True, True, a_v=1e3, seed=9)
+    with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        for bad in (-1, 3, 32, 8):   # 8 blocks need nz >= 15
+            with pytest.raises(mf.PCGError) as e:
+                s.set_substructuring(bad)
+            assert e.value.status == mf.PCG_EINVAL
+        bd = torch.from_numpy(b).to(DEV)
+        out = []
+        for nb in (4, 1, 2, 0, 4):
+            s.set_substructuring(nb)
+            # automatic: 8 tiles of 32 columns (fewer than half the SMs): 4 blocks
+            assert s.substructuring == (4 if nb == 0 else nb)
+            x = torch.zeros_like(bd)
+            it, _, st = s.solve(bd, x, rtol=1e-10)
+            assert st == mf.PCG_OK
+            out.append((nb, it, x.cpu().numpy()))
+    assert np.array_equal(out[0][2], out[4][2])   # switching back is exact
+    for nb, it, x in out[1:4]:
+        assert abs(it - out[0][1]) <= 1
+
+
+def test_substructuring_refuses_columns_too_tall_for_its_shared_tiles():
+    # 2 x 500 levels x 32 columns of doubles exceed a block's shared memory:
+    # an explicit request is refused, the automatic choice falls back to
+    # Thomas, and neither leaves an error behind for the next launch
+    prob, kw, b = case(6, 5, 500, False, False, a_v=1e3, seed=13)
+    with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        assert s.substructuring == 1
+        with pytest.raises(mf.PCGError) as e:
+            s.set_substructuring(2)
+        assert e.value.status == mf.PCG_EINVAL
+        bd = torch.from_numpy(b).to(DEV)
+        x = torch.zeros_like(bd)
+        it, _, st = s.solve(bd, x, rtol=1e-10)
+        assert st == mf.PCG_OK and s.substructuring == 1
