@@ -297,8 +297,8 @@ def run_ours(args, w):
     solver.enable_timing(True)
     iters = []
     launches = 0
-    # face values, diagonal, Thomas factors (+ the row-tiled copy of the diagonal)
-    setup_launches = (4 if args.layout == "tiled" else 3) if varying else 0
+    # face values; diagonal and Thomas factors (+ substructuring tables)
+    setup_launches = (2 if varying else 0) + (2 if solver.substructuring > 1 else 0)
     with ClockSampler(local) as clocks:
         barrier()
         torch.cuda.synchronize()

@@ -234,11 +234,9 @@ int load_coeffs(pcg_ctx* ctx, const pcg_coeffs* c, bool varying) {
       if (t0) cudaEventRecord(t0, ctx->stream);
     }
     if (e == cudaSuccess) e = pcg::launch_face_coeffs(ctx->op, ctx->faceE, ctx->faceN, ctx->stream);
-    if (e == cudaSuccess) e = pcg::launch_cell_diag(ctx->op, ctx->cdiag, ctx->stream);
     if (e == cudaSuccess)
-      e = pcg::launch_thomas_factors(ctx->op, ctx->state, ctx->tnphi, ctx->tinvd, ctx->stream);
-    if (e == cudaSuccess && ctx->cdiag_t)
-      e = pcg::launch_to_tiled(ctx->op, ctx->cdiag, ctx->cdiag_t, ctx->stream);
+      e = pcg::launch_column_setup(ctx->op, ctx->state, ctx->cdiag, ctx->cdiag_t, ctx->tnphi,
+                                   ctx->tinvd, ctx->stream);
     if (t1) cudaEventRecord(t1, ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "coefficient set-up kernels");
     int bad = 0;
@@ -249,7 +247,7 @@ int load_coeffs(pcg_ctx* ctx, const pcg_coeffs* c, bool varying) {
       float ms = 0.0f;
       if (e == cudaSuccess && cudaEventElapsedTime(&ms, t0, t1) == cudaSuccess) {
         ctx->ms[PCG_K_SETUP] += ms;
-        ctx->launches[PCG_K_SETUP] += ctx->cdiag_t ? 4 : 3;
+        ctx->launches[PCG_K_SETUP] += 2;
       }
     }
     if (t0) cudaEventDestroy(t0);

@@ -86,9 +86,10 @@ struct DevState {
 // ---- launchers (pcg_kernels.cu); all enqueue on `s` and return the launch error
 
 cudaError_t launch_face_coeffs(const Op& op, double* faceE, double* faceN, cudaStream_t s);
-cudaError_t launch_cell_diag(const Op& op, double* cdiag, cudaStream_t s);
-cudaError_t launch_thomas_factors(const Op& op, DevState* st, double* tnphi, double* tinvd,
-                                  cudaStream_t s);
+// Per-cell diagonal (column-contiguous, and row-tiled when cdiag_t is not
+// NULL) and Thomas factors (row-tiled) of an a_h field, after the face values.
+cudaError_t launch_column_setup(const Op& op, DevState* st, double* cdiag, double* cdiag_t,
+                                double* tnphi, double* tinvd, cudaStream_t s);
 
 // r = b - A x ; p = q = 0 ; scalar state reset for a new solve.
 cudaError_t launch_residual(const Op& op, DevState* st, const double* b, const double* x,
