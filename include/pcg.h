@@ -193,6 +193,17 @@ int pcg_solve(pcg_ctx* ctx, const double* b_dev, double* x_dev, double rtol, int
 int pcg_solve_host(pcg_ctx* ctx, const double* b_host, double* x_host, double rtol,
                    int maxit, int* iters_out, double* res_hist);
 
+/* As pcg_solve_host, with the initial guess separate from the output:
+ *   x0_host  (host, may be NULL) the initial guess; NULL means x0 = 0 (set on
+ *            the device: nothing is copied in for it); may equal x_host;
+ *   x_host   (host) receives the solution; with x0_host == NULL or another
+ *            buffer it is written only.
+ * A caller solving repeatedly from x0 = 0 can so keep one page-locked output
+ * buffer: no host memset, and one copy in instead of two.
+ * Errors: as pcg_solve_host; PCG_EINVAL also when x0 overlaps b. */
+int pcg_solve_host_x0(pcg_ctx* ctx, const double* b_host, const double* x0_host, double* x_host,
+                      double rtol, int maxit, int* iters_out, double* res_hist);
+
 /* z = M^{-1} r and *rz_dev = <r, z>, without allocating anything.
  * The paper has no counterpart: this entry point exists for callers that
  * must not allocate device memory while they run -- for instance code that

@@ -32,7 +32,7 @@ EXPORTED = ["pcg_create", "pcg_destroy", "pcg_update_coeffs", "pcg_set_stream", 
             "pcg_precond", "pcg_solve", "pcg_solve_host", "pcg_last_error",
             "pcg_enable_timing", "pcg_kernel_times", "pcg_launch_info",
             "pcg_precond_dot_noalloc", "pcg_set_layout", "pcg_set_factors",
-            "pcg_set_substructuring", "pcg_get_substructuring"]
+            "pcg_set_substructuring", "pcg_get_substructuring", "pcg_solve_host_x0"]
 PCG_LAYOUT_COLUMN, PCG_LAYOUT_TILED = 0, 1
 PCG_FACTORS_STORED, PCG_FACTORS_RECOMPUTE = 0, 1
 
@@ -63,6 +63,8 @@ def _load(path=LIB_PATH):
                                      ctypes.POINTER(ctypes.c_int), _vp]),
         "pcg_solve_host": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_double, ctypes.c_int,
                                           ctypes.POINTER(ctypes.c_int), _vp]),
+        "pcg_solve_host_x0": (ctypes.c_int, [_vp, _vp, _vp, _vp, ctypes.c_double, ctypes.c_int,
+                                             ctypes.POINTER(ctypes.c_int), _vp]),
         "pcg_last_error": (ctypes.c_char_p, [_vp]),
         "pcg_enable_timing": (ctypes.c_int, [_vp, ctypes.c_int]),
         "pcg_kernel_times": (ctypes.c_int, [_vp, _vp, _vp]),
@@ -233,6 +235,20 @@ def pcg_solve_host(ctx, n, b, x, rtol, maxit, history=True):
     return it.value, (hist[: it.value + 1] if history else None), st
 
 
+def pcg_solve_host_x0(ctx, n, b, x0, x, rtol, maxit, history=True):
+    """b, x0, x: host arrays; x0 None means a zero initial guess (x is then
+    written only)."""
+    it = ctypes.c_int(-1)
+    hist = np.full(int(maxit) + 1, np.nan) if history else None
+    x0p = None if x0 is None else _host_ptr(x0, n, "x0")
+    st = _lib.pcg_solve_host_x0(ctx, _host_ptr(b, n, "b"), x0p, _host_ptr(x, n, "x", writable=True),
+                                float(rtol), int(maxit), ctypes.byref(it),
+                                hist.ctypes.data_as(_vp) if history else None)
+    if st not in (PCG_OK, PCG_ENOTCONV, PCG_EBREAKDOWN):
+        _check(st, ctx)
+    return it.value, (hist[: it.value + 1] if history else None), st
+
+
 def pcg_precond_dot_noalloc(ctx, n, r, z, rz):
     """z = M^{-1} r and rz[0] = <r, z>, with no device allocation.
 
@@ -345,8 +361,12 @@ class Solver:
         Returns (iters, residual history, status)."""
         return pcg_solve(self.ctx, self.n, b, x, rtol, maxit, history)
 
-    def solve_host(self, b, x, rtol=1e-10, maxit=500, history=True):
-        return pcg_solve_host(self.ctx, self.n, b, x, rtol, maxit, history)
+    def solve_host(self, b, x, rtol=1e-10, maxit=500, history=True, x0="x"):
+        """x0="x": x holds the initial guess (pcg_solve_host); None: zero initial
+        guess; or a separate host array (pcg_solve_host_x0)."""
+        if isinstance(x0, str) and x0 == "x":
+            return pcg_solve_host(self.ctx, self.n, b, x, rtol, maxit, history)
+        return pcg_solve_host_x0(self.ctx, self.n, b, x0, x, rtol, maxit, history)
 
     def enable_timing(self, enable=True):
         pcg_enable_timing(self.ctx, enable)

@@ -706,11 +706,13 @@ int pcg_solve(pcg_ctx* ctx, const double* b_dev, double* x_dev, double rtol, int
   return solve_device(ctx, b_dev, x_dev, rtol, maxit, iters_out, res_hist);
 }
 
-int pcg_solve_host(pcg_ctx* ctx, const double* b_host, double* x_host, double rtol, int maxit,
-                   int* iters_out, double* res_hist) {
+int pcg_solve_host_x0(pcg_ctx* ctx, const double* b_host, const double* x0_host, double* x_host,
+                      double rtol, int maxit, int* iters_out, double* res_hist) {
   if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
   int st = check_solve_args(ctx, b_host, x_host, rtol, maxit);
   if (st) return st;
+  if (x0_host && x0_host != x_host && overlap(b_host, x0_host, ctx->op.n))
+    return fail(ctx, PCG_EINVAL, "b and x0 overlap");
   DeviceGuard g(ctx->device);
   if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
   cudaError_t e = cudaSuccess;
@@ -720,7 +722,9 @@ int pcg_solve_host(pcg_ctx* ctx, const double* b_host, double* x_host, double rt
   const size_t bytes = sizeof(double) * (size_t)ctx->op.n;
   e = cudaMemcpyAsync(ctx->b_host_api, b_host, bytes, cudaMemcpyHostToDevice, ctx->stream);
   if (e == cudaSuccess)
-    e = cudaMemcpyAsync(ctx->x_host_api, x_host, bytes, cudaMemcpyHostToDevice, ctx->stream);
+    e = x0_host ? cudaMemcpyAsync(ctx->x_host_api, x0_host, bytes, cudaMemcpyHostToDevice,
+                                  ctx->stream)
+                : cudaMemsetAsync(ctx->x_host_api, 0, bytes, ctx->stream);  // x0 = +0.0
   if (e != cudaSuccess) return cuda_fail(ctx, e, "host-to-device copy");
   st = solve_device(ctx, ctx->b_host_api, ctx->x_host_api, rtol, maxit, iters_out, res_hist);
   if (st != PCG_OK && st != PCG_ENOTCONV && st != PCG_EBREAKDOWN) return st;
@@ -728,6 +732,11 @@ int pcg_solve_host(pcg_ctx* ctx, const double* b_host, double* x_host, double rt
   if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "device-to-host copy");
   return st;
+}
+
+int pcg_solve_host(pcg_ctx* ctx, const double* b_host, double* x_host, double rtol, int maxit,
+                   int* iters_out, double* res_hist) {
+  return pcg_solve_host_x0(ctx, b_host, x_host, x_host, rtol, maxit, iters_out, res_hist);
 }
 
 int pcg_precond_dot_noalloc(pcg_ctx* ctx, const double* r_dev, double* z_dev, double* rz_dev) {

@@ -152,9 +152,24 @@ def test_solve_host_equals_solve_device():
         i2, h2, st2 = s.solve_host(bh, xh, rtol=1e-10)
         xn = np.zeros(prob.n)                       # pageable host memory works too
         i3, _, _ = s.solve_host(b, xn, rtol=1e-10)
-    assert (i1, st1) == (i2, st2) == (i3, mf.PCG_OK)
+        # zero initial guess without a host buffer for it; the output buffer's
+        # old contents (a previous solution) are not read
+        i4, _, st4 = s.solve_host(bh, xh, rtol=1e-10, x0=None)
+        # separate initial guess == the same guess passed in/out
+        x0 = 0.5 * xh.numpy()
+        xo = np.full(prob.n, np.nan)
+        i5, _, st5 = s.solve_host(b, xo, rtol=1e-10, x0=x0)
+        xio = x0.copy()
+        i6, _, st6 = s.solve_host(b, xio, rtol=1e-10)
+        with pytest.raises(mf.PCGError) as e:
+            mf.pcg_solve_host_x0(s.ctx, prob.n, b, b, xn, 1e-10, 10)   # x0 overlaps b
+        assert e.value.status == mf.PCG_EINVAL
+    assert (i1, st1) == (i2, st2) == (i3, mf.PCG_OK) == (i4, st4)
     assert np.array_equal(xd.cpu().numpy(), xh.numpy())
     assert np.array_equal(xh.numpy(), xn)
+    assert (i5, st5) == (i6, st6) and st5 == mf.PCG_OK
+    assert np.array_equal(xo, xio)
+    assert np.linalg.norm(xo - xn) <= 1e-8 * np.linalg.norm(xn)
 
 
 @pytest.mark.parametrize("layout", ["column", "tiled"])
