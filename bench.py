@@ -38,17 +38,20 @@ METRIC = "PCG iters/s & achieved HBM GB/s (fp64, 1024x1024x128 grid) vs HBM roof
 UNIT = "iters/s"
 # fp64 pipe operations per cell (FMA, MUL and ADD each count one) of the two
 # sweeps in this implementation; see the kernel sources.
-OPS_SPMV = {True: 12, False: 11}     # keyed by "a_h varies per column"
+# keyed by (layout, "a_h varies per column"); the row-tiled stencil sweep of an
+# a_h field reads per-cell horizontal weights (4 FMAs instead of 5 operations)
+OPS_SPMV = {("tiled", True): 11, ("tiled", False): 11, ("column", True): 12, ("column", False): 11}
 OPS_PRECOND = 6
 # Algorithmic bytes per cell: vectors read/written once per sweep.
-BYTES_SPMV = {True: 64, False: 56}   # u,p,z,q (+ per-cell diagonal) read; u,p,q written
+# u,p,z,q (+ per-cell diagonal, + 2 per-cell weights in the row-tiled layout) read; u,p,q written
+BYTES_SPMV = {("tiled", True): 80, ("tiled", False): 56, ("column", True): 64, ("column", False): 56}
 BYTES_PRECOND = {True: 48, False: 32}  # r,q (+ 2 per-cell Thomas factors) read; r,z written
 # With the factors of an a_h field rebuilt in every sweep (--factors recompute):
-# the stencil sweep forms the diagonal (a product and a sum), the
-# preconditioner sweep the diagonal, the pivot and the two quotients (the
-# reciprocal and the division counted as one operation each: a lower bound),
-# and neither reads per-cell coefficients.
-OPS_SPMV_RECOMPUTE, BYTES_SPMV_RECOMPUTE = 14, 56
+# the stencil sweep forms the diagonal (a product and a sum) and the four
+# horizontal weights, the preconditioner sweep the diagonal, the pivot and the
+# two quotients (the reciprocal and the division counted as one operation
+# each: a lower bound), and neither reads per-cell coefficients.
+OPS_SPMV_RECOMPUTE, BYTES_SPMV_RECOMPUTE = 17, 56
 OPS_PRECOND_RECOMPUTE, BYTES_PRECOND_RECOMPUTE = 12, 32
 FP64_LANES_PER_SM_CLK = 2.0          # GB300 non-tensor fp64 rate: 2 FMA lanes per SM per clock
 
@@ -322,7 +325,7 @@ def run_ours(args, w):
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
     clk = clocks.summary()
     ops_a, bytes_a = ((OPS_SPMV_RECOMPUTE, BYTES_SPMV_RECOMPUTE) if recompute
-                      else (OPS_SPMV[varying], BYTES_SPMV[varying]))
+                      else (OPS_SPMV[(args.layout, varying)], BYTES_SPMV[(args.layout, varying)]))
     ops_m, bytes_m = ((OPS_PRECOND_RECOMPUTE, BYTES_PRECOND_RECOMPUTE) if recompute
                       else (OPS_PRECOND, BYTES_PRECOND[varying]))
     bytes_iter = (bytes_a + bytes_m) * n

@@ -46,6 +46,7 @@ struct pcg_ctx {
   double *partials = nullptr, *hist = nullptr, *wscratch = nullptr;
   int layout = PCG_LAYOUT_COLUMN;       // layout of the solver's internal vectors
   double *u_t = nullptr, *cdiag_t = nullptr;  // row-tiled layout: iterate, diagonal
+  double *cwE_t = nullptr, *cwN_t = nullptr;  // row-tiled layout: horizontal weights
   int grid_tm = 1, grid_ta = 1;  // row-tiled preconditioner / stencil sweeps
   int factors = PCG_FACTORS_STORED;  // per-cell factors read (stored) or rebuilt per sweep
   double* nscratch = nullptr;        // recompute: per-warp T_{k+1/2}/D_k scratch
@@ -170,7 +171,8 @@ void free_all(pcg_ctx* ctx) {
   double* bufs[] = {ctx->r,     ctx->z,     ctx->p,     ctx->q,        ctx->lev,
                     ctx->ah,    ctx->faceE, ctx->faceN, ctx->cdiag,    ctx->tnphi,
                     ctx->tinvd, ctx->partials, ctx->hist, ctx->b_host_api, ctx->x_host_api,
-                    ctx->wscratch, ctx->u_t, ctx->cdiag_t, ctx->nscratch,
+                    ctx->wscratch, ctx->u_t, ctx->cdiag_t, ctx->cwE_t, ctx->cwN_t,
+                    ctx->nscratch,
                     ctx->op.sp_nphi, ctx->op.sp_invd, ctx->op.sp_ta, ctx->op.sp_tb,
                     ctx->op.sp_corners, ctx->op.sp_invdS, ctx->op.sp_nphiS};
   for (double* b : bufs)
@@ -235,8 +237,8 @@ int load_coeffs(pcg_ctx* ctx, const pcg_coeffs* c, bool varying) {
     }
     if (e == cudaSuccess) e = pcg::launch_face_coeffs(ctx->op, ctx->faceE, ctx->faceN, ctx->stream);
     if (e == cudaSuccess)
-      e = pcg::launch_column_setup(ctx->op, ctx->state, ctx->cdiag, ctx->cdiag_t, ctx->tnphi,
-                                   ctx->tinvd, ctx->stream);
+      e = pcg::launch_column_setup(ctx->op, ctx->state, ctx->cdiag, ctx->cdiag_t, ctx->cwE_t,
+                                   ctx->cwN_t, ctx->tnphi, ctx->tinvd, ctx->stream);
     if (t1) cudaEventRecord(t1, ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "coefficient set-up kernels");
     int bad = 0;
@@ -556,8 +558,15 @@ int pcg_set_layout(pcg_ctx* ctx, int layout) {
   if (e == cudaSuccess && layout == PCG_LAYOUT_TILED && !ctx->u_t) e = dalloc(&ctx->u_t, npad);
   if (e == cudaSuccess && layout == PCG_LAYOUT_TILED && ctx->has_field_buffers && !ctx->cdiag_t) {
     e = dalloc(&ctx->cdiag_t, npad);
+    if (e == cudaSuccess) e = dalloc(&ctx->cwE_t, npad);
+    if (e == cudaSuccess) e = dalloc(&ctx->cwN_t, npad);
     ctx->op.cdiag_t = ctx->cdiag_t;
-    if (e == cudaSuccess) e = pcg::launch_to_tiled(ctx->op, ctx->cdiag, ctx->cdiag_t, ctx->stream);
+    ctx->op.cwE_t = ctx->cwE_t;
+    ctx->op.cwN_t = ctx->cwN_t;
+    // the per-cell tables of the current field, now with their row-tiled copies
+    if (e == cudaSuccess && ctx->op.varying)
+      e = pcg::launch_column_setup(ctx->op, ctx->state, ctx->cdiag, ctx->cdiag_t, ctx->cwE_t,
+                                   ctx->cwN_t, ctx->tnphi, ctx->tinvd, ctx->stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
   }
   if (e != cudaSuccess) return cuda_fail(ctx, e, "layout change");

@@ -39,6 +39,8 @@ struct Op {
   int fixed_smem;      // dynamic shared memory of the height-specialised sweep
   double* wscratch;    // height-specialised sweep: 32*nz doubles per block (grid_precond blocks)
   const double* cdiag_t; // field, row-tiled solver layout: diagonal per cell, row-tiled
+  const double* cwE_t;   // field, row-tiled: -h_k * (east face value) per cell
+  const double* cwN_t;   // field, row-tiled: -h_k * (north face value) per cell
   int recompute;       // field, row-tiled layout: rebuild the diagonal and the Thomas
                        // factors in every sweep instead of reading them per cell
   double* nscratch;    // recompute: T_{k+1/2}/D_k of the tiles in flight, 32*nz doubles
@@ -87,9 +89,11 @@ struct DevState {
 
 cudaError_t launch_face_coeffs(const Op& op, double* faceE, double* faceN, cudaStream_t s);
 // Per-cell diagonal (column-contiguous, and row-tiled when cdiag_t is not
-// NULL) and Thomas factors (row-tiled) of an a_h field, after the face values.
+// NULL), horizontal weights (row-tiled, when cwE_t is not NULL) and Thomas
+// factors (row-tiled) of an a_h field, after the face values.
 cudaError_t launch_column_setup(const Op& op, DevState* st, double* cdiag, double* cdiag_t,
-                                double* tnphi, double* tinvd, cudaStream_t s);
+                                double* cwE_t, double* cwN_t, double* tnphi, double* tinvd,
+                                cudaStream_t s);
 
 // r = b - A x ; p = q = 0 ; scalar state reset for a new solve.
 cudaError_t launch_residual(const Op& op, DevState* st, const double* b, const double* x,

@@ -138,7 +138,8 @@ __device__ __forceinline__ double quotient_rn(double T, double D, double y) {
 // Per-cell tables of an a_h field, one thread per column (eqs. (8), (18),
 // (19)): the diagonal h_k*mass + T_{k+1/2} + T_{k-1/2} + h_k * (sum of the
 // four face values), stored column-contiguously and, when the context holds
-// the row-tiled copy, row-tiled; and the Thomas factors of the column in the
+// the row-tiled copy, row-tiled; the horizontal weights -h_k a_E and -h_k a_N
+// of the row-tiled stencil sweep; and the Thomas factors of the column in the
 // LDL^T form used by the sweeps, D_k = diag_k - T_{k-1/2} (T_{k-1/2}/D_{k-1}),
 // stored as T_{k+1/2}/D_k and 1/D_k, row-tiled, so that a warp reads 32
 // columns' level k as one 256-byte line.
@@ -151,7 +152,8 @@ __device__ __forceinline__ double quotient_rn(double T, double D, double y) {
 // eq. (19) produces.  1/D_k is the IEEE quotient; T_{k+1/2}/D_k is derived
 // from it exactly (quotient_rn).
 __global__ void k_column_setup(Op op, DevState* st, double* __restrict__ cdiag,
-                               double* __restrict__ cdiag_t, double* __restrict__ tnphi,
+                               double* __restrict__ cdiag_t, double* __restrict__ cwE_t,
+                               double* __restrict__ cwN_t, double* __restrict__ tnphi,
                                double* __restrict__ tinvd) {
   const int nz = op.nz;
   const double* __restrict__ lev = op.lev;
@@ -168,6 +170,10 @@ __global__ void k_column_setup(Op op, DevState* st, double* __restrict__ cdiag,
       const long long o = (t * nz + k) * kTile + lane;
       cdiag[c * nz + k] = diag;
       if (cdiag_t) cdiag_t[o] = diag;
+      if (cwE_t) {  // horizontal weights -h_k a_f of the east and north faces
+        cwE_t[o] = __dmul_rn(lev[LV_HW * nz + k], op.faceE[c]);
+        cwN_t[o] = __dmul_rn(lev[LV_HW * nz + k], op.faceN[c]);
+      }
       const double D = __dsub_rn(diag, __dmul_rn(lev[LV_TDN * nz + k], nphi_prev));
       if (!(D > 0.0)) bad = 1;
       const double invd = 1.0 / D;
@@ -1166,10 +1172,11 @@ cudaError_t launch_face_coeffs(const Op& op, double* faceE, double* faceN, cudaS
 }
 
 cudaError_t launch_column_setup(const Op& op, DevState* st, double* cdiag, double* cdiag_t,
-                                double* tnphi, double* tinvd, cudaStream_t s) {
+                                double* cwE_t, double* cwN_t, double* tnphi, double* tinvd,
+                                cudaStream_t s) {
   long long g = (op.ncols + 127) / 128;
   if (g > 65536) g = 65536;
-  k_column_setup<<<(int)g, 128, 0, s>>>(op, st, cdiag, cdiag_t, tnphi, tinvd);
+  k_column_setup<<<(int)g, 128, 0, s>>>(op, st, cdiag, cdiag_t, cwE_t, cwN_t, tnphi, tinvd);
   return cudaGetLastError();
 }
 

@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(256) k_spmv_tiled(Op op, DevState* st,
     const long long bE = tiled_base(nb.e, nz), bW = tiled_base(nb.w, nz);
     const long long bN = tiled_base(nb.n, nz), bS = tiled_base(nb.s, nz);
     double aE = 0.0, aW = 0.0, aN = 0.0, aS = 0.0;
-    if (VARY) {
+    if (RECOMP) {
       aE = __ldg(op.faceE + col);
       aW = __ldg(op.faceE + nb.w);
       aN = __ldg(op.faceN + col);
@@ -380,22 +380,40 @@ __global__ void __launch_bounds__(256) k_spmv_tiled(Op op, DevState* st,
       const double qc = __ldcs(q + o);
       uc = fma(alpha, pc, uc);
       pc = fma(beta, pc, zc);
-      double hs, d;
+      double a;
       if (VARY) {
-        hs = aE * zE;
-        hs = fma(aW, zW, hs);
-        hs = fma(aN, zN, hs);
-        hs = fma(aS, zS, hs);
-        d = RECOMP ? __dadd_rn(__ldg(lev + LV_DIAG * nz + k), __dmul_rn(__ldg(lev + LV_H * nz + k), sf))
-                   : __ldcs(op.cdiag_t + o);
+        // per-cell horizontal weights -h_k a_f (west and south: the
+        // neighbours' east and north weights), rebuilt with the set-up's
+        // rounding under RECOMP
+        double d, cE, cW, cN, cS;
+        if (RECOMP) {
+          const double hw = __ldg(lev + LV_HW * nz + k);
+          d = __dadd_rn(__ldg(lev + LV_DIAG * nz + k), __dmul_rn(__ldg(lev + LV_H * nz + k), sf));
+          cE = __dmul_rn(hw, aE);
+          cW = __dmul_rn(hw, aW);
+          cN = __dmul_rn(hw, aN);
+          cS = __dmul_rn(hw, aS);
+        } else {
+          d = __ldcs(op.cdiag_t + o);
+          cE = __ldg(op.cwE_t + o);
+          cW = __ldg(op.cwE_t + bW + ko);
+          cN = __ldg(op.cwN_t + o);
+          cS = __ldg(op.cwN_t + bS + ko);
+        }
+        a = fma(d, zc, beta * qc);
+        a = fma(__ldg(lev + LV_UP * nz + k), zu, a);
+        a = fma(__ldg(lev + LV_DN * nz + k), zd, a);
+        a = fma(cE, zE, a);
+        a = fma(cW, zW, a);
+        a = fma(cN, zN, a);
+        a = fma(cS, zS, a);
       } else {
-        hs = (zE + zW) + (zN + zS);
-        d = __ldg(lev + LV_DIAG * nz + k);
+        const double hs = (zE + zW) + (zN + zS);
+        a = fma(__ldg(lev + LV_DIAG * nz + k), zc, beta * qc);
+        a = fma(__ldg(lev + LV_UP * nz + k), zu, a);
+        a = fma(__ldg(lev + LV_DN * nz + k), zd, a);
+        a = fma(__ldg(lev + LV_HW * nz + k), hs, a);
       }
-      double a = fma(d, zc, beta * qc);
-      a = fma(__ldg(lev + LV_UP * nz + k), zu, a);
-      a = fma(__ldg(lev + LV_DN * nz + k), zd, a);
-      a = fma(__ldg(lev + LV_HW * nz + k), hs, a);
       sig = fma(pc, a, sig);
       __stcs(u + o, uc);
       __stcs(p + o, pc);
