@@ -1,5 +1,6 @@
 // Internal declarations shared by the host driver (pcg_api.cu) and the
-// kernel files (pcg_kernels.cu, pcg_tiled.cu, pcg_noalloc.cu).  Not part of the public ABI (include/pcg.h).
+// kernel files (pcg_setup.cu, pcg_kernels.cu, pcg_tiled.cu, pcg_split.cu,
+// pcg_noalloc.cu).  Not part of the public ABI (include/pcg.h).
 #pragma once
 
 #include <cstdint>
@@ -85,7 +86,8 @@ struct DevState {
   int dev_error;     // a bounded device wait ran out (pcg_status PCG_ETIMEOUT)
 };
 
-// ---- launchers (pcg_kernels.cu); all enqueue on `s` and return the launch error
+// ---- launchers (set-up: pcg_setup.cu; column-layout sweeps, stencil, residual and final
+// update: pcg_kernels.cu); all enqueue on `s` and return the launch error
 
 cudaError_t launch_face_coeffs(const Op& op, double* faceE, double* faceN, cudaStream_t s);
 // Per-cell diagonal (column-contiguous, and row-tiled when cdiag_t is not

@@ -106,86 +106,6 @@ __device__ __forceinline__ double stencil1(const Op& op, const double* __restric
   return fma(__ldg(lev + LV_HW * nz + k), hs, a);
 }
 
-// ------------------------------------------------------------------ setup
-
-__global__ void k_face_coeffs(Op op, double* __restrict__ faceE, double* __restrict__ faceN) {
-  for (long long c = blockIdx.x * (long long)blockDim.x + threadIdx.x; c < op.ncols;
-       c += (long long)gridDim.x * blockDim.x) {
-    const Nbr nb = neighbours(op, c);
-    faceE[c] = 0.5 * (op.ah[c] + op.ah[nb.e]);
-    faceN[c] = 0.5 * (op.ah[c] + op.ah[nb.n]);
-  }
-}
-
-// T/D rounded to nearest, from y = 1/D rounded to nearest, by Markstein's
-// correction (P. Markstein, "Computation of elementary functions on the IBM
-// RISC System/6000 processor", IBM J. Res. Develop. 34(1), 1990; Markstein's
-// theorem in Muller et al., "Handbook of Floating-Point Arithmetic"): with
-// y within half an ulp of 1/D and q within one ulp of T/D, the remainder
-// T - D q is exact as a fused multiply-add and q + (T - D q) y rounds to
-// T/D.  The first correction makes q = RN(T y) faithful, the second rounds
-// it.  Valid for the positive, normal operands of the Thomas set-up; bitwise
-// equal to the IEEE quotient (the row-tiled sweep that rebuilds its factors
-// divides, and the tests compare the two).
-__device__ __forceinline__ double quotient_rn(double T, double D, double y) {
-  double q = T * y;
-  double r = fma(-q, D, T);
-  q = fma(r, y, q);
-  r = fma(-q, D, T);
-  return fma(r, y, q);
-}
-
-// Per-cell tables of an a_h field, one thread per column (eqs. (8), (18),
-// (19)): the diagonal h_k*mass + T_{k+1/2} + T_{k-1/2} + h_k * (sum of the
-// four face values), stored column-contiguously and, when the context holds
-// the row-tiled copy, row-tiled; the horizontal weights -h_k a_E and -h_k a_N
-// of the row-tiled stencil sweep; and the Thomas factors of the column in the
-// LDL^T form used by the sweeps, D_k = diag_k - T_{k-1/2} (T_{k-1/2}/D_{k-1}),
-// stored as T_{k+1/2}/D_k and 1/D_k, row-tiled, so that a warp reads 32
-// columns' level k as one 256-byte line.
-//
-// The diagonal and the pivots are formed with explicitly rounded operations
-// (no fused multiply-add): the column systems of strongly graded, strongly
-// anisotropic grids amplify a one-ulp change of a pivot by up to ~1e5 in the
-// solution, so they are formed exactly as their definition rounds them
-// (product rounded, then sum), the numbers any plain fp64 evaluation of
-// eq. (19) produces.  1/D_k is the IEEE quotient; T_{k+1/2}/D_k is derived
-// from it exactly (quotient_rn).
-__global__ void k_column_setup(Op op, DevState* st, double* __restrict__ cdiag,
-                               double* __restrict__ cdiag_t, double* __restrict__ cwE_t,
-                               double* __restrict__ cwN_t, double* __restrict__ tnphi,
-                               double* __restrict__ tinvd) {
-  const int nz = op.nz;
-  const double* __restrict__ lev = op.lev;
-  for (long long c = blockIdx.x * (long long)blockDim.x + threadIdx.x; c < op.ncols;
-       c += (long long)gridDim.x * blockDim.x) {
-    const long long t = c / kTile;
-    const int lane = (int)(c - t * kTile);
-    const Nbr nb = neighbours(op, c);
-    const double sf = op.faceE[c] + op.faceE[nb.w] + op.faceN[c] + op.faceN[nb.s];
-    double nphi_prev = 0.0;
-    int bad = 0;
-    for (int k = 0; k < nz; ++k) {
-      const double diag = __dadd_rn(lev[LV_DIAG * nz + k], __dmul_rn(lev[LV_H * nz + k], sf));
-      const long long o = (t * nz + k) * kTile + lane;
-      cdiag[c * nz + k] = diag;
-      if (cdiag_t) cdiag_t[o] = diag;
-      if (cwE_t) {  // horizontal weights -h_k a_f of the east and north faces
-        cwE_t[o] = __dmul_rn(lev[LV_HW * nz + k], op.faceE[c]);
-        cwN_t[o] = __dmul_rn(lev[LV_HW * nz + k], op.faceN[c]);
-      }
-      const double D = __dsub_rn(diag, __dmul_rn(lev[LV_TDN * nz + k], nphi_prev));
-      if (!(D > 0.0)) bad = 1;
-      const double invd = 1.0 / D;
-      const double nphi = quotient_rn(lev[LV_TUP * nz + k], D, invd);
-      tnphi[o] = nphi;
-      tinvd[o] = invd;
-      nphi_prev = nphi;
-    }
-    if (bad) st->setup_error = 1;
-  }
-}
-
 // ------------------------------------------------- preconditioner sweep (K_M)
 
 // Shared-memory index of level k of a staged column: XOR swizzle of the low
@@ -1162,22 +1082,6 @@ int grid_spmv(const Op& op, int num_sms) {
   const long long work = (op.n + 2 * kSpmvThreads - 1) / (2 * kSpmvThreads);
   if (g > work) g = work;
   return (int)(g < 1 ? 1 : g);
-}
-
-cudaError_t launch_face_coeffs(const Op& op, double* faceE, double* faceN, cudaStream_t s) {
-  long long g = (op.ncols + 255) / 256;
-  if (g > 65536) g = 65536;
-  k_face_coeffs<<<(int)g, 256, 0, s>>>(op, faceE, faceN);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_column_setup(const Op& op, DevState* st, double* cdiag, double* cdiag_t,
-                                double* cwE_t, double* cwN_t, double* tnphi, double* tinvd,
-                                cudaStream_t s) {
-  long long g = (op.ncols + 127) / 128;
-  if (g > 65536) g = 65536;
-  k_column_setup<<<(int)g, 128, 0, s>>>(op, st, cdiag, cdiag_t, cwE_t, cwN_t, tnphi, tinvd);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_residual(const Op& op, DevState* st, const double* b, const double* x,
