@@ -422,3 +422,69 @@ def test_substructuring_refuses_columns_too_tall_for_its_shared_tiles():
         x = torch.zeros_like(bd)
         it, _, st = s.solve(bd, x, rtol=1e-10)
         assert st == mf.PCG_OK and s.substructuring == 1
+
+
+# ---- coefficient changes and degenerate grids in every solver mode
+
+def fixed_iterate_matches(s, prob, b, iters=6):
+    """Iterate after a fixed number of iterations against the oracle's."""
+    x_ref, it_ref, _, st_ref = oracle.pcg(prob, b, rtol=0.0, maxit=iters)
+    bd = torch.from_numpy(b).to(DEV)
+    x = torch.zeros_like(bd)
+    it, _, st = s.solve(bd, x, rtol=0.0, maxit=iters)
+    assert (it, st) == (it_ref, mf.PCG_OK) and st_ref == oracle.OK
+    xs = x.cpu().numpy()
+    return np.linalg.norm(xs - x_ref) <= SOL_TOL * np.linalg.norm(x_ref)
+
+
+@pytest.mark.parametrize("mode", ["column", "tiled", "tiled_recompute", "tiled_split2"])
+def test_solves_follow_coefficient_updates(mode):
+    # field -> another field -> constant a_h -> the first field again: the
+    # per-cell tables of every layout (diagonal, weights, factors, blocks)
+    # must follow each update
+    prob, kw, b = case(37, 21, 24, True, True, a_v=1e4, seed=14)
+    ah2 = W.horizontal_coefficient(37, 21, True)[::-1].copy() * 1.5
+    steps = [
+        (dict(a_h_field=ah2, a_v=3e3, mass=0.5, dz=prob.h), ah2, 3e3, 0.5),
+        (dict(a_h=0.8, a_v=1e4, mass=1.0, dz=prob.h), 0.8, 1e4, 1.0),
+        (kw, prob.ah, kw["a_v"], 1.0),
+    ]
+    with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        if mode == "column":
+            s.set_layout("column")
+        s.set_factors("recompute" if mode == "tiled_recompute" else "stored")
+        s.set_substructuring(2 if mode == "tiled_split2" else 1)
+        assert fixed_iterate_matches(s, prob, b)
+        for coeffs, ah, a_v, mass in steps:
+            s.update_coeffs(**coeffs)
+            p2 = oracle.Problem(prob.nx, prob.ny, prob.nz, ah=ah, a_v=a_v, mass=mass, h=prob.h)
+            assert fixed_iterate_matches(s, p2, b), coeffs.keys()
+
+
+DEGENERATE = [  # nx, ny, nz, varying, graded: self-neighbours, single columns, single levels
+    (1, 1, 9, True, True),
+    (1, 7, 12, True, False),
+    (7, 1, 12, False, True),
+    (3, 1, 2, True, True),
+    (33, 1, 5, True, True),     # one full tile and one column in the next
+    (40, 2, 1, True, False),    # a single level: M is diagonal
+]
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("cfg", DEGENERATE, ids=lambda c: "x".join(map(str, c[:3])))
+def test_degenerate_grids_solve_like_the_oracle(cfg, mode):
+    nx, ny, nz, varying, graded = cfg
+    prob, kw, b = case(nx, ny, nz, varying, graded, a_v=1e3, seed=15)
+    x_ref, it_ref, _, st_ref = oracle.pcg(prob, b, rtol=1e-10, maxit=500)
+    assert st_ref == oracle.OK
+    with mf.Solver(nx, ny, nz, **kw) as s:
+        configure(s, mode)
+        bd = torch.from_numpy(b).to(DEV)
+        x = torch.zeros_like(bd)
+        it, _, st = s.solve(bd, x, rtol=1e-10, maxit=500)
+        assert st == mf.PCG_OK and abs(it - it_ref) <= 1
+        x.zero_()
+        assert s.solve(bd, x, rtol=0.0, maxit=it_ref)[0] == it_ref
+        xs = x.cpu().numpy()
+    assert np.linalg.norm(xs - x_ref) <= SOL_TOL * np.linalg.norm(x_ref)
