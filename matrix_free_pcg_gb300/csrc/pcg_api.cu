@@ -31,6 +31,17 @@ struct KernelEvent {
   cudaEvent_t start, stop;
 };
 
+// One batch of the row-tiled solve loop (preconditioner and stencil sweeps of
+// `iters` iterations) as an instantiated CUDA graph.  With timing, event-record
+// nodes mark the boundaries between consecutive kernels: ev[2i] before the
+// preconditioner sweep of iteration i, ev[2i+1] between it and the stencil
+// sweep, ev[2i+2] after that (2*iters+1 events; each costs GPU time, so
+// neighbours share one).
+struct BatchGraph {
+  cudaGraphExec_t exec = nullptr;
+  std::vector<cudaEvent_t> ev;
+};
+
 }  // namespace
 
 struct pcg_ctx {
@@ -53,6 +64,16 @@ struct pcg_ctx {
   // substructured column solve: requested blocks (0 automatic), blocks in use, grid
   int split_req = 0, split_p = 1, grid_sp = 0;
   size_t partials_cap = 0;           // doubles in `partials`
+  // CUDA graphs of the row-tiled loop: two instances, launched alternately so
+  // that one can be read back (timing) while the other runs.  They are
+  // captured again whenever config_gen, the batch size or timing changed.
+  BatchGraph graphs[2];
+  cudaStream_t cap_stream = nullptr;  // private stream for the captures
+  unsigned long long config_gen = 1;  // bumped by every change a graph depends on
+  unsigned long long graph_gen = 0;
+  int graph_batch = 0;
+  bool graph_timing = false;
+  bool graphs_off = false;            // a capture failed: direct launches from then on
   int hist_cap = 0;
   DevState* state = nullptr;
   double *b_host_api = nullptr, *x_host_api = nullptr;  // device copies for pcg_solve_host
@@ -181,6 +202,14 @@ void free_all(pcg_ctx* ctx) {
   if (ctx->pinned) cudaFreeHost(ctx->pinned);
   for (cudaEvent_t e : ctx->event_pool) cudaEventDestroy(e);
   ctx->event_pool.clear();
+  for (BatchGraph& g : ctx->graphs) {
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+    g.exec = nullptr;
+    for (cudaEvent_t e : g.ev) cudaEventDestroy(e);
+    g.ev.clear();
+  }
+  if (ctx->cap_stream) cudaStreamDestroy(ctx->cap_stream);
+  ctx->cap_stream = nullptr;
 }
 
 // Upload coefficients and (for a field) rebuild the per-column and per-cell
@@ -217,6 +246,7 @@ int run_split_setup(pcg_ctx* ctx) {
 }
 
 int load_coeffs(pcg_ctx* ctx, const pcg_coeffs* c, bool varying) {
+  ctx->config_gen++;  // the sweeps' template choice follows op.varying
   std::vector<double> lev;
   int st = build_levels(ctx, ctx->op.nz, c, varying, lev);
   if (st) return st;
@@ -314,6 +344,71 @@ bool overlap(const double* a, const double* b, long long n) {
   return (a < b + n) && (b < a + n);
 }
 
+// The two sweeps of one iteration of the row-tiled loop, enqueued on `s`;
+// with `ev`, boundary events before the first and between the two.
+cudaError_t launch_tiled_iteration(pcg_ctx* ctx, const Op& op, bool split, int grid_pm,
+                                   cudaStream_t s, cudaEvent_t* ev) {
+  cudaError_t e = cudaSuccess;
+  if (ev) e = cudaEventRecordWithFlags(ev[0], s, cudaEventRecordExternal);
+  if (e == cudaSuccess)
+    e = split ? pcg::launch_precond_split(op, ctx->split_p, ctx->state, ctx->r, ctx->q, ctx->z,
+                                          ctx->partials, ctx->hist, grid_pm, s)
+              : pcg::launch_precond_tiled(op, ctx->state, ctx->r, ctx->q, ctx->z, ctx->partials,
+                                          ctx->hist, grid_pm, s);
+  if (e == cudaSuccess && ev) e = cudaEventRecordWithFlags(ev[1], s, cudaEventRecordExternal);
+  if (e == cudaSuccess)
+    e = pcg::launch_spmv_tiled(op, ctx->state, ctx->z, ctx->u_t, ctx->p, ctx->q,
+                               ctx->partials + 2 * grid_pm, ctx->grid_ta, s);
+  return e;
+}
+
+// Capture `iters` iterations of the row-tiled loop into g (on the private
+// capture stream; the graph is later launched on the context's stream).
+cudaError_t capture_batch(pcg_ctx* ctx, const Op& op, bool split, int grid_pm, int iters,
+                          bool timing, BatchGraph& g) {
+  cudaError_t e = cudaSuccess;
+  if (!ctx->cap_stream) e = cudaStreamCreateWithFlags(&ctx->cap_stream, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return e;
+  if (g.exec) cudaGraphExecDestroy(g.exec);
+  g.exec = nullptr;
+  if (timing) {
+    while (e == cudaSuccess && g.ev.size() < 2 * (size_t)iters + 1) {
+      cudaEvent_t ev = nullptr;
+      e = cudaEventCreate(&ev);
+      if (e == cudaSuccess) g.ev.push_back(ev);
+    }
+    if (e != cudaSuccess) return e;
+  }
+  e = cudaStreamBeginCapture(ctx->cap_stream, cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) return e;
+  for (int i = 0; i < iters && e == cudaSuccess; ++i)
+    e = launch_tiled_iteration(ctx, op, split, grid_pm, ctx->cap_stream,
+                               timing ? &g.ev[2 * (size_t)i] : nullptr);
+  if (e == cudaSuccess && timing)
+    e = cudaEventRecordWithFlags(g.ev[2 * (size_t)iters], ctx->cap_stream,
+                                 cudaEventRecordExternal);
+  cudaGraph_t graph = nullptr;
+  const cudaError_t ee = cudaStreamEndCapture(ctx->cap_stream, &graph);
+  if (e == cudaSuccess) e = ee;
+  if (e == cudaSuccess) e = cudaGraphInstantiate(&g.exec, graph, 0);
+  if (graph) cudaGraphDestroy(graph);
+  if (e != cudaSuccess) {
+    g.exec = nullptr;
+    (void)cudaGetLastError();
+  }
+  return e;
+}
+
+// Elapsed times of the sweeps of one finished batch graph, in launch order.
+void read_batch_times(const BatchGraph& g, int iters, std::vector<float>& tm_m,
+                      std::vector<float>& tm_a) {
+  for (int i = 0; i < iters; ++i) {
+    float ms = 0.0f;
+    if (cudaEventElapsedTime(&ms, g.ev[2 * i], g.ev[2 * i + 1]) == cudaSuccess) tm_m.push_back(ms);
+    if (cudaEventElapsedTime(&ms, g.ev[2 * i + 1], g.ev[2 * i + 2]) == cudaSuccess) tm_a.push_back(ms);
+  }
+}
+
 int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxit,
                  int* iters_out, double* res_hist) {
   cudaError_t e;
@@ -324,6 +419,7 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
     if (ctx->hist) cudaFree(ctx->hist);
     ctx->hist = nh;
     ctx->hist_cap = maxit + 1;
+    ctx->config_gen++;
   }
   Op op = ctx->op;
   cudaStream_t s = ctx->stream;
@@ -356,6 +452,44 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
   cudaEvent_t ev[2] = {pool_event(ctx), pool_event(ctx)};
   if (!ev[0] || !ev[1]) return fail(ctx, PCG_ECUDA, "event creation failed");
   bool stop = false;
+  // Row-tiled layout: every batch is one launch of a CUDA graph (all its
+  // operands are the context's own buffers).  Sweeps past the last
+  // iteration see `done` and return at once, so every batch is a full one.
+  bool use_graphs = tiled && !ctx->graphs_off;
+  if (use_graphs && (ctx->graph_gen != ctx->config_gen || ctx->graph_batch != batch ||
+                     ctx->graph_timing != ctx->timing)) {
+    for (BatchGraph& g : ctx->graphs) {
+      if (capture_batch(ctx, op, split, grid_pm, batch, ctx->timing, g) != cudaSuccess) {
+        use_graphs = false;
+        ctx->graphs_off = true;  // this driver or device refuses: launch directly from now on
+        break;
+      }
+    }
+    ctx->graph_gen = ctx->config_gen;
+    ctx->graph_batch = batch;
+    ctx->graph_timing = ctx->timing;
+  }
+  std::vector<float> tm_m, tm_a;  // graph sweep times in launch order (timing)
+  while (use_graphs && enq <= maxit && !stop) {
+    e = cudaGraphLaunch(ctx->graphs[slot].exec, s);
+    ctx->last_launches += 2 * batch;
+    enq += batch;
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(&ctx->pinned[slot], ctx->state, sizeof(DevState),
+                          cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[slot], s);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "solve batch launch");
+    if (pending >= 0) {
+      e = cudaEventSynchronize(ev[pending]);
+      if (e != cudaSuccess) return cuda_fail(ctx, e, "solve loop");
+      if (ctx->timing) read_batch_times(ctx->graphs[pending], batch, tm_m, tm_a);
+      if (ctx->pinned[pending].done) stop = true;
+    }
+    pending = slot;
+    slot ^= 1;
+  }
+  const int last_graph = (use_graphs && pending >= 0) ? pending : -1;  // read after the final sync
+  if (use_graphs) stop = true;
   while (enq <= maxit && !stop) {
     const int nb = std::min(batch, maxit + 1 - enq);
     for (int i = 0; i < nb; ++i) {
@@ -408,7 +542,18 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "residual history copy");
   }
-  if (ctx->timing) collect_events(ctx, fin.it, fin.it > 0 ? fin.it - 1 : 0);
+  if (ctx->timing) {
+    collect_events(ctx, fin.it, fin.it > 0 ? fin.it - 1 : 0);
+    if (last_graph >= 0) read_batch_times(ctx->graphs[last_graph], batch, tm_m, tm_a);
+    // only the sweeps that did work: the first `it` preconditioner and
+    // `it - 1` stencil sweeps in launch order
+    const size_t wm = std::min<size_t>(tm_m.size(), fin.it > 0 ? (size_t)fin.it : 0);
+    const size_t wa = std::min<size_t>(tm_a.size(), fin.it > 1 ? (size_t)fin.it - 1 : 0);
+    for (size_t i = 0; i < wm; ++i) ctx->ms[PCG_K_PRECOND_FUSED] += tm_m[i];
+    for (size_t i = 0; i < wa; ++i) ctx->ms[PCG_K_SPMV_FUSED] += tm_a[i];
+    ctx->launches[PCG_K_PRECOND_FUSED] += (long long)wm;
+    ctx->launches[PCG_K_SPMV_FUSED] += (long long)wa;
+  }
   if (iters_out) *iters_out = fin.iters;
   if (fin.status == PCG_ENOTCONV)
     return fail(ctx, PCG_ENOTCONV, "no convergence to rtol=%g in %d iterations (last ratio %g)",
@@ -571,6 +716,7 @@ int pcg_set_layout(pcg_ctx* ctx, int layout) {
   }
   if (e != cudaSuccess) return cuda_fail(ctx, e, "layout change");
   ctx->layout = layout;
+  ctx->config_gen++;
   return PCG_OK;
 }
 
@@ -589,6 +735,7 @@ int pcg_set_factors(pcg_ctx* ctx, int mode) {
     }
   }
   ctx->factors = mode;
+  ctx->config_gen++;
   return PCG_OK;
 }
 
@@ -657,6 +804,7 @@ int pcg_set_substructuring(pcg_ctx* ctx, int nblocks) {
   if (e != cudaSuccess) return cuda_fail(ctx, e, "substructuring tables");
   ctx->split_req = nblocks;
   ctx->split_p = P;
+  ctx->config_gen++;
   ctx->grid_sp = grid;
   return (P > 1) ? run_split_setup(ctx) : PCG_OK;
 }
