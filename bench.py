@@ -332,10 +332,14 @@ def run_ours(args, w):
     ops_iter = (ops_a + ops_m) * n
     hbm_gbs = bytes_iter * (total_iters / world) / (ms_max * 1e-3) / 1e9
 
-    # roofline of the dominant kernel, from its live CUDA-event times
-    kinds = {"spmv_fused": (ops_a, bytes_a), "precond_fused": (ops_m, bytes_m)}
+    # roofline of the dominant kernel, from its live CUDA-event times; a
+    # persistent loop (small grids) is one kernel for all iterations of a solve
+    kinds = {"spmv_fused": (ops_a, bytes_a), "precond_fused": (ops_m, bytes_m),
+             "loop": (ops_a + ops_m, bytes_a + bytes_m)}
     dom = max(kinds, key=lambda k: ktimes[k][0])
     dom_ms, dom_n = ktimes[dom]
+    if dom == "loop":  # per iteration: the loop's time over the iterations it ran
+        dom_n = max(total_iters // world, 1)
     avg_s = dom_ms * 1e-3 / max(dom_n, 1)
     ops_cell, bytes_cell = kinds[dom]
     sm_mhz = (clk or {}).get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))

@@ -142,7 +142,9 @@ int pcg_set_factors(pcg_ctx* ctx, int mode);
  *                      of shared memory per block of nblocks warps;
  *   nblocks = 0        (default) automatic: 4 (or 2) blocks only for grids
  *                      with fewer tiles of 32 columns than half the SMs,
- *                      where the sweep is latency-bound; else 1.  (The
+ *                      where the sweep is latency-bound, and only when the
+ *                      persistent loop (pcg_set_loop) does not take them,
+ *                      which is faster still there; else 1.  (The
  *                      substructured sweep does 8 fp64 operations per cell
  *                      against 6, and the fp64 rate bounds larger grids.)
  * The substructured sweep keeps its own per-cell tables (four doubles per
@@ -152,6 +154,31 @@ int pcg_set_factors(pcg_ctx* ctx, int mode);
  * PCG_EBREAKDOWN (a pivot of the block or interface system is not
  * positive). */
 int pcg_set_substructuring(pcg_ctx* ctx, int nblocks);
+
+/* How pcg_solve drives the iterations in the row-tiled layout:
+ *   PCG_LOOP_BATCHED     the two fused sweeps of every iteration are kernel
+ *                        launches, enqueued in batches (one CUDA graph each);
+ *                        the host polls the device's completion flag one batch
+ *                        behind;
+ *   PCG_LOOP_PERSISTENT  one cooperative kernel runs all iterations: the same
+ *                        two sweeps, separated by grid-wide barriers, every
+ *                        block taking the scalar decisions from the same
+ *                        fixed-order sums; for grids too small to fill the
+ *                        GPU, where launch latency dominates an iteration.  A
+ *                        barrier wait that runs out (about a second) ends the
+ *                        solve with PCG_ETIMEOUT;
+ *   PCG_LOOP_AUTO        (default) persistent for grids with fewer tiles of 32
+ *                        columns than 4 per SM, else batched.
+ * The persistent loop needs Thomas column solves (no substructuring) and
+ * stored factors, and the device must support cooperative launches; where it
+ * cannot run, the batched loop does.  The column layout always runs batched.
+ * Errors: PCG_EINVAL (unknown mode). */
+enum { PCG_LOOP_AUTO = 0, PCG_LOOP_BATCHED = 1, PCG_LOOP_PERSISTENT = 2 };
+int pcg_set_loop(pcg_ctx* ctx, int mode);
+
+/* The loop the next pcg_solve will run: PCG_LOOP_BATCHED or
+ * PCG_LOOP_PERSISTENT.  Errors: PCG_EINVAL (NULL). */
+int pcg_get_loop(const pcg_ctx* ctx, int* mode_out);
 
 /* Blocks per column the row-tiled preconditioner sweep currently uses
  * (1: Thomas), after the automatic choice.  Errors: PCG_EINVAL (NULL). */
@@ -245,7 +272,8 @@ typedef enum {
   PCG_K_PRECOND = 5,       /* standalone Thomas solve */
   PCG_K_SETUP = 6,         /* coefficient set-up kernels of pcg_update_coeffs (face values,
                               per-cell diagonal and Thomas factors), timed together */
-  PCG_K_COUNT = 7
+  PCG_K_LOOP = 7,          /* persistent solve loop: all iterations of both sweeps */
+  PCG_K_COUNT = 8
 } pcg_kernel_kind;
 
 int pcg_enable_timing(pcg_ctx* ctx, int enable);

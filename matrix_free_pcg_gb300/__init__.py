@@ -25,16 +25,18 @@ PCG_OK, PCG_EINVAL, PCG_ENOMEM, PCG_ECUDA, PCG_ENOTCONV, PCG_EBREAKDOWN, PCG_ETI
 STATUS_NAMES = {0: "PCG_OK", 1: "PCG_EINVAL", 2: "PCG_ENOMEM", 3: "PCG_ECUDA",
                 4: "PCG_ENOTCONV", 5: "PCG_EBREAKDOWN", 6: "PCG_ETIMEOUT"}
 KERNEL_KINDS = ["precond_fused", "spmv_fused", "residual", "finalize", "apply_A", "precond",
-                "setup"]
+                "setup", "loop"]
 PCG_K_COUNT = len(KERNEL_KINDS)
 
 EXPORTED = ["pcg_create", "pcg_destroy", "pcg_update_coeffs", "pcg_set_stream", "pcg_apply_A",
             "pcg_precond", "pcg_solve", "pcg_solve_host", "pcg_last_error",
             "pcg_enable_timing", "pcg_kernel_times", "pcg_launch_info",
             "pcg_precond_dot_noalloc", "pcg_set_layout", "pcg_set_factors",
-            "pcg_set_substructuring", "pcg_get_substructuring", "pcg_solve_host_x0"]
+            "pcg_set_substructuring", "pcg_get_substructuring", "pcg_solve_host_x0",
+            "pcg_set_loop", "pcg_get_loop"]
 PCG_LAYOUT_COLUMN, PCG_LAYOUT_TILED = 0, 1
 PCG_FACTORS_STORED, PCG_FACTORS_RECOMPUTE = 0, 1
+PCG_LOOP_AUTO, PCG_LOOP_BATCHED, PCG_LOOP_PERSISTENT = 0, 1, 2
 
 
 class pcg_coeffs(ctypes.Structure):
@@ -76,6 +78,8 @@ def _load(path=LIB_PATH):
         "pcg_set_factors": (ctypes.c_int, [_vp, ctypes.c_int]),
         "pcg_set_substructuring": (ctypes.c_int, [_vp, ctypes.c_int]),
         "pcg_get_substructuring": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int)]),
+        "pcg_set_loop": (ctypes.c_int, [_vp, ctypes.c_int]),
+        "pcg_get_loop": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -201,6 +205,18 @@ def pcg_get_substructuring(ctx):
     """Blocks per column in use by the row-tiled preconditioner sweep (1: Thomas)."""
     v = ctypes.c_int(0)
     _check(_lib.pcg_get_substructuring(ctx, ctypes.byref(v)), ctx)
+    return v.value
+
+
+def pcg_set_loop(ctx, mode):
+    """PCG_LOOP_AUTO (default), PCG_LOOP_BATCHED or PCG_LOOP_PERSISTENT."""
+    return _check(_lib.pcg_set_loop(ctx, int(mode)), ctx)
+
+
+def pcg_get_loop(ctx):
+    """The loop the next solve runs: PCG_LOOP_BATCHED or PCG_LOOP_PERSISTENT."""
+    v = ctypes.c_int(0)
+    _check(_lib.pcg_get_loop(ctx, ctypes.byref(v)), ctx)
     return v.value
 
 
@@ -330,6 +346,19 @@ class Solver:
     def set_substructuring(self, nblocks):
         """0 automatic, 1 off, or 2/4/8/16 blocks per column."""
         pcg_set_substructuring(self.ctx, nblocks)
+
+    def set_loop(self, mode):
+        """"auto", "batched" or "persistent" (or the PCG_LOOP_* values)."""
+        if isinstance(mode, str):
+            mode = {"auto": PCG_LOOP_AUTO, "batched": PCG_LOOP_BATCHED,
+                    "persistent": PCG_LOOP_PERSISTENT}[mode]
+        pcg_set_loop(self.ctx, mode)
+
+    @property
+    def loop(self):
+        """"batched" or "persistent": the loop the next solve runs."""
+        return {PCG_LOOP_BATCHED: "batched", PCG_LOOP_PERSISTENT: "persistent"}[
+            pcg_get_loop(self.ctx)]
 
     @property
     def substructuring(self):

@@ -202,6 +202,44 @@ __device__ __forceinline__ double ld_hint(const double* a, uint64_t pol) {
   return v;
 }
 
+// Grid-wide barrier for a cooperative launch (every block resident).  Thread 0
+// of each block reads the generation, publishes the block's writes and
+// arrives on the counter; the last arrival resets the counter and advances the
+// generation, the others poll it -- at most `limit` times, after which the
+// block records the timeout in *err and the barrier returns false (the caller
+// then leaves its loop; nothing waits without bound).  Global writes made
+// before the barrier are visible to every block after it (read them with
+// __ldcg, past the non-coherent L1).
+__device__ __forceinline__ bool grid_barrier(unsigned int* count, unsigned int* gen,
+                                             unsigned int nblocks, int* err, long long limit) {
+  __shared__ int ok_s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    const unsigned int g = *reinterpret_cast<volatile unsigned int*>(gen);
+    __threadfence();
+    if (atomicAdd(count, 1u) + 1u == nblocks) {
+      atomicExch(count, 0u);
+      __threadfence();
+      atomicAdd(gen, 1u);
+    } else {
+      long long polls = 0;
+      while (*reinterpret_cast<volatile unsigned int*>(gen) == g) {
+        if (++polls > limit) {
+          ok = 0;
+          atomicExch(err, 1);
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    __threadfence();
+    ok_s = ok;
+  }
+  __syncthreads();
+  return ok_s != 0;
+}
+
 __device__ __forceinline__ double2 lds2(const double* p) {
   return *reinterpret_cast<const double2*>(p);
 }

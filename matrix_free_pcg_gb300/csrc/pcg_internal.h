@@ -84,6 +84,7 @@ struct DevState {
   unsigned int ticket_a;
   int setup_error;   // a non-positive Thomas pivot was met in the setup kernel
   int dev_error;     // a bounded device wait ran out (pcg_status PCG_ETIMEOUT)
+  unsigned int bar_count, bar_gen;  // grid barrier of the persistent solve loop
 };
 
 // ---- launchers (set-up: pcg_setup.cu; column-layout sweeps, stencil, residual and final
@@ -145,6 +146,14 @@ cudaError_t launch_spmv_tiled(const Op& op, DevState* st, const double* z, doubl
 // nz = 128 and leave three warps per sub-partition to hide fp64 latency).
 constexpr int kTmWarpsPerBlock = 4;
 constexpr int kTmWarpsPerSm = 12;
+// Whole solve loop of the row-tiled layout (Thomas column solves, stored
+// factors) in one cooperative launch: grid_persistent gives its grid (0: not
+// available), launch_persistent runs iterations until the stopping test.
+int grid_persistent(const Op& op, int num_sms);
+cudaError_t launch_persistent(const Op& op, DevState* st, double* r, double* q, double* z,
+                              double* u, double* p, double* partials, double* hist, int grid,
+                              cudaStream_t s);
+
 // Grid sizes (blocks) of the two row-tiled sweeps.
 int grid_tiled_precond(const Op& op, int num_sms);
 int grid_tiled_spmv(const Op& op, int num_sms);

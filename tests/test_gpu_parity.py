@@ -92,15 +92,19 @@ SOLVE_CASES = [
 
 
 def configure(s, mode):
-    """mode: "column"; "tiled" (Thomas column solves, stored factors);
-    "tiled_recompute" (Thomas, factors rebuilt per sweep); "tiled_split"
-    (substructured column solves, blocks chosen automatically)."""
+    """mode: "column"; "tiled" (Thomas column solves, stored factors, batched
+    loop); "tiled_recompute" (Thomas, factors rebuilt per sweep);
+    "tiled_split" (substructured column solves, blocks chosen automatically);
+    "tiled_persistent" (Thomas, stored factors, one cooperative kernel)."""
     s.set_layout("column" if mode == "column" else "tiled")
     s.set_factors("recompute" if mode == "tiled_recompute" else "stored")
+    s.set_loop("persistent" if mode == "tiled_persistent" else "batched")
     s.set_substructuring(0 if mode == "tiled_split" else 1)
+    if mode == "tiled_persistent":
+        assert s.loop == "persistent"
 
 
-MODES = ["column", "tiled", "tiled_recompute", "tiled_split"]
+MODES = ["column", "tiled", "tiled_recompute", "tiled_split", "tiled_persistent"]
 
 
 @pytest.mark.parametrize("layout", MODES)
@@ -172,11 +176,11 @@ def test_solve_host_equals_solve_device():
     assert np.linalg.norm(xo - xn) <= 1e-8 * np.linalg.norm(xn)
 
 
-@pytest.mark.parametrize("layout", ["column", "tiled"])
+@pytest.mark.parametrize("layout", ["column", "tiled", "tiled_persistent"])
 def test_status_semantics_match_oracle(layout):
     prob, kw, b = case(20, 18, 16, True, True, a_v=1e3, seed=7)
     with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
-        s.set_layout(layout)
+        configure(s, layout)
         bd = torch.from_numpy(b).to(DEV)
         _, it_ref, _, _ = oracle.pcg(prob, b, rtol=1e-8)
         x = torch.zeros_like(bd)
@@ -251,7 +255,7 @@ def test_update_coeffs_and_streams():
 def test_kernel_timing_counts_launches(layout):
     prob, kw, b = case(40, 40, 64, True, True, a_v=1e4, seed=10)
     with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
-        s.set_layout(layout)
+        configure(s, layout)
         s.enable_timing(True)
         bd = torch.from_numpy(b).to(DEV)
         x = torch.zeros_like(bd)
@@ -294,6 +298,7 @@ def test_recomputed_factors_give_the_stored_iterates_bit_for_bit(cfg):
     nx, ny, nz, varying, graded, a_v = cfg
     prob, kw, b = case(nx, ny, nz, varying, graded, a_v=a_v, seed=7)
     with mf.Solver(nx, ny, nz, **kw) as s:
+        s.set_loop("batched")  # the same loop (and reduction trees) for both
         s.set_substructuring(1)
         bd = torch.from_numpy(b).to(DEV)
         out = {}
@@ -395,9 +400,14 @@ def test_substructuring_arguments():
             assert e.value.status == mf.PCG_EINVAL
         bd = torch.from_numpy(b).to(DEV)
         out = []
+        # with the automatic loop these 8 tiles run the persistent loop, which
+        # needs (and beats) Thomas column solves; with the batched loop they
+        # are substructured (fewer tiles than half the SMs): 4 blocks
+        s.set_substructuring(0)
+        assert (s.substructuring, s.loop) == (1, "persistent")
+        s.set_loop("batched")
         for nb in (4, 1, 2, 0, 4):
             s.set_substructuring(nb)
-            # automatic: 8 tiles of 32 columns (fewer than half the SMs): 4 blocks
             assert s.substructuring == (4 if nb == 0 else nb)
             x = torch.zeros_like(bd)
             it, _, st = s.solve(bd, x, rtol=1e-10)
@@ -488,3 +498,52 @@ def test_degenerate_grids_solve_like_the_oracle(cfg, mode):
         assert s.solve(bd, x, rtol=0.0, maxit=it_ref)[0] == it_ref
         xs = x.cpu().numpy()
     assert np.linalg.norm(xs - x_ref) <= SOL_TOL * np.linalg.norm(x_ref)
+
+
+# ---- the persistent solve loop (one cooperative kernel per solve)
+
+def test_persistent_loop_choice_and_timing():
+    prob, kw, b = case(30, 26, 24, True, True, a_v=1e3, seed=16)
+    with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        s.set_substructuring(1)
+        assert s.loop == "persistent"          # 25 tiles: the automatic choice
+        s.set_loop("batched")
+        assert s.loop == "batched"
+        s.set_loop("persistent")
+        s.set_factors("recompute")             # not for rebuilt factors ...
+        assert s.loop == "batched"
+        s.set_factors("stored")
+        s.set_substructuring(2)                # ... nor for substructured columns
+        assert s.loop == "batched"
+        s.set_substructuring(1)
+        assert s.loop == "persistent"
+        with pytest.raises(mf.PCGError):
+            mf.pcg_set_loop(s.ctx, 5)
+        s.enable_timing(True)
+        bd = torch.from_numpy(b).to(DEV)
+        x = torch.zeros_like(bd)
+        it, _, st = s.solve(bd, x, rtol=1e-10)
+        t = s.kernel_times()
+        assert st == mf.PCG_OK and t["loop"][1] == 1 and t["loop"][0] > 0
+        assert t["precond_fused"][1] == 0 and t["spmv_fused"][1] == 0
+        assert s.launch_info()["last_solve_launches"] == 5   # residual, 2 conversions, loop, final
+
+
+@pytest.mark.parametrize("cfg", SOLVE_CASES, ids=lambda c: "x".join(map(str, c[:3])))
+def test_persistent_and_batched_loops_agree(cfg):
+    # the same sweeps in the same arithmetic; only the reduction trees differ
+    nx, ny, nz, varying, graded, a_v = cfg
+    prob, kw, b = case(nx, ny, nz, varying, graded, a_v=a_v, seed=17)
+    with mf.Solver(nx, ny, nz, **kw) as s:
+        bd = torch.from_numpy(b).to(DEV)
+        out = {}
+        for mode in ["tiled", "tiled_persistent"]:
+            configure(s, mode)
+            x = torch.zeros_like(bd)
+            it, hist, st = s.solve(bd, x, rtol=1e-10)
+            out[mode] = (it, st, hist, x.cpu().numpy())
+    (i1, s1, h1, x1), (i2, s2, h2, x2) = out["tiled"], out["tiled_persistent"]
+    assert s1 == s2 == mf.PCG_OK and abs(i1 - i2) <= 1
+    n = min(i1, i2) + 1
+    np.testing.assert_allclose(h1[:n], h2[:n], rtol=1e-6, atol=1e-13)
+    assert np.linalg.norm(x1 - x2) <= SOL_TOL * np.linalg.norm(x1)
