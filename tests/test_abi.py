@@ -74,6 +74,20 @@ def test_null_context_calls_fail_cleanly(lib):
     assert lib._lib.pcg_precond(None, None, None) == lib.PCG_EINVAL
     assert lib._lib.pcg_solve(None, None, None, 1e-10, 10, None, None) == lib.PCG_EINVAL
     assert lib._lib.pcg_set_stream(None, None) == lib.PCG_EINVAL
+    assert lib._lib.pcg_solve_host(None, None, None, 1e-10, 10, None, None) == lib.PCG_EINVAL
+    assert lib._lib.pcg_solve_host_x0(None, None, None, None, 1e-10, 10, None, None) == \
+        lib.PCG_EINVAL
+    assert lib._lib.pcg_update_coeffs(None, None) == lib.PCG_EINVAL
+    assert lib._lib.pcg_set_layout(None, lib.PCG_LAYOUT_TILED) == lib.PCG_EINVAL
+    assert lib._lib.pcg_set_factors(None, lib.PCG_FACTORS_STORED) == lib.PCG_EINVAL
+    assert lib._lib.pcg_set_substructuring(None, 0) == lib.PCG_EINVAL
+    assert lib._lib.pcg_set_loop(None, lib.PCG_LOOP_AUTO) == lib.PCG_EINVAL
+    assert lib._lib.pcg_get_substructuring(None, None) == lib.PCG_EINVAL
+    assert lib._lib.pcg_get_loop(None, None) == lib.PCG_EINVAL
+    assert lib._lib.pcg_precond_dot_noalloc(None, None, None, None) == lib.PCG_EINVAL
+    assert lib._lib.pcg_enable_timing(None, 1) == lib.PCG_EINVAL
+    assert lib._lib.pcg_kernel_times(None, None, None) == lib.PCG_EINVAL
+    assert lib._lib.pcg_launch_info(None, None, None, None) == lib.PCG_EINVAL
     lib._lib.pcg_destroy(None)  # NULL-safe
     assert isinstance(lib.pcg_last_error(None), str)
 
