@@ -547,3 +547,46 @@ def test_persistent_and_batched_loops_agree(cfg):
     n = min(i1, i2) + 1
     np.testing.assert_allclose(h1[:n], h2[:n], rtol=1e-6, atol=1e-13)
     assert np.linalg.norm(x1 - x2) <= SOL_TOL * np.linalg.norm(x1)
+
+
+@pytest.mark.parametrize("loop", ["persistent", "batched"])
+def test_two_contexts_solve_concurrently_on_two_streams(loop):
+    # each context captures its graphs on a private stream and launches on
+    # the caller's; concurrent solves give the sequential results bit for bit
+    cases = [case(30, 26, 24, True, True, a_v=1e3, seed=18),
+             case(41, 17, 16, False, True, a_v=1e4, seed=19)]
+    solvers = [mf.Solver(p.nx, p.ny, p.nz, **kw) for p, kw, _ in cases]
+    try:
+        bs = [torch.from_numpy(b).to(DEV) for _, _, b in cases]
+        ref = []
+        for s, bd in zip(solvers, bs):
+            s.set_substructuring(1)
+            s.set_loop(loop)
+            x = torch.zeros_like(bd)
+            it, _, st = s.solve(bd, x, rtol=1e-10)
+            ref.append((it, st, x.cpu().numpy()))
+        streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+        xs = [torch.zeros_like(bd) for bd in bs]
+        for s, st_ in zip(solvers, streams):
+            s.set_stream(st_)
+        torch.cuda.synchronize()
+        import threading
+        out = [None, None]
+
+        def run(i):
+            with torch.cuda.stream(streams[i]):
+                out[i] = solvers[i].solve(bs[i], xs[i], rtol=1e-10)
+
+        threads = [threading.Thread(target=run, args=(i,)) for i in range(2)]
+        for t in threads:
+            t.start()
+        for t in threads:
+            t.join()
+        torch.cuda.synchronize()
+        for i in range(2):
+            it, _, st = out[i]
+            assert (it, st) == ref[i][:2]
+            assert np.array_equal(xs[i].cpu().numpy(), ref[i][2])
+    finally:
+        for s in solvers:
+            s.close()
