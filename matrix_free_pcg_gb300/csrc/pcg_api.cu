@@ -452,8 +452,10 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
   // The row-tiled layout forms r = b - A x0 column-contiguously in z, then
   // converts r and x0 into the solver's layout.
   e = timed(ctx, PCG_K_RESIDUAL, [&] {
-    return pcg::launch_residual(op, ctx->state, b, x, tiled ? ctx->z : ctx->r, ctx->p, ctx->q,
-                                rtol, maxit, ctx->grid_a, s);
+    // (the row-tiled layout clears p and q at its own positions in the conversion below)
+    return pcg::launch_residual(op, ctx->state, b, x, tiled ? ctx->z : ctx->r,
+                                tiled ? nullptr : ctx->p, tiled ? nullptr : ctx->q, rtol, maxit,
+                                ctx->grid_a, s);
   });
   if (e == cudaSuccess && tiled) {
     e = timed(ctx, PCG_K_RESIDUAL, [&] { return pcg::launch_to_tiled(op, ctx->z, ctx->r, s); });

@@ -810,9 +810,9 @@ __device__ __forceinline__ bool x_is_zero2(const Op& op, const double* __restric
   return bits == 0ull;
 }
 
-// MODE 0: y = A x.  MODE 1: r = b - A x, p = q = 0, and the scalar state of
-// a new solve (alpha = 0, kappa_old = 1: the first sweeps then give p = z_0,
-// q = A z_0).
+// MODE 0: y = A x.  MODE 1: r = b - A x, p = q = 0 (unless p is NULL), and
+// the scalar state of a new solve (alpha = 0, kappa_old = 1: the first sweeps
+// then give p = z_0, q = A z_0).
 template <bool VARY, bool VEC2, int MODE>
 __global__ void __launch_bounds__(kSpmvThreads) k_stencil(Op op, DevState* st,
                                                           const double* __restrict__ x,
@@ -859,8 +859,10 @@ __global__ void __launch_bounds__(kSpmvThreads) k_stencil(Op op, DevState* st,
       } else {
         const double2 bv = ld2(b + l);
         st2(y + l, make_double2(bv.x - ax.x, bv.y - ax.y));
-        st2(p + l, make_double2(0.0, 0.0));
-        st2(q + l, make_double2(0.0, 0.0));
+        if (p) {  // p = q = 0 here, or (NULL) by the caller in its own layout
+          st2(p + l, make_double2(0.0, 0.0));
+          st2(q + l, make_double2(0.0, 0.0));
+        }
       }
     }
   } else {
@@ -872,8 +874,10 @@ __global__ void __launch_bounds__(kSpmvThreads) k_stencil(Op op, DevState* st,
         y[l] = ax;
       } else {
         y[l] = b[l] - ax;
-        p[l] = 0.0;
-        q[l] = 0.0;
+        if (p) {
+          p[l] = 0.0;
+          q[l] = 0.0;
+        }
       }
     }
   }
