@@ -1,4 +1,6 @@
-// Device kernels of the matrix-free PCG solver (fp64, sm_103a).
+// Device kernels of the matrix-free PCG solver (fp64, sm_103a) for the
+// column-contiguous layout, plus the stencil kernels every layout uses (the
+// standalone operator and the initial residual) and the deferred update.
 //
 // Method: Mueller, Guo, Scheichl, Shi, "Matrix-free GPU implementation of a
 // preconditioned conjugate gradient solver for anisotropic elliptic PDEs".
@@ -8,15 +10,15 @@
 //   - fused sweeps: section 4.3, Algorithm 1, with the two kernels of
 //     Appendix A (Algorithm 2: SpMV sweep, Algorithm 3: preconditioner sweep).
 //
-// Design for GB300.  The fp64 pipe of this part retires about 1.6 lane
-// operations per SM per clock, so at the 88-112 bytes per cell and iteration
-// that the fused sweeps move, the iteration is bound by fp64 arithmetic, not
-// by HBM.  The kernels therefore spend integer and load/store instructions
-// freely and keep the fp64 instruction count at the minimum of the
-// formulation: 6 per cell in the preconditioner sweep, 11 (constant a_h) or
-// 12 (a_h per column) in the stencil sweep.  Both sweeps are persistent grids
-// (a few blocks per SM), so the per-thread partial sums are folded into the
-// grid reduction only once per launch.
+// Design for GB300.  The fp64 pipe of this part retires 2 lane operations per
+// SM per clock at most, so at the 88-112 bytes per cell and iteration that
+// these sweeps move, the iteration is bound by fp64 arithmetic, not by HBM.
+// The kernels therefore spend integer and load/store instructions freely and
+// keep the fp64 instruction count at the minimum of the formulation: 6 per
+// cell in the preconditioner sweep, 11 (constant a_h) or 12 (a_h per column:
+// face values per column) in the stencil sweep.  Both sweeps are persistent
+// grids (a few blocks per SM), so the per-thread partial sums are folded into
+// the grid reduction only once per launch.
 //
 // Vectors use the column-contiguous layout: cell (i,j,k) at ((j*nx)+i)*nz+k.
 #include <algorithm>

@@ -1,9 +1,12 @@
 // Row-tiled solver layout: the paper's eq. (22) ordering (horizontal index
-// fastest) in blocked form, with its two fused sweeps.
+// fastest) in blocked form, with its two fused sweeps (stored or rebuilt
+// factors), the conversions from and to the caller's layout, and the
+// persistent loop that runs every iteration of a small grid in one kernel.
 //
 // Method: Mueller, Guo, Scheichl, Shi, "Matrix-free GPU implementation of a
 // preconditioned conjugate gradient solver for anisotropic elliptic PDEs",
-// section 6.1, eq. (22) (layout), Appendix A Algorithms 2 and 3 (sweeps).
+// section 6.1, eq. (22) (layout), section 4.3 Algorithm 1 (loop), Appendix A
+// Algorithms 2 and 3 (sweeps).
 //
 // Cell (column c, level k) sits at (c/32 * nz + k) * 32 + c%32: level-major
 // within tiles of 32 consecutive columns, so it works for any nx.  A warp
