@@ -169,12 +169,18 @@ def reduce_over_ranks(ms, iters, device):
 
 
 def sources_sha256(names):
-    """sha256 over the named kernel sources (csrc/), concatenated in order."""
+    """sha256 over the code of the named kernel sources (csrc/), concatenated in
+    order, with comments and whitespace removed: a capture stays valid across
+    comment edits and goes stale with any change of the code itself."""
     import hashlib
+    import re
     hsh = hashlib.sha256()
     for name in names:
-        with open(os.path.join(ROOT, "matrix_free_pcg_gb300", "csrc", name), "rb") as f:
-            hsh.update(f.read())
+        with open(os.path.join(ROOT, "matrix_free_pcg_gb300", "csrc", name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        hsh.update(" ".join(text.split()).encode())
     return hsh.hexdigest()
 
 
