@@ -100,3 +100,27 @@ def test_create_without_gpu_reports_cuda_error(lib):
         lib.pcg_create(4, 4, 4, a_h=1.0, a_v=10.0)
     assert e.value.status == lib.PCG_ECUDA
     assert "no usable CUDA device" in lib.pcg_last_error()
+
+
+def header_constants():
+    """NAME = value pairs of the header's enums (comments removed)."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(PCG_\w+)\s*=\s*(\d+)", text)}
+
+
+def test_binding_constants_match_the_header(lib):
+    consts = header_constants()
+    for name, value in consts.items():
+        if name.startswith("PCG_K_"):
+            continue
+        assert getattr(lib, name) == value, name
+    # kernel kinds: the binding's list is indexed by the header's enum
+    kinds = sorted((v, k) for k, v in consts.items() if k.startswith("PCG_K_") and k != "PCG_K_COUNT")
+    assert len(lib.KERNEL_KINDS) == consts["PCG_K_COUNT"] == len(kinds)
+    expect = {"PCG_K_PRECOND_FUSED": "precond_fused", "PCG_K_SPMV_FUSED": "spmv_fused",
+              "PCG_K_RESIDUAL": "residual", "PCG_K_FINALIZE": "finalize",
+              "PCG_K_APPLY_A": "apply_A", "PCG_K_PRECOND": "precond", "PCG_K_SETUP": "setup",
+              "PCG_K_LOOP": "loop"}
+    for v, k in kinds:
+        assert lib.KERNEL_KINDS[v] == expect[k], (k, v)
