@@ -365,6 +365,16 @@ def run_ours(args, w):
         "hbm_frac": hbm_ach / hbm_peak, "hbm_peak_source": peak_src,
     }
     kernels = {k: {"ms": v[0], "launches": v[1]} for k, v in ktimes.items() if v[1]}
+    # DRAM bytes of one iteration (both sweeps, from the committed ncu captures)
+    # against the fused minimum of 88 B/cell (u, p, z, q, r moved once, no
+    # per-cell coefficients) and against this build's algorithmic bytes
+    dram_iter = None
+    t_m = measured_traffic("precond_fused", n, args.layout, args.factors)
+    t_a = measured_traffic("spmv_fused", n, args.layout, args.factors)
+    if t_m and t_a:
+        dram_iter = {"bytes": t_m + t_a, "per_cell": (t_m + t_a) / n,
+                     "vs_fused_min_88": (t_m + t_a) / (88.0 * n),
+                     "vs_algorithmic": (t_m + t_a) / bytes_iter}
 
     # end to end through the host-buffer entry point: pinned b in, x out, zero
     # initial guess (pcg_solve_host_x0 with x0 = NULL); one page-locked output
@@ -417,6 +427,7 @@ def run_ours(args, w):
                        "parallelism": "replicas" if world > 1 else "single"},
             "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / hbm_peak,
             "bytes_per_cell_iter": bytes_iter / n, "fp64_ops_per_cell_iter": ops_iter / n,
+            "dram_per_iter": dram_iter,
             "roofline": roofline, "kernels": kernels, "clocks": clk, "e2e": e2e,
             "cpu_baseline": cpu, "gpu_launches": launches,
             "time_to_solution_ms": ms_max / args.steps,
