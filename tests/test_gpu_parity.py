@@ -590,3 +590,22 @@ def test_two_contexts_solve_concurrently_on_two_streams(loop):
     finally:
         for s in solvers:
             s.close()
+
+
+@pytest.mark.parametrize("mode", ["column", "tiled", "tiled_persistent"])
+def test_very_tall_columns(mode):
+    # 1500 levels: the row-tiled sweeps stream any height in register chunks;
+    # the column layout takes its unstaged preconditioner sweep
+    prob, kw, b = case(5, 3, 1500, True, False, a_v=1e3, seed=20)
+    x_ref, it_ref, _, st_ref = oracle.pcg(prob, b, rtol=1e-10, maxit=500)
+    assert st_ref == oracle.OK
+    with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        configure(s, mode)
+        bd = torch.from_numpy(b).to(DEV)
+        x = torch.zeros_like(bd)
+        it, _, st = s.solve(bd, x, rtol=1e-10, maxit=500)
+        assert st == mf.PCG_OK and abs(it - it_ref) <= 1
+        x.zero_()
+        assert s.solve(bd, x, rtol=0.0, maxit=it_ref)[0] == it_ref
+        xs = x.cpu().numpy()
+    assert np.linalg.norm(xs - x_ref) <= SOL_TOL * np.linalg.norm(x_ref)
