@@ -68,6 +68,8 @@ def parse():
                          "2 per step for --impl reference)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-standalone", action="store_true",
+                    help="skip timing the standalone apply_A and precond")
     ap.add_argument("--layout", choices=["column", "tiled"], default="tiled",
                     help="layout of the solver's internal vectors")
     ap.add_argument("--factors", choices=["stored", "recompute"], default="stored",
@@ -166,6 +168,15 @@ def reduce_over_ranks(ms, iters, device):
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     dist.all_reduce(n, op=dist.ReduceOp.SUM)
     return float(t.item()), float(n.item())
+
+
+def alu_peak_g(dev, clocks):
+    """Nominal fp64 lane-ops/s (G) at the SM clock sampled under load."""
+    import torch
+    clk = clocks.summary() or {}
+    mhz = clk.get("sm_mhz") or 2070.0
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    return FP64_LANES_PER_SM_CLK * nsm * mhz * 1e6 / 1e9
 
 
 def sources_sha256(names):
@@ -326,6 +337,38 @@ def run_ours(args, w):
     ms_max, total_iters = reduce_over_ranks(ms, sum(iters), dev)
     value = total_iters / (ms_max * 1e-3)
 
+    # standalone operator and preconditioner (after the timed steps; not in
+    # `value`): y = A x and z = M^{-1} r on the caller's column-contiguous vectors
+    standalone = None
+    if not args.no_standalone:
+        y = torch.empty_like(bd)
+        reps = 5
+        out = {}
+        for name, fn in (("apply_A", lambda: solver.apply_A(bd, y)),
+                         ("precond", lambda: solver.precond(bd, y))):
+            fn()
+            torch.cuda.synchronize()
+            s0 = torch.cuda.Event(enable_timing=True)
+            s1 = torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            for _ in range(reps):
+                fn()
+            s1.record(stream)
+            torch.cuda.synchronize()
+            out[name] = s0.elapsed_time(s1) / reps
+        # fp64 operations and algorithmic bytes per cell: the stencil 8 (field:
+        # 4 horizontal, diagonal, 2 vertical, weight) or 7 (constant: 3 adds +
+        # 4), x and y (+ diagonal); the Thomas solve 3 (forward 2, back 1), r
+        # and z (+ 2 factors)
+        ops = {"apply_A": 8 if varying else 7, "precond": 3}
+        byt = {"apply_A": 24 if varying else 16, "precond": 32 if varying else 16}
+        standalone = {k: {"ms": v, "fp64_gops": ops[k] * w.n / (v * 1e-3) / 1e9,
+                          "frac_fp64": ops[k] * w.n / (v * 1e-3) / 1e9 / alu_peak_g(dev, clocks),
+                          "gbs": byt[k] * w.n / (v * 1e-3) / 1e9,
+                          "ops_per_cell": ops[k], "bytes_per_cell": byt[k]}
+                      for k, v in out.items()}
+        del y
+
     n = w.n
     peaks, peak_src = measured_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
@@ -427,7 +470,7 @@ def run_ours(args, w):
                        "parallelism": "replicas" if world > 1 else "single"},
             "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / hbm_peak,
             "bytes_per_cell_iter": bytes_iter / n, "fp64_ops_per_cell_iter": ops_iter / n,
-            "dram_per_iter": dram_iter,
+            "dram_per_iter": dram_iter, "standalone": standalone,
             "roofline": roofline, "kernels": kernels, "clocks": clk, "e2e": e2e,
             "cpu_baseline": cpu, "gpu_launches": launches,
             "time_to_solution_ms": ms_max / args.steps,
