@@ -90,18 +90,27 @@ def test_workload_large_parity(name, fixed_iters):
         bd = sampled_operator_checks(w, prob, s, b)
         x = torch.zeros_like(bd)
         got = {}
-        for layout, factors in [("tiled", "recompute"), ("tiled", "stored"), ("column", "stored")]:
+        modes = [("tiled", "recompute", 1, "batched"), ("tiled", "stored", 1, "batched"),
+                 ("column", "stored", 1, "batched"), ("tiled", "stored", 2, "batched"),
+                 ("tiled", "stored", 1, "persistent")]
+        for layout, factors, blocks, loop in modes:
             s.set_layout(layout)
             s.set_factors(factors)
+            s.set_loop(loop)
+            s.set_substructuring(blocks)
             x.zero_()
             it, _, st = s.solve(bd, x, rtol=0.0, maxit=fixed_iters)
             assert (it, st) == (fixed_iters, mf.PCG_OK)
             xs = x.cpu().numpy()
-            assert np.linalg.norm(xs - x_ref) <= 1e-8 * np.linalg.norm(x_ref), (layout, factors)
-            got[(layout, factors)] = xs
+            assert np.linalg.norm(xs - x_ref) <= 1e-8 * np.linalg.norm(x_ref), (layout, factors,
+                                                                                blocks, loop)
+            if blocks == 1 and loop == "batched" and layout == "tiled":
+                got[factors] = xs  # the two the bitwise comparison below needs
+        s.set_substructuring(1)
+        s.set_loop("auto")
         # the set-up derives T/D from 1/D (Markstein's correction), the sweep that
         # rebuilds its factors divides: bitwise equal on every cell of the grid
-        assert np.array_equal(got[("tiled", "recompute")], got[("tiled", "stored")])
+        assert np.array_equal(got["recompute"], got["stored"])
         del xs, x_ref, got
         s.set_layout("tiled")
         # the workload's own stopping rule, then the true residual on the CPU
