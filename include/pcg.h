@@ -180,6 +180,14 @@ int pcg_set_loop(pcg_ctx* ctx, int mode);
  * PCG_LOOP_PERSISTENT.  Errors: PCG_EINVAL (NULL). */
 int pcg_get_loop(const pcg_ctx* ctx, int* mode_out);
 
+/* Test hook for the persistent loop's bounded waits: with absent > 0, its
+ * grid barriers count `absent` arrivals that never come, so the first
+ * barrier wait of the next persistent solve runs out (about a second) and the
+ * solve returns PCG_ETIMEOUT; the context stays usable.  0 (default) is
+ * normal operation.  Nothing faults or waits without bound.
+ * Errors: PCG_EINVAL (NULL, absent < 0). */
+int pcg_test_barrier_absent(pcg_ctx* ctx, int absent);
+
 /* Blocks per column the row-tiled preconditioner sweep currently uses
  * (1: Thomas), after the automatic choice.  Errors: PCG_EINVAL (NULL). */
 int pcg_get_substructuring(const pcg_ctx* ctx, int* nblocks_out);

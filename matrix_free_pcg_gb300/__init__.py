@@ -33,7 +33,7 @@ EXPORTED = ["pcg_create", "pcg_destroy", "pcg_update_coeffs", "pcg_set_stream", 
             "pcg_enable_timing", "pcg_kernel_times", "pcg_launch_info",
             "pcg_precond_dot_noalloc", "pcg_set_layout", "pcg_set_factors",
             "pcg_set_substructuring", "pcg_get_substructuring", "pcg_solve_host_x0",
-            "pcg_set_loop", "pcg_get_loop"]
+            "pcg_set_loop", "pcg_get_loop", "pcg_test_barrier_absent"]
 PCG_LAYOUT_COLUMN, PCG_LAYOUT_TILED = 0, 1
 PCG_FACTORS_STORED, PCG_FACTORS_RECOMPUTE = 0, 1
 PCG_LOOP_AUTO, PCG_LOOP_BATCHED, PCG_LOOP_PERSISTENT = 0, 1, 2
@@ -80,6 +80,7 @@ def _load(path=LIB_PATH):
         "pcg_get_substructuring": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int)]),
         "pcg_set_loop": (ctypes.c_int, [_vp, ctypes.c_int]),
         "pcg_get_loop": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int)]),
+        "pcg_test_barrier_absent": (ctypes.c_int, [_vp, ctypes.c_int]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -218,6 +219,12 @@ def pcg_get_loop(ctx):
     v = ctypes.c_int(0)
     _check(_lib.pcg_get_loop(ctx, ctypes.byref(v)), ctx)
     return v.value
+
+
+def pcg_test_barrier_absent(ctx, absent):
+    """Test hook: the persistent loop's barriers miss `absent` arrivals, so the
+    next persistent solve's first barrier wait runs out (PCG_ETIMEOUT)."""
+    return _check(_lib.pcg_test_barrier_absent(ctx, int(absent)), ctx)
 
 
 def pcg_apply_A(ctx, n, x, y):

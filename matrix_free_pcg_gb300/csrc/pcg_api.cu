@@ -65,6 +65,7 @@ struct pcg_ctx {
   int split_req = 0, split_p = 1, grid_sp = 0;
   int loop_req = PCG_LOOP_AUTO;      // requested solve loop
   int grid_ps = 0;                   // blocks of the persistent loop (0: not available)
+  unsigned int test_absent = 0;      // test hook: arrivals the persistent barriers miss
   size_t partials_cap = 0;           // doubles in `partials`
   // CUDA graphs of the row-tiled loop: two instances, launched alternately so
   // that one can be read back (timing) while the other runs.  They are
@@ -470,7 +471,8 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
   if (persistent) {
     e = timed(ctx, PCG_K_LOOP, [&] {
       return pcg::launch_persistent(op, ctx->state, ctx->r, ctx->q, ctx->z, ctx->u_t, ctx->p,
-                                    ctx->partials, ctx->hist, ctx->grid_ps, s);
+                                    ctx->partials, ctx->hist, ctx->grid_ps, ctx->test_absent,
+                                    s);
     });
     if (e != cudaSuccess) return cuda_fail(ctx, e, "persistent solve loop launch");
   }
@@ -850,6 +852,13 @@ int pcg_set_loop(pcg_ctx* ctx, int mode) {
   if (mode != PCG_LOOP_AUTO && mode != PCG_LOOP_BATCHED && mode != PCG_LOOP_PERSISTENT)
     return fail(ctx, PCG_EINVAL, "unknown loop mode %d", mode);
   ctx->loop_req = mode;
+  return PCG_OK;
+}
+
+int pcg_test_barrier_absent(pcg_ctx* ctx, int absent) {
+  if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
+  if (absent < 0) return fail(ctx, PCG_EINVAL, "absent must be >= 0");
+  ctx->test_absent = (unsigned int)absent;
   return PCG_OK;
 }
 

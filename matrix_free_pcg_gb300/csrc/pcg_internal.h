@@ -152,7 +152,7 @@ constexpr int kTmWarpsPerSm = 12;
 int grid_persistent(const Op& op, int num_sms);
 cudaError_t launch_persistent(const Op& op, DevState* st, double* r, double* q, double* z,
                               double* u, double* p, double* partials, double* hist, int grid,
-                              cudaStream_t s);
+                              unsigned int absent, cudaStream_t s);
 
 // Grid sizes (blocks) of the two row-tiled sweeps.
 int grid_tiled_precond(const Op& op, int num_sms);

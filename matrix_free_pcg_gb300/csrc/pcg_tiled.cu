@@ -480,7 +480,8 @@ __global__ void __launch_bounds__(256) k_spmv_tiled(Op op, DevState* st,
 
 constexpr int kPsThreads = 256;
 // Polls of a barrier wait before the loop gives up with PCG_ETIMEOUT (with a
-// 64 ns sleep per poll: about a second).
+// 64 ns sleep per poll: about a second).  `absent` (0 in normal use) adds
+// arrivals that never come, so that a test can make the wait run out.
 constexpr long long kBarrierPolls = 1LL << 24;
 
 // Per-block sums of two values (fixed order) into out[0], out[1].
@@ -533,7 +534,8 @@ __global__ void __launch_bounds__(kPsThreads) k_pcg_persistent(Op op, DevState* 
                                                                double* __restrict__ p,
                                                                double* __restrict__ partials,
                                                                double* __restrict__ hist,
-                                                               int seglen) {
+                                                               int seglen,
+                                                               unsigned int absent) {
   const int lane = threadIdx.x & 31;
   // warps numbered across the blocks first, so that few tiles still spread
   // over every SM of the grid (one block per SM)
@@ -555,7 +557,7 @@ __global__ void __launch_bounds__(kPsThreads) k_pcg_persistent(Op op, DevState* 
     for (long long t = warp0; t < op.ntiles; t += nwarps)
       precond_tile<VARY, true, true>(op, t, lane, r, q, z, -alpha, keep, stream, accR, accK);
     block_partial2(accR, accK, partM + 2 * blockIdx.x);
-    if (!grid_barrier(&st->bar_count, &st->bar_gen, G, &st->dev_error, kBarrierPolls)) {
+    if (!grid_barrier(&st->bar_count, &st->bar_gen, G + absent, &st->dev_error, kBarrierPolls)) {
       timeout = true;
       break;
     }
@@ -590,7 +592,7 @@ __global__ void __launch_bounds__(kPsThreads) k_pcg_persistent(Op op, DevState* 
     for (long long unit = warp0; unit < nunits; unit += nwarps)
       spmv_unit<VARY, false, true>(op, unit, lane, z, u, p, q, alpha, beta, seglen, sig);
     block_partial2(sig, 0.0, partA + 2 * blockIdx.x);
-    if (!grid_barrier(&st->bar_count, &st->bar_gen, G, &st->dev_error, kBarrierPolls)) {
+    if (!grid_barrier(&st->bar_count, &st->bar_gen, G + absent, &st->dev_error, kBarrierPolls)) {
       timeout = true;
       break;
     }
@@ -727,10 +729,10 @@ int grid_persistent(const Op& op, int num_sms) {
 
 cudaError_t launch_persistent(const Op& op, DevState* st, double* r, double* q, double* z,
                               double* u, double* p, double* partials, double* hist, int grid,
-                              cudaStream_t s) {
+                              unsigned int absent, cudaStream_t s) {
   Op o = op;
   int seglen = tiled_spmv_seglen(op, grid);
-  void* args[] = {&o, &st, &r, &q, &z, &u, &p, &partials, &hist, &seglen};
+  void* args[] = {&o, &st, &r, &q, &z, &u, &p, &partials, &hist, &seglen, &absent};
   const void* fn = op.varying ? reinterpret_cast<const void*>(k_pcg_persistent<true>)
                               : reinterpret_cast<const void*>(k_pcg_persistent<false>);
   return cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kPsThreads), args, 0, s);

@@ -84,6 +84,7 @@ def test_null_context_calls_fail_cleanly(lib):
     assert lib._lib.pcg_set_loop(None, lib.PCG_LOOP_AUTO) == lib.PCG_EINVAL
     assert lib._lib.pcg_get_substructuring(None, None) == lib.PCG_EINVAL
     assert lib._lib.pcg_get_loop(None, None) == lib.PCG_EINVAL
+    assert lib._lib.pcg_test_barrier_absent(None, 0) == lib.PCG_EINVAL
     assert lib._lib.pcg_precond_dot_noalloc(None, None, None, None) == lib.PCG_EINVAL
     assert lib._lib.pcg_enable_timing(None, 1) == lib.PCG_EINVAL
     assert lib._lib.pcg_kernel_times(None, None, None) == lib.PCG_EINVAL

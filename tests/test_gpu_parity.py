@@ -609,3 +609,29 @@ def test_very_tall_columns(mode):
         assert s.solve(bd, x, rtol=0.0, maxit=it_ref)[0] == it_ref
         xs = x.cpu().numpy()
     assert np.linalg.norm(xs - x_ref) <= SOL_TOL * np.linalg.norm(x_ref)
+
+
+def test_persistent_barrier_wait_runs_out_and_the_context_recovers():
+    # the barriers count one arrival that never comes: the first wait runs out
+    # after its poll limit (about a second), the solve reports PCG_ETIMEOUT,
+    # and the next solve on the same context is normal
+    import time
+    prob, kw, b = case(30, 26, 24, True, True, a_v=1e3, seed=21)
+    _, it_ref, _, _ = oracle.pcg(prob, b, rtol=1e-10)
+    with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        s.set_loop("persistent")
+        s.set_substructuring(1)
+        assert s.loop == "persistent"
+        bd = torch.from_numpy(b).to(DEV)
+        x = torch.zeros_like(bd)
+        mf.pcg_test_barrier_absent(s.ctx, 1)
+        t0 = time.perf_counter()
+        with pytest.raises(mf.PCGError) as e:
+            s.solve(bd, x, rtol=1e-10)
+        assert e.value.status == mf.PCG_ETIMEOUT
+        assert "bounded device wait" in mf.pcg_last_error(s.ctx)
+        assert time.perf_counter() - t0 < 60.0
+        mf.pcg_test_barrier_absent(s.ctx, 0)
+        x.zero_()
+        it, _, st = s.solve(bd, x, rtol=1e-10)
+        assert st == mf.PCG_OK and abs(it - it_ref) <= 1
