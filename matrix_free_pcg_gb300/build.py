@@ -12,9 +12,10 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libpcg.so")
-SOURCES = ["pcg_kernels.cu", "pcg_setup.cu", "pcg_tiled.cu", "pcg_split.cu", "pcg_api.cu",
-           "pcg_noalloc.cu"]
+SOURCES = ["pcg_kernels.cu", "pcg_setup.cu", "pcg_tiled.cu", "pcg_persistent.cu", "pcg_split.cu",
+           "pcg_api.cu", "pcg_noalloc.cu"]
 HEADERS = [os.path.join(CSRC, "pcg_internal.h"), os.path.join(CSRC, "pcg_device.cuh"),
+           os.path.join(CSRC, "pcg_sweeps.cuh"),
            os.path.join(ROOT, "include", "pcg.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # Host code (the per-level tables) is compiled without floating-point

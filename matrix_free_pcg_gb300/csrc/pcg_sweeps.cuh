@@ -1,0 +1,230 @@
+// Per-tile and per-unit bodies of the two row-tiled sweeps, shared by the
+// sweep kernels (pcg_tiled.cu) and the persistent solve loop
+// (pcg_persistent.cu); the row-tiled layout, cell (column c, level k) at
+// (c/32*nz + k)*32 + c%32.
+//
+// Method: Mueller, Guo, Scheichl, Shi, "Matrix-free GPU implementation of a
+// preconditioned conjugate gradient solver for anisotropic elliptic PDEs",
+// section 6.1, eq. (22) (layout), Appendix A Algorithms 2 and 3 (sweeps).
+#pragma once
+
+#include <algorithm>
+#include <cstdint>
+
+#include "pcg_device.cuh"
+#include "pcg_internal.h"
+
+namespace pcg {
+namespace {
+
+// Preconditioner sweep: threads per block and levels per register chunk.
+constexpr int kTmThreads = kTmWarpsPerBlock * 32;
+constexpr int kTmChunk = 8;
+
+__device__ __forceinline__ long long tiled_base(long long col, int nz) {
+  return (col >> 5) * (long long)nz * kTile + (col & 31);
+}
+
+// One tile of the preconditioner sweep (see k_precond_tiled), for the lane's
+// column: accumulates r*.r* and <r*, z> into accR, accK (FUSED).  COHERENT:
+// q was written by other blocks of the same launch (the persistent loop), so
+// it is read from L2, past the SM's non-coherent L1.
+template <bool VARY, bool FUSED, bool COHERENT = false>
+__device__ __forceinline__ void precond_tile(const Op& op, long long t, int lane,
+                                             double* __restrict__ r, const double* __restrict__ q,
+                                             double* __restrict__ z, double nalpha, uint64_t keep,
+                                             uint64_t stream, double& accR, double& accK) {
+  const int nz = op.nz;
+  const int fs = VARY ? kTile : 1;  // factor stride between levels
+  if (t * kTile + lane >= op.ncols) return;
+  const long long base = t * nz * kTile + lane;
+  double* __restrict__ rt = r + base;
+  const double* __restrict__ qt = FUSED ? q + base : nullptr;
+  double* __restrict__ zt = z + base;
+  const double* __restrict__ fi = VARY ? op.tinvd + base : op.lev + LV_INVD * nz;
+  const double* __restrict__ fn = VARY ? op.tnphi + base : op.lev + LV_NPHI * nz;
+  // ---- forward: level k uses nphi_{k-1} (0 at k = 0) and 1/D_k
+  double cr[kTmChunk], cq[kTmChunk], ci[kTmChunk], cn[kTmChunk];
+#pragma unroll
+  for (int j = 0; j < kTmChunk; ++j) {
+    const bool in = j < nz;
+    cr[j] = in ? ld_hint(rt + j * kTile, stream) : 0.0;
+    cq[j] = (FUSED && in) ? (COHERENT ? __ldcg(qt + j * kTile) : ld_hint(qt + j * kTile, stream))
+                          : 0.0;
+    ci[j] = in ? (VARY ? ld_hint(fi + j * fs, stream) : __ldg(fi + j)) : 0.0;
+    cn[j] = in ? (VARY ? ld_hint(fn + j * fs, keep) : __ldg(fn + j)) : 0.0;
+  }
+  double y = 0.0, nprev = 0.0, w = 0.0;
+#pragma unroll 1
+  for (int k0 = 0; k0 < nz; k0 += kTmChunk) {
+    double nr[kTmChunk], nq[kTmChunk], ni[kTmChunk], nn[kTmChunk];
+#pragma unroll
+    for (int j = 0; j < kTmChunk; ++j) {
+      const int k = k0 + kTmChunk + j;
+      const bool in = k < nz;
+      nr[j] = in ? ld_hint(rt + k * kTile, stream) : 0.0;
+      nq[j] = (FUSED && in) ? (COHERENT ? __ldcg(qt + k * kTile) : ld_hint(qt + k * kTile, stream))
+                            : 0.0;
+      ni[j] = in ? (VARY ? ld_hint(fi + k * fs, stream) : __ldg(fi + k)) : 0.0;
+      nn[j] = in ? (VARY ? ld_hint(fn + k * fs, keep) : __ldg(fn + k)) : 0.0;
+    }
+#pragma unroll
+    for (int j = 0; j < kTmChunk; ++j) {
+      const int k = k0 + j;
+      if (k < nz) {
+        double rk = cr[j];
+        if (FUSED) {
+          rk = fma(nalpha, cq[j], rk);
+          accR = fma(rk, rk, accR);
+          st_hint(rt + k * kTile, rk, stream);
+        }
+        y = fma(nprev, y, rk);
+        w = y * ci[j];
+        if (FUSED) accK = fma(y, w, accK);
+        st_hint(zt + k * kTile, w, keep);
+        nprev = cn[j];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kTmChunk; ++j) {
+      cr[j] = nr[j];
+      cq[j] = nq[j];
+      ci[j] = ni[j];
+      cn[j] = nn[j];
+    }
+  }
+  // ---- backward: z_{nz-1} = w_{nz-1} (in place); level k uses nphi_k.
+  // Chunk b holds levels kb, kb-1, ..., kb-kTmChunk+1 with kb = nz-2-b*kTmChunk.
+  double zz = w;
+  double bw[kTmChunk], bn[kTmChunk];
+#pragma unroll
+  for (int j = 0; j < kTmChunk; ++j) {
+    const int k = nz - 2 - j;
+    bw[j] = (k >= 0) ? ld_hint(zt + k * kTile, stream) : 0.0;
+    bn[j] = (k >= 0) ? (VARY ? ld_hint(fn + k * fs, stream) : __ldg(fn + k)) : 0.0;
+  }
+#pragma unroll 1
+  for (int kb = nz - 2; kb >= 0; kb -= kTmChunk) {
+    double nw[kTmChunk], nb[kTmChunk];
+#pragma unroll
+    for (int j = 0; j < kTmChunk; ++j) {
+      const int k = kb - kTmChunk - j;
+      nw[j] = (k >= 0) ? ld_hint(zt + k * kTile, stream) : 0.0;
+      nb[j] = (k >= 0) ? (VARY ? ld_hint(fn + k * fs, stream) : __ldg(fn + k)) : 0.0;
+    }
+#pragma unroll
+    for (int j = 0; j < kTmChunk; ++j) {
+      const int k = kb - j;
+      if (k >= 0) {
+        zz = fma(bn[j], zz, bw[j]);
+        st_hint(zt + k * kTile, zz, stream);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kTmChunk; ++j) {
+      bw[j] = nw[j];
+      bn[j] = nb[j];
+    }
+  }
+}
+
+// One unit (a segment of seglen levels of one tile) of the stencil sweep (see
+// k_spmv_tiled) for the lane's column; accumulates <p, q> into sig.
+// COHERENT: z was written by other blocks of the same launch (the persistent
+// loop), so it is read from L2, past the SM's non-coherent L1.
+template <bool VARY, bool RECOMP, bool COHERENT = false>
+__device__ __forceinline__ void spmv_unit(const Op& op, long long unit, int lane,
+                                          const double* __restrict__ z, double* __restrict__ u,
+                                          double* __restrict__ p, double* __restrict__ q,
+                                          double alpha, double beta, int seglen, double& sig) {
+  const int nz = op.nz;
+  const double* __restrict__ lev = op.lev;
+  const long long t = unit % op.ntiles;
+  const int k0 = (int)(unit / op.ntiles) * seglen;
+  const int k1 = min(nz, k0 + seglen);
+  const long long col = t * kTile + lane;
+  if (col >= op.ncols) return;
+  const long long base = t * nz * kTile + lane;
+  const Nbr nb = neighbours(op, col);
+  const long long bE = tiled_base(nb.e, nz), bW = tiled_base(nb.w, nz);
+  const long long bN = tiled_base(nb.n, nz), bS = tiled_base(nb.s, nz);
+  double aE = 0.0, aW = 0.0, aN = 0.0, aS = 0.0;
+  if (RECOMP) {
+    aE = __ldg(op.faceE + col);
+    aW = __ldg(op.faceE + nb.w);
+    aN = __ldg(op.faceN + col);
+    aS = __ldg(op.faceN + nb.s);
+  }
+  // RECOMP: the diagonal rebuilt as the set-up kernel rounds it
+  const double sf = RECOMP ? aE + aW + aN + aS : 0.0;
+  auto ldz = [&](long long o) { return COHERENT ? __ldcg(z + o) : z[o]; };
+  double zd = (k0 > 0) ? ldz(base + (long long)(k0 - 1) * kTile) : 0.0;
+  double zc = ldz(base + (long long)k0 * kTile);
+#pragma unroll 4
+  for (int k = k0; k < k1; ++k) {
+    const long long o = base + (long long)k * kTile;
+    const long long ko = (long long)k * kTile;
+    const double zu = (k + 1 < nz) ? ldz(o + kTile) : 0.0;
+    const double zE = ldz(bE + ko), zW = ldz(bW + ko), zN = ldz(bN + ko), zS = ldz(bS + ko);
+    double uc = __ldcs(u + o);
+    double pc = __ldcs(p + o);
+    const double qc = __ldcs(q + o);
+    uc = fma(alpha, pc, uc);
+    pc = fma(beta, pc, zc);
+    double a;
+    if (VARY) {
+      // per-cell horizontal weights -h_k a_f (west and south: the
+      // neighbours' east and north weights), rebuilt with the set-up's
+      // rounding under RECOMP
+      double d, cE, cW, cN, cS;
+      if (RECOMP) {
+        const double hw = __ldg(lev + LV_HW * nz + k);
+        d = __dadd_rn(__ldg(lev + LV_DIAG * nz + k), __dmul_rn(__ldg(lev + LV_H * nz + k), sf));
+        cE = __dmul_rn(hw, aE);
+        cW = __dmul_rn(hw, aW);
+        cN = __dmul_rn(hw, aN);
+        cS = __dmul_rn(hw, aS);
+      } else {
+        d = __ldcs(op.cdiag_t + o);
+        cE = __ldg(op.cwE_t + o);
+        cW = __ldg(op.cwE_t + bW + ko);
+        cN = __ldg(op.cwN_t + o);
+        cS = __ldg(op.cwN_t + bS + ko);
+      }
+      a = fma(d, zc, beta * qc);
+      a = fma(__ldg(lev + LV_UP * nz + k), zu, a);
+      a = fma(__ldg(lev + LV_DN * nz + k), zd, a);
+      a = fma(cE, zE, a);
+      a = fma(cW, zW, a);
+      a = fma(cN, zN, a);
+      a = fma(cS, zS, a);
+    } else {
+      const double hs = (zE + zW) + (zN + zS);
+      a = fma(__ldg(lev + LV_DIAG * nz + k), zc, beta * qc);
+      a = fma(__ldg(lev + LV_UP * nz + k), zu, a);
+      a = fma(__ldg(lev + LV_DN * nz + k), zd, a);
+      a = fma(__ldg(lev + LV_HW * nz + k), hs, a);
+    }
+    sig = fma(pc, a, sig);
+    __stcs(u + o, uc);
+    __stcs(p + o, pc);
+    __stcs(q + o, a);
+    zd = zc;
+    zc = zu;
+  }
+}
+
+// Levels per work unit of the tiled stencil sweep: whole columns when there
+// are at least 8 tiles per resident warp, else segments short enough to give
+// every warp about 8 units (at least 4 levels each).
+inline int tiled_spmv_seglen(const Op& op, int grid) {
+  const long long warps = (long long)grid * 8;
+  const long long want = 8 * warps;
+  if (op.ntiles >= want || op.nz <= 4) return op.nz;
+  long long nseg = (want + op.ntiles - 1) / op.ntiles;
+  nseg = std::min<long long>(nseg, op.nz / 4);
+  return (int)((op.nz + nseg - 1) / nseg);
+}
+
+}  // namespace
+}  // namespace pcg

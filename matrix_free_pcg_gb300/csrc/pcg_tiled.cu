@@ -21,17 +21,10 @@
 
 #include "pcg_device.cuh"
 #include "pcg_internal.h"
+#include "pcg_sweeps.cuh"
 
 namespace pcg {
 namespace {
-
-// Preconditioner sweep: threads per block and levels per register chunk.
-constexpr int kTmThreads = kTmWarpsPerBlock * 32;
-constexpr int kTmChunk = 8;
-
-__device__ __forceinline__ long long tiled_base(long long col, int nz) {
-  return (col >> 5) * (long long)nz * kTile + (col & 31);
-}
 
 // Column-contiguous <-> row-tiled conversion, 32 columns x 32 levels per
 // block through a padded shared tile (coalesced on both sides).
@@ -76,109 +69,6 @@ __global__ void __launch_bounds__(256) k_retile(Op op, const DevState* st,
     __syncthreads();
     for (int c = ty; c < nc; c += 8)
       if (tx < nk) dst[(col0 + c) * nz + k0 + tx] = tile[c][tx];
-  }
-}
-
-// One tile of the preconditioner sweep (see k_precond_tiled), for the lane's
-// column: accumulates r*.r* and <r*, z> into accR, accK (FUSED).  COHERENT:
-// q was written by other blocks of the same launch (the persistent loop), so
-// it is read from L2, past the SM's non-coherent L1.
-template <bool VARY, bool FUSED, bool COHERENT = false>
-__device__ __forceinline__ void precond_tile(const Op& op, long long t, int lane,
-                                             double* __restrict__ r, const double* __restrict__ q,
-                                             double* __restrict__ z, double nalpha, uint64_t keep,
-                                             uint64_t stream, double& accR, double& accK) {
-  const int nz = op.nz;
-  const int fs = VARY ? kTile : 1;  // factor stride between levels
-  if (t * kTile + lane >= op.ncols) return;
-  const long long base = t * nz * kTile + lane;
-  double* __restrict__ rt = r + base;
-  const double* __restrict__ qt = FUSED ? q + base : nullptr;
-  double* __restrict__ zt = z + base;
-  const double* __restrict__ fi = VARY ? op.tinvd + base : op.lev + LV_INVD * nz;
-  const double* __restrict__ fn = VARY ? op.tnphi + base : op.lev + LV_NPHI * nz;
-  // ---- forward: level k uses nphi_{k-1} (0 at k = 0) and 1/D_k
-  double cr[kTmChunk], cq[kTmChunk], ci[kTmChunk], cn[kTmChunk];
-#pragma unroll
-  for (int j = 0; j < kTmChunk; ++j) {
-    const bool in = j < nz;
-    cr[j] = in ? ld_hint(rt + j * kTile, stream) : 0.0;
-    cq[j] = (FUSED && in) ? (COHERENT ? __ldcg(qt + j * kTile) : ld_hint(qt + j * kTile, stream))
-                          : 0.0;
-    ci[j] = in ? (VARY ? ld_hint(fi + j * fs, stream) : __ldg(fi + j)) : 0.0;
-    cn[j] = in ? (VARY ? ld_hint(fn + j * fs, keep) : __ldg(fn + j)) : 0.0;
-  }
-  double y = 0.0, nprev = 0.0, w = 0.0;
-#pragma unroll 1
-  for (int k0 = 0; k0 < nz; k0 += kTmChunk) {
-    double nr[kTmChunk], nq[kTmChunk], ni[kTmChunk], nn[kTmChunk];
-#pragma unroll
-    for (int j = 0; j < kTmChunk; ++j) {
-      const int k = k0 + kTmChunk + j;
-      const bool in = k < nz;
-      nr[j] = in ? ld_hint(rt + k * kTile, stream) : 0.0;
-      nq[j] = (FUSED && in) ? (COHERENT ? __ldcg(qt + k * kTile) : ld_hint(qt + k * kTile, stream))
-                            : 0.0;
-      ni[j] = in ? (VARY ? ld_hint(fi + k * fs, stream) : __ldg(fi + k)) : 0.0;
-      nn[j] = in ? (VARY ? ld_hint(fn + k * fs, keep) : __ldg(fn + k)) : 0.0;
-    }
-#pragma unroll
-    for (int j = 0; j < kTmChunk; ++j) {
-      const int k = k0 + j;
-      if (k < nz) {
-        double rk = cr[j];
-        if (FUSED) {
-          rk = fma(nalpha, cq[j], rk);
-          accR = fma(rk, rk, accR);
-          st_hint(rt + k * kTile, rk, stream);
-        }
-        y = fma(nprev, y, rk);
-        w = y * ci[j];
-        if (FUSED) accK = fma(y, w, accK);
-        st_hint(zt + k * kTile, w, keep);
-        nprev = cn[j];
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kTmChunk; ++j) {
-      cr[j] = nr[j];
-      cq[j] = nq[j];
-      ci[j] = ni[j];
-      cn[j] = nn[j];
-    }
-  }
-  // ---- backward: z_{nz-1} = w_{nz-1} (in place); level k uses nphi_k.
-  // Chunk b holds levels kb, kb-1, ..., kb-kTmChunk+1 with kb = nz-2-b*kTmChunk.
-  double zz = w;
-  double bw[kTmChunk], bn[kTmChunk];
-#pragma unroll
-  for (int j = 0; j < kTmChunk; ++j) {
-    const int k = nz - 2 - j;
-    bw[j] = (k >= 0) ? ld_hint(zt + k * kTile, stream) : 0.0;
-    bn[j] = (k >= 0) ? (VARY ? ld_hint(fn + k * fs, stream) : __ldg(fn + k)) : 0.0;
-  }
-#pragma unroll 1
-  for (int kb = nz - 2; kb >= 0; kb -= kTmChunk) {
-    double nw[kTmChunk], nb[kTmChunk];
-#pragma unroll
-    for (int j = 0; j < kTmChunk; ++j) {
-      const int k = kb - kTmChunk - j;
-      nw[j] = (k >= 0) ? ld_hint(zt + k * kTile, stream) : 0.0;
-      nb[j] = (k >= 0) ? (VARY ? ld_hint(fn + k * fs, stream) : __ldg(fn + k)) : 0.0;
-    }
-#pragma unroll
-    for (int j = 0; j < kTmChunk; ++j) {
-      const int k = kb - j;
-      if (k >= 0) {
-        zz = fma(bn[j], zz, bw[j]);
-        st_hint(zt + k * kTile, zz, stream);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kTmChunk; ++j) {
-      bw[j] = nw[j];
-      bn[j] = nb[j];
-    }
   }
 }
 
@@ -339,92 +229,6 @@ __global__ void __launch_bounds__(kTmThreads) k_precond_tiled_rc(Op op, DevState
   }
 }
 
-// One unit (a segment of seglen levels of one tile) of the stencil sweep (see
-// k_spmv_tiled) for the lane's column; accumulates <p, q> into sig.
-// COHERENT: z was written by other blocks of the same launch (the persistent
-// loop), so it is read from L2, past the SM's non-coherent L1.
-template <bool VARY, bool RECOMP, bool COHERENT = false>
-__device__ __forceinline__ void spmv_unit(const Op& op, long long unit, int lane,
-                                          const double* __restrict__ z, double* __restrict__ u,
-                                          double* __restrict__ p, double* __restrict__ q,
-                                          double alpha, double beta, int seglen, double& sig) {
-  const int nz = op.nz;
-  const double* __restrict__ lev = op.lev;
-  const long long t = unit % op.ntiles;
-  const int k0 = (int)(unit / op.ntiles) * seglen;
-  const int k1 = min(nz, k0 + seglen);
-  const long long col = t * kTile + lane;
-  if (col >= op.ncols) return;
-  const long long base = t * nz * kTile + lane;
-  const Nbr nb = neighbours(op, col);
-  const long long bE = tiled_base(nb.e, nz), bW = tiled_base(nb.w, nz);
-  const long long bN = tiled_base(nb.n, nz), bS = tiled_base(nb.s, nz);
-  double aE = 0.0, aW = 0.0, aN = 0.0, aS = 0.0;
-  if (RECOMP) {
-    aE = __ldg(op.faceE + col);
-    aW = __ldg(op.faceE + nb.w);
-    aN = __ldg(op.faceN + col);
-    aS = __ldg(op.faceN + nb.s);
-  }
-  // RECOMP: the diagonal rebuilt as the set-up kernel rounds it
-  const double sf = RECOMP ? aE + aW + aN + aS : 0.0;
-  auto ldz = [&](long long o) { return COHERENT ? __ldcg(z + o) : z[o]; };
-  double zd = (k0 > 0) ? ldz(base + (long long)(k0 - 1) * kTile) : 0.0;
-  double zc = ldz(base + (long long)k0 * kTile);
-#pragma unroll 4
-  for (int k = k0; k < k1; ++k) {
-    const long long o = base + (long long)k * kTile;
-    const long long ko = (long long)k * kTile;
-    const double zu = (k + 1 < nz) ? ldz(o + kTile) : 0.0;
-    const double zE = ldz(bE + ko), zW = ldz(bW + ko), zN = ldz(bN + ko), zS = ldz(bS + ko);
-    double uc = __ldcs(u + o);
-    double pc = __ldcs(p + o);
-    const double qc = __ldcs(q + o);
-    uc = fma(alpha, pc, uc);
-    pc = fma(beta, pc, zc);
-    double a;
-    if (VARY) {
-      // per-cell horizontal weights -h_k a_f (west and south: the
-      // neighbours' east and north weights), rebuilt with the set-up's
-      // rounding under RECOMP
-      double d, cE, cW, cN, cS;
-      if (RECOMP) {
-        const double hw = __ldg(lev + LV_HW * nz + k);
-        d = __dadd_rn(__ldg(lev + LV_DIAG * nz + k), __dmul_rn(__ldg(lev + LV_H * nz + k), sf));
-        cE = __dmul_rn(hw, aE);
-        cW = __dmul_rn(hw, aW);
-        cN = __dmul_rn(hw, aN);
-        cS = __dmul_rn(hw, aS);
-      } else {
-        d = __ldcs(op.cdiag_t + o);
-        cE = __ldg(op.cwE_t + o);
-        cW = __ldg(op.cwE_t + bW + ko);
-        cN = __ldg(op.cwN_t + o);
-        cS = __ldg(op.cwN_t + bS + ko);
-      }
-      a = fma(d, zc, beta * qc);
-      a = fma(__ldg(lev + LV_UP * nz + k), zu, a);
-      a = fma(__ldg(lev + LV_DN * nz + k), zd, a);
-      a = fma(cE, zE, a);
-      a = fma(cW, zW, a);
-      a = fma(cN, zN, a);
-      a = fma(cS, zS, a);
-    } else {
-      const double hs = (zE + zW) + (zN + zS);
-      a = fma(__ldg(lev + LV_DIAG * nz + k), zc, beta * qc);
-      a = fma(__ldg(lev + LV_UP * nz + k), zu, a);
-      a = fma(__ldg(lev + LV_DN * nz + k), zd, a);
-      a = fma(__ldg(lev + LV_HW * nz + k), hs, a);
-    }
-    sig = fma(pc, a, sig);
-    __stcs(u + o, uc);
-    __stcs(p + o, pc);
-    __stcs(q + o, a);
-    zd = zc;
-    zc = zu;
-  }
-}
-
 // Algorithm 2 sweep on row-tiled vectors: u += alpha p; p = z + beta p;
 // q = A z + beta q; <p,q>.  One thread per column walking up the levels
 // with z_{k-1}, z_k, z_{k+1} in registers; the horizontal neighbours are
@@ -463,178 +267,6 @@ __global__ void __launch_bounds__(256) k_spmv_tiled(Op op, DevState* st,
       st->alpha = st->kappa_old / S;
     }
   }
-}
-
-// ------------------------------------------------ persistent solve loop
-//
-// For grids too small to fill the GPU, the per-launch latency of the two
-// sweeps (launch, the first loads of the device scalars, the last-block
-// reduction) is most of an iteration.  This kernel runs the whole loop of
-// Algorithm 1 in one cooperative launch: the preconditioner sweep and the
-// stencil sweep of each iteration are the same tile and unit bodies as the
-// two kernels above, separated by grid barriers.  After each barrier every
-// block sums the per-block partials in the same fixed order, so every block
-// takes the same scalar decisions (stopping test, beta, alpha) from the same
-// numbers; block 0 writes the history and, at the end, the device state that
-// the host and the final update read.
-
-constexpr int kPsThreads = 256;
-// Polls of a barrier wait before the loop gives up with PCG_ETIMEOUT (with a
-// 64 ns sleep per poll: about a second).  `absent` (0 in normal use) adds
-// arrivals that never come, so that a test can make the wait run out.
-constexpr long long kBarrierPolls = 1LL << 24;
-
-// Per-block sums of two values (fixed order) into out[0], out[1].
-__device__ __forceinline__ void block_partial2(double v0, double v1, double* out) {
-  __shared__ double s0[kPsThreads / 32], s1[kPsThreads / 32];
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  v0 = warp_sum(v0);
-  v1 = warp_sum(v1);
-  if (lane == 0) {
-    s0[w] = v0;
-    s1[w] = v1;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double a = 0.0, b = 0.0;
-    for (int i = 0; i < kPsThreads / 32; ++i) {
-      a += s0[i];
-      b += s1[i];
-    }
-    out[0] = a;
-    out[1] = b;
-  }
-}
-
-// Sum of part[2*i + off], i < nparts, in one fixed order, in every thread.
-__device__ __forceinline__ double grid_total(const double* part, int nparts, int off) {
-  __shared__ double sh[kPsThreads / 32];
-  __shared__ double tot;
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  double a = 0.0;
-  for (int i = threadIdx.x; i < nparts; i += kPsThreads) a += __ldcg(part + 2 * i + off);
-  a = warp_sum(a);
-  if (lane == 0) sh[w] = a;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double b = 0.0;
-    for (int i = 0; i < kPsThreads / 32; ++i) b += sh[i];
-    tot = b;
-  }
-  __syncthreads();
-  return tot;
-}
-
-template <bool VARY>
-__global__ void __launch_bounds__(kPsThreads) k_pcg_persistent(Op op, DevState* st,
-                                                               double* __restrict__ r,
-                                                               double* __restrict__ q,
-                                                               double* __restrict__ z,
-                                                               double* __restrict__ u,
-                                                               double* __restrict__ p,
-                                                               double* __restrict__ partials,
-                                                               double* __restrict__ hist,
-                                                               int seglen,
-                                                               unsigned int absent) {
-  const int lane = threadIdx.x & 31;
-  // warps numbered across the blocks first, so that few tiles still spread
-  // over every SM of the grid (one block per SM)
-  const long long warp0 = (long long)(threadIdx.x >> 5) * gridDim.x + blockIdx.x;
-  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
-  const unsigned int G = gridDim.x;
-  double* partM = partials;          // 2 per block: r*.r*, <r*, z>
-  double* partA = partials + 2 * G;  // 2 per block: <p, q>, unused
-  const uint64_t keep = l2_keep(), stream = l2_stream();
-  const double rtol = st->rtol;
-  const int maxit = st->maxit;
-  const long long nunits = op.ntiles * ((op.nz + seglen - 1) / seglen);
-  double alpha = 0.0, beta = 0.0, kappa_old = 1.0, R0 = 0.0, R = 0.0, K = 0.0, S = 0.0;
-  int it = 0, iters = 0, status = kStOK;
-  bool timeout = false;
-  for (;;) {
-    // ---- Algorithm 3 sweep
-    double accR = 0.0, accK = 0.0;
-    for (long long t = warp0; t < op.ntiles; t += nwarps)
-      precond_tile<VARY, true, true>(op, t, lane, r, q, z, -alpha, keep, stream, accR, accK);
-    block_partial2(accR, accK, partM + 2 * blockIdx.x);
-    if (!grid_barrier(&st->bar_count, &st->bar_gen, G + absent, &st->dev_error, kBarrierPolls)) {
-      timeout = true;
-      break;
-    }
-    R = grid_total(partM, G, 0);
-    K = grid_total(partM, G, 1);
-    // ---- the scalar step of Algorithm 1 (as finish_precond_sweep)
-    if (it == 0) R0 = R;
-    const double ratio = (R0 > 0.0) ? sqrt(R / R0) : 0.0;
-    if (blockIdx.x == 0 && threadIdx.x == 0) hist[it] = ratio;
-    bool done = true;
-    if (R0 == 0.0) {
-      // r_0 = 0: the initial guess solves the system
-    } else if (!(R < INFINITY) || !(R0 < INFINITY)) {
-      status = kStBreakdown;  // NaN or Inf in the residual
-    } else if (ratio < rtol || R == 0.0) {
-    } else if (it >= maxit) {
-      status = (rtol > 0.0) ? kStNotConv : kStOK;
-    } else if (!(K > 0.0)) {
-      status = kStBreakdown;
-    } else {
-      done = false;
-    }
-    if (done) {
-      iters = it++;
-      break;
-    }
-    beta = K / kappa_old;
-    kappa_old = K;
-    ++it;
-    // ---- Algorithm 2 sweep
-    double sig = 0.0;
-    for (long long unit = warp0; unit < nunits; unit += nwarps)
-      spmv_unit<VARY, false, true>(op, unit, lane, z, u, p, q, alpha, beta, seglen, sig);
-    block_partial2(sig, 0.0, partA + 2 * blockIdx.x);
-    if (!grid_barrier(&st->bar_count, &st->bar_gen, G + absent, &st->dev_error, kBarrierPolls)) {
-      timeout = true;
-      break;
-    }
-    S = grid_total(partA, G, 0);
-    if (!(S > 0.0) || !(S < INFINITY)) {
-      alpha = 0.0;
-      iters = it - 1;
-      status = kStBreakdown;
-      break;
-    }
-    alpha = kappa_old / S;
-  }
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    st->alpha = alpha;
-    st->beta = beta;
-    st->kappa_old = kappa_old;
-    st->R0 = R0;
-    st->last_R = R;
-    st->last_kappa = K;
-    st->last_sigma = S;
-    st->it = it;
-    if (timeout) {
-      iters = it;
-      status = kStTimeout;
-    }
-    st->iters = iters;
-    st->status = status;
-    __threadfence();
-    st->done = 1;
-  }
-}
-
-// Levels per work unit of the tiled stencil sweep: whole columns when there
-// are at least 8 tiles per resident warp, else segments short enough to give
-// every warp about 8 units (at least 4 levels each).
-int tiled_spmv_seglen(const Op& op, int grid) {
-  const long long warps = (long long)grid * 8;
-  const long long want = 8 * warps;
-  if (op.ntiles >= want || op.nz <= 4) return op.nz;
-  long long nseg = (want + op.ntiles - 1) / op.ntiles;
-  nseg = std::min<long long>(nseg, op.nz / 4);
-  return (int)((op.nz + nseg - 1) / nseg);
 }
 
 }  // namespace
@@ -705,37 +337,6 @@ int grid_tiled_spmv(const Op& op, int num_sms) {
   const long long work = (units + 7) / 8;  // 8 warps per block
   if (g > work) g = work;
   return (int)(g < 1 ? 1 : g);
-}
-
-int grid_persistent(const Op& op, int num_sms) {
-  int dev = 0, coop = 0, a = 0, b = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, k_pcg_persistent<true>, kPsThreads, 0) !=
-          cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_pcg_persistent<false>, kPsThreads, 0) !=
-          cudaSuccess) {
-    (void)cudaGetLastError();
-    return 0;
-  }
-  const int per_sm = std::min(a, b);
-  if (!coop || per_sm < 1) return 0;
-  long long g = (long long)per_sm * num_sms;  // every block must be resident
-  // one block per tile at most: the preconditioner sweep has one tile per warp
-  // and the warps are spread over the blocks first
-  g = std::min(g, op.ntiles);
-  return (int)std::max<long long>(g, 1);
-}
-
-cudaError_t launch_persistent(const Op& op, DevState* st, double* r, double* q, double* z,
-                              double* u, double* p, double* partials, double* hist, int grid,
-                              unsigned int absent, cudaStream_t s) {
-  Op o = op;
-  int seglen = tiled_spmv_seglen(op, grid);
-  void* args[] = {&o, &st, &r, &q, &z, &u, &p, &partials, &hist, &seglen, &absent};
-  const void* fn = op.varying ? reinterpret_cast<const void*>(k_pcg_persistent<true>)
-                              : reinterpret_cast<const void*>(k_pcg_persistent<false>);
-  return cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kPsThreads), args, 0, s);
 }
 
 }  // namespace pcg
