@@ -107,6 +107,7 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self._summary = None
 
     def __enter__(self):
         try:
@@ -131,6 +132,10 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        """Median SM clock, maximum and active throttle reasons; read once
+        from the sample file, then cached."""
+        if self._summary is not None:
+            return self._summary
         if self.proc is None or not self.path or not os.path.exists(self.path):
             return None
         sm, smax, reasons = [], [], set()
@@ -151,8 +156,9 @@ class ClockSampler:
         os.unlink(self.path)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        self._summary = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                         "reasons": sorted(reasons), "samples": len(sm)}
+        return self._summary
 
 
 def reduce_over_ranks(ms, iters, device):
