@@ -38,21 +38,31 @@ METRIC = "PCG iters/s & achieved HBM GB/s (fp64, 1024x1024x128 grid) vs HBM roof
 UNIT = "iters/s"
 # fp64 pipe operations per cell (FMA, MUL and ADD each count one) of the two
 # sweeps in this implementation; see the kernel sources.
-# keyed by (layout, "a_h varies per column"); the row-tiled stencil sweep of an
-# a_h field reads per-cell horizontal weights (4 FMAs instead of 5 operations)
-OPS_SPMV = {("tiled", True): 11, ("tiled", False): 11, ("column", True): 12, ("column", False): 11}
+# The stencil sweep's entries are keyed by (layout, "a_h varies per column",
+# form of A z).  "stencil": the full 7-point stencil (the row-tiled sweep of an
+# a_h field reads per-cell horizontal weights: 4 FMAs instead of 5
+# operations).  "residual": A z = r + (A - M) z, the four horizontal terms
+# alone (row-tiled layout).
+OPS_SPMV = {("tiled", True, "stencil"): 11, ("tiled", False, "stencil"): 11,
+            ("column", True, "stencil"): 12, ("column", False, "stencil"): 11,
+            ("tiled", True, "residual"): 8, ("tiled", False, "residual"): 8}
 OPS_PRECOND = 6
 # Algorithmic bytes per cell: vectors read/written once per sweep.
-# u,p,z,q (+ per-cell diagonal, + 2 per-cell weights in the row-tiled layout) read; u,p,q written
-BYTES_SPMV = {("tiled", True): 80, ("tiled", False): 56, ("column", True): 64, ("column", False): 56}
+# u,p,z,q (+ per-cell diagonal, + 2 per-cell weights in the row-tiled layout)
+# read, or u,p,z,q,r (+ 2 weights) for the residual form; u,p,q written
+BYTES_SPMV = {("tiled", True, "stencil"): 80, ("tiled", False, "stencil"): 56,
+              ("column", True, "stencil"): 64, ("column", False, "stencil"): 56,
+              ("tiled", True, "residual"): 80, ("tiled", False, "residual"): 64}
 BYTES_PRECOND = {True: 48, False: 32}  # r,q (+ 2 per-cell Thomas factors) read; r,z written
 # With the factors of an a_h field rebuilt in every sweep (--factors recompute):
-# the stencil sweep forms the diagonal (a product and a sum) and the four
-# horizontal weights, the preconditioner sweep the diagonal, the pivot and the
-# two quotients (the reciprocal and the division counted as one operation
-# each: a lower bound), and neither reads per-cell coefficients.
-OPS_SPMV_RECOMPUTE, BYTES_SPMV_RECOMPUTE = 17, 56
+# the stencil sweep forms the four horizontal weights (and, in the stencil
+# form, the diagonal: a product and a sum), the preconditioner sweep the
+# diagonal, the pivot and the two quotients (the reciprocal and the division
+# counted as one operation each: a lower bound), and neither reads per-cell
+# coefficients.
+OPS_BYTES_SPMV_RECOMPUTE = {"stencil": (17, 56), "residual": (12, 64)}
 OPS_PRECOND_RECOMPUTE, BYTES_PRECOND_RECOMPUTE = 12, 32
+L2_BYTES = 129e6                     # GB300 L2
 FP64_LANES_PER_SM_CLK = 2.0          # GB300 non-tensor fp64 rate: 2 FMA lanes per SM per clock
 
 
@@ -78,6 +88,9 @@ def parse():
     ap.add_argument("--substructuring", type=int, default=0,
                     help="blocks per column of the substructured preconditioner solve "
                          "(0 automatic, 1 off, 2/4/8/16)")
+    ap.add_argument("--az-form", choices=["auto", "stencil", "residual"], default="auto",
+                    help="how the stencil sweep forms A z: the full 7-point stencil, or "
+                         "r + (A - M) z from the preconditioner sweep's M z = r")
     ap.add_argument("--grid", type=int, nargs=3, metavar=("NX", "NY", "NZ"),
                     help="same coefficients on another grid size (profiling captures)")
     return ap.parse_args()
@@ -201,15 +214,17 @@ def sources_sha256(names):
     return hsh.hexdigest()
 
 
-def measured_traffic(kernel, cells, layout, factors):
+def measured_traffic(kernel, cells, layout, factors, az_form):
     """DRAM bytes per launch of `kernel` from the committed ncu summary
     (profiles/traffic.json), or None when no capture matches the layout, the
-    factor mode and the size, or the kernel sources changed since."""
+    factor mode, the form of A z and the size, or the kernel sources changed
+    since."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             t = json.load(f)
         for c in t["captures"]:
-            if (c["layout"], c["factors"], c["full_cells"]) != (layout, factors, cells):
+            if ((c["layout"], c["factors"], c.get("az_form", "stencil"), c["full_cells"])
+                    != (layout, factors, az_form, cells)):
                 continue
             if c["sha256"] != sources_sha256(c["sources"]) or kernel not in c["kernels"]:
                 return None
@@ -302,6 +317,8 @@ def run_ours(args, w):
     solver.set_layout(args.layout)
     solver.set_factors(args.factors)
     solver.set_substructuring(args.substructuring)
+    solver.set_az_form(args.az_form)
+    az_form = solver.az_form
     recompute = args.factors == "recompute" and varying and args.layout == "tiled"
 
     def step():
@@ -379,8 +396,9 @@ def run_ours(args, w):
     peaks, peak_src = measured_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
     clk = clocks.summary()
-    ops_a, bytes_a = ((OPS_SPMV_RECOMPUTE, BYTES_SPMV_RECOMPUTE) if recompute
-                      else (OPS_SPMV[(args.layout, varying)], BYTES_SPMV[(args.layout, varying)]))
+    key = (args.layout, varying, az_form)
+    ops_a, bytes_a = (OPS_BYTES_SPMV_RECOMPUTE[az_form] if recompute
+                      else (OPS_SPMV[key], BYTES_SPMV[key]))
     ops_m, bytes_m = ((OPS_PRECOND_RECOMPUTE, BYTES_PRECOND_RECOMPUTE) if recompute
                       else (OPS_PRECOND, BYTES_PRECOND[varying]))
     bytes_iter = (bytes_a + bytes_m) * n
@@ -402,7 +420,7 @@ def run_ours(args, w):
     alu_peak = FP64_LANES_PER_SM_CLK * nsm * sm_mhz * 1e6 / 1e9  # G fp64 ops / s
     alu_ach = ops_cell * n / avg_s / 1e9
     hbm_ach = bytes_cell * n / avg_s / 1e9
-    traffic = measured_traffic(dom, n, args.layout, args.factors)
+    traffic = measured_traffic(dom, n, args.layout, args.factors, az_form)
     roofline = {
         "bound": "alu", "kernel": dom, "achieved": alu_ach, "peak": alu_peak,
         "unit": "G fp64 ops/s", "frac": alu_ach / alu_peak, "traffic": traffic,
@@ -418,8 +436,8 @@ def run_ours(args, w):
     # against the fused minimum of 88 B/cell (u, p, z, q, r moved once, no
     # per-cell coefficients) and against this build's algorithmic bytes
     dram_iter = None
-    t_m = measured_traffic("precond_fused", n, args.layout, args.factors)
-    t_a = measured_traffic("spmv_fused", n, args.layout, args.factors)
+    t_m = measured_traffic("precond_fused", n, args.layout, args.factors, az_form)
+    t_a = measured_traffic("spmv_fused", n, args.layout, args.factors, az_form)
     if t_m and t_a:
         dram_iter = {"bytes": t_m + t_a, "per_cell": (t_m + t_a) / n,
                      "vs_fused_min_88": (t_m + t_a) / (88.0 * n),
@@ -470,9 +488,12 @@ def run_ours(args, w):
             "config": {"workload": w.name, "grid": [w.nx, w.ny, w.nz], "cells": n,
                        "rtol": w.rtol, "iters_per_step": iters[0], "a_v": w.a_v,
                        "graded": w.graded, "varying_ah": varying,
-                       "l2": "inputs larger than L2 (1.07 GB per vector)",
+                       "l2": ("inputs larger than L2 (%.2f GB per vector)" % (8e-9 * n)
+                              if 8 * n > L2_BYTES else
+                              "working set L2-resident (%.1f MB per vector), no flush"
+                              % (8e-6 * n)),
                        "layout": args.layout, "factors": args.factors,
-                       "substructuring": solver.substructuring,
+                       "substructuring": solver.substructuring, "az_form": az_form,
                        "parallelism": "replicas" if world > 1 else "single"},
             "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / hbm_peak,
             "bytes_per_cell_iter": bytes_iter / n, "fp64_ops_per_cell_iter": ops_iter / n,

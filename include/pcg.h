@@ -180,6 +180,30 @@ int pcg_set_loop(pcg_ctx* ctx, int mode);
  * PCG_LOOP_PERSISTENT.  Errors: PCG_EINVAL (NULL). */
 int pcg_get_loop(const pcg_ctx* ctx, int* mode_out);
 
+/* How the stencil sweep of pcg_solve forms A z (Appendix A, Algorithm 2:
+ * q = A z + beta q), in the row-tiled layout:
+ *   PCG_AZ_STENCIL   the full 7-point stencil of eq. (18), as the paper's
+ *                    sweep computes it: 7 fp64 operations per cell for A z;
+ *   PCG_AZ_RESIDUAL  A z = r + (A - M) z.  The preconditioner sweep of the
+ *                    same iteration has just solved M z = r (eq. (19)), and
+ *                    M holds the whole diagonal of A and its vertical
+ *                    couplings, so A z - r is the sum over the four
+ *                    horizontal neighbours alone: 4 fp64 operations per
+ *                    cell, r read in place of the diagonal.  Equal in exact
+ *                    arithmetic; in floating point q differs by the column
+ *                    solve's backward error, of the same order (eps |A||z|)
+ *                    as the stencil's own rounding;
+ *   PCG_AZ_AUTO      (default) RESIDUAL wherever it applies.
+ * RESIDUAL needs the row-tiled layout and Thomas column solves (no
+ * substructuring); elsewhere the full stencil runs.  pcg_apply_A always
+ * evaluates the full stencil.  Errors: PCG_EINVAL (unknown form). */
+enum { PCG_AZ_AUTO = 0, PCG_AZ_STENCIL = 1, PCG_AZ_RESIDUAL = 2 };
+int pcg_set_az_form(pcg_ctx* ctx, int form);
+
+/* The form of A z the next pcg_solve will use: PCG_AZ_STENCIL or
+ * PCG_AZ_RESIDUAL.  Errors: PCG_EINVAL (NULL). */
+int pcg_get_az_form(const pcg_ctx* ctx, int* form_out);
+
 /* Test hook for the persistent loop's bounded waits: with absent > 0, its
  * grid barriers count `absent` arrivals that never come, so the first
  * barrier wait of the next persistent solve runs out (about a second) and the

@@ -33,10 +33,12 @@ EXPORTED = ["pcg_create", "pcg_destroy", "pcg_update_coeffs", "pcg_set_stream", 
             "pcg_enable_timing", "pcg_kernel_times", "pcg_launch_info",
             "pcg_precond_dot_noalloc", "pcg_set_layout", "pcg_set_factors",
             "pcg_set_substructuring", "pcg_get_substructuring", "pcg_solve_host_x0",
-            "pcg_set_loop", "pcg_get_loop", "pcg_test_barrier_absent"]
+            "pcg_set_loop", "pcg_get_loop", "pcg_test_barrier_absent", "pcg_set_az_form",
+            "pcg_get_az_form"]
 PCG_LAYOUT_COLUMN, PCG_LAYOUT_TILED = 0, 1
 PCG_FACTORS_STORED, PCG_FACTORS_RECOMPUTE = 0, 1
 PCG_LOOP_AUTO, PCG_LOOP_BATCHED, PCG_LOOP_PERSISTENT = 0, 1, 2
+PCG_AZ_AUTO, PCG_AZ_STENCIL, PCG_AZ_RESIDUAL = 0, 1, 2
 
 
 class pcg_coeffs(ctypes.Structure):
@@ -80,6 +82,8 @@ def _load(path=LIB_PATH):
         "pcg_get_substructuring": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int)]),
         "pcg_set_loop": (ctypes.c_int, [_vp, ctypes.c_int]),
         "pcg_get_loop": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int)]),
+        "pcg_set_az_form": (ctypes.c_int, [_vp, ctypes.c_int]),
+        "pcg_get_az_form": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int)]),
         "pcg_test_barrier_absent": (ctypes.c_int, [_vp, ctypes.c_int]),
     }
     for name, (res, args) in sig.items():
@@ -218,6 +222,18 @@ def pcg_get_loop(ctx):
     """The loop the next solve runs: PCG_LOOP_BATCHED or PCG_LOOP_PERSISTENT."""
     v = ctypes.c_int(0)
     _check(_lib.pcg_get_loop(ctx, ctypes.byref(v)), ctx)
+    return v.value
+
+
+def pcg_set_az_form(ctx, form):
+    """PCG_AZ_AUTO (default), PCG_AZ_STENCIL or PCG_AZ_RESIDUAL."""
+    return _check(_lib.pcg_set_az_form(ctx, int(form)), ctx)
+
+
+def pcg_get_az_form(ctx):
+    """The form of A z the next solve uses: PCG_AZ_STENCIL or PCG_AZ_RESIDUAL."""
+    v = ctypes.c_int(0)
+    _check(_lib.pcg_get_az_form(ctx, ctypes.byref(v)), ctx)
     return v.value
 
 
@@ -360,6 +376,19 @@ class Solver:
             mode = {"auto": PCG_LOOP_AUTO, "batched": PCG_LOOP_BATCHED,
                     "persistent": PCG_LOOP_PERSISTENT}[mode]
         pcg_set_loop(self.ctx, mode)
+
+    def set_az_form(self, form):
+        """"auto", "stencil" or "residual" (or the PCG_AZ_* values)."""
+        if isinstance(form, str):
+            form = {"auto": PCG_AZ_AUTO, "stencil": PCG_AZ_STENCIL,
+                    "residual": PCG_AZ_RESIDUAL}[form]
+        pcg_set_az_form(self.ctx, form)
+
+    @property
+    def az_form(self):
+        """"stencil" or "residual": how the next solve's stencil sweeps form A z."""
+        return {PCG_AZ_STENCIL: "stencil", PCG_AZ_RESIDUAL: "residual"}[
+            pcg_get_az_form(self.ctx)]
 
     @property
     def loop(self):

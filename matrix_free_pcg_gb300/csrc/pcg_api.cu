@@ -64,6 +64,7 @@ struct pcg_ctx {
   // substructured column solve: requested blocks (0 automatic), blocks in use, grid
   int split_req = 0, split_p = 1, grid_sp = 0;
   int loop_req = PCG_LOOP_AUTO;      // requested solve loop
+  int az_req = PCG_AZ_AUTO;          // requested form of A z in the stencil sweep
   int grid_ps = 0;                   // blocks of the persistent loop (0: not available)
   unsigned int test_absent = 0;      // test hook: arrivals the persistent barriers miss
   size_t partials_cap = 0;           // doubles in `partials`
@@ -363,6 +364,14 @@ int resolved_loop(const pcg_ctx* ctx) {
   return persistent_grid(ctx) ? PCG_LOOP_PERSISTENT : PCG_LOOP_BATCHED;
 }
 
+// The form of A z that the next solve's stencil sweeps use (PCG_AZ_STENCIL
+// or PCG_AZ_RESIDUAL): the residual form needs the row-tiled layout and the
+// Thomas column solve, whose z the sweep pairs with r.
+int resolved_az(const pcg_ctx* ctx) {
+  const bool eligible = ctx->layout == PCG_LAYOUT_TILED && ctx->split_p == 1;
+  return (eligible && ctx->az_req != PCG_AZ_STENCIL) ? PCG_AZ_RESIDUAL : PCG_AZ_STENCIL;
+}
+
 // The two sweeps of one iteration of the row-tiled loop, enqueued on `s`;
 // with `ev`, boundary events before the first and between the two.
 cudaError_t launch_tiled_iteration(pcg_ctx* ctx, const Op& op, bool split, int grid_pm,
@@ -376,7 +385,7 @@ cudaError_t launch_tiled_iteration(pcg_ctx* ctx, const Op& op, bool split, int g
                                           ctx->hist, grid_pm, s);
   if (e == cudaSuccess && ev) e = cudaEventRecordWithFlags(ev[1], s, cudaEventRecordExternal);
   if (e == cudaSuccess)
-    e = pcg::launch_spmv_tiled(op, ctx->state, ctx->z, ctx->u_t, ctx->p, ctx->q,
+    e = pcg::launch_spmv_tiled(op, ctx->state, ctx->z, ctx->r, ctx->u_t, ctx->p, ctx->q,
                                ctx->partials + 2 * grid_pm, ctx->grid_ta, s);
   return e;
 }
@@ -447,6 +456,7 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
   ctx->pool_used = 0;
   const bool tiled = ctx->layout == PCG_LAYOUT_TILED;
   op.recompute = (tiled && op.varying && ctx->factors == PCG_FACTORS_RECOMPUTE) ? 1 : 0;
+  op.az_resid = resolved_az(ctx) == PCG_AZ_RESIDUAL ? 1 : 0;
   const bool split = tiled && ctx->split_p > 1;
   const int grid_pm = split ? ctx->grid_sp : ctx->grid_tm;  // preconditioner sweep blocks
   op.nscratch = ctx->nscratch;
@@ -537,7 +547,8 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
       if (e != cudaSuccess) return cuda_fail(ctx, e, "preconditioner sweep launch");
       if (enq + i < maxit) {
         e = timed(ctx, PCG_K_SPMV_FUSED, [&] {
-          return tiled ? pcg::launch_spmv_tiled(op, ctx->state, ctx->z, ctx->u_t, ctx->p, ctx->q,
+          return tiled ? pcg::launch_spmv_tiled(op, ctx->state, ctx->z, ctx->r, ctx->u_t, ctx->p,
+                                                ctx->q,
                                                 ctx->partials + 2 * grid_pm, ctx->grid_ta, s)
                        : pcg::launch_spmv_fused(op, ctx->state, ctx->z, x, ctx->p, ctx->q,
                                                 ctx->partials + 2 * ctx->grid_m, ctx->grid_a, s);
@@ -852,6 +863,21 @@ int pcg_set_loop(pcg_ctx* ctx, int mode) {
   if (mode != PCG_LOOP_AUTO && mode != PCG_LOOP_BATCHED && mode != PCG_LOOP_PERSISTENT)
     return fail(ctx, PCG_EINVAL, "unknown loop mode %d", mode);
   ctx->loop_req = mode;
+  return PCG_OK;
+}
+
+int pcg_set_az_form(pcg_ctx* ctx, int form) {
+  if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
+  if (form != PCG_AZ_AUTO && form != PCG_AZ_STENCIL && form != PCG_AZ_RESIDUAL)
+    return fail(ctx, PCG_EINVAL, "unknown form of A z %d", form);
+  if (form != ctx->az_req) ctx->config_gen++;  // the captured sweeps change
+  ctx->az_req = form;
+  return PCG_OK;
+}
+
+int pcg_get_az_form(const pcg_ctx* ctx, int* form_out) {
+  if (!ctx || !form_out) return fail(nullptr, PCG_EINVAL, "NULL argument");
+  *form_out = resolved_az(ctx);
   return PCG_OK;
 }
 

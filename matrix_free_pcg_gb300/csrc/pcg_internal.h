@@ -46,6 +46,8 @@ struct Op {
                        // factors in every sweep instead of reading them per cell
   double* nscratch;    // recompute: T_{k+1/2}/D_k of the tiles in flight, 32*nz doubles
                        // per warp of the preconditioner grid
+  int az_resid;        // row-tiled stencil sweep: A z = r + (A - M) z (M z = r from the
+                       // preconditioner sweep) instead of the full 7-point stencil
   // substructured column solve (pcg_split.cu), row-tiled tables
   double* sp_nphi;     // per cell: T_{k+1/2}/D_k of the block's own LDL^T (0 at its top)
   double* sp_invd;     // per cell: 1/D_k of the block's LDL^T
@@ -138,8 +140,11 @@ cudaError_t launch_from_tiled(const Op& op, const DevState* st, const double* sr
 cudaError_t launch_precond_tiled(const Op& op, DevState* st, double* r, const double* q,
                                  double* z, double* partials, double* hist, int grid,
                                  cudaStream_t s);
-cudaError_t launch_spmv_tiled(const Op& op, DevState* st, const double* z, double* u, double* p,
-                              double* q, double* partials, int grid, cudaStream_t s);
+// With op.az_resid the stencil sweep reads r (the residual that the
+// preconditioner sweep's z solves M z = r for) instead of the diagonal.
+cudaError_t launch_spmv_tiled(const Op& op, DevState* st, const double* z, const double* r,
+                              double* u, double* p, double* q, double* partials, int grid,
+                              cudaStream_t s);
 // Warps per block of the row-tiled preconditioner sweep, and its resident
 // warps per SM (each warp keeps the w of its tile and the factors the
 // backward pass reads again live in L2; 12 per SM keep this within L2 at

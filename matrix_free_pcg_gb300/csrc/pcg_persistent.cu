@@ -75,7 +75,7 @@ __device__ __forceinline__ double grid_total(const double* part, int nparts, int
   return tot;
 }
 
-template <bool VARY>
+template <bool VARY, bool RESID>
 __global__ void __launch_bounds__(kPsThreads) k_pcg_persistent(Op op, DevState* st,
                                                                double* __restrict__ r,
                                                                double* __restrict__ q,
@@ -140,7 +140,8 @@ __global__ void __launch_bounds__(kPsThreads) k_pcg_persistent(Op op, DevState* 
     // ---- Algorithm 2 sweep
     double sig = 0.0;
     for (long long unit = warp0; unit < nunits; unit += nwarps)
-      spmv_unit<VARY, false, true>(op, unit, lane, z, u, p, q, alpha, beta, seglen, sig);
+      spmv_unit<VARY, false, RESID, true>(op, unit, lane, z, r, u, p, q, alpha, beta, seglen,
+                                          sig);
     block_partial2(sig, 0.0, partA + 2 * blockIdx.x);
     if (!grid_barrier(&st->bar_count, &st->bar_gen, G + absent, &st->dev_error, kBarrierPolls)) {
       timeout = true;
@@ -178,17 +179,23 @@ __global__ void __launch_bounds__(kPsThreads) k_pcg_persistent(Op op, DevState* 
 }  // namespace
 
 int grid_persistent(const Op& op, int num_sms) {
-  int dev = 0, coop = 0, a = 0, b = 0;
+  int dev = 0, coop = 0;
+  int occ[4] = {0, 0, 0, 0};
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, k_pcg_persistent<true>, kPsThreads, 0) !=
-          cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_pcg_persistent<false>, kPsThreads, 0) !=
-          cudaSuccess) {
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[0], k_pcg_persistent<true, false>,
+                                                    kPsThreads, 0) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[1], k_pcg_persistent<false, false>,
+                                                    kPsThreads, 0) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[2], k_pcg_persistent<true, true>,
+                                                    kPsThreads, 0) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ[3], k_pcg_persistent<false, true>,
+                                                    kPsThreads, 0) != cudaSuccess) {
     (void)cudaGetLastError();
     return 0;
   }
-  const int per_sm = std::min(a, b);
+  // the smallest over the variants: any of them may run with this grid
+  const int per_sm = std::min(std::min(occ[0], occ[1]), std::min(occ[2], occ[3]));
   if (!coop || per_sm < 1) return 0;
   long long g = (long long)per_sm * num_sms;  // every block must be resident
   // one block per tile at most: the preconditioner sweep has one tile per warp
@@ -203,8 +210,13 @@ cudaError_t launch_persistent(const Op& op, DevState* st, double* r, double* q, 
   Op o = op;
   int seglen = tiled_spmv_seglen(op, grid);
   void* args[] = {&o, &st, &r, &q, &z, &u, &p, &partials, &hist, &seglen, &absent};
-  const void* fn = op.varying ? reinterpret_cast<const void*>(k_pcg_persistent<true>)
-                              : reinterpret_cast<const void*>(k_pcg_persistent<false>);
+  const void* fn;
+  if (op.varying)
+    fn = op.az_resid ? reinterpret_cast<const void*>(k_pcg_persistent<true, true>)
+                     : reinterpret_cast<const void*>(k_pcg_persistent<true, false>);
+  else
+    fn = op.az_resid ? reinterpret_cast<const void*>(k_pcg_persistent<false, true>)
+                     : reinterpret_cast<const void*>(k_pcg_persistent<false, false>);
   return cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kPsThreads), args, 0, s);
 }
 

@@ -130,11 +130,21 @@ __device__ __forceinline__ void precond_tile(const Op& op, long long t, int lane
 
 // One unit (a segment of seglen levels of one tile) of the stencil sweep (see
 // k_spmv_tiled) for the lane's column; accumulates <p, q> into sig.
-// COHERENT: z was written by other blocks of the same launch (the persistent
-// loop), so it is read from L2, past the SM's non-coherent L1.
-template <bool VARY, bool RECOMP, bool COHERENT = false>
+//
+// RESID: A z is formed as r + (A - M) z.  The preconditioner sweep has just
+// solved M z = r, and M (eq. (19)) holds the whole diagonal of A and its
+// vertical couplings, so A z - r is the horizontal neighbour sum alone:
+// 4 fp64 operations per cell instead of 7, with r read in place of the
+// diagonal.  Exact in real arithmetic; in floating point q differs from the
+// explicit stencil by the column solve's backward error, of the same order
+// (eps |A| |z|) as the stencil's own rounding.
+//
+// COHERENT: z and r were written by other blocks of the same launch (the
+// persistent loop), so they are read from L2, past the SM's non-coherent L1.
+template <bool VARY, bool RECOMP, bool RESID, bool COHERENT = false>
 __device__ __forceinline__ void spmv_unit(const Op& op, long long unit, int lane,
-                                          const double* __restrict__ z, double* __restrict__ u,
+                                          const double* __restrict__ z,
+                                          const double* __restrict__ r, double* __restrict__ u,
                                           double* __restrict__ p, double* __restrict__ q,
                                           double alpha, double beta, int seglen, double& sig) {
   const int nz = op.nz;
@@ -156,15 +166,17 @@ __device__ __forceinline__ void spmv_unit(const Op& op, long long unit, int lane
     aS = __ldg(op.faceN + nb.s);
   }
   // RECOMP: the diagonal rebuilt as the set-up kernel rounds it
-  const double sf = RECOMP ? aE + aW + aN + aS : 0.0;
+  const double sf = (RECOMP && !RESID) ? aE + aW + aN + aS : 0.0;
   auto ldz = [&](long long o) { return COHERENT ? __ldcg(z + o) : z[o]; };
-  double zd = (k0 > 0) ? ldz(base + (long long)(k0 - 1) * kTile) : 0.0;
-  double zc = ldz(base + (long long)k0 * kTile);
+  // the column window z_{k-1}, z_k, z_{k+1} (the explicit stencil only)
+  double zd = (!RESID && k0 > 0) ? ldz(base + (long long)(k0 - 1) * kTile) : 0.0;
+  double zc = RESID ? 0.0 : ldz(base + (long long)k0 * kTile);
 #pragma unroll 4
   for (int k = k0; k < k1; ++k) {
     const long long o = base + (long long)k * kTile;
     const long long ko = (long long)k * kTile;
-    const double zu = (k + 1 < nz) ? ldz(o + kTile) : 0.0;
+    const double zu = (!RESID && k + 1 < nz) ? ldz(o + kTile) : 0.0;
+    if (RESID) zc = ldz(o);
     const double zE = ldz(bE + ko), zW = ldz(bW + ko), zN = ldz(bN + ko), zS = ldz(bS + ko);
     double uc = __ldcs(u + o);
     double pc = __ldcs(p + o);
@@ -176,41 +188,52 @@ __device__ __forceinline__ void spmv_unit(const Op& op, long long unit, int lane
       // per-cell horizontal weights -h_k a_f (west and south: the
       // neighbours' east and north weights), rebuilt with the set-up's
       // rounding under RECOMP
-      double d, cE, cW, cN, cS;
+      double d = 0.0, cE, cW, cN, cS;
       if (RECOMP) {
         const double hw = __ldg(lev + LV_HW * nz + k);
-        d = __dadd_rn(__ldg(lev + LV_DIAG * nz + k), __dmul_rn(__ldg(lev + LV_H * nz + k), sf));
+        if (!RESID)
+          d = __dadd_rn(__ldg(lev + LV_DIAG * nz + k), __dmul_rn(__ldg(lev + LV_H * nz + k), sf));
         cE = __dmul_rn(hw, aE);
         cW = __dmul_rn(hw, aW);
         cN = __dmul_rn(hw, aN);
         cS = __dmul_rn(hw, aS);
       } else {
-        d = __ldcs(op.cdiag_t + o);
+        if (!RESID) d = __ldcs(op.cdiag_t + o);
         cE = __ldg(op.cwE_t + o);
         cW = __ldg(op.cwE_t + bW + ko);
         cN = __ldg(op.cwN_t + o);
         cS = __ldg(op.cwN_t + bS + ko);
       }
-      a = fma(d, zc, beta * qc);
-      a = fma(__ldg(lev + LV_UP * nz + k), zu, a);
-      a = fma(__ldg(lev + LV_DN * nz + k), zd, a);
+      if (RESID) {
+        a = fma(beta, qc, COHERENT ? __ldcg(r + o) : __ldcs(r + o));
+      } else {
+        a = fma(d, zc, beta * qc);
+        a = fma(__ldg(lev + LV_UP * nz + k), zu, a);
+        a = fma(__ldg(lev + LV_DN * nz + k), zd, a);
+      }
       a = fma(cE, zE, a);
       a = fma(cW, zW, a);
       a = fma(cN, zN, a);
       a = fma(cS, zS, a);
     } else {
       const double hs = (zE + zW) + (zN + zS);
-      a = fma(__ldg(lev + LV_DIAG * nz + k), zc, beta * qc);
-      a = fma(__ldg(lev + LV_UP * nz + k), zu, a);
-      a = fma(__ldg(lev + LV_DN * nz + k), zd, a);
+      if (RESID) {
+        a = fma(beta, qc, COHERENT ? __ldcg(r + o) : __ldcs(r + o));
+      } else {
+        a = fma(__ldg(lev + LV_DIAG * nz + k), zc, beta * qc);
+        a = fma(__ldg(lev + LV_UP * nz + k), zu, a);
+        a = fma(__ldg(lev + LV_DN * nz + k), zd, a);
+      }
       a = fma(__ldg(lev + LV_HW * nz + k), hs, a);
     }
     sig = fma(pc, a, sig);
     __stcs(u + o, uc);
     __stcs(p + o, pc);
     __stcs(q + o, a);
-    zd = zc;
-    zc = zu;
+    if (!RESID) {
+      zd = zc;
+      zc = zu;
+    }
   }
 }
 

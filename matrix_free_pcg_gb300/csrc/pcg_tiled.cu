@@ -231,15 +231,17 @@ __global__ void __launch_bounds__(kTmThreads) k_precond_tiled_rc(Op op, DevState
 
 // Algorithm 2 sweep on row-tiled vectors: u += alpha p; p = z + beta p;
 // q = A z + beta q; <p,q>.  One thread per column walking up the levels
-// with z_{k-1}, z_k, z_{k+1} in registers; the horizontal neighbours are
-// fixed offsets from the column's own.  The unit of work is a segment of
+// with z_{k-1}, z_k, z_{k+1} in registers (RESID: A z = r + (A - M) z, no
+// vertical terms); the horizontal neighbours are fixed offsets from the
+// column's own.  The unit of work is a segment of
 // seglen levels of one tile (the stencil has no recurrence along k), so that
 // grids with few tiles still give every warp several units; units are
 // assigned statically (segment-major), which keeps the sum bitwise
 // repeatable.
-template <bool VARY, bool RECOMP>
+template <bool VARY, bool RECOMP, bool RESID>
 __global__ void __launch_bounds__(256) k_spmv_tiled(Op op, DevState* st,
                                                     const double* __restrict__ z,
+                                                    const double* __restrict__ r,
                                                     double* __restrict__ u,
                                                     double* __restrict__ p,
                                                     double* __restrict__ q,
@@ -253,7 +255,7 @@ __global__ void __launch_bounds__(256) k_spmv_tiled(Op op, DevState* st,
   double sig = 0.0;
   const long long nunits = op.ntiles * ((op.nz + seglen - 1) / seglen);
   for (long long unit = warp0; unit < nunits; unit += nwarps)
-    spmv_unit<VARY, RECOMP>(op, unit, lane, z, u, p, q, alpha, beta, seglen, sig);
+    spmv_unit<VARY, RECOMP, RESID>(op, unit, lane, z, r, u, p, q, alpha, beta, seglen, sig);
   double S, unused;
   if (grid_sum2<256>(sig, 0.0, partials, &st->ticket_a, S, unused)) {
     st->last_sigma = S;
@@ -300,15 +302,30 @@ cudaError_t launch_precond_tiled(const Op& op, DevState* st, double* r, const do
   return cudaGetLastError();
 }
 
-cudaError_t launch_spmv_tiled(const Op& op, DevState* st, const double* z, double* u, double* p,
-                              double* q, double* partials, int grid, cudaStream_t s) {
+cudaError_t launch_spmv_tiled(const Op& op, DevState* st, const double* z, const double* r,
+                              double* u, double* p, double* q, double* partials, int grid,
+                              cudaStream_t s) {
   const int seglen = tiled_spmv_seglen(op, grid);
-  if (op.varying && op.recompute)
-    k_spmv_tiled<true, true><<<grid, 256, 0, s>>>(op, st, z, u, p, q, partials, seglen);
-  else if (op.varying)
-    k_spmv_tiled<true, false><<<grid, 256, 0, s>>>(op, st, z, u, p, q, partials, seglen);
-  else
-    k_spmv_tiled<false, false><<<grid, 256, 0, s>>>(op, st, z, u, p, q, partials, seglen);
+  const bool rs = op.az_resid != 0;
+  if (op.varying && op.recompute) {
+    if (rs)
+      k_spmv_tiled<true, true, true><<<grid, 256, 0, s>>>(op, st, z, r, u, p, q, partials, seglen);
+    else
+      k_spmv_tiled<true, true, false><<<grid, 256, 0, s>>>(op, st, z, r, u, p, q, partials, seglen);
+  } else if (op.varying) {
+    if (rs)
+      k_spmv_tiled<true, false, true><<<grid, 256, 0, s>>>(op, st, z, r, u, p, q, partials, seglen);
+    else
+      k_spmv_tiled<true, false, false><<<grid, 256, 0, s>>>(op, st, z, r, u, p, q, partials,
+                                                             seglen);
+  } else {
+    if (rs)
+      k_spmv_tiled<false, false, true><<<grid, 256, 0, s>>>(op, st, z, r, u, p, q, partials,
+                                                             seglen);
+    else
+      k_spmv_tiled<false, false, false><<<grid, 256, 0, s>>>(op, st, z, r, u, p, q, partials,
+                                                              seglen);
+  }
   return cudaGetLastError();
 }
 
@@ -328,9 +345,9 @@ int grid_tiled_precond(const Op& op, int num_sms) {
 int grid_tiled_spmv(const Op& op, int num_sms) {
   int b = 0;
   if (op.varying)
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_spmv_tiled<true, false>, 256, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_spmv_tiled<true, false, false>, 256, 0);
   else
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_spmv_tiled<false, false>, 256, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_spmv_tiled<false, false, false>, 256, 0);
   long long g = (long long)std::max(1, b) * num_sms;
   // enough blocks for one unit per warp at the shortest segments
   const long long units = op.ntiles * std::max(1, op.nz / 4);

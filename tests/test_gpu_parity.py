@@ -95,16 +95,25 @@ def configure(s, mode):
     """mode: "column"; "tiled" (Thomas column solves, stored factors, batched
     loop); "tiled_recompute" (Thomas, factors rebuilt per sweep);
     "tiled_split" (substructured column solves, blocks chosen automatically);
-    "tiled_persistent" (Thomas, stored factors, one cooperative kernel)."""
+    "tiled_persistent" (Thomas, stored factors, one cooperative kernel).
+    The row-tiled modes form A z as r + (A - M) z wherever that applies (the
+    default); a "_stencil" suffix selects the full 7-point stencil."""
+    stencil = mode.endswith("_stencil")
+    mode = mode[: -len("_stencil")] if stencil else mode
     s.set_layout("column" if mode == "column" else "tiled")
     s.set_factors("recompute" if mode == "tiled_recompute" else "stored")
     s.set_loop("persistent" if mode == "tiled_persistent" else "batched")
     s.set_substructuring(0 if mode == "tiled_split" else 1)
+    s.set_az_form("stencil" if stencil else "auto")
     if mode == "tiled_persistent":
         assert s.loop == "persistent"
+    # the residual form needs the row-tiled layout and Thomas column solves
+    thomas = mode != "column" and s.substructuring == 1
+    assert s.az_form == ("residual" if thomas and not stencil else "stencil")
 
 
-MODES = ["column", "tiled", "tiled_recompute", "tiled_split", "tiled_persistent"]
+MODES = ["column", "tiled", "tiled_stencil", "tiled_recompute", "tiled_split", "tiled_persistent",
+         "tiled_persistent_stencil"]
 
 
 @pytest.mark.parametrize("layout", MODES)
@@ -276,6 +285,7 @@ def test_layouts_agree_and_switch_back_and_forth():
     prob, kw, b = case(45, 33, 64, True, True, a_v=1e4, seed=12)
     with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
         s.set_substructuring(1)  # Thomas column solves in both layouts
+        s.set_az_form("stencil")  # and the same arithmetic for A z
         bd = torch.from_numpy(b).to(DEV)
         xs = {}
         for layout in ["tiled", "column", "tiled"]:
@@ -291,15 +301,18 @@ def test_layouts_agree_and_switch_back_and_forth():
     assert np.linalg.norm(xt - xc) <= 1e-12 * np.linalg.norm(xc)
 
 
+@pytest.mark.parametrize("form", ["residual", "stencil"])
 @pytest.mark.parametrize("cfg", [c for c in SOLVE_CASES if c[3]], ids=lambda c: "x".join(map(str, c[:3])))
-def test_recomputed_factors_give_the_stored_iterates_bit_for_bit(cfg):
-    # the sweeps rebuild the diagonal and the Thomas factors with the set-up's
-    # rounding, so nothing but the data source differs
+def test_recomputed_factors_give_the_stored_iterates_bit_for_bit(cfg, form):
+    # the sweeps rebuild the diagonal, the weights and the Thomas factors with
+    # the set-up's rounding, so nothing but the data source differs
     nx, ny, nz, varying, graded, a_v = cfg
     prob, kw, b = case(nx, ny, nz, varying, graded, a_v=a_v, seed=7)
     with mf.Solver(nx, ny, nz, **kw) as s:
         s.set_loop("batched")  # the same loop (and reduction trees) for both
         s.set_substructuring(1)
+        s.set_az_form(form)
+        assert s.az_form == form
         bd = torch.from_numpy(b).to(DEV)
         out = {}
         for mode in ["stored", "recompute", "stored"]:
@@ -313,6 +326,56 @@ def test_recomputed_factors_give_the_stored_iterates_bit_for_bit(cfg):
     assert i0 == i1 == i2
     assert np.array_equal(h0, h1) and np.array_equal(h0, h2)
     assert np.array_equal(x0, x1) and np.array_equal(x0, x2)
+
+
+@pytest.mark.parametrize("loop", ["batched", "persistent"])
+@pytest.mark.parametrize("cfg", SOLVE_CASES, ids=lambda c: "x".join(map(str, c[:3])))
+def test_residual_form_of_Az_agrees_with_the_stencil(cfg, loop):
+    # A z = r + (A - M) z holds exactly for the z of M z = r; in floating
+    # point the two forms differ by rounding, which the iteration carries: the
+    # same iteration count within one and solutions far inside the solver's
+    # 1e-8 parity bound
+    nx, ny, nz, varying, graded, a_v = cfg
+    prob, kw, b = case(nx, ny, nz, varying, graded, a_v=a_v, seed=13)
+    out = {}
+    with mf.Solver(nx, ny, nz, **kw) as s:
+        s.set_substructuring(1)
+        s.set_loop(loop)
+        bd = torch.from_numpy(b).to(DEV)
+        for form in ["stencil", "residual"]:
+            s.set_az_form(form)
+            assert s.az_form == form
+            x = torch.zeros_like(bd)
+            it, hist, st = s.solve(bd, x, rtol=1e-10, maxit=500)
+            assert st == mf.PCG_OK
+            out[form] = (it, hist, x.cpu().numpy())
+    (i0, h0, x0), (i1, h1, x1) = out["stencil"], out["residual"]
+    assert abs(i0 - i1) <= 1
+    m = min(i0, i1) + 1
+    np.testing.assert_allclose(h1[:m], h0[:m], rtol=1e-6, atol=1e-13)
+    assert np.linalg.norm(x1 - x0) <= 1e-9 * np.linalg.norm(x0)
+    # the true residual of the residual-form solution meets the tolerance as
+    # well as the stencil form's does (to a factor 2 of rounding)
+    tr = [np.linalg.norm(b - oracle.apply_A(prob, xx)) / np.linalg.norm(b) for xx in (x0, x1)]
+    assert tr[1] <= max(2.0 * tr[0], 1e-10)
+
+
+def test_az_form_resolution_and_arguments():
+    prob, kw, b = case(20, 12, 16, True, True, a_v=1e3, seed=8)
+    with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        assert s.az_form == "residual"          # the default: row-tiled, Thomas
+        s.set_az_form("stencil")
+        assert s.az_form == "stencil"
+        s.set_az_form("residual")
+        s.set_substructuring(2)                 # substructured solves: the stencil
+        assert s.az_form == "stencil"
+        s.set_substructuring(1)
+        assert s.az_form == "residual"
+        s.set_layout("column")                  # column layout: the stencil
+        assert s.az_form == "stencil"
+        with pytest.raises(mf.PCGError) as e:
+            mf.pcg_set_az_form(s.ctx, 3)
+        assert e.value.status == mf.PCG_EINVAL
 
 
 def test_factor_mode_arguments_and_column_layout():

@@ -59,8 +59,9 @@ def test_workload_full_solve_parity(name):
     assert st_ref == oracle.OK
     with mf.Solver(w.nx, w.ny, w.nz, **kw) as s:
         bd = sampled_operator_checks(w, prob, s, b)
-        for layout in ["column", "tiled"]:
+        for layout, form in [("column", "auto"), ("tiled", "residual"), ("tiled", "stencil")]:
             s.set_layout(layout)
+            s.set_az_form(form)
             x = torch.zeros_like(bd)
             iters, hist, st = s.solve(bd, x, rtol=w.rtol, maxit=w.maxit)
             assert st == mf.PCG_OK and abs(iters - it_ref) <= 1, (layout, iters, it_ref)
@@ -68,7 +69,7 @@ def test_workload_full_solve_parity(name):
             it2, _, st2 = s.solve(bd, x, rtol=0.0, maxit=it_ref)
             assert (it2, st2) == (it_ref, mf.PCG_OK)
             xs = x.cpu().numpy()
-            assert np.linalg.norm(xs - x_ref) <= 1e-8 * np.linalg.norm(x_ref), layout
+            assert np.linalg.norm(xs - x_ref) <= 1e-8 * np.linalg.norm(x_ref), (layout, form)
         s.set_layout("column")
     if w.rhs == "manufactured":
         # the manufactured solution comes back to 1e-9 with a tight tolerance
@@ -90,24 +91,29 @@ def test_workload_large_parity(name, fixed_iters):
         bd = sampled_operator_checks(w, prob, s, b)
         x = torch.zeros_like(bd)
         got = {}
-        modes = [("tiled", "recompute", 1, "batched"), ("tiled", "stored", 1, "batched"),
-                 ("column", "stored", 1, "batched"), ("tiled", "stored", 2, "batched"),
-                 ("tiled", "stored", 1, "persistent")]
-        for layout, factors, blocks, loop in modes:
+        # (layout, factors, blocks per column, loop, form of A z)
+        modes = [("tiled", "recompute", 1, "batched", "auto"),
+                 ("tiled", "stored", 1, "batched", "auto"),
+                 ("tiled", "stored", 1, "batched", "stencil"),
+                 ("column", "stored", 1, "batched", "auto"), ("tiled", "stored", 2, "batched", "auto"),
+                 ("tiled", "stored", 1, "persistent", "auto")]
+        for layout, factors, blocks, loop, form in modes:
             s.set_layout(layout)
             s.set_factors(factors)
             s.set_loop(loop)
             s.set_substructuring(blocks)
+            s.set_az_form(form)
             x.zero_()
             it, _, st = s.solve(bd, x, rtol=0.0, maxit=fixed_iters)
             assert (it, st) == (fixed_iters, mf.PCG_OK)
             xs = x.cpu().numpy()
             assert np.linalg.norm(xs - x_ref) <= 1e-8 * np.linalg.norm(x_ref), (layout, factors,
-                                                                                blocks, loop)
-            if blocks == 1 and loop == "batched" and layout == "tiled":
+                                                                                blocks, loop, form)
+            if blocks == 1 and loop == "batched" and layout == "tiled" and form == "auto":
                 got[factors] = xs  # the two the bitwise comparison below needs
         s.set_substructuring(1)
         s.set_loop("auto")
+        s.set_az_form("auto")
         # the set-up derives T/D from 1/D (Markstein's correction), the sweep that
         # rebuilds its factors divides: bitwise equal on every cell of the grid
         assert np.array_equal(got["recompute"], got["stored"])
