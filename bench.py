@@ -457,17 +457,20 @@ def run_ours(args, w):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         e2e_it = 0
+        step_ms = []
         for _ in range(nsteps):
+            ts = time.perf_counter()
             solver.update_coeffs(**coeffs)
             it, _, st = solver.solve_host(bh, xh, rtol=w.rtol, maxit=w.maxit, history=False,
                                           x0=None)
             e2e_it += it
+            step_ms.append(round(1e3 * (time.perf_counter() - ts), 3))
         torch.cuda.synchronize()
         t_e2e = time.perf_counter() - t0
         t_e2e_ms, e2e_iters = reduce_over_ranks(1e3 * t_e2e, e2e_it, dev)
         e2e = {"value": e2e_iters / (1e-3 * t_e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": 8 * n, "d2h_bytes_per_step": 8 * n,
-               "api": "pcg_solve_host_x0 (x0 = 0)", "steps": nsteps}
+               "api": "pcg_solve_host_x0 (x0 = 0)", "steps": nsteps, "step_ms": step_ms}
         del xh, bh
 
     cpu = None
