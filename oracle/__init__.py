@@ -37,8 +37,19 @@ def _load():
         lib.oracle_precond_columns.argtypes = common + [_dp, _i64p, ctypes.c_int64, _dp]
         lib.oracle_pcg.argtypes = common + [_dp, _dp, ctypes.c_double, ctypes.c_int,
                                             ctypes.POINTER(ctypes.c_int), _dp]
+        lib.oracle_mg_levels.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        lib.oracle_mg_level_ah.argtypes = [ctypes.c_int, ctypes.c_int, _dp, ctypes.c_int, _dp]
+        lib.oracle_apply_A_area.argtypes = common + [ctypes.c_double, _dp, _dp]
+        lib.oracle_mg_restrict.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _dp, _dp]
+        lib.oracle_mg_prolong_add.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _dp, _dp]
+        mgp = [ctypes.c_int, ctypes.c_double, ctypes.c_int]
+        lib.oracle_mg_vcycle.argtypes = common + mgp + [_dp, _dp]
+        lib.oracle_mg_pcg.argtypes = common + mgp + [_dp, _dp, ctypes.c_double, ctypes.c_int,
+                                                     ctypes.POINTER(ctypes.c_int), _dp]
         for f in (lib.oracle_apply_A, lib.oracle_apply_A_cells, lib.oracle_precond,
-                  lib.oracle_precond_columns, lib.oracle_pcg):
+                  lib.oracle_precond_columns, lib.oracle_pcg, lib.oracle_mg_levels,
+                  lib.oracle_mg_level_ah, lib.oracle_apply_A_area, lib.oracle_mg_restrict,
+                  lib.oracle_mg_prolong_add, lib.oracle_mg_vcycle, lib.oracle_mg_pcg):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -145,4 +156,88 @@ def pcg(prob, b, x0=None, rtol=1e-10, maxit=500, check=True):
                         ctypes.byref(iters), _ptr(hist))
     if check and st not in (OK, ENOTCONV):
         raise OracleError(st, "oracle_pcg")
+    return x, iters.value, hist[: max(iters.value, 0) + 1], st
+
+
+# ---------------------------------------------------------------- multigrid
+# Tensor-product multigrid with the column solve as smoother (the paper's
+# sections 1, 2 and 9; readings of the open parts in oracle_pcg.c).
+
+MG_NU, MG_OMEGA = 1, 0.8   # defaults: one smoothing step each way, damping 0.8
+
+
+def mg_levels(nx, ny, max_levels=0):
+    """Number of levels of the horizontal semi-coarsening hierarchy."""
+    return _load().oracle_mg_levels(int(nx), int(ny), int(max_levels))
+
+
+def mg_level_ah(prob, level):
+    """a_h of multigrid level `level`, shape (ny >> level, nx >> level)."""
+    lib = _load()
+    nxc, nyc = prob.nx >> level, prob.ny >> level
+    out = np.empty(nxc * nyc)
+    st = lib.oracle_mg_level_ah(prob.nx, prob.ny, _ptr(prob.ah), int(level), _ptr(out))
+    if st:
+        raise OracleError(st, "oracle_mg_level_ah")
+    return out.reshape(nyc, nxc)
+
+
+def apply_A_area(prob, x, area):
+    """y = A x with the zero-order and vertical terms scaled by the
+    horizontal cell area (the operator of a multigrid level)."""
+    lib = _load()
+    x = _arr(x, prob.n)
+    y = np.empty(prob.n)
+    st = lib.oracle_apply_A_area(*prob._common(), float(area), _ptr(x), _ptr(y))
+    if st:
+        raise OracleError(st, "oracle_apply_A_area")
+    return y
+
+
+def mg_restrict(nx, ny, nz, rf):
+    """R rf: per layer, sums over the 2x2 fine columns of each coarse column."""
+    lib = _load()
+    rf = _arr(rf, nx * ny * nz)
+    rc = np.empty((nx // 2) * (ny // 2) * nz)
+    st = lib.oracle_mg_restrict(nx, ny, nz, _ptr(rf), _ptr(rc))
+    if st:
+        raise OracleError(st, "oracle_mg_restrict")
+    return rc
+
+
+def mg_prolong_add(nx, ny, nz, ec, xf):
+    """xf + P ec (piecewise constant over the 2x2 fine columns)."""
+    lib = _load()
+    ec = _arr(ec, (nx // 2) * (ny // 2) * nz)
+    out = _arr(xf, nx * ny * nz).copy()
+    st = lib.oracle_mg_prolong_add(nx, ny, nz, _ptr(ec), _ptr(out))
+    if st:
+        raise OracleError(st, "oracle_mg_prolong_add")
+    return out
+
+
+def mg_vcycle(prob, r, nu=MG_NU, omega=MG_OMEGA, max_levels=0):
+    """z = B r: one V-cycle."""
+    lib = _load()
+    r = _arr(r, prob.n)
+    z = np.empty(prob.n)
+    st = lib.oracle_mg_vcycle(*prob._common(), int(nu), float(omega), int(max_levels),
+                              _ptr(r), _ptr(z))
+    if st:
+        raise OracleError(st, "oracle_mg_vcycle")
+    return z
+
+
+def mg_pcg(prob, b, x0=None, rtol=1e-10, maxit=500, nu=MG_NU, omega=MG_OMEGA, max_levels=0,
+           check=True):
+    """PCG preconditioned by one V-cycle.  Returns (x, iters, hist, status)."""
+    lib = _load()
+    b = _arr(b, prob.n)
+    x = np.zeros(prob.n) if x0 is None else _arr(x0, prob.n).copy()
+    hist = np.full(maxit + 1, np.nan)
+    iters = ctypes.c_int(-1)
+    st = lib.oracle_mg_pcg(*prob._common(), int(nu), float(omega), int(max_levels), _ptr(b),
+                           _ptr(x), float(rtol), int(maxit), ctypes.byref(iters), _ptr(hist))
+    if check and st not in (OK, ENOTCONV):
+        raise OracleError(st, "oracle_mg_pcg")
     return x, iters.value, hist[: max(iters.value, 0) + 1], st

@@ -58,16 +58,19 @@ def vertical_laplacian(h, a_v):
     return sp.diags([main, -t, -t], [0, 1, -1], shape=(nz, nz), format="csr")
 
 
-def assemble_A(ah, h, a_v, mass):
+def assemble_A(ah, h, a_v, mass, area=1.0):
+    """The operator on cells of horizontal area `area` (square cells): the
+    horizontal face weights keep their form, the vertical and zero-order
+    terms are integrated over the larger cells."""
     ny, nx = ah.shape
     Dh = horizontal_laplacian(ah)
     Dv = vertical_laplacian(h, a_v)
     H = sp.diags(h)
     I = sp.identity(nx * ny, format="csr")
-    return (sp.kron(Dh, H) + sp.kron(I, Dv) + mass * sp.kron(I, H)).tocsr()
+    return (sp.kron(Dh, H) + area * (sp.kron(I, Dv) + mass * sp.kron(I, H))).tocsr()
 
 
-def assemble_M(ah, h, a_v, mass):
+def assemble_M(ah, h, a_v, mass, area=1.0):
     """Column preconditioner of eq. (19): per column, the vertical operator
     plus the horizontal diagonal sum(a_f) h_k plus the mass term."""
     ny, nx = ah.shape
@@ -75,7 +78,20 @@ def assemble_M(ah, h, a_v, mass):
     H = sp.diags(h)
     I = sp.identity(nx * ny, format="csr")
     S = sp.diags(face_sums(ah))
-    return (sp.kron(I, Dv) + sp.kron(S, H) + mass * sp.kron(I, H)).tocsr()
+    return (sp.kron(S, H) + area * (sp.kron(I, Dv) + mass * sp.kron(I, H))).tocsr()
+
+
+def piecewise_constant_prolongation(nx, ny, nz):
+    """P: (nx*ny*nz) x (nx/2*ny/2*nz) 0/1 matrix, fine cell (i,j,k) <- coarse
+    cell (i//2, j//2, k), built from index maps."""
+    rows, cols = [], []
+    for j in range(ny):
+        for i in range(nx):
+            for k in range(nz):
+                rows.append((j * nx + i) * nz + k)
+                cols.append(((j // 2) * (nx // 2) + i // 2) * nz + k)
+    return sp.csr_matrix((np.ones(len(rows)), (rows, cols)),
+                         shape=(nx * ny * nz, (nx // 2) * (ny // 2) * nz))
 
 
 def block_diagonal_part(A, nz):
