@@ -34,11 +34,13 @@ EXPORTED = ["pcg_create", "pcg_destroy", "pcg_update_coeffs", "pcg_set_stream", 
             "pcg_precond_dot_noalloc", "pcg_set_layout", "pcg_set_factors",
             "pcg_set_substructuring", "pcg_get_substructuring", "pcg_solve_host_x0",
             "pcg_set_loop", "pcg_get_loop", "pcg_test_barrier_absent", "pcg_set_az_form",
-            "pcg_get_az_form"]
+            "pcg_get_az_form", "pcg_set_preconditioner", "pcg_set_multigrid",
+            "pcg_get_multigrid", "pcg_mg_vcycle"]
 PCG_LAYOUT_COLUMN, PCG_LAYOUT_TILED = 0, 1
 PCG_FACTORS_STORED, PCG_FACTORS_RECOMPUTE = 0, 1
 PCG_LOOP_AUTO, PCG_LOOP_BATCHED, PCG_LOOP_PERSISTENT = 0, 1, 2
 PCG_AZ_AUTO, PCG_AZ_STENCIL, PCG_AZ_RESIDUAL = 0, 1, 2
+PCG_PREC_LINE, PCG_PREC_MULTIGRID = 0, 1
 
 
 class pcg_coeffs(ctypes.Structure):
@@ -83,6 +85,10 @@ def _load(path=LIB_PATH):
         "pcg_set_loop": (ctypes.c_int, [_vp, ctypes.c_int]),
         "pcg_get_loop": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int)]),
         "pcg_set_az_form": (ctypes.c_int, [_vp, ctypes.c_int]),
+        "pcg_set_preconditioner": (ctypes.c_int, [_vp, ctypes.c_int]),
+        "pcg_set_multigrid": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_double, ctypes.c_int]),
+        "pcg_get_multigrid": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int)]),
+        "pcg_mg_vcycle": (ctypes.c_int, [_vp, ctypes.c_void_p, ctypes.c_void_p]),
         "pcg_get_az_form": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int)]),
         "pcg_test_barrier_absent": (ctypes.c_int, [_vp, ctypes.c_int]),
     }
@@ -237,6 +243,28 @@ def pcg_get_az_form(ctx):
     return v.value
 
 
+def pcg_set_preconditioner(ctx, prec):
+    """PCG_PREC_LINE (default) or PCG_PREC_MULTIGRID."""
+    return _check(_lib.pcg_set_preconditioner(ctx, int(prec)), ctx)
+
+
+def pcg_set_multigrid(ctx, nu=1, omega=0.8, max_levels=0):
+    """Smoothing steps per side, damping, level cap (0: none)."""
+    return _check(_lib.pcg_set_multigrid(ctx, int(nu), float(omega), int(max_levels)), ctx)
+
+
+def pcg_get_multigrid(ctx):
+    """Levels of the multigrid preconditioner in use (0: not selected)."""
+    v = ctypes.c_int(0)
+    _check(_lib.pcg_get_multigrid(ctx, ctypes.byref(v)), ctx)
+    return v.value
+
+
+def pcg_mg_vcycle(ctx, n, r, z):
+    """z = B r, one V-cycle (device tensors of n values, caller's layout)."""
+    return _check(_lib.pcg_mg_vcycle(ctx, _dev_ptr(r, n, "r"), _dev_ptr(z, n, "z")), ctx)
+
+
 def pcg_test_barrier_absent(ctx, absent):
     """Test hook: the persistent loop's barriers miss `absent` arrivals, so the
     next persistent solve's first barrier wait runs out (PCG_ETIMEOUT)."""
@@ -376,6 +404,28 @@ class Solver:
             mode = {"auto": PCG_LOOP_AUTO, "batched": PCG_LOOP_BATCHED,
                     "persistent": PCG_LOOP_PERSISTENT}[mode]
         pcg_set_loop(self.ctx, mode)
+
+    def set_preconditioner(self, prec):
+        """"line" (column solve, default) or "multigrid" (or the PCG_PREC_* values)."""
+        if isinstance(prec, str):
+            prec = {"line": PCG_PREC_LINE, "multigrid": PCG_PREC_MULTIGRID}[prec]
+        pcg_set_preconditioner(self.ctx, prec)
+
+    def set_multigrid(self, nu=1, omega=0.8, max_levels=0):
+        pcg_set_multigrid(self.ctx, nu, omega, max_levels)
+
+    @property
+    def multigrid_levels(self):
+        """Levels of the multigrid preconditioner in use (0: not selected)."""
+        return pcg_get_multigrid(self.ctx)
+
+    def mg_vcycle(self, r, z=None):
+        """z = B r, one V-cycle on device fp64 tensors of N values."""
+        import torch
+        if z is None:
+            z = torch.empty_like(r)
+        pcg_mg_vcycle(self.ctx, self.n, r, z)
+        return z
 
     def set_az_form(self, form):
         """"auto", "stencil" or "residual" (or the PCG_AZ_* values)."""

@@ -65,6 +65,19 @@ struct pcg_ctx {
   int split_req = 0, split_p = 1, grid_sp = 0;
   int loop_req = PCG_LOOP_AUTO;      // requested solve loop
   int az_req = PCG_AZ_AUTO;          // requested form of A z in the stencil sweep
+  // multigrid preconditioner (row-tiled layout): levels 1..L-1 (level 0 is
+  // the solver's own grid), the finest level's two iterates, and the number
+  // of kernels one V-cycle launches
+  int prec = PCG_PREC_LINE;
+  int mg_nu = 1, mg_max_levels = 0;
+  double mg_omega = 0.8;
+  std::vector<pcg::MgLevel> mg;
+  double *mg_x0 = nullptr, *mg_y0 = nullptr;
+  int mg_grid_first = 1, mg_grid_smooth = 1;
+  int mg_launches = 0;
+  // host copies of the coefficients, from which the coarse levels are built
+  std::vector<double> ah_host, dz_host;
+  double a_h_host = 0.0, a_v_host = 0.0, mass_host = 0.0;
   int grid_ps = 0;                   // blocks of the persistent loop (0: not available)
   unsigned int test_absent = 0;      // test hook: arrivals the persistent barriers miss
   size_t partials_cap = 0;           // doubles in `partials`
@@ -153,17 +166,23 @@ int validate_coeffs(pcg_ctx* ctx, int nx, int ny, int nz, const pcg_coeffs* c) {
 // Per-level tables (eq. (17): the vertical discretisation is the same in
 // every column and only nz long).  For a constant a_h the Thomas factors are
 // identical in every column and are computed here once.
+//
+// `area` is the horizontal cell area (1 on the solver's grid, 4^l on
+// multigrid level l): the zero-order and vertical terms are integrated over
+// it, the horizontal face weights keep their form.  Powers of two scale
+// exactly, so a level's table is the area times the unit one, bit for bit.
 int build_levels(pcg_ctx* ctx, int nz, const pcg_coeffs* c, bool varying,
-                 std::vector<double>& lev) {
+                 std::vector<double>& lev, double area = 1.0) {
   using namespace pcg;
   lev.assign((size_t)kLevCount * nz, 0.0);
   std::vector<double> h(nz), tup(nz), tdn(nz);
   for (int k = 0; k < nz; ++k) h[k] = c->dz ? c->dz[k] : 1.0;
-  for (int k = 0; k < nz; ++k) tup[k] = (k < nz - 1) ? c->a_v / (0.5 * (h[k] + h[k + 1])) : 0.0;
+  for (int k = 0; k < nz; ++k)
+    tup[k] = (k < nz - 1) ? c->a_v / (0.5 * (h[k] + h[k + 1])) * area : 0.0;
   for (int k = 0; k < nz; ++k) tdn[k] = (k > 0) ? tup[k - 1] : 0.0;
   double nphi_prev = 0.0;
   for (int k = 0; k < nz; ++k) {
-    const double base = c->mass * h[k] + tup[k] + tdn[k];
+    const double base = c->mass * h[k] * area + tup[k] + tdn[k];
     lev[LV_UP * nz + k] = -tup[k];
     lev[LV_DN * nz + k] = -tdn[k];
     lev[LV_H * nz + k] = h[k];
@@ -192,6 +211,8 @@ cudaError_t dalloc(T** p, size_t count) {
   return cudaMalloc(reinterpret_cast<void**>(p), count * sizeof(T));
 }
 
+void mg_release(pcg_ctx* ctx);
+
 void free_all(pcg_ctx* ctx) {
   double* bufs[] = {ctx->r,     ctx->z,     ctx->p,     ctx->q,        ctx->lev,
                     ctx->ah,    ctx->faceE, ctx->faceN, ctx->cdiag,    ctx->tnphi,
@@ -214,6 +235,7 @@ void free_all(pcg_ctx* ctx) {
   }
   if (ctx->cap_stream) cudaStreamDestroy(ctx->cap_stream);
   ctx->cap_stream = nullptr;
+  mg_release(ctx);
 }
 
 // Upload coefficients and (for a field) rebuild the per-column and per-cell
@@ -249,11 +271,239 @@ int run_split_setup(pcg_ctx* ctx) {
   return PCG_OK;
 }
 
+// ------------------------------------------------ multigrid levels
+//
+// Level l+1 merges the 2x2 columns of level l (nx, ny even), keeps the nz
+// layers, and is eqs. (5)-(8) on cells of horizontal area 4^(l+1) with a_h
+// averaged over the merged columns.  Coarsening stops when nx or ny is odd,
+// or at mg_max_levels levels (0: no cap).
+int mg_count_levels(int nx, int ny, int max_levels) {
+  int L = 1;
+  while ((max_levels <= 0 || L < max_levels) && nx % 2 == 0 && ny % 2 == 0) {
+    nx /= 2;
+    ny /= 2;
+    ++L;
+  }
+  return L;
+}
+
+void mg_release(pcg_ctx* ctx) {
+  for (pcg::MgLevel& m : ctx->mg) {
+    double* bufs[] = {m.lev,   m.ah,    m.faceE, m.faceN, m.cdiag, m.cdiag_t, m.cwE_t,
+                      m.cwN_t, m.tnphi, m.tinvd, m.b,     m.x,     m.y};
+    for (double* b : bufs)
+      if (b) cudaFree(b);
+  }
+  ctx->mg.clear();
+  if (ctx->mg_x0) cudaFree(ctx->mg_x0);
+  if (ctx->mg_y0) cudaFree(ctx->mg_y0);
+  ctx->mg_x0 = ctx->mg_y0 = nullptr;
+}
+
+// Allocate the coarse levels and the finest level's iterates.
+int mg_allocate(pcg_ctx* ctx) {
+  mg_release(ctx);
+  const Op& f = ctx->op;
+  const int L = mg_count_levels(f.nx, f.ny, ctx->mg_max_levels);
+  if (L < 2)
+    return fail(ctx, PCG_EINVAL, "multigrid needs a grid with even nx and ny (got %d x %d)", f.nx,
+                f.ny);
+  const bool fields = ctx->has_field_buffers;
+  cudaError_t e = dalloc(&ctx->mg_x0, (size_t)f.ntiles * pcg::kTile * f.nz);
+  if (e == cudaSuccess) e = dalloc(&ctx->mg_y0, (size_t)f.ntiles * pcg::kTile * f.nz);
+  int nx = f.nx, ny = f.ny;
+  ctx->mg.resize(L - 1);
+  for (int l = 1; l < L && e == cudaSuccess; ++l) {
+    nx /= 2;
+    ny /= 2;
+    pcg::MgLevel& m = ctx->mg[l - 1];
+    Op& o = m.op;
+    o = Op{};
+    o.nx = nx;
+    o.ny = ny;
+    o.nz = f.nz;
+    o.ncols = (long long)nx * ny;
+    o.n = o.ncols * f.nz;
+    o.ntiles = (o.ncols + pcg::kTile - 1) / pcg::kTile;
+    const size_t npad = (size_t)o.ntiles * pcg::kTile * f.nz;
+    e = dalloc(&m.lev, (size_t)pcg::kLevCount * f.nz);
+    if (e == cudaSuccess) e = dalloc(&m.b, npad);
+    if (e == cudaSuccess) e = dalloc(&m.x, npad);
+    if (e == cudaSuccess) e = dalloc(&m.y, npad);
+    if (e == cudaSuccess && fields) {
+      e = dalloc(&m.ah, o.ncols);
+      if (e == cudaSuccess) e = dalloc(&m.faceE, o.ncols);
+      if (e == cudaSuccess) e = dalloc(&m.faceN, o.ncols);
+      if (e == cudaSuccess) e = dalloc(&m.cdiag, o.n);
+      if (e == cudaSuccess) e = dalloc(&m.cdiag_t, npad);
+      if (e == cudaSuccess) e = dalloc(&m.cwE_t, npad);
+      if (e == cudaSuccess) e = dalloc(&m.cwN_t, npad);
+      if (e == cudaSuccess) e = dalloc(&m.tnphi, npad);
+      if (e == cudaSuccess) e = dalloc(&m.tinvd, npad);
+    }
+    o.lev = m.lev;
+    o.ah = m.ah;
+    o.faceE = m.faceE;
+    o.faceN = m.faceN;
+    o.cdiag = m.cdiag;
+    o.cdiag_t = m.cdiag_t;
+    o.cwE_t = m.cwE_t;
+    o.cwN_t = m.cwN_t;
+    o.tnphi = m.tnphi;
+    o.tinvd = m.tinvd;
+  }
+  if (e != cudaSuccess) {
+    mg_release(ctx);
+    return cuda_fail(ctx, e, "multigrid level allocation");
+  }
+  return PCG_OK;
+}
+
+// Coarse level tables for the current coefficients (host copies), and the
+// grids of the Thomas sweeps on every level.  Synchronous.
+int mg_setup(pcg_ctx* ctx) {
+  const Op& f = ctx->op;
+  const bool varying = f.varying != 0;
+  pcg_coeffs c{};
+  c.a_h = ctx->a_h_host;
+  c.a_v = ctx->a_v_host;
+  c.mass = ctx->mass_host;
+  c.dz = ctx->dz_host.data();
+  std::vector<double> ah = ctx->ah_host, ahc;
+  int nx = f.nx;
+  double area = 1.0;
+  cudaError_t e = cudaMemsetAsync(&ctx->state->setup_error, 0, sizeof(int), ctx->stream);
+  for (size_t l = 0; l < ctx->mg.size() && e == cudaSuccess; ++l) {
+    pcg::MgLevel& m = ctx->mg[l];
+    Op& o = m.op;
+    area *= 4.0;
+    o.varying = varying ? 1 : 0;
+    std::vector<double> lev;
+    int st = build_levels(ctx, f.nz, &c, varying, lev, area);
+    if (st) return st;
+    e = cudaMemcpy(m.lev, lev.data(), lev.size() * sizeof(double), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && varying) {
+      // a_h of the merged columns: the mean of the four, level by level
+      const int nxc = nx / 2;
+      ahc.assign((size_t)o.ncols, 0.0);
+      for (long long J = 0; J < o.ny; ++J)
+        for (int I = 0; I < nxc; ++I) {
+          const double s = ah[(2 * J) * nx + 2 * I] + ah[(2 * J) * nx + 2 * I + 1] +
+                           ah[(2 * J + 1) * nx + 2 * I] + ah[(2 * J + 1) * nx + 2 * I + 1];
+          ahc[J * nxc + I] = 0.25 * s;
+        }
+      ah.swap(ahc);
+      e = cudaMemcpy(m.ah, ah.data(), o.ncols * sizeof(double), cudaMemcpyHostToDevice);
+      if (e == cudaSuccess) e = pcg::launch_face_coeffs(o, m.faceE, m.faceN, ctx->stream);
+      if (e == cudaSuccess)
+        e = pcg::launch_column_setup(o, ctx->state, m.cdiag, m.cdiag_t, m.cwE_t, m.cwN_t,
+                                     m.tnphi, m.tinvd, ctx->stream);
+    }
+    nx /= 2;
+    m.grid_first = pcg::grid_mg_first(o, ctx->num_sms);
+    m.grid_smooth = pcg::grid_mg_smooth(o, ctx->num_sms);
+  }
+  ctx->mg_grid_first = pcg::grid_mg_first(f, ctx->num_sms);
+  ctx->mg_grid_smooth = pcg::grid_mg_smooth(f, ctx->num_sms);
+  int bad = 0;
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(&bad, &ctx->state->setup_error, sizeof(int), cudaMemcpyDeviceToHost,
+                        ctx->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "multigrid level set-up");
+  if (bad) return fail(ctx, PCG_EBREAKDOWN, "a Thomas pivot on a multigrid level is not positive");
+  // reduction partials for the finest level's fused sweeps
+  const size_t need = 2 * (size_t)std::max(ctx->mg_grid_first, ctx->mg_grid_smooth);
+  if (need > ctx->partials_cap) {
+    double* np = nullptr;
+    e = dalloc(&np, need);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "reduction partials");
+    cudaFree(ctx->partials);
+    ctx->partials = np;
+    ctx->partials_cap = need;
+  }
+  ctx->config_gen++;
+  return PCG_OK;
+}
+
+// Enqueue one V-cycle, out = B b on the solver's grid (op0, row-tiled).
+// fused: b is the solver's r, updated first (r <- r - alpha q), and the last
+// smoothing step takes the scalar step of Algorithm 1.  *launches receives
+// the number of kernels enqueued.
+cudaError_t mg_enqueue(pcg_ctx* ctx, const Op& op0, double* b0, double* out, bool fused,
+                       cudaStream_t s, int* launches) {
+  const int L = (int)ctx->mg.size() + 1;
+  const double w = ctx->mg_omega;
+  const int nu = ctx->mg_nu;
+  DevState* st = ctx->state;
+  int cnt = 0;
+  auto lvl_op = [&](int l) -> const Op& { return l ? ctx->mg[l - 1].op : op0; };
+  auto lvl_b = [&](int l) { return l ? ctx->mg[l - 1].b : b0; };
+  auto lvl_x = [&](int l) { return l ? ctx->mg[l - 1].x : ctx->mg_x0; };
+  auto lvl_y = [&](int l) { return l ? ctx->mg[l - 1].y : ctx->mg_y0; };
+  auto g_first = [&](int l) { return l ? ctx->mg[l - 1].grid_first : ctx->mg_grid_first; };
+  auto g_smooth = [&](int l) { return l ? ctx->mg[l - 1].grid_smooth : ctx->mg_grid_smooth; };
+  std::vector<double*> cur(L, nullptr);
+  cudaError_t e = cudaSuccess;
+  // down: smoothing from zero, then the restricted residual
+  for (int l = 0; l < L && e == cudaSuccess; ++l) {
+    const Op& o = lvl_op(l);
+    double* c = lvl_x(l);
+    double* other = lvl_y(l);
+    e = pcg::launch_mg_first(o, st, lvl_b(l), ctx->q, c, w, fused && l == 0, ctx->partials,
+                             g_first(l), s);
+    ++cnt;
+    for (int i = 1; i < nu && e == cudaSuccess; ++i) {
+      e = pcg::launch_mg_smooth(o, st, lvl_b(l), c, other, w, false, ctx->partials, ctx->hist,
+                                g_smooth(l), s);
+      ++cnt;
+      std::swap(c, other);
+    }
+    cur[l] = c;
+    if (l + 1 < L && e == cudaSuccess) {
+      e = pcg::launch_mg_restrict(o, lvl_op(l + 1), st, lvl_b(l), c, lvl_b(l + 1), ctx->num_sms,
+                                  s);
+      ++cnt;
+    }
+  }
+  // up: coarse-grid correction, then smoothing; the finest level's last step
+  // writes `out`
+  for (int l = L - 2; l >= 0 && e == cudaSuccess; --l) {
+    const Op& o = lvl_op(l);
+    double* c = cur[l];
+    double* other = (c == lvl_x(l)) ? lvl_y(l) : lvl_x(l);
+    e = pcg::launch_mg_prolong(o, lvl_op(l + 1), st, c, cur[l + 1], ctx->num_sms, s);
+    ++cnt;
+    for (int i = 0; i < nu && e == cudaSuccess; ++i) {
+      const bool last = (i == nu - 1);
+      double* dst = (l == 0 && last) ? out : other;
+      e = pcg::launch_mg_smooth(o, st, lvl_b(l), c, dst, w, fused && l == 0 && last,
+                                ctx->partials, ctx->hist, g_smooth(l), s);
+      ++cnt;
+      other = c;
+      c = dst;
+    }
+    cur[l] = c;
+  }
+  if (launches) *launches = cnt;
+  return e;
+}
+
 int load_coeffs(pcg_ctx* ctx, const pcg_coeffs* c, bool varying) {
   ctx->config_gen++;  // the sweeps' template choice follows op.varying
   std::vector<double> lev;
   int st = build_levels(ctx, ctx->op.nz, c, varying, lev);
   if (st) return st;
+  // host copies for the multigrid levels
+  ctx->a_h_host = c->a_h;
+  ctx->a_v_host = c->a_v;
+  ctx->mass_host = c->mass;
+  ctx->dz_host.assign((size_t)ctx->op.nz, 1.0);
+  if (c->dz) ctx->dz_host.assign(c->dz, c->dz + ctx->op.nz);
+  if (varying)
+    ctx->ah_host.assign(c->a_h_field, c->a_h_field + ctx->op.ncols);
+  else
+    ctx->ah_host.clear();
   cudaError_t e = cudaMemcpyAsync(ctx->lev, lev.data(), lev.size() * sizeof(double),
                                   cudaMemcpyHostToDevice, ctx->stream);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "upload of the level table");
@@ -294,7 +544,11 @@ int load_coeffs(pcg_ctx* ctx, const pcg_coeffs* c, bool varying) {
     e = cudaStreamSynchronize(ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "coefficient upload");
   }
-  if (ctx->split_p > 1) return run_split_setup(ctx);
+  if (ctx->split_p > 1) {
+    st = run_split_setup(ctx);
+    if (st) return st;
+  }
+  if (ctx->prec == PCG_PREC_MULTIGRID) return mg_setup(ctx);
   return PCG_OK;
 }
 
@@ -357,6 +611,7 @@ bool persistent_grid(const pcg_ctx* ctx) {
 // The loop the next solve runs (PCG_LOOP_BATCHED or PCG_LOOP_PERSISTENT).
 int resolved_loop(const pcg_ctx* ctx) {
   const bool eligible = ctx->layout == PCG_LAYOUT_TILED && ctx->split_p == 1 &&
+                        ctx->prec == PCG_PREC_LINE &&
                         !(ctx->op.varying && ctx->factors == PCG_FACTORS_RECOMPUTE) &&
                         ctx->grid_ps > 0;
   if (!eligible || ctx->loop_req == PCG_LOOP_BATCHED) return PCG_LOOP_BATCHED;
@@ -368,7 +623,8 @@ int resolved_loop(const pcg_ctx* ctx) {
 // or PCG_AZ_RESIDUAL): the residual form needs the row-tiled layout and the
 // Thomas column solve, whose z the sweep pairs with r.
 int resolved_az(const pcg_ctx* ctx) {
-  const bool eligible = ctx->layout == PCG_LAYOUT_TILED && ctx->split_p == 1;
+  const bool eligible = ctx->layout == PCG_LAYOUT_TILED && ctx->split_p == 1 &&
+                        ctx->prec == PCG_PREC_LINE;
   return (eligible && ctx->az_req != PCG_AZ_STENCIL) ? PCG_AZ_RESIDUAL : PCG_AZ_STENCIL;
 }
 
@@ -378,11 +634,16 @@ cudaError_t launch_tiled_iteration(pcg_ctx* ctx, const Op& op, bool split, int g
                                    cudaStream_t s, cudaEvent_t* ev) {
   cudaError_t e = cudaSuccess;
   if (ev) e = cudaEventRecordWithFlags(ev[0], s, cudaEventRecordExternal);
-  if (e == cudaSuccess)
-    e = split ? pcg::launch_precond_split(op, ctx->split_p, ctx->state, ctx->r, ctx->q, ctx->z,
-                                          ctx->partials, ctx->hist, grid_pm, s)
-              : pcg::launch_precond_tiled(op, ctx->state, ctx->r, ctx->q, ctx->z, ctx->partials,
-                                          ctx->hist, grid_pm, s);
+  if (e == cudaSuccess) {
+    if (ctx->prec == PCG_PREC_MULTIGRID)
+      e = mg_enqueue(ctx, op, ctx->r, ctx->z, true, s, &ctx->mg_launches);
+    else if (split)
+      e = pcg::launch_precond_split(op, ctx->split_p, ctx->state, ctx->r, ctx->q, ctx->z,
+                                    ctx->partials, ctx->hist, grid_pm, s);
+    else
+      e = pcg::launch_precond_tiled(op, ctx->state, ctx->r, ctx->q, ctx->z, ctx->partials,
+                                    ctx->hist, grid_pm, s);
+  }
   if (e == cudaSuccess && ev) e = cudaEventRecordWithFlags(ev[1], s, cudaEventRecordExternal);
   if (e == cudaSuccess)
     e = pcg::launch_spmv_tiled(op, ctx->state, ctx->z, ctx->r, ctx->u_t, ctx->p, ctx->q,
@@ -457,7 +718,8 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
   const bool tiled = ctx->layout == PCG_LAYOUT_TILED;
   op.recompute = (tiled && op.varying && ctx->factors == PCG_FACTORS_RECOMPUTE) ? 1 : 0;
   op.az_resid = resolved_az(ctx) == PCG_AZ_RESIDUAL ? 1 : 0;
-  const bool split = tiled && ctx->split_p > 1;
+  const bool mgrid = tiled && ctx->prec == PCG_PREC_MULTIGRID;
+  const bool split = tiled && ctx->split_p > 1 && !mgrid;
   const int grid_pm = split ? ctx->grid_sp : ctx->grid_tm;  // preconditioner sweep blocks
   op.nscratch = ctx->nscratch;
   // The row-tiled layout forms r = b - A x0 column-contiguously in z, then
@@ -514,7 +776,7 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
   std::vector<float> tm_m, tm_a;  // graph sweep times in launch order (timing)
   while (use_graphs && enq <= maxit && !stop) {
     e = cudaGraphLaunch(ctx->graphs[slot].exec, s);
-    ctx->last_launches += 2 * batch;
+    ctx->last_launches += (long long)(mgrid ? ctx->mg_launches + 1 : 2) * batch;
     enq += batch;
     if (e == cudaSuccess)
       e = cudaMemcpyAsync(&ctx->pinned[slot], ctx->state, sizeof(DevState),
@@ -536,6 +798,11 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
     const int nb = std::min(batch, maxit + 1 - enq);
     for (int i = 0; i < nb; ++i) {
       e = timed(ctx, PCG_K_PRECOND_FUSED, [&] {
+        if (mgrid) {
+          cudaError_t ee = mg_enqueue(ctx, op, ctx->r, ctx->z, true, s, &ctx->mg_launches);
+          ctx->last_launches += ctx->mg_launches - 1;  // timed() counts one
+          return ee;
+        }
         if (split)
           return pcg::launch_precond_split(op, ctx->split_p, ctx->state, ctx->r, ctx->q, ctx->z,
                                            ctx->partials, ctx->hist, ctx->grid_sp, s);
@@ -742,6 +1009,8 @@ int pcg_set_layout(pcg_ctx* ctx, int layout) {
   if (layout != PCG_LAYOUT_COLUMN && layout != PCG_LAYOUT_TILED)
     return fail(ctx, PCG_EINVAL, "unknown layout %d", layout);
   if (layout == ctx->layout) return PCG_OK;
+  if (ctx->prec == PCG_PREC_MULTIGRID)
+    return fail(ctx, PCG_EINVAL, "the multigrid preconditioner needs the row-tiled layout");
   DeviceGuard g(ctx->device);
   if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
   cudaError_t e = cudaStreamSynchronize(ctx->stream);
@@ -863,6 +1132,94 @@ int pcg_set_loop(pcg_ctx* ctx, int mode) {
   if (mode != PCG_LOOP_AUTO && mode != PCG_LOOP_BATCHED && mode != PCG_LOOP_PERSISTENT)
     return fail(ctx, PCG_EINVAL, "unknown loop mode %d", mode);
   ctx->loop_req = mode;
+  return PCG_OK;
+}
+
+int pcg_set_preconditioner(pcg_ctx* ctx, int prec) {
+  if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
+  if (prec != PCG_PREC_LINE && prec != PCG_PREC_MULTIGRID)
+    return fail(ctx, PCG_EINVAL, "unknown preconditioner %d", prec);
+  if (prec == ctx->prec) return PCG_OK;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
+  if (prec == PCG_PREC_MULTIGRID) {
+    if (ctx->layout != PCG_LAYOUT_TILED)
+      return fail(ctx, PCG_EINVAL, "the multigrid preconditioner needs the row-tiled layout");
+    cudaError_t e = cudaStreamSynchronize(ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "preconditioner change");
+    int st = mg_allocate(ctx);
+    if (st) return st;
+    ctx->prec = prec;
+    st = mg_setup(ctx);
+    if (st) {
+      ctx->prec = PCG_PREC_LINE;
+      mg_release(ctx);
+      return st;
+    }
+  } else {
+    cudaError_t e = cudaStreamSynchronize(ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "preconditioner change");
+    mg_release(ctx);
+    ctx->prec = prec;
+  }
+  ctx->config_gen++;
+  return PCG_OK;
+}
+
+int pcg_set_multigrid(pcg_ctx* ctx, int nu, double omega, int max_levels) {
+  if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
+  if (nu < 1 || nu > 16) return fail(ctx, PCG_EINVAL, "nu must be in 1..16 (got %d)", nu);
+  if (!(omega > 0.0 && omega <= 1.0))
+    return fail(ctx, PCG_EINVAL, "omega must be in (0, 1] (got %g)", omega);
+  if (max_levels < 0) return fail(ctx, PCG_EINVAL, "max_levels must be >= 0");
+  const bool relevel = max_levels != ctx->mg_max_levels;
+  if (relevel && ctx->prec == PCG_PREC_MULTIGRID &&
+      mg_count_levels(ctx->op.nx, ctx->op.ny, max_levels) < 2)
+    return fail(ctx, PCG_EINVAL, "multigrid needs at least two levels");
+  ctx->mg_nu = nu;
+  ctx->mg_omega = omega;
+  ctx->mg_max_levels = max_levels;
+  ctx->config_gen++;
+  if (relevel && ctx->prec == PCG_PREC_MULTIGRID) {
+    DeviceGuard g(ctx->device);
+    if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
+    cudaError_t e = cudaStreamSynchronize(ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "multigrid change");
+    int st = mg_allocate(ctx);
+    if (st == PCG_OK) st = mg_setup(ctx);
+    if (st) {
+      ctx->prec = PCG_PREC_LINE;
+      mg_release(ctx);
+      return st;
+    }
+  }
+  return PCG_OK;
+}
+
+int pcg_get_multigrid(const pcg_ctx* ctx, int* levels_out) {
+  if (!ctx || !levels_out) return fail(nullptr, PCG_EINVAL, "NULL argument");
+  *levels_out = ctx->prec == PCG_PREC_MULTIGRID ? (int)ctx->mg.size() + 1 : 0;
+  return PCG_OK;
+}
+
+int pcg_mg_vcycle(pcg_ctx* ctx, const double* r_dev, double* z_dev) {
+  if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
+  if (ctx->prec != PCG_PREC_MULTIGRID)
+    return fail(ctx, PCG_EINVAL, "the multigrid preconditioner is not selected");
+  if (!r_dev || !z_dev) return fail(ctx, PCG_EINVAL, "r and z must be non-NULL device pointers");
+  if (overlap(r_dev, z_dev, ctx->op.n)) return fail(ctx, PCG_EINVAL, "r and z overlap");
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
+  // the solver's own vectors serve as row-tiled scratch between solves;
+  // `done` is cleared so that the cycle's kernels run
+  Op op = ctx->op;
+  cudaStream_t s = ctx->stream;
+  cudaError_t e = cudaMemsetAsync(&ctx->state->done, 0, sizeof(int), s);
+  if (e == cudaSuccess) e = pcg::launch_to_tiled(op, r_dev, ctx->p, s);
+  int cnt = 0;
+  if (e == cudaSuccess) e = mg_enqueue(ctx, op, ctx->p, ctx->u_t, false, s, &cnt);
+  if (e == cudaSuccess) e = pcg::launch_from_tiled(op, ctx->state, ctx->u_t, nullptr, z_dev, s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "multigrid V-cycle launch");
   return PCG_OK;
 }
 

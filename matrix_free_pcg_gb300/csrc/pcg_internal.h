@@ -84,6 +84,8 @@ struct DevState {
   int maxit;
   unsigned int ticket_m;  // last-block tickets of the two grid reductions
   unsigned int ticket_a;
+  double mg_R;       // multigrid preconditioner: ||r||^2 of the current iteration, from the
+                     // fine level's first smoothing sweep, for the stopping test
   int setup_error;   // a non-positive Thomas pivot was met in the setup kernel
   int dev_error;     // a bounded device wait ran out (pcg_status PCG_ETIMEOUT)
   unsigned int bar_count, bar_gen;  // grid barrier of the persistent solve loop
@@ -173,6 +175,38 @@ cudaError_t launch_split_setup(const Op& op, int P, DevState* st, cudaStream_t s
 cudaError_t launch_precond_split(const Op& op, int P, DevState* st, double* r, const double* q,
                                  double* z, double* partials, double* hist, int grid,
                                  cudaStream_t s);
+
+// Tensor-product multigrid preconditioner (pcg_mg.cu), row-tiled vectors on
+// every level.  A level is an Op (its own per-level table, and for an a_h
+// field its face values and per-cell diagonal, weights and Thomas factors)
+// on cells of horizontal area 4^l; coarse level l+1 merges 2x2 columns.
+struct MgLevel {
+  Op op{};
+  double *lev = nullptr, *ah = nullptr, *faceE = nullptr, *faceN = nullptr;
+  double *cdiag = nullptr, *cdiag_t = nullptr, *cwE_t = nullptr, *cwN_t = nullptr;
+  double *tnphi = nullptr, *tinvd = nullptr;
+  double *b = nullptr, *x = nullptr, *y = nullptr;  // right-hand side, two iterates
+  int grid_first = 1, grid_smooth = 1;              // blocks of the two Thomas sweeps
+};
+// x = omega M^{-1} b.  fused (finest level inside the solve): first b <- b -
+// alpha q with alpha from the device state and ||b||^2 into st->mg_R.
+cudaError_t launch_mg_first(const Op& op, DevState* st, double* b, const double* q, double* x,
+                            double omega, bool fused, double* partials, int grid,
+                            cudaStream_t s);
+// bc = R (b - A x): per layer, the residuals of the 2x2 fine columns summed.
+cudaError_t launch_mg_restrict(const Op& fine, const Op& coarse, const DevState* st,
+                               const double* b, const double* x, double* bc, int num_sms,
+                               cudaStream_t s);
+// x += P e: every fine column gets its coarse column's value.
+cudaError_t launch_mg_prolong(const Op& fine, const Op& coarse, const DevState* st, double* x,
+                              const double* e, int num_sms, cudaStream_t s);
+// xout = xin + omega M^{-1} (b - A xin).  fused (finest level, last step):
+// <b, xout> reduced and the scalar step of Algorithm 1 taken with st->mg_R.
+cudaError_t launch_mg_smooth(const Op& op, DevState* st, const double* b, const double* xin,
+                             double* xout, double omega, bool fused, double* partials,
+                             double* hist, int grid, cudaStream_t s);
+int grid_mg_first(const Op& op, int num_sms);
+int grid_mg_smooth(const Op& op, int num_sms);
 
 // Occupancy-derived grid sizes (blocks) for the persistent sweeps.  The
 // preconditioner's also fixes op.stream_smem (see pcg_kernels.cu).

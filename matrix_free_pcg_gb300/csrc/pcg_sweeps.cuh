@@ -28,12 +28,14 @@ __device__ __forceinline__ long long tiled_base(long long col, int nz) {
 // One tile of the preconditioner sweep (see k_precond_tiled), for the lane's
 // column: accumulates r*.r* and <r*, z> into accR, accK (FUSED).  COHERENT:
 // q was written by other blocks of the same launch (the persistent loop), so
-// it is read from L2, past the SM's non-coherent L1.
-template <bool VARY, bool FUSED, bool COHERENT = false>
+// it is read from L2, past the SM's non-coherent L1.  SCALE: z is stored as
+// zscale * M^{-1} r (the damped line relaxation of the multigrid smoother).
+template <bool VARY, bool FUSED, bool COHERENT = false, bool SCALE = false>
 __device__ __forceinline__ void precond_tile(const Op& op, long long t, int lane,
                                              double* __restrict__ r, const double* __restrict__ q,
                                              double* __restrict__ z, double nalpha, uint64_t keep,
-                                             uint64_t stream, double& accR, double& accK) {
+                                             uint64_t stream, double& accR, double& accK,
+                                             double zscale = 1.0) {
   const int nz = op.nz;
   const int fs = VARY ? kTile : 1;  // factor stride between levels
   if (t * kTile + lane >= op.ncols) return;
@@ -96,6 +98,7 @@ __device__ __forceinline__ void precond_tile(const Op& op, long long t, int lane
   // ---- backward: z_{nz-1} = w_{nz-1} (in place); level k uses nphi_k.
   // Chunk b holds levels kb, kb-1, ..., kb-kTmChunk+1 with kb = nz-2-b*kTmChunk.
   double zz = w;
+  if (SCALE) st_hint(zt + (long long)(nz - 1) * kTile, w * zscale, stream);
   double bw[kTmChunk], bn[kTmChunk];
 #pragma unroll
   for (int j = 0; j < kTmChunk; ++j) {
@@ -117,7 +120,7 @@ __device__ __forceinline__ void precond_tile(const Op& op, long long t, int lane
       const int k = kb - j;
       if (k >= 0) {
         zz = fma(bn[j], zz, bw[j]);
-        st_hint(zt + k * kTile, zz, stream);
+        st_hint(zt + k * kTile, SCALE ? zz * zscale : zz, stream);
       }
     }
 #pragma unroll

@@ -85,6 +85,12 @@ def test_null_context_calls_fail_cleanly(lib):
     assert lib._lib.pcg_get_substructuring(None, None) == lib.PCG_EINVAL
     assert lib._lib.pcg_get_loop(None, None) == lib.PCG_EINVAL
     assert lib._lib.pcg_test_barrier_absent(None, 0) == lib.PCG_EINVAL
+    assert lib._lib.pcg_set_az_form(None, lib.PCG_AZ_AUTO) == lib.PCG_EINVAL
+    assert lib._lib.pcg_get_az_form(None, None) == lib.PCG_EINVAL
+    assert lib._lib.pcg_set_preconditioner(None, lib.PCG_PREC_LINE) == lib.PCG_EINVAL
+    assert lib._lib.pcg_set_multigrid(None, 1, 0.8, 0) == lib.PCG_EINVAL
+    assert lib._lib.pcg_get_multigrid(None, None) == lib.PCG_EINVAL
+    assert lib._lib.pcg_mg_vcycle(None, None, None) == lib.PCG_EINVAL
     assert lib._lib.pcg_precond_dot_noalloc(None, None, None, None) == lib.PCG_EINVAL
     assert lib._lib.pcg_enable_timing(None, 1) == lib.PCG_EINVAL
     assert lib._lib.pcg_kernel_times(None, None, None) == lib.PCG_EINVAL

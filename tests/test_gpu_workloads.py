@@ -71,6 +71,19 @@ def test_workload_full_solve_parity(name):
             xs = x.cpu().numpy()
             assert np.linalg.norm(xs - x_ref) <= 1e-8 * np.linalg.norm(x_ref), (layout, form)
         s.set_layout("column")
+    # the multigrid preconditioner against the oracle's multigrid PCG
+    xm_ref, itm_ref, _, stm_ref = oracle.mg_pcg(prob, b, rtol=w.rtol, maxit=w.maxit)
+    assert stm_ref == oracle.OK and itm_ref < it_ref
+    with mf.Solver(w.nx, w.ny, w.nz, **kw) as s:
+        s.set_preconditioner("multigrid")
+        x = torch.zeros_like(bd)
+        iters, _, st = s.solve(bd, x, rtol=w.rtol, maxit=w.maxit)
+        assert st == mf.PCG_OK and abs(iters - itm_ref) <= 1, (iters, itm_ref)
+        x.zero_()
+        it2, _, st2 = s.solve(bd, x, rtol=0.0, maxit=itm_ref)
+        assert (it2, st2) == (itm_ref, mf.PCG_OK)
+        xs = x.cpu().numpy()
+    assert np.linalg.norm(xs - xm_ref) <= 1e-8 * np.linalg.norm(xm_ref), "multigrid"
     if w.rhs == "manufactured":
         # the manufactured solution comes back to 1e-9 with a tight tolerance
         with mf.Solver(w.nx, w.ny, w.nz, **kw) as s:
@@ -134,3 +147,27 @@ def test_workload_large_parity(name, fixed_iters):
         # a fixed iteration count can drive the recursively updated residual far
         # below what fp64 can attain; the true residual stops at that floor
         assert true_rel <= max(10 * hist[-1], 1e-9), (true_rel, hist[-1])
+
+
+def test_headline_multigrid_parity():
+    # two fixed multigrid-preconditioned iterations on the full headline grid,
+    # then a converged solve checked by its true residual
+    w, prob, b, vec, kw = setup("graded_varcoef_1024x1024x128")
+    x_ref, it_ref, _, st_ref = oracle.mg_pcg(prob, b, rtol=0.0, maxit=2)
+    assert (it_ref, st_ref) == (2, oracle.OK)
+    with mf.Solver(w.nx, w.ny, w.nz, **kw) as s:
+        s.set_preconditioner("multigrid")
+        assert s.multigrid_levels == 11
+        bd = torch.from_numpy(b).to(DEV)
+        x = torch.zeros_like(bd)
+        it, _, st = s.solve(bd, x, rtol=0.0, maxit=2)
+        assert (it, st) == (2, mf.PCG_OK)
+        xs = x.cpu().numpy()
+        assert np.linalg.norm(xs - x_ref) <= 1e-8 * np.linalg.norm(x_ref)
+        del x_ref
+        x.zero_()
+        it, hist, st = s.solve(bd, x, rtol=w.rtol, maxit=w.maxit)
+        assert st == mf.PCG_OK and hist[-1] < w.rtol and it < 20
+        xs = x.cpu().numpy()
+    true_rel = np.linalg.norm(b - oracle.apply_A(prob, xs)) / np.linalg.norm(b)
+    assert true_rel <= 100 * w.rtol, true_rel
