@@ -62,6 +62,39 @@ BYTES_PRECOND = {True: 48, False: 32}  # r,q (+ 2 per-cell Thomas factors) read;
 # coefficients.
 OPS_BYTES_SPMV_RECOMPUTE = {"stencil": (17, 56), "residual": (12, 64)}
 OPS_PRECOND_RECOMPUTE, BYTES_PRECOND_RECOMPUTE = 12, 32
+# Multigrid V-cycle (--preconditioner multigrid), per cell of the level a
+# kernel runs on: fp64 operations and algorithmic bytes with an a_h field
+# (constant a_h: no per-cell diagonal, weights or factors), from the kernel
+# sources.  first: x = omega M^-1 b (finest level: also r -= alpha q, ||r||^2
+# and the <r, M^-1 r> accumulation of the shared Thomas body); smooth: residual
+# stencil, Thomas, x + omega z (finest level's last step: also <r, z>);
+# restrict: the fine residual and 3 adds per 4 fine cells, per fine cell;
+# prolong: one add per fine cell.
+# restrict after one smoothing step from zero (nu = 1) takes the residual from
+# the horizontal terms alone: 5 operations and 3 adds per 4 fine cells.
+MG_OPS = {"first_fused": 7, "first": 4, "smooth": 12, "smooth_fused": 13, "restrict": 8.75,
+          "restrict_first": 5.75, "prolong": 1}
+MG_BYTES = {True: {"first_fused": 48, "first": 32, "smooth": 64, "smooth_fused": 64,
+                   "restrict": 42, "restrict_first": 34, "prolong": 18},
+            False: {"first_fused": 32, "first": 16, "smooth": 24, "smooth_fused": 24,
+                    "restrict": 18, "restrict_first": 18, "prolong": 18}}
+
+
+def mg_vcycle_cost(nx, ny, nz, levels, nu, varying):
+    """(fp64 ops, algorithmic bytes) of one V-cycle per cell of the finest grid."""
+    n0 = nx * ny * nz
+    ops = byt = 0.0
+    for l in range(levels):
+        cells = (nx >> l) * (ny >> l) * nz / n0
+        ks = ["first_fused" if l == 0 else "first"] + ["smooth"] * (nu - 1)
+        if l + 1 < levels:
+            ks += ["restrict_first" if nu == 1 else "restrict", "prolong"] + ["smooth"] * (nu - 1)
+            ks.append("smooth_fused" if l == 0 else "smooth")
+        ops += cells * sum(MG_OPS[k] for k in ks)
+        byt += cells * sum(MG_BYTES[varying][k] for k in ks)
+    return ops, byt
+
+
 L2_BYTES = 129e6                     # GB300 L2
 FP64_LANES_PER_SM_CLK = 2.0          # GB300 non-tensor fp64 rate: 2 FMA lanes per SM per clock
 
@@ -91,6 +124,11 @@ def parse():
     ap.add_argument("--az-form", choices=["auto", "stencil", "residual"], default="auto",
                     help="how the stencil sweep forms A z: the full 7-point stencil, or "
                          "r + (A - M) z from the preconditioner sweep's M z = r")
+    ap.add_argument("--preconditioner", choices=["line", "multigrid"], default="line",
+                    help="column (line) solve of eq. (19), or one V-cycle of tensor-product "
+                         "multigrid with it as smoother")
+    ap.add_argument("--mg-levels", type=int, default=0,
+                    help="multigrid levels at most (0: coarsen while nx and ny are even)")
     ap.add_argument("--grid", type=int, nargs=3, metavar=("NX", "NY", "NZ"),
                     help="same coefficients on another grid size (profiling captures)")
     return ap.parse_args()
@@ -250,12 +288,14 @@ def oracle_rhs(w, h, ah, vec):
     return oracle.apply_A(prob, vec)
 
 
-def cpu_oracle_sample(w, h, ah, b, iters):
-    """The oracle as it stands on the full grid, `iters` fixed iterations."""
+def cpu_oracle_sample(w, h, ah, b, iters, multigrid=False):
+    """The oracle as it stands on the full grid, `iters` fixed iterations
+    (with the multigrid preconditioner: the oracle's MG-PCG)."""
     import oracle
     prob = oracle.Problem(w.nx, w.ny, w.nz, ah=ah, a_v=w.a_v, mass=w.mass, h=h)
     t0 = time.perf_counter()
-    _, it, _, _ = oracle.pcg(prob, b, rtol=0.0, maxit=iters)
+    solve = oracle.mg_pcg if multigrid else oracle.pcg
+    _, it, _, _ = solve(prob, b, rtol=0.0, maxit=iters)
     dt = time.perf_counter() - t0
     return it, dt
 
@@ -318,6 +358,10 @@ def run_ours(args, w):
     solver.set_factors(args.factors)
     solver.set_substructuring(args.substructuring)
     solver.set_az_form(args.az_form)
+    mgrid = args.preconditioner == "multigrid"
+    if mgrid:
+        solver.set_multigrid(1, 0.8, args.mg_levels)
+        solver.set_preconditioner("multigrid")
     az_form = solver.az_form
     recompute = args.factors == "recompute" and varying and args.layout == "tiled"
 
@@ -401,6 +445,10 @@ def run_ours(args, w):
                       else (OPS_SPMV[key], BYTES_SPMV[key]))
     ops_m, bytes_m = ((OPS_PRECOND_RECOMPUTE, BYTES_PRECOND_RECOMPUTE) if recompute
                       else (OPS_PRECOND, BYTES_PRECOND[varying]))
+    if mgrid:  # the preconditioner step is one V-cycle (the stored factors)
+        key = (args.layout, varying, "stencil")
+        ops_a, bytes_a = OPS_SPMV[key], BYTES_SPMV[key]
+        ops_m, bytes_m = mg_vcycle_cost(w.nx, w.ny, w.nz, solver.multigrid_levels, 1, varying)
     bytes_iter = (bytes_a + bytes_m) * n
     ops_iter = (ops_a + ops_m) * n
     hbm_gbs = bytes_iter * (total_iters / world) / (ms_max * 1e-3) / 1e9
@@ -422,7 +470,8 @@ def run_ours(args, w):
     hbm_ach = bytes_cell * n / avg_s / 1e9
     traffic = measured_traffic(dom, n, args.layout, args.factors, az_form)
     roofline = {
-        "bound": "alu", "kernel": dom, "achieved": alu_ach, "peak": alu_peak,
+        "bound": "alu", "kernel": "mg_vcycle" if (mgrid and dom == "precond_fused") else dom,
+        "achieved": alu_ach, "peak": alu_peak,
         "unit": "G fp64 ops/s", "frac": alu_ach / alu_peak, "traffic": traffic,
         "peak_source": "derived: %.0f fp64 lanes/SM/clk x %d SMs x %.0f MHz (median under load)"
                        % (FP64_LANES_PER_SM_CLK, nsm, sm_mhz),
@@ -475,12 +524,14 @@ def run_ours(args, w):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        it_c, dt_c = cpu_oracle_sample(w, h, ah, oracle_rhs(w, h, ah, vec), args.cpu_iters)
+        mgi = max(1, args.cpu_iters // 2) if mgrid else args.cpu_iters
+        it_c, dt_c = cpu_oracle_sample(w, h, ah, oracle_rhs(w, h, ah, vec), mgi, mgrid)
         cpu = {"value": it_c / dt_c, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": "oracle_pcg on the full %dx%dx%d grid, %d fixed PCG iterations "
+               "sample": "%s on the full %dx%dx%d grid, %d fixed PCG iterations "
                          "(initial residual and first preconditioner solve included), "
-                         "sequential C, 1 thread, %.1f s" % (w.nx, w.ny, w.nz, args.cpu_iters,
-                                                            dt_c)}
+                         "sequential C, 1 thread, %.1f s"
+                         % ("oracle_mg_pcg" if mgrid else "oracle_pcg", w.nx, w.ny, w.nz, mgi,
+                            dt_c)}
 
     if rank == 0:
         line = {
@@ -497,6 +548,9 @@ def run_ours(args, w):
                               % (8e-6 * n)),
                        "layout": args.layout, "factors": args.factors,
                        "substructuring": solver.substructuring, "az_form": az_form,
+                       "preconditioner": args.preconditioner,
+                       "multigrid": ({"levels": solver.multigrid_levels, "nu": 1, "omega": 0.8}
+                                     if mgrid else None),
                        "parallelism": "replicas" if world > 1 else "single"},
             "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / hbm_peak,
             "bytes_per_cell_iter": bytes_iter / n, "fp64_ops_per_cell_iter": ops_iter / n,

@@ -75,8 +75,9 @@ struct pcg_ctx {
   double *mg_x0 = nullptr, *mg_y0 = nullptr;
   int mg_grid_first = 1, mg_grid_smooth = 1;
   int mg_launches = 0;
-  // host copies of the coefficients, from which the coarse levels are built
-  std::vector<double> ah_host, dz_host;
+  // host copies of the scalar coefficients, from which the coarse levels'
+  // tables are built (a_h is averaged on the device)
+  std::vector<double> dz_host;
   double a_h_host = 0.0, a_v_host = 0.0, mass_host = 0.0;
   int grid_ps = 0;                   // blocks of the persistent loop (0: not available)
   unsigned int test_absent = 0;      // test hook: arrivals the persistent barriers miss
@@ -359,8 +360,10 @@ int mg_allocate(pcg_ctx* ctx) {
   return PCG_OK;
 }
 
-// Coarse level tables for the current coefficients (host copies), and the
-// grids of the Thomas sweeps on every level.  Synchronous.
+// Coarse level tables for the current coefficients, and the grids of the
+// Thomas sweeps on every level.  The per-level tables come from the host
+// copies of the scalar coefficients; a_h is averaged level by level on the
+// device.  Synchronous (one wait, for the pivot check).
 int mg_setup(pcg_ctx* ctx) {
   const Op& f = ctx->op;
   const bool varying = f.varying != 0;
@@ -369,37 +372,27 @@ int mg_setup(pcg_ctx* ctx) {
   c.a_v = ctx->a_v_host;
   c.mass = ctx->mass_host;
   c.dz = ctx->dz_host.data();
-  std::vector<double> ah = ctx->ah_host, ahc;
-  int nx = f.nx;
   double area = 1.0;
   cudaError_t e = cudaMemsetAsync(&ctx->state->setup_error, 0, sizeof(int), ctx->stream);
   for (size_t l = 0; l < ctx->mg.size() && e == cudaSuccess; ++l) {
     pcg::MgLevel& m = ctx->mg[l];
     Op& o = m.op;
+    const Op& fine = l ? ctx->mg[l - 1].op : f;
     area *= 4.0;
     o.varying = varying ? 1 : 0;
     std::vector<double> lev;
     int st = build_levels(ctx, f.nz, &c, varying, lev, area);
     if (st) return st;
-    e = cudaMemcpy(m.lev, lev.data(), lev.size() * sizeof(double), cudaMemcpyHostToDevice);
+    // (a pageable source: the call returns once the table is staged)
+    e = cudaMemcpyAsync(m.lev, lev.data(), lev.size() * sizeof(double), cudaMemcpyHostToDevice,
+                        ctx->stream);
     if (e == cudaSuccess && varying) {
-      // a_h of the merged columns: the mean of the four, level by level
-      const int nxc = nx / 2;
-      ahc.assign((size_t)o.ncols, 0.0);
-      for (long long J = 0; J < o.ny; ++J)
-        for (int I = 0; I < nxc; ++I) {
-          const double s = ah[(2 * J) * nx + 2 * I] + ah[(2 * J) * nx + 2 * I + 1] +
-                           ah[(2 * J + 1) * nx + 2 * I] + ah[(2 * J + 1) * nx + 2 * I + 1];
-          ahc[J * nxc + I] = 0.25 * s;
-        }
-      ah.swap(ahc);
-      e = cudaMemcpy(m.ah, ah.data(), o.ncols * sizeof(double), cudaMemcpyHostToDevice);
+      e = pcg::launch_mg_coarse_ah(fine, o, fine.ah, m.ah, ctx->num_sms, ctx->stream);
       if (e == cudaSuccess) e = pcg::launch_face_coeffs(o, m.faceE, m.faceN, ctx->stream);
       if (e == cudaSuccess)
         e = pcg::launch_column_setup(o, ctx->state, m.cdiag, m.cdiag_t, m.cwE_t, m.cwN_t,
                                      m.tnphi, m.tinvd, ctx->stream);
     }
-    nx /= 2;
     m.grid_first = pcg::grid_mg_first(o, ctx->num_sms);
     m.grid_smooth = pcg::grid_mg_smooth(o, ctx->num_sms);
   }
@@ -451,18 +444,18 @@ cudaError_t mg_enqueue(pcg_ctx* ctx, const Op& op0, double* b0, double* out, boo
     double* c = lvl_x(l);
     double* other = lvl_y(l);
     e = pcg::launch_mg_first(o, st, lvl_b(l), ctx->q, c, w, fused && l == 0, ctx->partials,
-                             g_first(l), s);
+                             ctx->hist, g_first(l), s);
     ++cnt;
     for (int i = 1; i < nu && e == cudaSuccess; ++i) {
       e = pcg::launch_mg_smooth(o, st, lvl_b(l), c, other, w, false, ctx->partials, ctx->hist,
-                                g_smooth(l), s);
-      ++cnt;
+                                g_smooth(l), ctx->num_sms, s);
+      cnt += 2;
       std::swap(c, other);
     }
     cur[l] = c;
     if (l + 1 < L && e == cudaSuccess) {
-      e = pcg::launch_mg_restrict(o, lvl_op(l + 1), st, lvl_b(l), c, lvl_b(l + 1), ctx->num_sms,
-                                  s);
+      e = pcg::launch_mg_restrict(o, lvl_op(l + 1), st, lvl_b(l), c, nu == 1, w, lvl_b(l + 1),
+                                  ctx->num_sms, s);
       ++cnt;
     }
   }
@@ -478,8 +471,8 @@ cudaError_t mg_enqueue(pcg_ctx* ctx, const Op& op0, double* b0, double* out, boo
       const bool last = (i == nu - 1);
       double* dst = (l == 0 && last) ? out : other;
       e = pcg::launch_mg_smooth(o, st, lvl_b(l), c, dst, w, fused && l == 0 && last,
-                                ctx->partials, ctx->hist, g_smooth(l), s);
-      ++cnt;
+                                ctx->partials, ctx->hist, g_smooth(l), ctx->num_sms, s);
+      cnt += 2;
       other = c;
       c = dst;
     }
@@ -500,10 +493,6 @@ int load_coeffs(pcg_ctx* ctx, const pcg_coeffs* c, bool varying) {
   ctx->mass_host = c->mass;
   ctx->dz_host.assign((size_t)ctx->op.nz, 1.0);
   if (c->dz) ctx->dz_host.assign(c->dz, c->dz + ctx->op.nz);
-  if (varying)
-    ctx->ah_host.assign(c->a_h_field, c->a_h_field + ctx->op.ncols);
-  else
-    ctx->ah_host.clear();
   cudaError_t e = cudaMemcpyAsync(ctx->lev, lev.data(), lev.size() * sizeof(double),
                                   cudaMemcpyHostToDevice, ctx->stream);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "upload of the level table");

@@ -189,22 +189,30 @@ struct MgLevel {
   int grid_first = 1, grid_smooth = 1;              // blocks of the two Thomas sweeps
 };
 // x = omega M^{-1} b.  fused (finest level inside the solve): first b <- b -
-// alpha q with alpha from the device state and ||b||^2 into st->mg_R.
+// alpha q with alpha from the device state and ||b||^2 into st->mg_R; if the
+// stopping test passes on it, the scalar step is taken (hist) and the rest of
+// the cycle is skipped.
 cudaError_t launch_mg_first(const Op& op, DevState* st, double* b, const double* q, double* x,
-                            double omega, bool fused, double* partials, int grid,
+                            double omega, bool fused, double* partials, double* hist, int grid,
                             cudaStream_t s);
 // bc = R (b - A x): per layer, the residuals of the 2x2 fine columns summed.
+// first: x = omega M^{-1} b exactly as launch_mg_first left it, so that
+// b - A x = (1 - omega) b - (A - M) x.
 cudaError_t launch_mg_restrict(const Op& fine, const Op& coarse, const DevState* st,
-                               const double* b, const double* x, double* bc, int num_sms,
-                               cudaStream_t s);
+                               const double* b, const double* x, bool first, double omega,
+                               double* bc, int num_sms, cudaStream_t s);
 // x += P e: every fine column gets its coarse column's value.
 cudaError_t launch_mg_prolong(const Op& fine, const Op& coarse, const DevState* st, double* x,
                               const double* e, int num_sms, cudaStream_t s);
-// xout = xin + omega M^{-1} (b - A xin).  fused (finest level, last step):
+// xout = xin + omega M^{-1} (b - A xin), two launches: the residual into
+// xout, then the column solves in place.  fused (finest level, last step):
 // <b, xout> reduced and the scalar step of Algorithm 1 taken with st->mg_R.
 cudaError_t launch_mg_smooth(const Op& op, DevState* st, const double* b, const double* xin,
                              double* xout, double omega, bool fused, double* partials,
-                             double* hist, int grid, cudaStream_t s);
+                             double* hist, int grid, int num_sms, cudaStream_t s);
+// a_h of a coarse level from the finer one (the mean of the 4 merged columns).
+cudaError_t launch_mg_coarse_ah(const Op& fine, const Op& coarse, const double* ahf, double* ahc,
+                                int num_sms, cudaStream_t s);
 int grid_mg_first(const Op& op, int num_sms);
 int grid_mg_smooth(const Op& op, int num_sms);
 
