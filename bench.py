@@ -96,6 +96,8 @@ def mg_vcycle_cost(nx, ny, nz, levels, nu, varying):
 
 
 L2_BYTES = 129e6                     # GB300 L2
+NOMINAL_HBM_GBS = 8000.0             # the ~8 TB/s HBM3e figure the fraction is also quoted on
+FUSED_MIN_BYTES = 88                 # u, p, z, q read + u, p, q written; r, q read + r, z written
 FP64_LANES_PER_SM_CLK = 2.0          # GB300 non-tensor fp64 rate: 2 FMA lanes per SM per clock
 
 
@@ -481,6 +483,19 @@ def run_ours(args, w):
         "hbm_frac": hbm_ach / hbm_peak, "hbm_peak_source": peak_src,
     }
     kernels = {k: {"ms": v[0], "launches": v[1]} for k, v in ktimes.items() if v[1]}
+    # the iteration loop alone (both sweeps, or the persistent loop), per
+    # solve, and the bandwidth it implies at the fused minimum of 88 B/cell
+    # per iteration (u, p, z, q, r moved once, no per-cell coefficients)
+    loop_ms = sum(ktimes[k][0] for k in ("precond_fused", "spmv_fused", "loop")) / args.steps
+    iters_solve = total_iters / world / args.steps
+    loop_stats = {
+        "ms_per_solve": loop_ms, "iters_per_solve": iters_solve,
+        "ms_per_iter": loop_ms / max(iters_solve, 1),
+        "algorithmic_gbs": bytes_iter * iters_solve / (loop_ms * 1e-3) / 1e9,
+        "fused_min_gbs": FUSED_MIN_BYTES * n * iters_solve / (loop_ms * 1e-3) / 1e9,
+    }
+    loop_stats["algorithmic_frac"] = loop_stats["algorithmic_gbs"] / hbm_peak
+    loop_stats["fused_min_frac_nominal_8tbs"] = loop_stats["fused_min_gbs"] / NOMINAL_HBM_GBS
     # DRAM bytes of one iteration (both sweeps, from the committed ncu captures)
     # against the fused minimum of 88 B/cell (u, p, z, q, r moved once, no
     # per-cell coefficients) and against this build's algorithmic bytes
@@ -553,6 +568,8 @@ def run_ours(args, w):
                                      if mgrid else None),
                        "parallelism": "replicas" if world > 1 else "single"},
             "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / hbm_peak,
+            "hbm_frac_nominal_8tbs": hbm_gbs / NOMINAL_HBM_GBS,
+            "loop": loop_stats,
             "bytes_per_cell_iter": bytes_iter / n, "fp64_ops_per_cell_iter": ops_iter / n,
             "dram_per_iter": dram_iter, "standalone": standalone,
             "roofline": roofline, "kernels": kernels, "clocks": clk, "e2e": e2e,
