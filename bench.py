@@ -65,14 +65,14 @@ OPS_PRECOND_RECOMPUTE, BYTES_PRECOND_RECOMPUTE = 12, 32
 # Multigrid V-cycle (--preconditioner multigrid), per cell of the level a
 # kernel runs on: fp64 operations and algorithmic bytes with an a_h field
 # (constant a_h: no per-cell diagonal, weights or factors), from the kernel
-# sources.  first: x = omega M^-1 b (finest level: also r -= alpha q, ||r||^2
-# and the <r, M^-1 r> accumulation of the shared Thomas body); smooth: residual
+# sources.  first: x = omega M^-1 b (finest level: also r -= alpha q and
+# ||r||^2); smooth: residual
 # stencil, Thomas, x + omega z (finest level's last step: also <r, z>);
 # restrict: the fine residual and 3 adds per 4 fine cells, per fine cell;
 # prolong: one add per fine cell.
 # restrict after one smoothing step from zero (nu = 1) takes the residual from
 # the horizontal terms alone: 5 operations and 3 adds per 4 fine cells.
-MG_OPS = {"first_fused": 7, "first": 4, "smooth": 12, "smooth_fused": 13, "restrict": 8.75,
+MG_OPS = {"first_fused": 6, "first": 4, "smooth": 12, "smooth_fused": 13, "restrict": 8.75,
           "restrict_first": 5.75, "prolong": 1}
 MG_BYTES = {True: {"first_fused": 48, "first": 32, "smooth": 64, "smooth_fused": 64,
                    "restrict": 42, "restrict_first": 34, "prolong": 18},

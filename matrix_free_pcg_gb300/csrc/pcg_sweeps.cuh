@@ -29,7 +29,8 @@ __device__ __forceinline__ long long tiled_base(long long col, int nz) {
 // column: accumulates r*.r* and <r*, z> into accR, accK (FUSED).  COHERENT:
 // q was written by other blocks of the same launch (the persistent loop), so
 // it is read from L2, past the SM's non-coherent L1.  SCALE: z is stored as
-// zscale * M^{-1} r (the damped line relaxation of the multigrid smoother).
+// zscale * M^{-1} r (the damped line relaxation of the multigrid smoother),
+// and <r*, z> is not accumulated (the smoother's caller reduces its own).
 template <bool VARY, bool FUSED, bool COHERENT = false, bool SCALE = false>
 __device__ __forceinline__ void precond_tile(const Op& op, long long t, int lane,
                                              double* __restrict__ r, const double* __restrict__ q,
@@ -82,7 +83,7 @@ __device__ __forceinline__ void precond_tile(const Op& op, long long t, int lane
         }
         y = fma(nprev, y, rk);
         w = y * ci[j];
-        if (FUSED) accK = fma(y, w, accK);
+        if (FUSED && !SCALE) accK = fma(y, w, accK);
         st_hint(zt + k * kTile, w, keep);
         nprev = cn[j];
       }
