@@ -17,9 +17,13 @@
 namespace pcg {
 namespace {
 
-// Preconditioner sweep: threads per block and levels per register chunk.
+// Preconditioner sweep: threads per block and levels per register chunk, of
+// the forward pass (4 operands per level) and of the backward pass with
+// per-cell factors (2 per level, one dependent fma: it needs twice the lead
+// to cover an L2 round trip, in the registers the forward pass frees).
 constexpr int kTmThreads = kTmWarpsPerBlock * 32;
 constexpr int kTmChunk = 8;
+constexpr int kTmChunkB = 16;
 
 __device__ __forceinline__ long long tiled_base(long long col, int nz) {
   return (col >> 5) * (long long)nz * kTile + (col & 31);
@@ -96,28 +100,31 @@ __device__ __forceinline__ void precond_tile(const Op& op, long long t, int lane
       cn[j] = nn[j];
     }
   }
-  // ---- backward: z_{nz-1} = w_{nz-1} (in place); level k uses nphi_k.
-  // Chunk b holds levels kb, kb-1, ..., kb-kTmChunk+1 with kb = nz-2-b*kTmChunk.
+  // ---- backward: z_{nz-1} = w_{nz-1} (in place); level k uses nphi_k.  With a
+  // constant a_h the factors come from the per-level table and the longer
+  // chunk costs registers (218 against 167): 8 levels there.
+  constexpr int CB = VARY ? kTmChunkB : kTmChunk;
+  // Chunk b holds levels kb, kb-1, ..., kb-CB+1 with kb = nz-2-b*CB.
   double zz = w;
   if (SCALE) st_hint(zt + (long long)(nz - 1) * kTile, w * zscale, stream);
-  double bw[kTmChunk], bn[kTmChunk];
+  double bw[CB], bn[CB];
 #pragma unroll
-  for (int j = 0; j < kTmChunk; ++j) {
+  for (int j = 0; j < CB; ++j) {
     const int k = nz - 2 - j;
     bw[j] = (k >= 0) ? ld_hint(zt + k * kTile, stream) : 0.0;
     bn[j] = (k >= 0) ? (VARY ? ld_hint(fn + k * fs, stream) : __ldg(fn + k)) : 0.0;
   }
 #pragma unroll 1
-  for (int kb = nz - 2; kb >= 0; kb -= kTmChunk) {
-    double nw[kTmChunk], nb[kTmChunk];
+  for (int kb = nz - 2; kb >= 0; kb -= CB) {
+    double nw[CB], nb[CB];
 #pragma unroll
-    for (int j = 0; j < kTmChunk; ++j) {
-      const int k = kb - kTmChunk - j;
+    for (int j = 0; j < CB; ++j) {
+      const int k = kb - CB - j;
       nw[j] = (k >= 0) ? ld_hint(zt + k * kTile, stream) : 0.0;
       nb[j] = (k >= 0) ? (VARY ? ld_hint(fn + k * fs, stream) : __ldg(fn + k)) : 0.0;
     }
 #pragma unroll
-    for (int j = 0; j < kTmChunk; ++j) {
+    for (int j = 0; j < CB; ++j) {
       const int k = kb - j;
       if (k >= 0) {
         zz = fma(bn[j], zz, bw[j]);
@@ -125,7 +132,7 @@ __device__ __forceinline__ void precond_tile(const Op& op, long long t, int lane
       }
     }
 #pragma unroll
-    for (int j = 0; j < kTmChunk; ++j) {
+    for (int j = 0; j < CB; ++j) {
       bw[j] = nw[j];
       bn[j] = nb[j];
     }
