@@ -711,20 +711,14 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
   const bool split = tiled && ctx->split_p > 1 && !mgrid;
   const int grid_pm = split ? ctx->grid_sp : ctx->grid_tm;  // preconditioner sweep blocks
   op.nscratch = ctx->nscratch;
-  // The row-tiled layout forms r = b - A x0 column-contiguously in z, then
-  // converts r and x0 into the solver's layout.
+  // r = b - A x0, the solver's start; the row-tiled layout writes r, u = x0
+  // and p = q = 0 at its own positions in the same launch.
   e = timed(ctx, PCG_K_RESIDUAL, [&] {
-    // (the row-tiled layout clears p and q at its own positions in the conversion below)
-    return pcg::launch_residual(op, ctx->state, b, x, tiled ? ctx->z : ctx->r,
-                                tiled ? nullptr : ctx->p, tiled ? nullptr : ctx->q, rtol, maxit,
-                                ctx->grid_a, s);
+    return tiled ? pcg::launch_residual_tiled(op, ctx->state, b, x, ctx->r, ctx->u_t, ctx->p,
+                                              ctx->q, rtol, maxit, s)
+                 : pcg::launch_residual(op, ctx->state, b, x, ctx->r, ctx->p, ctx->q, rtol,
+                                        maxit, ctx->grid_a, s);
   });
-  if (e == cudaSuccess && tiled) {
-    e = timed(ctx, PCG_K_RESIDUAL, [&] { return pcg::launch_to_tiled(op, ctx->z, ctx->r, s); });
-    if (e == cudaSuccess)  // x0 -> u, and p = q = 0 at the row-tiled positions
-      e = timed(ctx, PCG_K_RESIDUAL,
-                [&] { return pcg::launch_to_tiled(op, x, ctx->u_t, s, ctx->p, ctx->q); });
-  }
   if (e != cudaSuccess) return cuda_fail(ctx, e, "residual kernel launch");
 
   // Persistent loop: every iteration in one cooperative kernel.

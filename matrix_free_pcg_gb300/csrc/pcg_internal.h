@@ -106,6 +106,12 @@ cudaError_t launch_column_setup(const Op& op, DevState* st, double* cdiag, doubl
 cudaError_t launch_residual(const Op& op, DevState* st, const double* b, const double* x,
                             double* r, double* p, double* q, double rtol, int maxit, int grid,
                             cudaStream_t s);
+// The same for the row-tiled solver layout, in one launch: r_t = b - A x0,
+// u_t = x0 and p_t = q_t = 0 at the row-tiled positions (b and x0 in the
+// caller's column-contiguous layout).
+cudaError_t launch_residual_tiled(const Op& op, DevState* st, const double* b, const double* x,
+                                  double* r_t, double* u_t, double* p_t, double* q_t, double rtol,
+                                  int maxit, cudaStream_t s);
 // y = A x
 cudaError_t launch_apply(const Op& op, const double* x, double* y, int grid, cudaStream_t s);
 // z = M^{-1} r  (st receives dev_error if a bounded wait runs out)

@@ -885,6 +885,79 @@ __global__ void __launch_bounds__(kSpmvThreads) k_stencil(Op op, DevState* st,
   }
 }
 
+// Start of a solve in the row-tiled layout, one kernel: r = b - A x0 from the
+// caller's column-contiguous b and x0, written row-tiled together with u = x0
+// and p = q = 0, and the scalar state of a new solve (as k_stencil MODE 1).
+// A block takes one tile of 32 columns and 32 levels: it reads along k
+// (coalesced in the caller's layout), turns the 32 x 32 patch around in
+// shared memory, and writes along the columns (coalesced in the solver's).
+// Where x0 is +0.0 at a cell and at every point its stencil reads, r = b
+// exactly and no fp64 work is done (the common zero initial guess).
+template <bool VARY>
+__global__ void __launch_bounds__(256) k_residual_tiled(Op op, DevState* st,
+                                                        const double* __restrict__ x,
+                                                        const double* __restrict__ b,
+                                                        double* __restrict__ r_t,
+                                                        double* __restrict__ u_t,
+                                                        double* __restrict__ p_t,
+                                                        double* __restrict__ q_t, double rtol,
+                                                        int maxit) {
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    st->alpha = 0.0;
+    st->beta = 0.0;
+    st->kappa_old = 1.0;
+    st->R0 = 0.0;
+    st->rtol = rtol;
+    st->last_sigma = st->last_kappa = st->last_R = 0.0;
+    st->it = 0;
+    st->status = kStOK;
+    st->iters = 0;
+    st->maxit = maxit;
+    st->ticket_m = 0u;
+    st->ticket_a = 0u;
+    st->bar_count = 0u;
+    st->bar_gen = 0u;
+    st->dev_error = 0;
+    st->done = 0;
+  }
+  __shared__ double sr[kTile][kTile + 1], sx[kTile][kTile + 1];
+  const int nz = op.nz;
+  const long long t = blockIdx.x;
+  const int k0 = blockIdx.y * kTile;
+  const int lane = threadIdx.x & 31, row = threadIdx.x >> 5;  // 8 rows of 32 threads
+#pragma unroll
+  for (int pass = 0; pass < kTile / 8; ++pass) {
+    const int cl = row + 8 * pass, k = k0 + lane;
+    const long long col = t * kTile + cl;
+    double rv = 0.0, xv = 0.0;
+    if (col < op.ncols && k < nz) {
+      const long long l = col * nz + k;
+      xv = x[l];
+      const Nbr nb = neighbours(op, col);
+      unsigned long long bits = __double_as_longlong(xv);
+      if (k > 0) bits |= __double_as_longlong(x[l - 1]);
+      if (k + 1 < nz) bits |= __double_as_longlong(x[l + 1]);
+      bits |= __double_as_longlong(x[nb.e * nz + k]) | __double_as_longlong(x[nb.w * nz + k]) |
+              __double_as_longlong(x[nb.n * nz + k]) | __double_as_longlong(x[nb.s * nz + k]);
+      rv = (bits == 0ull) ? b[l] : b[l] - stencil1<VARY>(op, x, l, col, k, 0.0, xv);
+    }
+    sr[lane][cl] = rv;
+    sx[lane][cl] = xv;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int pass = 0; pass < kTile / 8; ++pass) {
+    const int kk = row + 8 * pass, k = k0 + kk;
+    if (k < nz) {
+      const long long o = (t * nz + k) * kTile + lane;
+      r_t[o] = sr[kk][lane];
+      u_t[o] = sx[kk][lane];
+      p_t[o] = 0.0;
+      q_t[o] = 0.0;
+    }
+  }
+}
+
 template <bool VEC2>
 __global__ void __launch_bounds__(kSpmvThreads) k_finalize(Op op, const DevState* st,
                                                            double* __restrict__ x,
@@ -1104,6 +1177,17 @@ cudaError_t launch_residual(const Op& op, DevState* st, const double* b, const d
     if (v2) k_stencil<false, true, 1><<<grid, kSpmvThreads, 0, s>>>(op, st, x, b, r, p, q, rtol, maxit);
     else k_stencil<false, false, 1><<<grid, kSpmvThreads, 0, s>>>(op, st, x, b, r, p, q, rtol, maxit);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_residual_tiled(const Op& op, DevState* st, const double* b, const double* x,
+                                  double* r_t, double* u_t, double* p_t, double* q_t, double rtol,
+                                  int maxit, cudaStream_t s) {
+  const dim3 g((unsigned)op.ntiles, (unsigned)((op.nz + kTile - 1) / kTile));
+  if (op.varying)
+    k_residual_tiled<true><<<g, 256, 0, s>>>(op, st, x, b, r_t, u_t, p_t, q_t, rtol, maxit);
+  else
+    k_residual_tiled<false><<<g, 256, 0, s>>>(op, st, x, b, r_t, u_t, p_t, q_t, rtol, maxit);
   return cudaGetLastError();
 }
 

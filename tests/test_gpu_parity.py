@@ -271,8 +271,9 @@ def test_kernel_timing_counts_launches(layout):
         it, _, _ = s.solve(bd, x, rtol=1e-10)
         t = s.kernel_times()
         info = s.launch_info()
-    # the row-tiled solve also converts r and x0 into its layout
-    assert t["residual"][1] == (1 if layout == "column" else 3) and t["finalize"][1] == 1
+    # one residual launch in either layout (the row-tiled one writes r, x0, p
+    # and q at its own positions in it)
+    assert t["residual"][1] == 1 and t["finalize"][1] == 1
     assert t["precond_fused"][1] >= it + 1 and t["spmv_fused"][1] >= it
     # sweeps enqueued after convergence return at once and are launched but
     # not timed: at most two polling batches of 16 iterations
@@ -589,7 +590,7 @@ def test_persistent_loop_choice_and_timing():
         t = s.kernel_times()
         assert st == mf.PCG_OK and t["loop"][1] == 1 and t["loop"][0] > 0
         assert t["precond_fused"][1] == 0 and t["spmv_fused"][1] == 0
-        assert s.launch_info()["last_solve_launches"] == 5   # residual, 2 conversions, loop, final
+        assert s.launch_info()["last_solve_launches"] == 3   # residual, loop, final update
 
 
 @pytest.mark.parametrize("cfg", SOLVE_CASES, ids=lambda c: "x".join(map(str, c[:3])))
