@@ -42,17 +42,19 @@ UNIT = "iters/s"
 # form of A z).  "stencil": the full 7-point stencil (the row-tiled sweep of an
 # a_h field reads per-cell horizontal weights: 4 FMAs instead of 5
 # operations).  "residual": A z = r + (A - M) z, the four horizontal terms
-# alone (row-tiled layout).
+# alone (the column layout weights its face values: one product more).
 OPS_SPMV = {("tiled", True, "stencil"): 11, ("tiled", False, "stencil"): 11,
             ("column", True, "stencil"): 12, ("column", False, "stencil"): 11,
-            ("tiled", True, "residual"): 8, ("tiled", False, "residual"): 8}
+            ("tiled", True, "residual"): 8, ("tiled", False, "residual"): 8,
+            ("column", True, "residual"): 9, ("column", False, "residual"): 8}
 OPS_PRECOND = 6
 # Algorithmic bytes per cell: vectors read/written once per sweep.
 # u,p,z,q (+ per-cell diagonal, + 2 per-cell weights in the row-tiled layout)
 # read, or u,p,z,q,r (+ 2 weights) for the residual form; u,p,q written
 BYTES_SPMV = {("tiled", True, "stencil"): 80, ("tiled", False, "stencil"): 56,
               ("column", True, "stencil"): 64, ("column", False, "stencil"): 56,
-              ("tiled", True, "residual"): 80, ("tiled", False, "residual"): 64}
+              ("tiled", True, "residual"): 80, ("tiled", False, "residual"): 64,
+              ("column", True, "residual"): 64, ("column", False, "residual"): 64}
 BYTES_PRECOND = {True: 48, False: 32}  # r,q (+ 2 per-cell Thomas factors) read; r,z written
 # With the factors of an a_h field rebuilt in every sweep (--factors recompute):
 # the stencil sweep forms the four horizontal weights (and, in the stencil

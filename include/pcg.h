@@ -181,7 +181,7 @@ int pcg_set_loop(pcg_ctx* ctx, int mode);
 int pcg_get_loop(const pcg_ctx* ctx, int* mode_out);
 
 /* How the stencil sweep of pcg_solve forms A z (Appendix A, Algorithm 2:
- * q = A z + beta q), in the row-tiled layout:
+ * q = A z + beta q):
  *   PCG_AZ_STENCIL   the full 7-point stencil of eq. (18), as the paper's
  *                    sweep computes it: 7 fp64 operations per cell for A z;
  *   PCG_AZ_RESIDUAL  A z = r + (A - M) z.  The preconditioner sweep of the
@@ -194,9 +194,10 @@ int pcg_get_loop(const pcg_ctx* ctx, int* mode_out);
  *                    solve's backward error, of the same order (eps |A||z|)
  *                    as the stencil's own rounding;
  *   PCG_AZ_AUTO      (default) RESIDUAL wherever it applies.
- * RESIDUAL needs the row-tiled layout and Thomas column solves (no
- * substructuring); elsewhere the full stencil runs.  pcg_apply_A always
- * evaluates the full stencil.  Errors: PCG_EINVAL (unknown form). */
+ * RESIDUAL needs Thomas column solves (no substructuring, and the line
+ * preconditioner); elsewhere the full stencil runs.  Both layouts have both
+ * forms.  pcg_apply_A always evaluates the full stencil.  Errors: PCG_EINVAL
+ * (unknown form). */
 enum { PCG_AZ_AUTO = 0, PCG_AZ_STENCIL = 1, PCG_AZ_RESIDUAL = 2 };
 int pcg_set_az_form(pcg_ctx* ctx, int form);
 

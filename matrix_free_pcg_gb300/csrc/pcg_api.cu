@@ -609,11 +609,11 @@ int resolved_loop(const pcg_ctx* ctx) {
 }
 
 // The form of A z that the next solve's stencil sweeps use (PCG_AZ_STENCIL
-// or PCG_AZ_RESIDUAL): the residual form needs the row-tiled layout and the
-// Thomas column solve, whose z the sweep pairs with r.
+// or PCG_AZ_RESIDUAL): the residual form needs the Thomas column solve, whose
+// z the sweep pairs with r (no substructuring, no multigrid).
 int resolved_az(const pcg_ctx* ctx) {
-  const bool eligible = ctx->layout == PCG_LAYOUT_TILED && ctx->split_p == 1 &&
-                        ctx->prec == PCG_PREC_LINE;
+  const bool split = ctx->layout == PCG_LAYOUT_TILED && ctx->split_p > 1;
+  const bool eligible = !split && ctx->prec == PCG_PREC_LINE;
   return (eligible && ctx->az_req != PCG_AZ_STENCIL) ? PCG_AZ_RESIDUAL : PCG_AZ_STENCIL;
 }
 
@@ -800,8 +800,9 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
           return tiled ? pcg::launch_spmv_tiled(op, ctx->state, ctx->z, ctx->r, ctx->u_t, ctx->p,
                                                 ctx->q,
                                                 ctx->partials + 2 * grid_pm, ctx->grid_ta, s)
-                       : pcg::launch_spmv_fused(op, ctx->state, ctx->z, x, ctx->p, ctx->q,
-                                                ctx->partials + 2 * ctx->grid_m, ctx->grid_a, s);
+                       : pcg::launch_spmv_fused(op, ctx->state, ctx->z, ctx->r, x, ctx->p,
+                                                ctx->q, ctx->partials + 2 * ctx->grid_m,
+                                                ctx->grid_a, s);
         });
         if (e != cudaSuccess) return cuda_fail(ctx, e, "SpMV sweep launch");
       }

@@ -121,9 +121,11 @@ cudaError_t launch_precond(const Op& op, DevState* st, const double* r, double* 
 cudaError_t launch_precond_fused(const Op& op, DevState* st, double* r, const double* q,
                                  double* z, double* partials, double* hist, int grid,
                                  cudaStream_t s);
-// Algorithm 2 sweep
-cudaError_t launch_spmv_fused(const Op& op, DevState* st, const double* z, double* u,
-                              double* p, double* q, double* partials, int grid, cudaStream_t s);
+// Algorithm 2 sweep (with op.az_resid: A z from r, the residual M z = r was
+// solved for)
+cudaError_t launch_spmv_fused(const Op& op, DevState* st, const double* z, const double* r,
+                              double* u, double* p, double* q, double* partials, int grid,
+                              cudaStream_t s);
 // x += alpha p (the update deferred past the last sweep)
 cudaError_t launch_finalize(const Op& op, const DevState* st, double* x, const double* p,
                             int grid, cudaStream_t s);

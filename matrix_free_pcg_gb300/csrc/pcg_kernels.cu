@@ -729,13 +729,69 @@ __global__ void __launch_bounds__(kTile) k_precond_direct(Op op, DevState* st,
   }
 }
 
+// acc + ((A - M) z) at the two cells l, l+1 of one column: the horizontal
+// neighbour terms alone (M, eq. (19), holds A's diagonal and vertical
+// couplings).  acc = r + beta q turns it into A z + beta q for the z of
+// M z = r (the residual form of the stencil sweep).
+template <bool VARY>
+__device__ __forceinline__ double2 horizontal2(const Op& op, const double* __restrict__ z,
+                                               long long l, long long col, int k, double2 acc) {
+  const int nz = op.nz;
+  const double* __restrict__ lev = op.lev;
+  const Nbr nb = neighbours(op, col);
+  const double2 zE = ld2(z + nb.e * nz + k);
+  const double2 zW = ld2(z + nb.w * nz + k);
+  const double2 zN = ld2(z + nb.n * nz + k);
+  const double2 zS = ld2(z + nb.s * nz + k);
+  double h0, h1;
+  if (VARY) {
+    const double aE = __ldg(op.faceE + col), aW = __ldg(op.faceE + nb.w);
+    const double aN = __ldg(op.faceN + col), aS = __ldg(op.faceN + nb.s);
+    h0 = aE * zE.x;
+    h0 = fma(aW, zW.x, h0);
+    h0 = fma(aN, zN.x, h0);
+    h0 = fma(aS, zS.x, h0);
+    h1 = aE * zE.y;
+    h1 = fma(aW, zW.y, h1);
+    h1 = fma(aN, zN.y, h1);
+    h1 = fma(aS, zS.y, h1);
+  } else {
+    h0 = (zE.x + zW.x) + (zN.x + zS.x);
+    h1 = (zE.y + zW.y) + (zN.y + zS.y);
+  }
+  return make_double2(fma(__ldg(lev + LV_HW * nz + k), h0, acc.x),
+                      fma(__ldg(lev + LV_HW * nz + k + 1), h1, acc.y));
+}
+
+// acc + ((A - M) z) at one cell l.
+template <bool VARY>
+__device__ __forceinline__ double horizontal1(const Op& op, const double* __restrict__ z,
+                                              long long l, long long col, int k, double acc) {
+  const int nz = op.nz;
+  const Nbr nb = neighbours(op, col);
+  const double zE = z[nb.e * nz + k], zW = z[nb.w * nz + k];
+  const double zN = z[nb.n * nz + k], zS = z[nb.s * nz + k];
+  double hs;
+  if (VARY) {
+    hs = __ldg(op.faceE + col) * zE;
+    hs = fma(__ldg(op.faceE + nb.w), zW, hs);
+    hs = fma(__ldg(op.faceN + col), zN, hs);
+    hs = fma(__ldg(op.faceN + nb.s), zS, hs);
+  } else {
+    hs = (zE + zW) + (zN + zS);
+  }
+  return fma(__ldg(op.lev + LV_HW * nz + k), hs, acc);
+}
+
 // ----------------------------------------------------- stencil sweeps (K_A)
 
 // Algorithm 2: u += alpha p; p = z + beta p; q = A z + beta q; sigma = <p,q>;
-// then alpha = kappa_old / sigma in the last block.
-template <bool VARY, bool VEC2>
+// then alpha = kappa_old / sigma in the last block.  RESID: A z = r + (A - M) z
+// for the z of M z = r from the preconditioner sweep (horizontal terms only).
+template <bool VARY, bool VEC2, bool RESID>
 __global__ void __launch_bounds__(kSpmvThreads) k_spmv_fused(Op op, DevState* st,
                                                              const double* __restrict__ z,
+                                                             const double* __restrict__ r,
                                                              double* __restrict__ u,
                                                              double* __restrict__ p,
                                                              double* __restrict__ q,
@@ -759,8 +815,14 @@ __global__ void __launch_bounds__(kSpmvThreads) k_spmv_fused(Op op, DevState* st
       uc.y = fma(alpha, pc.y, uc.y);
       pc.x = fma(beta, pc.x, zc.x);
       pc.y = fma(beta, pc.y, zc.y);
-      const double2 qn =
-          stencil2<VARY>(op, z, l, col, k, make_double2(beta * qc.x, beta * qc.y), zc);
+      double2 qn;
+      if (RESID) {
+        const double2 rc = ld2(r + l);
+        qn = horizontal2<VARY>(op, z, l, col, k,
+                               make_double2(fma(beta, qc.x, rc.x), fma(beta, qc.y, rc.y)));
+      } else {
+        qn = stencil2<VARY>(op, z, l, col, k, make_double2(beta * qc.x, beta * qc.y), zc);
+      }
       sig = fma(pc.x, qn.x, sig);
       sig = fma(pc.y, qn.y, sig);
       st2(u + l, uc);
@@ -774,7 +836,8 @@ __global__ void __launch_bounds__(kSpmvThreads) k_spmv_fused(Op op, DevState* st
       const double zc = z[l];
       const double pc = fma(beta, p[l], zc);
       u[l] = fma(alpha, p[l], u[l]);
-      const double qn = stencil1<VARY>(op, z, l, col, k, beta * q[l], zc);
+      const double qn = RESID ? horizontal1<VARY>(op, z, l, col, k, fma(beta, q[l], r[l]))
+                              : stencil1<VARY>(op, z, l, col, k, beta * q[l], zc);
       sig = fma(pc, qn, sig);
       p[l] = pc;
       q[l] = qn;
@@ -1155,9 +1218,9 @@ int grid_precond(Op& op, int num_sms) {
 int grid_spmv(const Op& op, int num_sms) {
   int per_sm = 0;
   cudaError_t e = op.varying ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                                   &per_sm, k_spmv_fused<true, true>, kSpmvThreads, 0)
+                                   &per_sm, k_spmv_fused<true, true, false>, kSpmvThreads, 0)
                              : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                                   &per_sm, k_spmv_fused<false, true>, kSpmvThreads, 0);
+                                   &per_sm, k_spmv_fused<false, true, false>, kSpmvThreads, 0);
   if (e != cudaSuccess || per_sm < 1) per_sm = 1;
   long long g = (long long)per_sm * num_sms;
   const long long work = (op.n + 2 * kSpmvThreads - 1) / (2 * kSpmvThreads);
@@ -1215,18 +1278,28 @@ cudaError_t launch_precond_fused(const Op& op, DevState* st, double* r, const do
   return run_precond_any<true>(op, st, r, q, z, partials, hist, grid, s);
 }
 
-cudaError_t launch_spmv_fused(const Op& op, DevState* st, const double* z, double* u,
-                              double* p, double* q, double* partials, int grid,
+cudaError_t launch_spmv_fused(const Op& op, DevState* st, const double* z, const double* r,
+                              double* u, double* p, double* q, double* partials, int grid,
                               cudaStream_t s) {
-  const bool v2 = (op.nz % 2 == 0) && aligned16(z) && aligned16(u) && aligned16(p) &&
-                  aligned16(q);
+  const bool v2 = (op.nz % 2 == 0) && aligned16(z) && aligned16(r) && aligned16(u) &&
+                  aligned16(p) && aligned16(q);
+  const bool rs = op.az_resid != 0;
+#define PCG_SPMV(VY, V2, RS) \
+  k_spmv_fused<VY, V2, RS><<<grid, kSpmvThreads, 0, s>>>(op, st, z, r, u, p, q, partials)
   if (op.varying) {
-    if (v2) k_spmv_fused<true, true><<<grid, kSpmvThreads, 0, s>>>(op, st, z, u, p, q, partials);
-    else k_spmv_fused<true, false><<<grid, kSpmvThreads, 0, s>>>(op, st, z, u, p, q, partials);
+    if (rs) {
+      if (v2) PCG_SPMV(true, true, true); else PCG_SPMV(true, false, true);
+    } else {
+      if (v2) PCG_SPMV(true, true, false); else PCG_SPMV(true, false, false);
+    }
   } else {
-    if (v2) k_spmv_fused<false, true><<<grid, kSpmvThreads, 0, s>>>(op, st, z, u, p, q, partials);
-    else k_spmv_fused<false, false><<<grid, kSpmvThreads, 0, s>>>(op, st, z, u, p, q, partials);
+    if (rs) {
+      if (v2) PCG_SPMV(false, true, true); else PCG_SPMV(false, false, true);
+    } else {
+      if (v2) PCG_SPMV(false, true, false); else PCG_SPMV(false, false, false);
+    }
   }
+#undef PCG_SPMV
   return cudaGetLastError();
 }
 

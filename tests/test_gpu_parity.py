@@ -107,13 +107,13 @@ def configure(s, mode):
     s.set_az_form("stencil" if stencil else "auto")
     if mode == "tiled_persistent":
         assert s.loop == "persistent"
-    # the residual form needs the row-tiled layout and Thomas column solves
-    thomas = mode != "column" and s.substructuring == 1
+    # the residual form needs Thomas column solves (no substructuring)
+    thomas = s.substructuring == 1
     assert s.az_form == ("residual" if thomas and not stencil else "stencil")
 
 
-MODES = ["column", "tiled", "tiled_stencil", "tiled_recompute", "tiled_split", "tiled_persistent",
-         "tiled_persistent_stencil"]
+MODES = ["column", "column_stencil", "tiled", "tiled_stencil", "tiled_recompute", "tiled_split",
+         "tiled_persistent", "tiled_persistent_stencil"]
 
 
 @pytest.mark.parametrize("layout", MODES)
@@ -372,7 +372,9 @@ def test_az_form_resolution_and_arguments():
         assert s.az_form == "stencil"
         s.set_substructuring(1)
         assert s.az_form == "residual"
-        s.set_layout("column")                  # column layout: the stencil
+        s.set_layout("column")                  # the column layout has both forms
+        assert s.az_form == "residual"
+        s.set_az_form("stencil")
         assert s.az_form == "stencil"
         with pytest.raises(mf.PCGError) as e:
             mf.pcg_set_az_form(s.ctx, 3)
