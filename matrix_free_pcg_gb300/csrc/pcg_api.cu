@@ -712,10 +712,18 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
   const int grid_pm = split ? ctx->grid_sp : ctx->grid_tm;  // preconditioner sweep blocks
   op.nscratch = ctx->nscratch;
   // r = b - A x0, the solver's start; the row-tiled layout writes r, u = x0
-  // and p = q = 0 at its own positions in the same launch.
+  // and p = q = 0 at its own positions in the same launch.  On large grids a
+  // pass over x0 first finds out whether it is all +0.0, so that the start
+  // reads neither x0 nor its neighbours then (small grids: one launch less).
+  const bool x0_check = tiled && op.n >= (1LL << 22);
+  if (x0_check) {
+    e = timed(ctx, PCG_K_RESIDUAL,
+              [&] { return pcg::launch_x0_nonzero(x, op.n, ctx->state, ctx->num_sms, s); });
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "initial guess check launch");
+  }
   e = timed(ctx, PCG_K_RESIDUAL, [&] {
     return tiled ? pcg::launch_residual_tiled(op, ctx->state, b, x, ctx->r, ctx->u_t, ctx->p,
-                                              ctx->q, rtol, maxit, s)
+                                              ctx->q, rtol, maxit, x0_check, s)
                  : pcg::launch_residual(op, ctx->state, b, x, ctx->r, ctx->p, ctx->q, rtol,
                                         maxit, ctx->grid_a, s);
   });

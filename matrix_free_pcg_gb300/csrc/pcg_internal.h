@@ -84,6 +84,8 @@ struct DevState {
   int maxit;
   unsigned int ticket_m;  // last-block tickets of the two grid reductions
   unsigned int ticket_a;
+  int x0_nonzero;    // start of a row-tiled solve: some bit of x0 is set (see
+                     // launch_x0_nonzero)
   double mg_R;       // multigrid preconditioner: ||r||^2 of the current iteration, from the
                      // fine level's first smoothing sweep, for the stopping test
   int setup_error;   // a non-positive Thomas pivot was met in the setup kernel
@@ -108,10 +110,15 @@ cudaError_t launch_residual(const Op& op, DevState* st, const double* b, const d
                             cudaStream_t s);
 // The same for the row-tiled solver layout, in one launch: r_t = b - A x0,
 // u_t = x0 and p_t = q_t = 0 at the row-tiled positions (b and x0 in the
-// caller's column-contiguous layout).
+// caller's column-contiguous layout).  With x0_checked, st->x0_nonzero (from
+// launch_x0_nonzero) tells whether x0 may be skipped entirely.
 cudaError_t launch_residual_tiled(const Op& op, DevState* st, const double* b, const double* x,
                                   double* r_t, double* u_t, double* p_t, double* q_t, double rtol,
-                                  int maxit, cudaStream_t s);
+                                  int maxit, bool x0_checked, cudaStream_t s);
+// st->x0_nonzero = whether any of the n values of x has a bit set (all +0.0:
+// the zero initial guess).  Clears the flag first.
+cudaError_t launch_x0_nonzero(const double* x, long long n, DevState* st, int num_sms,
+                              cudaStream_t s);
 // y = A x
 cudaError_t launch_apply(const Op& op, const double* x, double* y, int grid, cudaStream_t s);
 // z = M^{-1} r  (st receives dev_error if a bounded wait runs out)

@@ -948,6 +948,18 @@ __global__ void __launch_bounds__(kSpmvThreads) k_stencil(Op op, DevState* st,
   }
 }
 
+// st->x0_nonzero |= (some value of x has a bit set); one atomic per warp that
+// saw one.
+__global__ void __launch_bounds__(256) k_x0_nonzero(const double* __restrict__ x, long long n,
+                                                    DevState* st) {
+  unsigned long long bits = 0ull;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x)
+    bits |= __double_as_longlong(x[i]);
+  if (__any_sync(0xffffffffu, bits != 0ull) && (threadIdx.x & 31) == 0)
+    atomicOr(&st->x0_nonzero, 1);
+}
+
 // Start of a solve in the row-tiled layout, one kernel: r = b - A x0 from the
 // caller's column-contiguous b and x0, written row-tiled together with u = x0
 // and p = q = 0, and the scalar state of a new solve (as k_stencil MODE 1).
@@ -955,8 +967,10 @@ __global__ void __launch_bounds__(kSpmvThreads) k_stencil(Op op, DevState* st,
 // (coalesced in the caller's layout), turns the 32 x 32 patch around in
 // shared memory, and writes along the columns (coalesced in the solver's).
 // Where x0 is +0.0 at a cell and at every point its stencil reads, r = b
-// exactly and no fp64 work is done (the common zero initial guess).
-template <bool VARY>
+// exactly and no fp64 work is done (the common zero initial guess).  With
+// CHECKED, st->x0_nonzero == 0 says that all of x0 is +0.0: then neither x0
+// nor its neighbours are read at all (r = b, u = 0).
+template <bool VARY, bool CHECKED>
 __global__ void __launch_bounds__(256) k_residual_tiled(Op op, DevState* st,
                                                         const double* __restrict__ x,
                                                         const double* __restrict__ b,
@@ -965,6 +979,7 @@ __global__ void __launch_bounds__(256) k_residual_tiled(Op op, DevState* st,
                                                         double* __restrict__ p_t,
                                                         double* __restrict__ q_t, double rtol,
                                                         int maxit) {
+  const bool x_zero = CHECKED && st->x0_nonzero == 0;  // (the reset below leaves the flag)
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
     st->alpha = 0.0;
     st->beta = 0.0;
@@ -993,7 +1008,9 @@ __global__ void __launch_bounds__(256) k_residual_tiled(Op op, DevState* st,
     const int cl = row + 8 * pass, k = k0 + lane;
     const long long col = t * kTile + cl;
     double rv = 0.0, xv = 0.0;
-    if (col < op.ncols && k < nz) {
+    if (x_zero) {
+      if (col < op.ncols && k < nz) rv = b[col * nz + k];
+    } else if (col < op.ncols && k < nz) {
       const long long l = col * nz + k;
       xv = x[l];
       const Nbr nb = neighbours(op, col);
@@ -1245,12 +1262,26 @@ cudaError_t launch_residual(const Op& op, DevState* st, const double* b, const d
 
 cudaError_t launch_residual_tiled(const Op& op, DevState* st, const double* b, const double* x,
                                   double* r_t, double* u_t, double* p_t, double* q_t, double rtol,
-                                  int maxit, cudaStream_t s) {
+                                  int maxit, bool x0_checked, cudaStream_t s) {
   const dim3 g((unsigned)op.ntiles, (unsigned)((op.nz + kTile - 1) / kTile));
-  if (op.varying)
-    k_residual_tiled<true><<<g, 256, 0, s>>>(op, st, x, b, r_t, u_t, p_t, q_t, rtol, maxit);
-  else
-    k_residual_tiled<false><<<g, 256, 0, s>>>(op, st, x, b, r_t, u_t, p_t, q_t, rtol, maxit);
+#define PCG_RES(VY, CK) \
+  k_residual_tiled<VY, CK><<<g, 256, 0, s>>>(op, st, x, b, r_t, u_t, p_t, q_t, rtol, maxit)
+  if (op.varying) {
+    if (x0_checked) PCG_RES(true, true); else PCG_RES(true, false);
+  } else {
+    if (x0_checked) PCG_RES(false, true); else PCG_RES(false, false);
+  }
+#undef PCG_RES
+  return cudaGetLastError();
+}
+
+cudaError_t launch_x0_nonzero(const double* x, long long n, DevState* st, int num_sms,
+                              cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(&st->x0_nonzero, 0, sizeof(int), s);
+  if (e != cudaSuccess) return e;
+  const long long g = std::max<long long>(1, std::min<long long>((n + 1023) / 1024,
+                                                                 16LL * num_sms));
+  k_x0_nonzero<<<(int)g, 256, 0, s>>>(x, n, st);
   return cudaGetLastError();
 }
 
