@@ -144,10 +144,9 @@ cudaError_t launch_precond_dot_noalloc(const Op& op, const double* r, double* z,
                                        int num_sms, cudaStream_t s);
 
 // Row-tiled solver layout (pcg_tiled.cu): cell (c,k) at (c/32*nz + k)*32 + c%32.
-// zero1/zero2 (optional) are cleared at the same row-tiled positions.  Row-tiled
-// vectors hold ntiles*32*nz values (the last tile padded to 32 columns).
-cudaError_t launch_to_tiled(const Op& op, const double* src_k, double* dst_t, cudaStream_t s,
-                            double* zero1 = nullptr, double* zero2 = nullptr);
+// Row-tiled vectors hold ntiles*32*nz values (the last tile padded to 32
+// columns).  dst_t = src_k (the standalone V-cycle's input).
+cudaError_t launch_to_tiled(const Op& op, const double* src_k, double* dst_t, cudaStream_t s);
 // dst_k = src_t + alpha p_t (alpha from the device state), or a copy when p_t is NULL.
 cudaError_t launch_from_tiled(const Op& op, const DevState* st, const double* src_t,
                               const double* p_t, double* dst_k, cudaStream_t s);

@@ -875,7 +875,7 @@ __device__ __forceinline__ bool x_is_zero2(const Op& op, const double* __restric
   return bits == 0ull;
 }
 
-// MODE 0: y = A x.  MODE 1: r = b - A x, p = q = 0 (unless p is NULL), and
+// MODE 0: y = A x.  MODE 1: r = b - A x, p = q = 0, and
 // the scalar state of a new solve (alpha = 0, kappa_old = 1: the first sweeps
 // then give p = z_0, q = A z_0).
 template <bool VARY, bool VEC2, int MODE>
@@ -924,10 +924,8 @@ __global__ void __launch_bounds__(kSpmvThreads) k_stencil(Op op, DevState* st,
       } else {
         const double2 bv = ld2(b + l);
         st2(y + l, make_double2(bv.x - ax.x, bv.y - ax.y));
-        if (p) {  // p = q = 0 here, or (NULL) by the caller in its own layout
-          st2(p + l, make_double2(0.0, 0.0));
-          st2(q + l, make_double2(0.0, 0.0));
-        }
+        st2(p + l, make_double2(0.0, 0.0));
+        st2(q + l, make_double2(0.0, 0.0));
       }
     }
   } else {
@@ -939,10 +937,8 @@ __global__ void __launch_bounds__(kSpmvThreads) k_stencil(Op op, DevState* st,
         y[l] = ax;
       } else {
         y[l] = b[l] - ax;
-        if (p) {
-          p[l] = 0.0;
-          q[l] = 0.0;
-        }
+        p[l] = 0.0;
+        q[l] = 0.0;
       }
     }
   }

@@ -31,15 +31,11 @@ namespace {
 // TO_TILED: dst_t = src_k.  Otherwise dst_k = src_t + alpha * p_t (AXPY,
 // alpha from the device state: the deferred x += alpha p of Algorithm 1), or
 // a plain copy.
-// With TO_TILED, zero1/zero2 (may be NULL) are cleared at the same row-tiled
-// positions (p and q at the start of a solve).
 template <bool TO_TILED, bool AXPY>
 __global__ void __launch_bounds__(256) k_retile(Op op, const DevState* st,
                                                 const double* __restrict__ src,
                                                 const double* __restrict__ pt,
-                                                double* __restrict__ dst,
-                                                double* __restrict__ zero1,
-                                                double* __restrict__ zero2) {
+                                                double* __restrict__ dst) {
   __shared__ double tile[kTile][kTile + 1];
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int nz = op.nz;
@@ -55,10 +51,7 @@ __global__ void __launch_bounds__(256) k_retile(Op op, const DevState* st,
     __syncthreads();
     for (int k = ty; k < nk; k += 8)
       if (tx < nc) {
-        const long long o = (t * nz + k0 + k) * kTile + tx;
-        dst[o] = tile[tx][k];
-        if (zero1) zero1[o] = 0.0;
-        if (zero2) zero2[o] = 0.0;
+        dst[(t * nz + k0 + k) * kTile + tx] = tile[tx][k];
       }
   } else {
     for (int k = ty; k < nk; k += 8)
@@ -273,10 +266,9 @@ __global__ void __launch_bounds__(256) k_spmv_tiled(Op op, DevState* st,
 
 }  // namespace
 
-cudaError_t launch_to_tiled(const Op& op, const double* src_k, double* dst_t, cudaStream_t s,
-                            double* zero1, double* zero2) {
+cudaError_t launch_to_tiled(const Op& op, const double* src_k, double* dst_t, cudaStream_t s) {
   dim3 g((unsigned)op.ntiles, (unsigned)((op.nz + kTile - 1) / kTile));
-  k_retile<true, false><<<g, 256, 0, s>>>(op, nullptr, src_k, nullptr, dst_t, zero1, zero2);
+  k_retile<true, false><<<g, 256, 0, s>>>(op, nullptr, src_k, nullptr, dst_t);
   return cudaGetLastError();
 }
 
@@ -284,9 +276,9 @@ cudaError_t launch_from_tiled(const Op& op, const DevState* st, const double* sr
                               const double* p_t, double* dst_k, cudaStream_t s) {
   dim3 g((unsigned)op.ntiles, (unsigned)((op.nz + kTile - 1) / kTile));
   if (p_t)
-    k_retile<false, true><<<g, 256, 0, s>>>(op, st, src_t, p_t, dst_k, nullptr, nullptr);
+    k_retile<false, true><<<g, 256, 0, s>>>(op, st, src_t, p_t, dst_k);
   else
-    k_retile<false, false><<<g, 256, 0, s>>>(op, st, src_t, nullptr, dst_k, nullptr, nullptr);
+    k_retile<false, false><<<g, 256, 0, s>>>(op, st, src_t, nullptr, dst_k);
   return cudaGetLastError();
 }
 
