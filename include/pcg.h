@@ -167,17 +167,28 @@ int pcg_set_substructuring(pcg_ctx* ctx, int nblocks);
  *                        GPU, where launch latency dominates an iteration.  A
  *                        barrier wait that runs out (about a second) ends the
  *                        solve with PCG_ETIMEOUT;
- *   PCG_LOOP_AUTO        (default) persistent for grids with fewer tiles of 32
+ *   PCG_LOOP_CLUSTER     one thread-block cluster (16 CTAs, or 8) runs all
+ *                        iterations with every vector of the solve in its
+ *                        distributed shared memory: the stencil sweep reads
+ *                        the neighbouring tiles' z from the owning CTA's shared
+ *                        memory, partial sums go to every CTA's shared memory,
+ *                        and hardware cluster barriers separate the sweeps; for
+ *                        grids that fit (about 40 K cells with an a_h field,
+ *                        70 K with a constant one);
+ *   PCG_LOOP_AUTO        (default) the cluster loop where the grid fits,
+ *                        else persistent for grids with fewer tiles of 32
  *                        columns than 4 per SM, else batched.
- * The persistent loop needs Thomas column solves (no substructuring) and
- * stored factors, and the device must support cooperative launches; where it
- * cannot run, the batched loop does.  The column layout always runs batched.
- * Errors: PCG_EINVAL (unknown mode). */
-enum { PCG_LOOP_AUTO = 0, PCG_LOOP_BATCHED = 1, PCG_LOOP_PERSISTENT = 2 };
+ * The persistent and cluster loops need Thomas column solves (no
+ * substructuring), stored factors and the line preconditioner; the cluster
+ * loop also the residual form of A z (pcg_set_az_form), and a device that
+ * launches clusters.  The persistent loop needs cooperative launches.  Where a
+ * loop cannot run, the next one in the order above does.  The column layout
+ * always runs batched.  Errors: PCG_EINVAL (unknown mode). */
+enum { PCG_LOOP_AUTO = 0, PCG_LOOP_BATCHED = 1, PCG_LOOP_PERSISTENT = 2, PCG_LOOP_CLUSTER = 3 };
 int pcg_set_loop(pcg_ctx* ctx, int mode);
 
-/* The loop the next pcg_solve will run: PCG_LOOP_BATCHED or
- * PCG_LOOP_PERSISTENT.  Errors: PCG_EINVAL (NULL). */
+/* The loop the next pcg_solve will run: PCG_LOOP_BATCHED,
+ * PCG_LOOP_PERSISTENT or PCG_LOOP_CLUSTER.  Errors: PCG_EINVAL (NULL). */
 int pcg_get_loop(const pcg_ctx* ctx, int* mode_out);
 
 /* How the stencil sweep of pcg_solve forms A z (Appendix A, Algorithm 2:

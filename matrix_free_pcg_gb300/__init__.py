@@ -38,7 +38,7 @@ EXPORTED = ["pcg_create", "pcg_destroy", "pcg_update_coeffs", "pcg_set_stream", 
             "pcg_get_multigrid", "pcg_mg_vcycle"]
 PCG_LAYOUT_COLUMN, PCG_LAYOUT_TILED = 0, 1
 PCG_FACTORS_STORED, PCG_FACTORS_RECOMPUTE = 0, 1
-PCG_LOOP_AUTO, PCG_LOOP_BATCHED, PCG_LOOP_PERSISTENT = 0, 1, 2
+PCG_LOOP_AUTO, PCG_LOOP_BATCHED, PCG_LOOP_PERSISTENT, PCG_LOOP_CLUSTER = 0, 1, 2, 3
 PCG_AZ_AUTO, PCG_AZ_STENCIL, PCG_AZ_RESIDUAL = 0, 1, 2
 PCG_PREC_LINE, PCG_PREC_MULTIGRID = 0, 1
 
@@ -220,12 +220,12 @@ def pcg_get_substructuring(ctx):
 
 
 def pcg_set_loop(ctx, mode):
-    """PCG_LOOP_AUTO (default), PCG_LOOP_BATCHED or PCG_LOOP_PERSISTENT."""
+    """PCG_LOOP_AUTO (default), PCG_LOOP_BATCHED, PCG_LOOP_PERSISTENT or PCG_LOOP_CLUSTER."""
     return _check(_lib.pcg_set_loop(ctx, int(mode)), ctx)
 
 
 def pcg_get_loop(ctx):
-    """The loop the next solve runs: PCG_LOOP_BATCHED or PCG_LOOP_PERSISTENT."""
+    """The loop the next solve runs: PCG_LOOP_BATCHED, PCG_LOOP_PERSISTENT or PCG_LOOP_CLUSTER."""
     v = ctypes.c_int(0)
     _check(_lib.pcg_get_loop(ctx, ctypes.byref(v)), ctx)
     return v.value
@@ -399,10 +399,10 @@ class Solver:
         pcg_set_substructuring(self.ctx, nblocks)
 
     def set_loop(self, mode):
-        """"auto", "batched" or "persistent" (or the PCG_LOOP_* values)."""
+        """"auto", "batched", "persistent" or "cluster" (or the PCG_LOOP_* values)."""
         if isinstance(mode, str):
             mode = {"auto": PCG_LOOP_AUTO, "batched": PCG_LOOP_BATCHED,
-                    "persistent": PCG_LOOP_PERSISTENT}[mode]
+                    "persistent": PCG_LOOP_PERSISTENT, "cluster": PCG_LOOP_CLUSTER}[mode]
         pcg_set_loop(self.ctx, mode)
 
     def set_preconditioner(self, prec):
@@ -442,9 +442,9 @@ class Solver:
 
     @property
     def loop(self):
-        """"batched" or "persistent": the loop the next solve runs."""
-        return {PCG_LOOP_BATCHED: "batched", PCG_LOOP_PERSISTENT: "persistent"}[
-            pcg_get_loop(self.ctx)]
+        """"batched", "persistent" or "cluster": the loop the next solve runs."""
+        return {PCG_LOOP_BATCHED: "batched", PCG_LOOP_PERSISTENT: "persistent",
+                PCG_LOOP_CLUSTER: "cluster"}[pcg_get_loop(self.ctx)]
 
     @property
     def substructuring(self):

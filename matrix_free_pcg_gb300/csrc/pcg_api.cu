@@ -80,6 +80,7 @@ struct pcg_ctx {
   std::vector<double> dz_host;
   double a_h_host = 0.0, a_v_host = 0.0, mass_host = 0.0;
   int grid_ps = 0;                   // blocks of the persistent loop (0: not available)
+  int cl_ctas = 0;                   // CTAs of the cluster loop (0: does not fit)
   unsigned int test_absent = 0;      // test hook: arrivals the persistent barriers miss
   size_t partials_cap = 0;           // doubles in `partials`
   // CUDA graphs of the row-tiled loop: two instances, launched alternately so
@@ -496,7 +497,10 @@ int load_coeffs(pcg_ctx* ctx, const pcg_coeffs* c, bool varying) {
   cudaError_t e = cudaMemcpyAsync(ctx->lev, lev.data(), lev.size() * sizeof(double),
                                   cudaMemcpyHostToDevice, ctx->stream);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "upload of the level table");
-  ctx->op.varying = varying ? 1 : 0;
+  if (ctx->op.varying != (varying ? 1 : 0)) {
+    ctx->op.varying = varying ? 1 : 0;
+    if (ctx->num_sms > 0) ctx->cl_ctas = pcg::cluster_ctas(ctx->op);  // the tables it holds
+  }
   if (varying) {
     e = cudaMemcpyAsync(ctx->ah, c->a_h_field, ctx->op.ncols * sizeof(double),
                         cudaMemcpyHostToDevice, ctx->stream);
@@ -597,15 +601,21 @@ bool persistent_grid(const pcg_ctx* ctx) {
   return ctx->grid_ps > 0 && ctx->op.ntiles < 4LL * ctx->num_sms;
 }
 
-// The loop the next solve runs (PCG_LOOP_BATCHED or PCG_LOOP_PERSISTENT).
+// The loop the next solve runs (PCG_LOOP_BATCHED, PCG_LOOP_PERSISTENT or
+// PCG_LOOP_CLUSTER).
+int resolved_az(const pcg_ctx* ctx);
 int resolved_loop(const pcg_ctx* ctx) {
   const bool eligible = ctx->layout == PCG_LAYOUT_TILED && ctx->split_p == 1 &&
                         ctx->prec == PCG_PREC_LINE &&
-                        !(ctx->op.varying && ctx->factors == PCG_FACTORS_RECOMPUTE) &&
-                        ctx->grid_ps > 0;
+                        !(ctx->op.varying && ctx->factors == PCG_FACTORS_RECOMPUTE);
   if (!eligible || ctx->loop_req == PCG_LOOP_BATCHED) return PCG_LOOP_BATCHED;
-  if (ctx->loop_req == PCG_LOOP_PERSISTENT) return PCG_LOOP_PERSISTENT;
-  return persistent_grid(ctx) ? PCG_LOOP_PERSISTENT : PCG_LOOP_BATCHED;
+  const bool cluster = ctx->cl_ctas > 0 && resolved_az(ctx) == PCG_AZ_RESIDUAL;
+  if ((ctx->loop_req == PCG_LOOP_CLUSTER || ctx->loop_req == PCG_LOOP_AUTO) && cluster)
+    return PCG_LOOP_CLUSTER;
+  if (ctx->grid_ps > 0 && (ctx->loop_req == PCG_LOOP_PERSISTENT || persistent_grid(ctx) ||
+                           ctx->loop_req == PCG_LOOP_CLUSTER))
+    return PCG_LOOP_PERSISTENT;
+  return PCG_LOOP_BATCHED;
 }
 
 // The form of A z that the next solve's stencil sweeps use (PCG_AZ_STENCIL
@@ -729,9 +739,17 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
   });
   if (e != cudaSuccess) return cuda_fail(ctx, e, "residual kernel launch");
 
-  // Persistent loop: every iteration in one cooperative kernel.
-  const bool persistent = resolved_loop(ctx) == PCG_LOOP_PERSISTENT;
-  if (persistent) {
+  // Persistent loop: every iteration in one cooperative kernel; cluster loop:
+  // every iteration in one cluster, the vectors in its shared memory.
+  const int loop = resolved_loop(ctx);
+  const bool persistent = loop == PCG_LOOP_PERSISTENT || loop == PCG_LOOP_CLUSTER;
+  if (loop == PCG_LOOP_CLUSTER) {
+    e = timed(ctx, PCG_K_LOOP, [&] {
+      return pcg::launch_cluster_loop(op, ctx->state, ctx->r, ctx->u_t, ctx->p, ctx->hist,
+                                      ctx->cl_ctas, s);
+    });
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cluster solve loop launch");
+  } else if (persistent) {
     e = timed(ctx, PCG_K_LOOP, [&] {
       return pcg::launch_persistent(op, ctx->state, ctx->r, ctx->q, ctx->z, ctx->u_t, ctx->p,
                                     ctx->partials, ctx->hist, ctx->grid_ps, ctx->test_absent,
@@ -957,6 +975,7 @@ int pcg_create(int nx, int ny, int nz, const pcg_coeffs* coeffs, pcg_ctx** out) 
   ctx->grid_tm = pcg::grid_tiled_precond(op, ctx->num_sms);
   ctx->grid_ta = pcg::grid_tiled_spmv(op, ctx->num_sms);
   ctx->grid_ps = pcg::grid_persistent(op, ctx->num_sms);
+  ctx->cl_ctas = pcg::cluster_ctas(op);
   ctx->partials_cap = 2 * (size_t)std::max(std::max(ctx->grid_m + ctx->grid_a,
                                                      ctx->grid_tm + ctx->grid_ta),
                                             2 * ctx->grid_ps);
@@ -1055,9 +1074,10 @@ int pcg_set_factors(pcg_ctx* ctx, int mode) {
 // or fewer if the column is too short.
 int auto_split(pcg_ctx* ctx) {
   if (ctx->op.ntiles * 2 >= ctx->num_sms) return 1;
-  // the persistent loop (Thomas only) is faster still on these grids
-  // (32x32x16: 21.8 us per iteration against 24.3 us with 4 blocks, batched)
-  if (ctx->loop_req != PCG_LOOP_BATCHED && persistent_grid(ctx)) return 1;
+  // the persistent and cluster loops (Thomas only) are faster still on these
+  // grids (32x32x16: 21.8 us per iteration persistent against 24.3 us with 4
+  // blocks, batched)
+  if (ctx->loop_req != PCG_LOOP_BATCHED && (persistent_grid(ctx) || ctx->cl_ctas > 0)) return 1;
   for (int P = 4; P >= 2; P /= 2)
     if (pcg::split_valid(ctx->op.nz, P) && pcg::split_grid(ctx->op, P, ctx->num_sms) > 0) return P;
   return 1;
@@ -1121,7 +1141,8 @@ int pcg_set_substructuring(pcg_ctx* ctx, int nblocks) {
 
 int pcg_set_loop(pcg_ctx* ctx, int mode) {
   if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
-  if (mode != PCG_LOOP_AUTO && mode != PCG_LOOP_BATCHED && mode != PCG_LOOP_PERSISTENT)
+  if (mode != PCG_LOOP_AUTO && mode != PCG_LOOP_BATCHED && mode != PCG_LOOP_PERSISTENT &&
+      mode != PCG_LOOP_CLUSTER)
     return fail(ctx, PCG_EINVAL, "unknown loop mode %d", mode);
   ctx->loop_req = mode;
   return PCG_OK;

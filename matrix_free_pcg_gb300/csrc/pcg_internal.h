@@ -175,6 +175,15 @@ cudaError_t launch_persistent(const Op& op, DevState* st, double* r, double* q, 
                               double* u, double* p, double* partials, double* hist, int grid,
                               unsigned int absent, cudaStream_t s);
 
+// Whole solve loop in the shared memory of one thread-block cluster
+// (pcg_cluster.cu; row-tiled layout, Thomas column solves, stored factors, A z
+// in the residual form): cluster_ctas gives the cluster's CTAs (16 or 8; 0:
+// the grid does not fit or clusters are not available), launch_cluster_loop
+// runs iterations until the stopping test and leaves u and p row-tiled.
+int cluster_ctas(const Op& op);
+cudaError_t launch_cluster_loop(const Op& op, DevState* st, double* r, double* u, double* p,
+                                double* hist, int ctas, cudaStream_t s);
+
 // Grid sizes (blocks) of the two row-tiled sweeps.
 int grid_tiled_precond(const Op& op, int num_sms);
 int grid_tiled_spmv(const Op& op, int num_sms);

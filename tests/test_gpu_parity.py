@@ -466,11 +466,11 @@ def test_substructuring_arguments():
             assert e.value.status == mf.PCG_EINVAL
         bd = torch.from_numpy(b).to(DEV)
         out = []
-        # with the automatic loop these 8 tiles run the persistent loop, which
+        # with the automatic loop these 8 tiles run the cluster loop, which
         # needs (and beats) Thomas column solves; with the batched loop they
         # are substructured (fewer tiles than half the SMs): 4 blocks
         s.set_substructuring(0)
-        assert (s.substructuring, s.loop) == (1, "persistent")
+        assert (s.substructuring, s.loop) == (1, "cluster")
         s.set_loop("batched")
         for nb in (4, 1, 2, 0, 4):
             s.set_substructuring(nb)
@@ -572,7 +572,10 @@ def test_persistent_loop_choice_and_timing():
     prob, kw, b = case(30, 26, 24, True, True, a_v=1e3, seed=16)
     with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
         s.set_substructuring(1)
-        assert s.loop == "persistent"          # 25 tiles: the automatic choice
+        assert s.loop == "cluster"             # 25 tiles fit one cluster: the automatic choice
+        s.set_az_form("stencil")               # the cluster loop has the residual form only
+        assert s.loop == "persistent"          # 25 tiles: the next automatic choice
+        s.set_az_form("auto")
         s.set_loop("batched")
         assert s.loop == "batched"
         s.set_loop("persistent")
@@ -701,3 +704,86 @@ def test_persistent_barrier_wait_runs_out_and_the_context_recovers():
         x.zero_()
         it, _, st = s.solve(bd, x, rtol=1e-10)
         assert st == mf.PCG_OK and abs(it - it_ref) <= 1
+
+
+CLUSTER_CASES = [
+    # nx, ny, nz, varying, graded, a_v: grids whose vectors fit one cluster
+    (37, 29, 16, True, True, 1e3),
+    (33, 5, 7, True, True, 1e2),
+    (32, 32, 16, False, False, 1e2),
+    (30, 26, 24, True, True, 1e4),
+    (1, 1, 40, True, True, 1e3),
+    (64, 3, 9, False, True, 1e3),
+]
+
+
+@pytest.mark.parametrize("cfg", CLUSTER_CASES, ids=lambda c: "x".join(map(str, c[:3])))
+def test_cluster_loop_matches_oracle(cfg):
+    nx, ny, nz, varying, graded, a_v = cfg
+    prob, kw, b = case(nx, ny, nz, varying, graded, a_v=a_v, seed=17)
+    x_ref, it_ref, hist_ref, st_ref = oracle.pcg(prob, b, rtol=1e-10, maxit=500)
+    assert st_ref == oracle.OK
+    with mf.Solver(nx, ny, nz, **kw) as s:
+        s.set_substructuring(1)
+        s.set_loop("cluster")
+        assert s.loop == "cluster"
+        bd = torch.from_numpy(b).to(DEV)
+        x = torch.zeros_like(bd)
+        iters, hist, st = s.solve(bd, x, rtol=1e-10, maxit=500)
+        assert st == mf.PCG_OK and abs(iters - it_ref) <= 1
+        m = min(iters, it_ref) + 1
+        np.testing.assert_allclose(hist[:m], hist_ref[:m], rtol=1e-6, atol=1e-13)
+        x2 = torch.zeros_like(bd)
+        i2, h2, _ = s.solve(bd, x2, rtol=1e-10, maxit=500)
+        assert i2 == iters and np.array_equal(h2, hist) and torch.equal(x, x2)  # repeatable
+        x.zero_()
+        it3, _, st3 = s.solve(bd, x, rtol=0.0, maxit=it_ref)
+        assert (it3, st3) == (it_ref, mf.PCG_OK)
+        xs = x.cpu().numpy()
+        # the persistent loop computes the same iterates up to rounding
+        s.set_loop("persistent")
+        assert s.loop == "persistent"
+        xp = torch.zeros_like(bd)
+        s.solve(bd, xp, rtol=0.0, maxit=it_ref)
+    assert np.linalg.norm(xs - x_ref) <= SOL_TOL * np.linalg.norm(x_ref)
+    assert np.linalg.norm(xs - xp.cpu().numpy()) <= 1e-10 * np.linalg.norm(x_ref)
+
+
+def test_cluster_loop_status_semantics_and_timing():
+    prob, kw, b = case(20, 18, 16, True, True, a_v=1e3, seed=18)
+    with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        s.set_substructuring(1)
+        assert s.loop == "cluster"
+        bd = torch.from_numpy(b).to(DEV)
+        _, it_ref, _, _ = oracle.pcg(prob, b, rtol=1e-8)
+        x = torch.zeros_like(bd)
+        it, _, st = s.solve(bd, x, rtol=1e-8, maxit=it_ref - 2)
+        assert (it, st) == (it_ref - 2, mf.PCG_ENOTCONV)
+        x.zero_()
+        it, hist, st = s.solve(bd, x, rtol=0.0, maxit=3)
+        assert (it, st, len(hist)) == (3, mf.PCG_OK, 4)
+        x.zero_()
+        it, hist, st = s.solve(torch.zeros_like(bd), x, rtol=1e-10)
+        assert (it, st) == (0, mf.PCG_OK) and float(x.abs().max()) == 0.0
+        bad = bd.clone()
+        bad[40] = float("nan")
+        x.zero_()
+        _, _, st = s.solve(bad, x, rtol=1e-10)
+        assert st == mf.PCG_EBREAKDOWN
+        x0 = np.random.default_rng(19).standard_normal(prob.n)
+        x.copy_(torch.from_numpy(x0))
+        it, _, st = s.solve(bd, x, rtol=1e-8)
+        x_ref, it_ref2, _, _ = oracle.pcg(prob, b, x0=x0, rtol=1e-8)
+        assert st == mf.PCG_OK and abs(it - it_ref2) <= 1
+        assert np.linalg.norm(x.cpu().numpy() - x_ref) <= 1e-6 * np.linalg.norm(x_ref)
+        s.enable_timing(True)
+        x.zero_()
+        it, _, st = s.solve(bd, x, rtol=1e-10)
+        t = s.kernel_times()
+        assert st == mf.PCG_OK and t["loop"][1] == 1 and t["loop"][0] > 0
+        assert s.launch_info()["last_solve_launches"] == 3   # residual, loop, final update
+        # a grid too large for one cluster runs persistent when the cluster loop is asked for
+    with mf.Solver(128, 128, 64, a_h=1.0, a_v=1e3) as s:
+        s.set_substructuring(1)
+        s.set_loop("cluster")
+        assert s.loop == "persistent"
