@@ -44,44 +44,52 @@ __device__ __forceinline__ int cl_off(int a, int j, int k, int lane, int slots, 
   return ((a * slots + j) * nz + k) * kTile + lane;
 }
 
-// Block sum of two values in a fixed order (every thread gets the result via
-// the caller's barrier); written by thread 0 into slot `rank` of array `slot`
-// on every CTA of the cluster.
-__device__ __forceinline__ void cl_publish(cg::cluster_group& cluster, double v0, double v1,
-                                           double* slot, int C) {
-  __shared__ double s0[kClWarps], s1[kClWarps];
+// Block sums of NV values in a fixed order, written by thread 0 into slot
+// `rank` of array `slot` (NV doubles per CTA) on every CTA of the cluster.
+// Only the warps that had work in the sweep reduce with shuffles; the others
+// contribute exact zeros without fp64 work (an fp64 warp instruction holds a
+// sub-partition's fp64 pipe for 64 cycles whether its values are zero or not),
+// and warp 0 adds the warp totals in a shuffle tree.
+template <int NV>
+__device__ __forceinline__ void cl_publish(cg::cluster_group& cluster, const double (&v)[NV],
+                                           bool warp_busy, double* slot, int C) {
+  __shared__ double sw[NV][kClWarps];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  v0 = warp_sum(v0);
-  v1 = warp_sum(v1);
-  if (lane == 0) {
-    s0[w] = v0;
-    s1[w] = v1;
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    const double s = warp_busy ? warp_sum(v[j]) : 0.0;
+    if (lane == 0) sw[j][w] = s;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    double a = 0.0, b = 0.0;
-    for (int i = 0; i < kClWarps; ++i) {
-      a += s0[i];
-      b += s1[i];
+  if (w == 0) {
+    double tot[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      double a = (lane < kClWarps) ? sw[j][lane] : 0.0;
+#pragma unroll
+      for (int o = kClWarps / 2; o > 0; o >>= 1) a += __shfl_down_sync(0xffffffffu, a, o);
+      tot[j] = a;
     }
-    const unsigned rank = cluster.block_rank();
-    for (int r = 0; r < C; ++r) {
-      double* remote = cluster.map_shared_rank(slot, r);
-      remote[2 * rank] = a;
-      remote[2 * rank + 1] = b;
+    if (lane == 0) {
+      const unsigned rank = cluster.block_rank();
+      for (int r = 0; r < C; ++r) {
+        double* remote = cluster.map_shared_rank(slot, r);
+#pragma unroll
+        for (int j = 0; j < NV; ++j) remote[NV * rank + j] = tot[j];
+      }
     }
   }
 }
 
-// The cluster totals of a published pair, in rank order.
-__device__ __forceinline__ void cl_totals(const double* slot, int C, double& t0, double& t1) {
-  double a = 0.0, b = 0.0;
+// The cluster totals of published values, in rank order.
+template <int NV>
+__device__ __forceinline__ void cl_totals(const double* slot, int C, double (&t)[NV]) {
+#pragma unroll
+  for (int j = 0; j < NV; ++j) t[j] = 0.0;
   for (int r = 0; r < C; ++r) {
-    a += slot[2 * r];
-    b += slot[2 * r + 1];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) t[j] += slot[NV * r + j];
   }
-  t0 = a;
-  t1 = b;
 }
 
 template <bool VARY>
@@ -138,6 +146,7 @@ __global__ void __launch_bounds__(kClThreads, 1) k_pcg_cluster(Op op, DevState* 
   for (;;) {
     // ---- Algorithm 3 sweep on the own tiles: one warp per tile slot
     double accR = 0.0, accK = 0.0;
+    const bool busyM = warp < slots && (long long)warp * C + rank < op.ntiles;
     for (int j = warp; j < slots; j += kClWarps) {
       const long long t = (long long)j * C + rank;
       if (t >= op.ntiles || t * kTile + lane >= op.ncols) continue;
@@ -161,11 +170,17 @@ __global__ void __launch_bounds__(kClThreads, 1) k_pcg_cluster(Op op, DevState* 
         zs = zz;
       }
     }
-    cl_publish(cluster, accR, accK, slotM, C);
+    {
+      const double acc[2] = {accR, accK};
+      cl_publish<2>(cluster, acc, busyM, slotM, C);
+    }
     cluster.sync();  // every CTA's z and partial sums are in place
     if (threadIdx.x == 0) {
       // ---- the scalar step of Algorithm 1 (as finish_precond_sweep)
-      cl_totals(slotM, C, R, K);
+      double tot[2];
+      cl_totals<2>(slotM, C, tot);
+      R = tot[0];
+      K = tot[1];
       if (it == 0) R0 = R;
       const double ratio = (R0 > 0.0) ? sqrt(R / R0) : 0.0;
       if (rank == 0) hist[it] = ratio;
@@ -242,11 +257,15 @@ __global__ void __launch_bounds__(kClThreads, 1) k_pcg_cluster(Op op, DevState* 
         qs = a;
       }
     }
-    cl_publish(cluster, sig, 0.0, slotA, C);
+    {
+      const double acc[1] = {sig};
+      cl_publish<1>(cluster, acc, warp < slots * segs, slotA, C);
+    }
     cluster.sync();  // every CTA's partial sum is in place; no z is read any more
     if (threadIdx.x == 0) {
-      double unused;
-      cl_totals(slotA, C, S, unused);
+      double tot[1];
+      cl_totals<1>(slotA, C, tot);
+      S = tot[0];
       if (!(S > 0.0) || !(S < INFINITY)) {
         alpha = 0.0;
         iters = it - 1;

@@ -202,36 +202,42 @@ __device__ __forceinline__ double ld_hint(const double* a, uint64_t pol) {
   return v;
 }
 
-// Grid-wide barrier for a cooperative launch (every block resident).  Thread 0
-// of each block reads the generation, publishes the block's writes and
-// arrives on the counter; the last arrival resets the counter and advances the
-// generation, the others poll it -- at most `limit` times, after which the
-// block records the timeout in *err and the barrier returns false (the caller
-// then leaves its loop; nothing waits without bound).  Global writes made
-// before the barrier are visible to every block after it (read them with
-// __ldcg, past the non-coherent L1).
-__device__ __forceinline__ bool grid_barrier(unsigned int* count, unsigned int* gen,
-                                             unsigned int nblocks, int* err, long long limit) {
+// Grid-wide barrier for a cooperative launch (every block resident), on a
+// counter that only grows during the launch (zeroed before it).  Thread 0 of
+// each block publishes the block's writes, adds its arrival (a reduction in
+// L2: no value comes back) and polls until the count reaches `target` =
+// nblocks times the number of barriers passed so far, this one included.
+// Nothing is reset or released after the last arrival: a waiting block sees
+// the barrier open on its next poll.  The poll gives up after `wait_ns`
+// nanoseconds of the global timer, or after `limit` tries, whichever comes
+// first; the block then records the timeout in *err and the barrier returns false
+// (the caller leaves its loop; nothing waits without bound).  Global writes
+// made before the barrier are visible to every block after it (read them
+// with __ldcg, past the non-coherent L1).  The unsigned difference keeps the
+// test right across a wrap of the counter.
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool grid_barrier(unsigned int* count, unsigned int target, int* err,
+                                             long long limit, unsigned long long wait_ns) {
   __shared__ int ok_s;
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
-    const unsigned int g = *reinterpret_cast<volatile unsigned int*>(gen);
     __threadfence();
-    if (atomicAdd(count, 1u) + 1u == nblocks) {
-      atomicExch(count, 0u);
-      __threadfence();
-      atomicAdd(gen, 1u);
-    } else {
-      long long polls = 0;
-      while (*reinterpret_cast<volatile unsigned int*>(gen) == g) {
-        if (++polls > limit) {
-          ok = 0;
-          atomicExch(err, 1);
-          break;
-        }
-        __nanosleep(64);
+    atomicAdd(count, 1u);
+    const unsigned long long t0 = global_ns();
+    long long polls = 0;
+    while ((int)(*reinterpret_cast<volatile unsigned int*>(count) - target) < 0) {
+      if (++polls > limit || global_ns() - t0 > wait_ns) {
+        ok = 0;
+        atomicExch(err, 1);
+        break;
       }
+      __nanosleep(32);
     }
     __threadfence();
     ok_s = ok;

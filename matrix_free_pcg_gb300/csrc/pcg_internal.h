@@ -90,7 +90,7 @@ struct DevState {
                      // fine level's first smoothing sweep, for the stopping test
   int setup_error;   // a non-positive Thomas pivot was met in the setup kernel
   int dev_error;     // a bounded device wait ran out (pcg_status PCG_ETIMEOUT)
-  unsigned int bar_count, bar_gen;  // grid barrier of the persistent solve loop
+  unsigned int bar_count;  // arrivals at the grid barriers of the persistent solve loop
 };
 
 // ---- launchers (set-up: pcg_setup.cu; column-layout sweeps, stencil, residual and final

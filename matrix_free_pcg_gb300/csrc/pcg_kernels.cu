@@ -900,7 +900,6 @@ __global__ void __launch_bounds__(kSpmvThreads) k_stencil(Op op, DevState* st,
     st->ticket_m = 0u;
     st->ticket_a = 0u;
     st->bar_count = 0u;
-    st->bar_gen = 0u;
     st->dev_error = 0;
     st->done = 0;
   }
@@ -990,7 +989,6 @@ __global__ void __launch_bounds__(256) k_residual_tiled(Op op, DevState* st,
     st->ticket_m = 0u;
     st->ticket_a = 0u;
     st->bar_count = 0u;
-    st->bar_gen = 0u;
     st->dev_error = 0;
     st->done = 0;
   }

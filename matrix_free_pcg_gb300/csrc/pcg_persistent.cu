@@ -22,57 +22,76 @@ namespace {
 // reduction) is most of an iteration.  This kernel runs the whole loop of
 // Algorithm 1 in one cooperative launch: the preconditioner sweep and the
 // stencil sweep of each iteration run the tile and unit bodies of
-// pcg_sweeps.cuh (those of the batched kernels), separated by grid barriers.  After each barrier every
-// block sums the per-block partials in the same fixed order, so every block
-// takes the same scalar decisions (stopping test, beta, alpha) from the same
-// numbers; block 0 writes the history and, at the end, the device state that
-// the host and the final update read.
+// pcg_sweeps.cuh (those of the batched kernels), separated by grid barriers.  After each barrier
+// warp 0 of every block sums the per-block partials in the same fixed order
+// and thread 0 takes the scalar step, so every block takes the same
+// decisions (stopping test, beta, alpha) from the same numbers; block 0
+// writes the history and, at the end, the device state that the host and the
+// final update read.  The reductions and the scalar steps run in as few
+// warps as possible: the fp64 pipe, not the issue rate, bounds them.
 
 constexpr int kPsThreads = 256;
-// Polls of a barrier wait before the loop gives up with PCG_ETIMEOUT (with a
-// 64 ns sleep per poll: about a second).  `absent` (0 in normal use) adds
-// arrivals that never come, so that a test can make the wait run out.
+// A barrier wait gives up with PCG_ETIMEOUT after a second of the global
+// timer, or after 2^24 polls (each an L2 round trip plus a 32 ns sleep).
 constexpr long long kBarrierPolls = 1LL << 24;
+constexpr unsigned long long kBarrierWaitNs = 1000000000ull;
 
-// Per-block sums of two values (fixed order) into out[0], out[1].
-__device__ __forceinline__ void block_partial2(double v0, double v1, double* out) {
-  __shared__ double s0[kPsThreads / 32], s1[kPsThreads / 32];
+// Block partials of NV values, in one fixed order.  Only the warps that had
+// work in the sweep reduce their values with shuffles; the others contribute
+// exact zeros without fp64 work (on GB300 every fp64 warp instruction holds
+// the SM sub-partition's fp64 pipe for 64 cycles, so idle warps' shuffle
+// trees would cost as much as busy ones').  Warp 0 adds the eight warp totals
+// in a shuffle tree and thread 0 writes out[0..NV-1].
+template <int NV>
+__device__ __forceinline__ void block_partials(const double (&v)[NV], bool warp_busy,
+                                               double* out) {
+  __shared__ double sw[NV][kPsThreads / 32];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  v0 = warp_sum(v0);
-  v1 = warp_sum(v1);
-  if (lane == 0) {
-    s0[w] = v0;
-    s1[w] = v1;
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    const double s = warp_busy ? warp_sum(v[j]) : 0.0;
+    if (lane == 0) sw[j][w] = s;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    double a = 0.0, b = 0.0;
-    for (int i = 0; i < kPsThreads / 32; ++i) {
-      a += s0[i];
-      b += s1[i];
+  if (w == 0) {
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      double a = (lane < kPsThreads / 32) ? sw[j][lane] : 0.0;
+#pragma unroll
+      for (int o = kPsThreads / 64; o > 0; o >>= 1) a += __shfl_down_sync(0xffffffffu, a, o);
+      if (lane == 0) out[j] = a;
     }
-    out[0] = a;
-    out[1] = b;
   }
 }
 
-// Sum of part[2*i + off], i < nparts, in one fixed order, in every thread.
-__device__ __forceinline__ double grid_total(const double* part, int nparts, int off) {
-  __shared__ double sh[kPsThreads / 32];
-  __shared__ double tot;
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  double a = 0.0;
-  for (int i = threadIdx.x; i < nparts; i += kPsThreads) a += __ldcg(part + 2 * i + off);
-  a = warp_sum(a);
-  if (lane == 0) sh[w] = a;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double b = 0.0;
-    for (int i = 0; i < kPsThreads / 32; ++i) b += sh[i];
-    tot = b;
+// Grid totals of NV values from the G blocks' partials part[NV*i + j], in one
+// fixed order (lane l adds the partials of blocks l, l+32, l+64, ... in turn,
+// then a shuffle tree), in lane 0 of the calling warp.  Called by warp 0 of
+// every block, so every block obtains the same numbers.  The loads of up to
+// 8 partials per lane are issued together, ahead of the adds: one L2 round
+// trip instead of one per partial.
+template <int NV>
+__device__ __forceinline__ void grid_totals(const double* part, int G, int lane,
+                                            double (&tot)[NV]) {
+  constexpr int U = 8;
+#pragma unroll
+  for (int j = 0; j < NV; ++j) tot[j] = 0.0;
+  for (int i0 = 0; i0 < G; i0 += 32 * U) {
+    double v[U][NV];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + 32 * u + lane;
+#pragma unroll
+      for (int j = 0; j < NV; ++j) v[u][j] = (i < G) ? __ldcg(part + NV * i + j) : 0.0;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+#pragma unroll
+      for (int j = 0; j < NV; ++j) tot[j] += v[u][j];
+    }
   }
-  __syncthreads();
-  return tot;
+#pragma unroll
+  for (int j = 0; j < NV; ++j) tot[j] = warp_sum(tot[j]);
 }
 
 template <bool VARY, bool RESID>
@@ -86,75 +105,113 @@ __global__ void __launch_bounds__(kPsThreads) k_pcg_persistent(Op op, DevState* 
                                                                double* __restrict__ hist,
                                                                int seglen,
                                                                unsigned int absent) {
+  // the scalars of Algorithm 1 live in thread 0 of each block, which takes
+  // the scalar steps; the rest of the block reads alpha, beta and whether
+  // the loop goes on from shared memory after a block barrier
+  __shared__ double sh_alpha, sh_beta;
+  __shared__ int sh_go;
   const int lane = threadIdx.x & 31;
   // warps numbered across the blocks first, so that few tiles still spread
   // over every SM of the grid (one block per SM)
   const long long warp0 = (long long)(threadIdx.x >> 5) * gridDim.x + blockIdx.x;
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
   const unsigned int G = gridDim.x;
-  double* partM = partials;          // 2 per block: r*.r*, <r*, z>
-  double* partA = partials + 2 * G;  // 2 per block: <p, q>, unused
+  double* partM = partials;      // 2 per block: r*.r*, <r*, z>
+  double* partA = partials + 2 * G;  // 1 per block: <p, q>
   const uint64_t keep = l2_keep(), stream = l2_stream();
+  const long long nunits = op.ntiles * ((op.nz + seglen - 1) / seglen);
+  double alpha = 0.0, beta = 0.0;
+  // thread 0 only
   const double rtol = st->rtol;
   const int maxit = st->maxit;
-  const long long nunits = op.ntiles * ((op.nz + seglen - 1) / seglen);
-  double alpha = 0.0, beta = 0.0, kappa_old = 1.0, R0 = 0.0, R = 0.0, K = 0.0, S = 0.0;
+  double kappa_old = 1.0, R0 = 0.0, R = 0.0, K = 0.0, S = 0.0;
   int it = 0, iters = 0, status = kStOK;
   bool timeout = false;
+  // arrivals the grid barrier waits for; `absent` (0 in normal use) adds
+  // arrivals that never come, so that a test can make the wait run out
+  const unsigned int arrivals = G + absent;
+  unsigned int bar_target = 0u;
   for (;;) {
     // ---- Algorithm 3 sweep
-    double accR = 0.0, accK = 0.0;
+    double acc[2] = {0.0, 0.0};  // r*.r*, <r*, z>
     for (long long t = warp0; t < op.ntiles; t += nwarps)
-      precond_tile<VARY, true, true>(op, t, lane, r, q, z, -alpha, keep, stream, accR, accK);
-    block_partial2(accR, accK, partM + 2 * blockIdx.x);
-    if (!grid_barrier(&st->bar_count, &st->bar_gen, G + absent, &st->dev_error, kBarrierPolls)) {
+      precond_tile<VARY, true, true>(op, t, lane, r, q, z, -alpha, keep, stream, acc[0], acc[1]);
+    block_partials<2>(acc, warp0 < op.ntiles, partM + 2 * blockIdx.x);
+    bar_target += arrivals;
+    if (!grid_barrier(&st->bar_count, bar_target, &st->dev_error, kBarrierPolls,
+                      kBarrierWaitNs)) {
       timeout = true;
       break;
     }
-    R = grid_total(partM, G, 0);
-    K = grid_total(partM, G, 1);
-    // ---- the scalar step of Algorithm 1 (as finish_precond_sweep)
-    if (it == 0) R0 = R;
-    const double ratio = (R0 > 0.0) ? sqrt(R / R0) : 0.0;
-    if (blockIdx.x == 0 && threadIdx.x == 0) hist[it] = ratio;
-    bool done = true;
-    if (R0 == 0.0) {
-      // r_0 = 0: the initial guess solves the system
-    } else if (!(R < INFINITY) || !(R0 < INFINITY)) {
-      status = kStBreakdown;  // NaN or Inf in the residual
-    } else if (ratio < rtol || R == 0.0) {
-    } else if (it >= maxit) {
-      status = (rtol > 0.0) ? kStNotConv : kStOK;
-    } else if (!(K > 0.0)) {
-      status = kStBreakdown;
-    } else {
-      done = false;
+    if (threadIdx.x < 32) {
+      double tot[2];
+      grid_totals<2>(partM, G, lane, tot);
+      if (lane == 0) {
+        // ---- the scalar step of Algorithm 1 (as finish_precond_sweep)
+        R = tot[0];
+        K = tot[1];
+        if (it == 0) R0 = R;
+        const double ratio = (R0 > 0.0) ? sqrt(R / R0) : 0.0;
+        if (blockIdx.x == 0) hist[it] = ratio;
+        bool done = true;
+        if (R0 == 0.0) {
+          // r_0 = 0: the initial guess solves the system
+        } else if (!(R < INFINITY) || !(R0 < INFINITY)) {
+          status = kStBreakdown;  // NaN or Inf in the residual
+        } else if (ratio < rtol || R == 0.0) {
+        } else if (it >= maxit) {
+          status = (rtol > 0.0) ? kStNotConv : kStOK;
+        } else if (!(K > 0.0)) {
+          status = kStBreakdown;
+        } else {
+          done = false;
+        }
+        if (done) {
+          iters = it;
+        } else {
+          beta = K / kappa_old;
+          kappa_old = K;
+        }
+        ++it;
+        sh_beta = beta;
+        sh_go = done ? 0 : 1;
+      }
     }
-    if (done) {
-      iters = it++;
-      break;
-    }
-    beta = K / kappa_old;
-    kappa_old = K;
-    ++it;
+    __syncthreads();
+    if (!sh_go) break;
+    beta = sh_beta;
     // ---- Algorithm 2 sweep
-    double sig = 0.0;
+    double sig[1] = {0.0};
     for (long long unit = warp0; unit < nunits; unit += nwarps)
       spmv_unit<VARY, false, RESID, true>(op, unit, lane, z, r, u, p, q, alpha, beta, seglen,
-                                          sig);
-    block_partial2(sig, 0.0, partA + 2 * blockIdx.x);
-    if (!grid_barrier(&st->bar_count, &st->bar_gen, G + absent, &st->dev_error, kBarrierPolls)) {
+                                          sig[0]);
+    block_partials<1>(sig, warp0 < nunits, partA + blockIdx.x);
+    bar_target += arrivals;
+    if (!grid_barrier(&st->bar_count, bar_target, &st->dev_error, kBarrierPolls,
+                      kBarrierWaitNs)) {
       timeout = true;
       break;
     }
-    S = grid_total(partA, G, 0);
-    if (!(S > 0.0) || !(S < INFINITY)) {
-      alpha = 0.0;
-      iters = it - 1;
-      status = kStBreakdown;
-      break;
+    if (threadIdx.x < 32) {
+      double tot[1];
+      grid_totals<1>(partA, G, lane, tot);
+      if (lane == 0) {
+        S = tot[0];
+        const bool ok = (S > 0.0) && (S < INFINITY);
+        if (ok) {
+          alpha = kappa_old / S;
+        } else {
+          alpha = 0.0;
+          iters = it - 1;
+          status = kStBreakdown;
+        }
+        sh_alpha = alpha;
+        sh_go = ok ? 1 : 0;
+      }
     }
-    alpha = kappa_old / S;
+    __syncthreads();
+    if (!sh_go) break;
+    alpha = sh_alpha;
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     st->alpha = alpha;
