@@ -509,16 +509,18 @@ def run_ours(args, w):
                      "vs_fused_min_88": (t_m + t_a) / (88.0 * n),
                      "vs_algorithmic": (t_m + t_a) / bytes_iter}
 
-    # end to end through the host-buffer entry point: pinned b in, x out, zero
-    # initial guess (pcg_solve_host_x0 with x0 = NULL); one page-locked output
-    # buffer for every step, as a caller solving repeatedly would keep it
+    # end to end through the host-buffer entry point that takes the step's
+    # coefficients and right-hand side together (pcg_update_solve_host with
+    # x0 = NULL): pinned b in -- copied while the set-up kernels run -- and x
+    # out; one page-locked output buffer for every step, as a caller solving
+    # repeatedly would keep it
     e2e = None
     if not args.no_e2e:
         nsteps = args.steps
         bh = torch.from_numpy(b).pin_memory()
         xh = torch.zeros(n, dtype=torch.float64).pin_memory()
-        solver.update_coeffs(**coeffs)
-        solver.solve_host(bh, xh, rtol=w.rtol, maxit=w.maxit, history=False, x0=None)  # warm-up
+        solver.update_solve_host(bh, xh, rtol=w.rtol, maxit=w.maxit, history=False, x0=None,
+                                 **coeffs)  # warm-up
         barrier()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
@@ -526,17 +528,18 @@ def run_ours(args, w):
         step_ms = []
         for _ in range(nsteps):
             ts = time.perf_counter()
-            solver.update_coeffs(**coeffs)
-            it, _, st = solver.solve_host(bh, xh, rtol=w.rtol, maxit=w.maxit, history=False,
-                                          x0=None)
+            it, _, st = solver.update_solve_host(bh, xh, rtol=w.rtol, maxit=w.maxit,
+                                                 history=False, x0=None, **coeffs)
             e2e_it += it
             step_ms.append(round(1e3 * (time.perf_counter() - ts), 3))
         torch.cuda.synchronize()
         t_e2e = time.perf_counter() - t0
         t_e2e_ms, e2e_iters = reduce_over_ranks(1e3 * t_e2e, e2e_it, dev)
         e2e = {"value": e2e_iters / (1e-3 * t_e2e_ms), "unit": UNIT,
-               "h2d_bytes_per_step": 8 * n, "d2h_bytes_per_step": 8 * n,
-               "api": "pcg_solve_host_x0 (x0 = 0)", "steps": nsteps, "step_ms": step_ms}
+               # b, plus the coefficient arrays the step hands over (a_h field, dz)
+               "h2d_bytes_per_step": 8 * n + (8 * w.nx * w.ny if varying else 0) + 8 * w.nz,
+               "d2h_bytes_per_step": 8 * n,
+               "api": "pcg_update_solve_host (x0 = 0)", "steps": nsteps, "step_ms": step_ms}
         del xh, bh
 
     cpu = None

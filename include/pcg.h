@@ -321,6 +321,24 @@ int pcg_solve_host(pcg_ctx* ctx, const double* b_host, double* x_host, double rt
 int pcg_solve_host_x0(pcg_ctx* ctx, const double* b_host, const double* x0_host, double* x_host,
                       double rtol, int maxit, int* iters_out, double* res_hist);
 
+/* pcg_update_coeffs followed by pcg_solve_host_x0, in one call, for callers
+ * that replace the coefficients before every solve: the copies of b and x0
+ * go in on a second stream of the context while the set-up kernels of the
+ * new coefficients run (section 6: the vertical coefficient vectors and the
+ * right-hand side are copied to the device, the solution back).
+ *   coeffs   as pcg_update_coeffs (read during the call);
+ *   b_host, x0_host, x_host, rtol, maxit, iters_out, res_hist
+ *            as pcg_solve_host_x0.
+ * b_host and x0_host must hold their values when the call is made: they are
+ * read at once, not after earlier work on the context's stream.  With
+ * page-locked host memory the host-to-device copies overlap the set-up; with
+ * pageable memory the host copies while the set-up runs.  Synchronous.
+ * Errors: those of pcg_update_coeffs (checked first; on PCG_EBREAKDOWN for a
+ * non-positive pivot nothing is solved) and of pcg_solve_host_x0. */
+int pcg_update_solve_host(pcg_ctx* ctx, const pcg_coeffs* coeffs, const double* b_host,
+                          const double* x0_host, double* x_host, double rtol, int maxit,
+                          int* iters_out, double* res_hist);
+
 /* z = M^{-1} r and *rz_dev = <r, z>, without allocating anything.
  * The paper has no counterpart: this entry point exists for callers that
  * must not allocate device memory while they run -- for instance code that

@@ -10,6 +10,7 @@
 #include <cstdio>
 #include <cstring>
 #include <algorithm>
+#include <functional>
 #include <new>
 #include <string>
 #include <vector>
@@ -96,6 +97,9 @@ struct pcg_ctx {
   int hist_cap = 0;
   DevState* state = nullptr;
   double *b_host_api = nullptr, *x_host_api = nullptr;  // device copies for pcg_solve_host
+  // second stream of pcg_update_solve_host: b and x0 go in while the set-up runs
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t copy_done = nullptr;
   DevState* pinned = nullptr;                           // 3 host slots
   int grid_m = 1, grid_a = 1;
   long long last_launches = 0;
@@ -237,6 +241,10 @@ void free_all(pcg_ctx* ctx) {
   }
   if (ctx->cap_stream) cudaStreamDestroy(ctx->cap_stream);
   ctx->cap_stream = nullptr;
+  if (ctx->copy_done) cudaEventDestroy(ctx->copy_done);
+  ctx->copy_done = nullptr;
+  if (ctx->copy_stream) cudaStreamDestroy(ctx->copy_stream);
+  ctx->copy_stream = nullptr;
   mg_release(ctx);
 }
 
@@ -483,7 +491,11 @@ cudaError_t mg_enqueue(pcg_ctx* ctx, const Op& op0, double* b0, double* out, boo
   return e;
 }
 
-int load_coeffs(pcg_ctx* ctx, const pcg_coeffs* c, bool varying) {
+// `meanwhile`, when given, is called once the set-up work is enqueued and
+// before the host waits for it: work it enqueues on another stream runs
+// alongside the set-up.
+int load_coeffs(pcg_ctx* ctx, const pcg_coeffs* c, bool varying,
+                const std::function<cudaError_t()>& meanwhile = {}) {
   ctx->config_gen++;  // the sweeps' template choice follows op.varying
   std::vector<double> lev;
   int st = build_levels(ctx, ctx->op.nz, c, varying, lev);
@@ -518,6 +530,10 @@ int load_coeffs(pcg_ctx* ctx, const pcg_coeffs* c, bool varying) {
                                    ctx->cwN_t, ctx->tnphi, ctx->tinvd, ctx->stream);
     if (t1) cudaEventRecord(t1, ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "coefficient set-up kernels");
+    if (meanwhile) {
+      e = meanwhile();
+      if (e != cudaSuccess) return cuda_fail(ctx, e, "host-to-device copy");
+    }
     int bad = 0;
     e = cudaMemcpyAsync(&bad, &ctx->state->setup_error, sizeof(int), cudaMemcpyDeviceToHost,
                         ctx->stream);
@@ -534,6 +550,10 @@ int load_coeffs(pcg_ctx* ctx, const pcg_coeffs* c, bool varying) {
     if (e != cudaSuccess) return cuda_fail(ctx, e, "coefficient set-up");
     if (bad) return fail(ctx, PCG_EBREAKDOWN, "a Thomas pivot of some column is not positive");
   } else {
+    if (meanwhile) {
+      e = meanwhile();
+      if (e != cudaSuccess) return cuda_fail(ctx, e, "host-to-device copy");
+    }
     e = cudaStreamSynchronize(ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "coefficient upload");
   }
@@ -1318,18 +1338,43 @@ int pcg_solve(pcg_ctx* ctx, const double* b_dev, double* x_dev, double rtol, int
   return solve_device(ctx, b_dev, x_dev, rtol, maxit, iters_out, res_hist);
 }
 
+// Device copies of b and x for the host-buffer entry points (made on first use).
+static cudaError_t host_api_buffers(pcg_ctx* ctx) {
+  cudaError_t e = cudaSuccess;
+  if (!ctx->b_host_api) e = dalloc(&ctx->b_host_api, ctx->op.n);
+  if (e == cudaSuccess && !ctx->x_host_api) e = dalloc(&ctx->x_host_api, ctx->op.n);
+  return e;
+}
+
+static int check_host_x0(pcg_ctx* ctx, const double* b_host, const double* x0_host,
+                         const double* x_host) {
+  if (x0_host && x0_host != x_host && overlap(b_host, x0_host, ctx->op.n))
+    return fail(ctx, PCG_EINVAL, "b and x0 overlap");
+  return PCG_OK;
+}
+
+// Solve from the device copies, then copy x out and wait for it.
+static int solve_copy_out(pcg_ctx* ctx, double* x_host, double rtol, int maxit, int* iters_out,
+                          double* res_hist) {
+  int st = solve_device(ctx, ctx->b_host_api, ctx->x_host_api, rtol, maxit, iters_out, res_hist);
+  if (st != PCG_OK && st != PCG_ENOTCONV && st != PCG_EBREAKDOWN) return st;
+  const size_t bytes = sizeof(double) * (size_t)ctx->op.n;
+  cudaError_t e =
+      cudaMemcpyAsync(x_host, ctx->x_host_api, bytes, cudaMemcpyDeviceToHost, ctx->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "device-to-host copy");
+  return st;
+}
+
 int pcg_solve_host_x0(pcg_ctx* ctx, const double* b_host, const double* x0_host, double* x_host,
                       double rtol, int maxit, int* iters_out, double* res_hist) {
   if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
   int st = check_solve_args(ctx, b_host, x_host, rtol, maxit);
+  if (!st) st = check_host_x0(ctx, b_host, x0_host, x_host);
   if (st) return st;
-  if (x0_host && x0_host != x_host && overlap(b_host, x0_host, ctx->op.n))
-    return fail(ctx, PCG_EINVAL, "b and x0 overlap");
   DeviceGuard g(ctx->device);
   if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
-  cudaError_t e = cudaSuccess;
-  if (!ctx->b_host_api) e = dalloc(&ctx->b_host_api, ctx->op.n);
-  if (e == cudaSuccess && !ctx->x_host_api) e = dalloc(&ctx->x_host_api, ctx->op.n);
+  cudaError_t e = host_api_buffers(ctx);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "device buffers for b and x");
   const size_t bytes = sizeof(double) * (size_t)ctx->op.n;
   e = cudaMemcpyAsync(ctx->b_host_api, b_host, bytes, cudaMemcpyHostToDevice, ctx->stream);
@@ -1338,12 +1383,53 @@ int pcg_solve_host_x0(pcg_ctx* ctx, const double* b_host, const double* x0_host,
                                   ctx->stream)
                 : cudaMemsetAsync(ctx->x_host_api, 0, bytes, ctx->stream);  // x0 = +0.0
   if (e != cudaSuccess) return cuda_fail(ctx, e, "host-to-device copy");
-  st = solve_device(ctx, ctx->b_host_api, ctx->x_host_api, rtol, maxit, iters_out, res_hist);
-  if (st != PCG_OK && st != PCG_ENOTCONV && st != PCG_EBREAKDOWN) return st;
-  e = cudaMemcpyAsync(x_host, ctx->x_host_api, bytes, cudaMemcpyDeviceToHost, ctx->stream);
+  return solve_copy_out(ctx, x_host, rtol, maxit, iters_out, res_hist);
+}
+
+int pcg_update_solve_host(pcg_ctx* ctx, const pcg_coeffs* coeffs, const double* b_host,
+                          const double* x0_host, double* x_host, double rtol, int maxit,
+                          int* iters_out, double* res_hist) {
+  if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
+  int st = validate_coeffs(ctx, ctx->op.nx, ctx->op.ny, ctx->op.nz, coeffs);
+  if (st) return st;
+  const bool varying = coeffs->a_h_field != nullptr;
+  if (varying && !ctx->has_field_buffers)
+    return fail(ctx, PCG_EINVAL,
+                "context was created with a constant a_h; it cannot take an a_h field");
+  st = check_solve_args(ctx, b_host, x_host, rtol, maxit);
+  if (!st) st = check_host_x0(ctx, b_host, x0_host, x_host);
+  if (st) return st;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
+  cudaError_t e = host_api_buffers(ctx);
+  if (e == cudaSuccess && !ctx->copy_stream)
+    e = cudaStreamCreateWithFlags(&ctx->copy_stream, cudaStreamNonBlocking);
+  if (e == cudaSuccess && !ctx->copy_done)
+    e = cudaEventCreateWithFlags(&ctx->copy_done, cudaEventDisableTiming);
+  // no earlier work on the context's stream may still use the device copies
   if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
-  if (e != cudaSuccess) return cuda_fail(ctx, e, "device-to-host copy");
-  return st;
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "device buffers for b and x");
+  const size_t bytes = sizeof(double) * (size_t)ctx->op.n;
+  bool copies_enqueued = false;
+  auto copy_in = [&]() -> cudaError_t {
+    copies_enqueued = true;
+    cudaError_t ce = cudaMemcpyAsync(ctx->b_host_api, b_host, bytes, cudaMemcpyHostToDevice,
+                                     ctx->copy_stream);
+    if (ce == cudaSuccess)
+      ce = x0_host ? cudaMemcpyAsync(ctx->x_host_api, x0_host, bytes, cudaMemcpyHostToDevice,
+                                     ctx->copy_stream)
+                   : cudaMemsetAsync(ctx->x_host_api, 0, bytes, ctx->copy_stream);  // x0 = +0.0
+    if (ce == cudaSuccess) ce = cudaEventRecord(ctx->copy_done, ctx->copy_stream);
+    return ce;
+  };
+  st = load_coeffs(ctx, coeffs, varying, copy_in);
+  if (st) {
+    if (copies_enqueued) cudaStreamSynchronize(ctx->copy_stream);
+    return st;
+  }
+  e = cudaStreamWaitEvent(ctx->stream, ctx->copy_done, 0);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "host-to-device copy");
+  return solve_copy_out(ctx, x_host, rtol, maxit, iters_out, res_hist);
 }
 
 int pcg_solve_host(pcg_ctx* ctx, const double* b_host, double* x_host, double rtol, int maxit,

@@ -31,6 +31,9 @@ namespace {
 // warps as possible: the fp64 pipe, not the issue rate, bounds them.
 
 constexpr int kPsThreads = 256;
+constexpr int kPsWarps = kPsThreads / 32;
+// lanes of the shuffle tree over the warps' sums: a power of two >= kPsWarps
+constexpr int kPsTree = kPsWarps <= 8 ? 8 : (kPsWarps <= 16 ? 16 : 32);
 // A barrier wait gives up with PCG_ETIMEOUT after a second of the global
 // timer, or after 2^24 polls (each an L2 round trip plus a 32 ns sleep).
 constexpr long long kBarrierPolls = 1LL << 24;
@@ -45,7 +48,7 @@ constexpr unsigned long long kBarrierWaitNs = 1000000000ull;
 template <int NV>
 __device__ __forceinline__ void block_partials(const double (&v)[NV], bool warp_busy,
                                                double* out) {
-  __shared__ double sw[NV][kPsThreads / 32];
+  __shared__ double sw[NV][kPsWarps];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 #pragma unroll
   for (int j = 0; j < NV; ++j) {
@@ -56,9 +59,9 @@ __device__ __forceinline__ void block_partials(const double (&v)[NV], bool warp_
   if (w == 0) {
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
-      double a = (lane < kPsThreads / 32) ? sw[j][lane] : 0.0;
+      double a = (lane < kPsWarps) ? sw[j][lane] : 0.0;
 #pragma unroll
-      for (int o = kPsThreads / 64; o > 0; o >>= 1) a += __shfl_down_sync(0xffffffffu, a, o);
+      for (int o = kPsTree / 2; o > 0; o >>= 1) a += __shfl_down_sync(0xffffffffu, a, o);
       if (lane == 0) out[j] = a;
     }
   }

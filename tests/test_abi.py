@@ -78,6 +78,8 @@ def test_null_context_calls_fail_cleanly(lib):
     assert lib._lib.pcg_solve_host_x0(None, None, None, None, 1e-10, 10, None, None) == \
         lib.PCG_EINVAL
     assert lib._lib.pcg_update_coeffs(None, None) == lib.PCG_EINVAL
+    assert lib._lib.pcg_update_solve_host(None, None, None, None, None, 1e-10, 10, None,
+                                          None) == lib.PCG_EINVAL
     assert lib._lib.pcg_set_layout(None, lib.PCG_LAYOUT_TILED) == lib.PCG_EINVAL
     assert lib._lib.pcg_set_factors(None, lib.PCG_FACTORS_STORED) == lib.PCG_EINVAL
     assert lib._lib.pcg_set_substructuring(None, 0) == lib.PCG_EINVAL

@@ -154,6 +154,102 @@ def test_solve_is_bitwise_repeatable(layout):
     assert torch.equal(x1, x2)
 
 
+UPDATE_SOLVE_CASES = [
+    # nx, ny, nz, varying, graded, a_v, solver set-up
+    (30, 20, 32, True, True, 1e3, "default"),
+    (37, 29, 16, False, False, 1e2, "default"),     # cluster loop
+    (64, 48, 64, True, True, 1e4, "column"),
+    (40, 36, 33, True, True, 1e4, "multigrid"),
+    (96, 80, 24, True, True, 1e3, "persistent"),
+]
+
+
+def _setup(s, how):
+    if how == "column":
+        s.set_layout("column")
+    elif how == "multigrid":
+        s.set_preconditioner("multigrid")
+    elif how == "persistent":
+        s.set_loop("persistent")
+
+
+@pytest.mark.parametrize("cfg", UPDATE_SOLVE_CASES, ids=lambda c: "x".join(map(str, c[:3])) +
+                         "-" + c[6])
+def test_update_solve_host_equals_update_then_solve(cfg):
+    # the one-call form (b copied in on a second stream while the set-up of
+    # the new coefficients runs) gives the two-call form's results bit for
+    # bit, and the oracle's for the new coefficients
+    nx, ny, nz, varying, graded, a_v, how = cfg
+    prob, kw, b = case(nx, ny, nz, varying, graded, a_v=a_v, seed=31)
+    ah2 = prob.ah * 1.5 if varying else 0.75
+    kw2 = dict(kw, a_h_field=ah2 if varying else None, a_h=1.0 if varying else ah2,
+               a_v=2.0 * a_v, mass=0.5)
+    prob2 = oracle.Problem(nx, ny, nz, ah=ah2, a_v=2.0 * a_v, mass=0.5, h=prob.h)
+    bh = torch.from_numpy(b).pin_memory()
+    with mf.Solver(nx, ny, nz, **kw) as s:
+        _setup(s, how)
+        x1 = torch.full((prob.n,), float("nan"), dtype=torch.float64).pin_memory()
+        i1, h1, st1 = s.update_solve_host(bh, x1, rtol=1e-10, x0=None, **kw2)
+        x2 = np.full(prob.n, np.nan)                # pageable output and input
+        i2, h2, st2 = s.update_solve_host(b, x2, rtol=1e-10, x0=None, **kw2)
+    if how == "multigrid":
+        x_ref, it_ref, _, _ = oracle.mg_pcg(prob2, b, rtol=1e-10)
+    else:
+        x_ref, it_ref, _, _ = oracle.pcg(prob2, b, rtol=1e-10)
+    with mf.Solver(nx, ny, nz, **kw) as s:
+        _setup(s, how)
+        s.update_coeffs(**kw2)
+        x3 = np.zeros(prob.n)
+        i3, h3, st3 = s.solve_host(b, x3, rtol=1e-10, x0=None)
+        # the iterate at the oracle's count
+        x4 = np.zeros(prob.n)
+        i4, _, st4 = s.update_solve_host(b, x4, rtol=0.0, maxit=it_ref, x0=None, **kw2)
+    assert st1 == st2 == st3 == mf.PCG_OK and i1 == i2 == i3
+    assert np.array_equal(h1, h3) and np.array_equal(h2, h3)
+    assert np.array_equal(x1.numpy(), x3) and np.array_equal(x2, x3)
+    assert abs(i1 - it_ref) <= 1 and (i4, st4) == (it_ref, mf.PCG_OK)
+    assert np.linalg.norm(x4 - x_ref) <= SOL_TOL * np.linalg.norm(x_ref)
+
+
+def test_update_solve_host_initial_guess_and_errors():
+    prob, kw, b = case(30, 26, 24, True, True, a_v=1e3, seed=32)
+    x0 = np.random.default_rng(33).standard_normal(prob.n)
+    with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        x = np.full(prob.n, np.nan)
+        it, hist, st = s.update_solve_host(b, x, rtol=1e-9, x0=x0, **kw)
+        x_ref, it_ref, _, _ = oracle.pcg(prob, b, x0=x0, rtol=1e-9)
+        assert st == mf.PCG_OK and abs(it - it_ref) <= 1
+        assert np.linalg.norm(x - x_ref) <= 1e-7 * np.linalg.norm(x_ref)
+        xio = x0.copy()                             # x0 and x the same buffer
+        it2, hist2, st2 = s.update_solve_host(b, xio, rtol=1e-9, x0=xio, **kw)
+        assert (it2, st2) == (it, st) and np.array_equal(xio, x) and np.array_equal(hist2, hist)
+        # stopped at maxit: the last iterate comes back
+        it3, _, st3 = s.update_solve_host(b, x, rtol=1e-9, maxit=3, x0=None, **kw)
+        assert (it3, st3) == (3, mf.PCG_ENOTCONV) and np.all(np.isfinite(x))
+        bad = b.copy()
+        bad[11] = np.nan
+        _, _, st4 = s.update_solve_host(bad, x, rtol=1e-9, x0=None, **kw)
+        assert st4 == mf.PCG_EBREAKDOWN
+        for args, kwargs in [((b, b), dict(x0=None)),          # b and x overlap
+                             ((b, x), dict(x0=b))]:            # b and x0 overlap
+            with pytest.raises(mf.PCGError) as e:
+                s.update_solve_host(*args, rtol=1e-9, **kwargs, **kw)
+            assert e.value.status == mf.PCG_EINVAL
+        with pytest.raises(mf.PCGError) as e:
+            s.update_solve_host(b, x, rtol=1e-9, **dict(kw, mass=0.0))
+        assert e.value.status == mf.PCG_EINVAL
+        # the context still solves normally afterwards
+        it5, _, st5 = s.update_solve_host(b, x, rtol=1e-9, x0=x0, **kw)
+        assert (it5, st5) == (it, st)
+    # a context made with a constant a_h takes no field, and solves nothing
+    prob_c, kw_c, b_c = case(16, 12, 8, False, True, a_v=1e2, seed=34)
+    with mf.Solver(prob_c.nx, prob_c.ny, prob_c.nz, **kw_c) as s:
+        xc = np.full(prob_c.n, 7.0)
+        with pytest.raises(mf.PCGError) as e:
+            s.update_solve_host(b_c, xc, x0=None, **dict(kw_c, a_h_field=np.ones(16 * 12)))
+        assert e.value.status == mf.PCG_EINVAL and np.all(xc == 7.0)
+
+
 def test_solve_host_equals_solve_device():
     prob, kw, b = case(30, 20, 32, True, True, a_v=1e3, seed=6)
     with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
