@@ -100,6 +100,10 @@ struct pcg_ctx {
   // second stream of pcg_update_solve_host: b and x0 go in while the set-up runs
   cudaStream_t copy_stream = nullptr;
   cudaEvent_t copy_done = nullptr;
+  // set by the host-buffer entry points right before their solve (and taken
+  // back at its start): the initial guess is zero and its device copy was not
+  // written, so the row-tiled start reads no x
+  bool x0_zero = false;
   DevState* pinned = nullptr;                           // 3 host slots
   int grid_m = 1, grid_a = 1;
   long long last_launches = 0;
@@ -719,6 +723,8 @@ void read_batch_times(const BatchGraph& g, int iters, std::vector<float>& tm_m,
 
 int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxit,
                  int* iters_out, double* res_hist) {
+  const bool x0_zero_given = ctx->x0_zero;
+  ctx->x0_zero = false;
   cudaError_t e;
   if (maxit + 1 > ctx->hist_cap) {
     double* nh = nullptr;
@@ -745,8 +751,14 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
   // and p = q = 0 at its own positions in the same launch.  On large grids a
   // pass over x0 first finds out whether it is all +0.0, so that the start
   // reads neither x0 nor its neighbours then (small grids: one launch less).
-  const bool x0_check = tiled && op.n >= (1LL << 22);
-  if (x0_check) {
+  // A zero initial guess that a host-buffer entry point did not copy in needs
+  // no pass at all: the flag is cleared and x is never read.
+  const bool x0_zero = x0_zero_given && tiled;
+  const bool x0_check = tiled && (x0_zero || op.n >= (1LL << 22));
+  if (x0_zero) {
+    e = cudaMemsetAsync(&ctx->state->x0_nonzero, 0, sizeof(int), s);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "initial guess flag");
+  } else if (x0_check) {
     e = timed(ctx, PCG_K_RESIDUAL,
               [&] { return pcg::launch_x0_nonzero(x, op.n, ctx->state, ctx->num_sms, s); });
     if (e != cudaSuccess) return cuda_fail(ctx, e, "initial guess check launch");
@@ -1353,9 +1365,17 @@ static int check_host_x0(pcg_ctx* ctx, const double* b_host, const double* x0_ho
   return PCG_OK;
 }
 
+// A zero initial guess (x0_host NULL) is set on the device only where the
+// solve reads it: the column layout's start does, the row-tiled start is told
+// instead (pcg_ctx::x0_zero).
+static bool zero_x0_skips_copy(const pcg_ctx* ctx, const double* x0_host) {
+  return !x0_host && ctx->layout == PCG_LAYOUT_TILED;
+}
+
 // Solve from the device copies, then copy x out and wait for it.
-static int solve_copy_out(pcg_ctx* ctx, double* x_host, double rtol, int maxit, int* iters_out,
-                          double* res_hist) {
+static int solve_copy_out(pcg_ctx* ctx, bool x0_zero, double* x_host, double rtol, int maxit,
+                          int* iters_out, double* res_hist) {
+  ctx->x0_zero = x0_zero;
   int st = solve_device(ctx, ctx->b_host_api, ctx->x_host_api, rtol, maxit, iters_out, res_hist);
   if (st != PCG_OK && st != PCG_ENOTCONV && st != PCG_EBREAKDOWN) return st;
   const size_t bytes = sizeof(double) * (size_t)ctx->op.n;
@@ -1377,13 +1397,14 @@ int pcg_solve_host_x0(pcg_ctx* ctx, const double* b_host, const double* x0_host,
   cudaError_t e = host_api_buffers(ctx);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "device buffers for b and x");
   const size_t bytes = sizeof(double) * (size_t)ctx->op.n;
+  const bool x0_zero = zero_x0_skips_copy(ctx, x0_host);
   e = cudaMemcpyAsync(ctx->b_host_api, b_host, bytes, cudaMemcpyHostToDevice, ctx->stream);
-  if (e == cudaSuccess)
-    e = x0_host ? cudaMemcpyAsync(ctx->x_host_api, x0_host, bytes, cudaMemcpyHostToDevice,
-                                  ctx->stream)
-                : cudaMemsetAsync(ctx->x_host_api, 0, bytes, ctx->stream);  // x0 = +0.0
+  if (e == cudaSuccess && x0_host)
+    e = cudaMemcpyAsync(ctx->x_host_api, x0_host, bytes, cudaMemcpyHostToDevice, ctx->stream);
+  if (e == cudaSuccess && !x0_host && !x0_zero)
+    e = cudaMemsetAsync(ctx->x_host_api, 0, bytes, ctx->stream);  // x0 = +0.0
   if (e != cudaSuccess) return cuda_fail(ctx, e, "host-to-device copy");
-  return solve_copy_out(ctx, x_host, rtol, maxit, iters_out, res_hist);
+  return solve_copy_out(ctx, x0_zero, x_host, rtol, maxit, iters_out, res_hist);
 }
 
 int pcg_update_solve_host(pcg_ctx* ctx, const pcg_coeffs* coeffs, const double* b_host,
@@ -1410,15 +1431,17 @@ int pcg_update_solve_host(pcg_ctx* ctx, const pcg_coeffs* coeffs, const double* 
   if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "device buffers for b and x");
   const size_t bytes = sizeof(double) * (size_t)ctx->op.n;
+  const bool x0_zero = zero_x0_skips_copy(ctx, x0_host);
   bool copies_enqueued = false;
   auto copy_in = [&]() -> cudaError_t {
     copies_enqueued = true;
     cudaError_t ce = cudaMemcpyAsync(ctx->b_host_api, b_host, bytes, cudaMemcpyHostToDevice,
                                      ctx->copy_stream);
-    if (ce == cudaSuccess)
-      ce = x0_host ? cudaMemcpyAsync(ctx->x_host_api, x0_host, bytes, cudaMemcpyHostToDevice,
-                                     ctx->copy_stream)
-                   : cudaMemsetAsync(ctx->x_host_api, 0, bytes, ctx->copy_stream);  // x0 = +0.0
+    if (ce == cudaSuccess && x0_host)
+      ce = cudaMemcpyAsync(ctx->x_host_api, x0_host, bytes, cudaMemcpyHostToDevice,
+                           ctx->copy_stream);
+    if (ce == cudaSuccess && !x0_host && !x0_zero)
+      ce = cudaMemsetAsync(ctx->x_host_api, 0, bytes, ctx->copy_stream);  // x0 = +0.0
     if (ce == cudaSuccess) ce = cudaEventRecord(ctx->copy_done, ctx->copy_stream);
     return ce;
   };
@@ -1429,7 +1452,7 @@ int pcg_update_solve_host(pcg_ctx* ctx, const pcg_coeffs* coeffs, const double* 
   }
   e = cudaStreamWaitEvent(ctx->stream, ctx->copy_done, 0);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "host-to-device copy");
-  return solve_copy_out(ctx, x_host, rtol, maxit, iters_out, res_hist);
+  return solve_copy_out(ctx, x0_zero, x_host, rtol, maxit, iters_out, res_hist);
 }
 
 int pcg_solve_host(pcg_ctx* ctx, const double* b_host, double* x_host, double rtol, int maxit,

@@ -241,6 +241,13 @@ def test_update_solve_host_initial_guess_and_errors():
         # the context still solves normally afterwards
         it5, _, st5 = s.update_solve_host(b, x, rtol=1e-9, x0=x0, **kw)
         assert (it5, st5) == (it, st)
+        # a zero initial guess from the host call is not carried into the next
+        # device solve, whose x0 is read as usual
+        s.update_solve_host(b, x, rtol=1e-9, x0=None, **kw)
+        xd = torch.from_numpy(x0).to(DEV)
+        it6, _, st6 = s.solve(torch.from_numpy(b).to(DEV), xd, rtol=1e-9)
+        assert (it6, st6) == (it, st)
+        assert np.linalg.norm(xd.cpu().numpy() - x_ref) <= 1e-7 * np.linalg.norm(x_ref)
     # a context made with a constant a_h takes no field, and solves nothing
     prob_c, kw_c, b_c = case(16, 12, 8, False, True, a_v=1e2, seed=34)
     with mf.Solver(prob_c.nx, prob_c.ny, prob_c.nz, **kw_c) as s:
