@@ -56,7 +56,7 @@ typedef enum {
   PCG_ECUDA = 3,       /* a CUDA runtime call failed (no device, launch error, ...) */
   PCG_ENOTCONV = 4,    /* rtol > 0 and maxit iterations did not reach it */
   PCG_EBREAKDOWN = 5,  /* <p,Ap> <= 0, <r,z> <= 0 or a non-finite residual (NaN/Inf input) */
-  PCG_ETIMEOUT = 6     /* a bounded device wait (bulk-copy completion) ran out; reported by pcg_solve */
+  PCG_ETIMEOUT = 6     /* a bounded device wait (a grid barrier of the persistent loop) ran out; reported by pcg_solve */
 } pcg_status;
 
 typedef struct pcg_ctx pcg_ctx; /* opaque; owns every internal device buffer */
@@ -177,7 +177,8 @@ int pcg_set_substructuring(pcg_ctx* ctx, int nblocks);
  *                        70 K with a constant one);
  *   PCG_LOOP_AUTO        (default) the cluster loop where the grid fits,
  *                        else persistent for grids with fewer tiles of 32
- *                        columns than 4 per SM, else batched.
+ *                        columns than 4 per SM, or than 16 per SM with at
+ *                        most 6 * 2^20 cells, else batched.
  * The persistent and cluster loops need Thomas column solves (no
  * substructuring), stored factors and the line preconditioner; the cluster
  * loop also the residual form of A z (pcg_set_az_form), and a device that

@@ -620,9 +620,14 @@ bool overlap(const double* a, const double* b, long long n) {
 }
 
 // Grids that the automatic loop choice runs persistent (and the layout the
-// automatic choices assume: row-tiled).
+// automatic choices assume: row-tiled): fewer than 4 tiles of 32 columns per
+// SM, where the batched sweeps are launch-bound, and up to 16 per SM while the
+// grid has at most 6 M cells, where the persistent loop's 16 warps per SM
+// still beat the batched sweeps (256x256x64: 137 against 146 us per
+// iteration; at 384x384x64 the two are level).
 bool persistent_grid(const pcg_ctx* ctx) {
-  return ctx->grid_ps > 0 && ctx->op.ntiles < 4LL * ctx->num_sms;
+  const long long nt = ctx->op.ntiles, sms = ctx->num_sms;
+  return ctx->grid_ps > 0 && (nt < 4 * sms || (nt < 16 * sms && ctx->op.n <= (6LL << 20)));
 }
 
 // The loop the next solve runs (PCG_LOOP_BATCHED, PCG_LOOP_PERSISTENT or

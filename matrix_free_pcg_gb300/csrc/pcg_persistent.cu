@@ -30,7 +30,7 @@ namespace {
 // final update read.  The reductions and the scalar steps run in as few
 // warps as possible: the fp64 pipe, not the issue rate, bounds them.
 
-constexpr int kPsThreads = 256;
+constexpr int kPsThreads = 512;  // 16 warps, 128 registers (the short chunks of precond_tile)
 constexpr int kPsWarps = kPsThreads / 32;
 // lanes of the shuffle tree over the warps' sums: a power of two >= kPsWarps
 constexpr int kPsTree = kPsWarps <= 8 ? 8 : (kPsWarps <= 16 ? 16 : 32);
@@ -98,7 +98,7 @@ __device__ __forceinline__ void grid_totals(const double* part, int G, int lane,
 }
 
 template <bool VARY, bool RESID>
-__global__ void __launch_bounds__(kPsThreads) k_pcg_persistent(Op op, DevState* st,
+__global__ void __launch_bounds__(kPsThreads, 1) k_pcg_persistent(Op op, DevState* st,
                                                                double* __restrict__ r,
                                                                double* __restrict__ q,
                                                                double* __restrict__ z,

@@ -24,6 +24,11 @@ namespace {
 constexpr int kTmThreads = kTmWarpsPerBlock * 32;
 constexpr int kTmChunk = 8;
 constexpr int kTmChunkB = 16;
+// The persistent loop's chunks (COHERENT): half as long, so that the whole
+// loop fits 128 registers and runs 16 warps per SM.  Its grids have at most
+// a few tiles per warp and live in L2, and its stencil phase needs the warps.
+constexpr int kTmChunkP = 4;
+constexpr int kTmChunkPB = 8;
 
 __device__ __forceinline__ long long tiled_base(long long col, int nz) {
   return (col >> 5) * (long long)nz * kTile + (col & 31);
@@ -51,9 +56,10 @@ __device__ __forceinline__ void precond_tile(const Op& op, long long t, int lane
   const double* __restrict__ fi = VARY ? op.tinvd + base : op.lev + LV_INVD * nz;
   const double* __restrict__ fn = VARY ? op.tnphi + base : op.lev + LV_NPHI * nz;
   // ---- forward: level k uses nphi_{k-1} (0 at k = 0) and 1/D_k
-  double cr[kTmChunk], cq[kTmChunk], ci[kTmChunk], cn[kTmChunk];
+  constexpr int CF = COHERENT ? kTmChunkP : kTmChunk;
+  double cr[CF], cq[CF], ci[CF], cn[CF];
 #pragma unroll
-  for (int j = 0; j < kTmChunk; ++j) {
+  for (int j = 0; j < CF; ++j) {
     const bool in = j < nz;
     cr[j] = in ? ld_hint(rt + j * kTile, stream) : 0.0;
     cq[j] = (FUSED && in) ? (COHERENT ? __ldcg(qt + j * kTile) : ld_hint(qt + j * kTile, stream))
@@ -63,11 +69,11 @@ __device__ __forceinline__ void precond_tile(const Op& op, long long t, int lane
   }
   double y = 0.0, nprev = 0.0, w = 0.0;
 #pragma unroll 1
-  for (int k0 = 0; k0 < nz; k0 += kTmChunk) {
-    double nr[kTmChunk], nq[kTmChunk], ni[kTmChunk], nn[kTmChunk];
+  for (int k0 = 0; k0 < nz; k0 += CF) {
+    double nr[CF], nq[CF], ni[CF], nn[CF];
 #pragma unroll
-    for (int j = 0; j < kTmChunk; ++j) {
-      const int k = k0 + kTmChunk + j;
+    for (int j = 0; j < CF; ++j) {
+      const int k = k0 + CF + j;
       const bool in = k < nz;
       nr[j] = in ? ld_hint(rt + k * kTile, stream) : 0.0;
       nq[j] = (FUSED && in) ? (COHERENT ? __ldcg(qt + k * kTile) : ld_hint(qt + k * kTile, stream))
@@ -76,7 +82,7 @@ __device__ __forceinline__ void precond_tile(const Op& op, long long t, int lane
       nn[j] = in ? (VARY ? ld_hint(fn + k * fs, keep) : __ldg(fn + k)) : 0.0;
     }
 #pragma unroll
-    for (int j = 0; j < kTmChunk; ++j) {
+    for (int j = 0; j < CF; ++j) {
       const int k = k0 + j;
       if (k < nz) {
         double rk = cr[j];
@@ -93,7 +99,7 @@ __device__ __forceinline__ void precond_tile(const Op& op, long long t, int lane
       }
     }
 #pragma unroll
-    for (int j = 0; j < kTmChunk; ++j) {
+    for (int j = 0; j < CF; ++j) {
       cr[j] = nr[j];
       cq[j] = nq[j];
       ci[j] = ni[j];
@@ -103,7 +109,7 @@ __device__ __forceinline__ void precond_tile(const Op& op, long long t, int lane
   // ---- backward: z_{nz-1} = w_{nz-1} (in place); level k uses nphi_k.  With a
   // constant a_h the factors come from the per-level table and the longer
   // chunk costs registers (218 against 167): 8 levels there.
-  constexpr int CB = VARY ? kTmChunkB : kTmChunk;
+  constexpr int CB = COHERENT ? (VARY ? kTmChunkPB : kTmChunkP) : (VARY ? kTmChunkB : kTmChunk);
   // Chunk b holds levels kb, kb-1, ..., kb-CB+1 with kb = nz-2-b*CB.
   double zz = w;
   if (SCALE) st_hint(zt + (long long)(nz - 1) * kTile, w * zscale, stream);

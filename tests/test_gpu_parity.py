@@ -701,6 +701,27 @@ def test_persistent_loop_choice_and_timing():
         assert s.launch_info()["last_solve_launches"] == 3   # residual, loop, final update
 
 
+def test_persistent_loop_automatic_choice_on_mid_grids():
+    # 1000 tiles (6.6 per SM): persistent by the cell-count rule, and equal to
+    # the oracle's iterate; 2048 tiles with 6.55 M cells: batched
+    prob, kw, b = case(200, 160, 24, True, True, a_v=1e3, seed=19)
+    with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        assert s.loop == "persistent"
+        x_ref, it_ref, _, _ = oracle.pcg(prob, b, rtol=1e-10)
+        bd = torch.from_numpy(b).to(DEV)
+        x = torch.zeros_like(bd)
+        it, _, st = s.solve(bd, x, rtol=1e-10)
+        assert st == mf.PCG_OK and abs(it - it_ref) <= 1
+        x.zero_()
+        it2, _, st2 = s.solve(bd, x, rtol=0.0, maxit=it_ref)
+        assert (it2, st2) == (it_ref, mf.PCG_OK)
+        assert np.linalg.norm(x.cpu().numpy() - x_ref) <= SOL_TOL * np.linalg.norm(x_ref)
+    with mf.Solver(256, 256, 100, a_h=1.0, a_v=1e3) as s:
+        assert s.loop == "batched"
+    with mf.Solver(256, 256, 96, a_h=1.0, a_v=1e3) as s:      # 6 * 2^20 cells
+        assert s.loop == "persistent"
+
+
 @pytest.mark.parametrize("cfg", SOLVE_CASES, ids=lambda c: "x".join(map(str, c[:3])))
 def test_persistent_and_batched_loops_agree(cfg):
     # the same sweeps in the same arithmetic; only the reduction trees differ
