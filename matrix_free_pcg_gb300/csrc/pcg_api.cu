@@ -133,6 +133,10 @@ int fail(pcg_ctx* ctx, int status, const char* fmt, ...) {
 }
 
 int cuda_fail(pcg_ctx* ctx, cudaError_t e, const char* what) {
+  // a failed runtime call also leaves its error as the thread's last error;
+  // taken back here, so that the next launch check of this or another context
+  // does not see it (a sticky error stays with the device whatever this does)
+  (void)cudaGetLastError();
   const int st = (e == cudaErrorMemoryAllocation) ? PCG_ENOMEM : PCG_ECUDA;
   return fail(ctx, st, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
