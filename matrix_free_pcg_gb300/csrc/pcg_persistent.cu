@@ -43,8 +43,8 @@ constexpr unsigned long long kBarrierWaitNs = 1000000000ull;
 // work in the sweep reduce their values with shuffles; the others contribute
 // exact zeros without fp64 work (on GB300 every fp64 warp instruction holds
 // the SM sub-partition's fp64 pipe for 64 cycles, so idle warps' shuffle
-// trees would cost as much as busy ones').  Warp 0 adds the eight warp totals
-// in a shuffle tree and thread 0 writes out[0..NV-1].
+// trees would cost as much as busy ones').  Warp 0 adds the warp totals in a
+// shuffle tree and thread 0 writes out[0..NV-1].
 template <int NV>
 __device__ __forceinline__ void block_partials(const double (&v)[NV], bool warp_busy,
                                                double* out) {
