@@ -100,7 +100,11 @@ def mg_vcycle_cost(nx, ny, nz, levels, nu, varying):
 L2_BYTES = 129e6                     # GB300 L2
 NOMINAL_HBM_GBS = 8000.0             # the ~8 TB/s HBM3e figure the fraction is also quoted on
 FUSED_MIN_BYTES = 88                 # u, p, z, q read + u, p, q written; r, q read + r, z written
-FP64_LANES_PER_SM_CLK = 2.0          # GB300 non-tensor fp64 rate: 2 FMA lanes per SM per clock
+FP64_LANES_PER_SM_CLK = 2.0          # GB300 nominal non-tensor fp64 rate: 2 FMA lanes per SM per clock
+# SURVEY-fixed algorithmic bytes per cell of the paper's fused kernels, with no
+# per-cell coefficients: the SpMV sweep reads u, p, z, q and writes u, p, q;
+# the preconditioner sweep reads r, q and writes r, z
+SURVEY_BYTES_SPMV, SURVEY_BYTES_PRECOND = 56, 32
 
 
 def parse():
@@ -135,6 +139,9 @@ def parse():
                     help="multigrid levels at most (0: coarsen while nx and ny are even)")
     ap.add_argument("--grid", type=int, nargs=3, metavar=("NX", "NY", "NZ"),
                     help="same coefficients on another grid size (profiling captures)")
+    ap.add_argument("--cpu-all", action="store_true",
+                    help="time the CPU oracle (1 thread) on every workload with its own "
+                         "stopping rule, one JSON line per workload (no GPU work)")
     return ap.parse_args()
 
 
@@ -231,13 +238,28 @@ def reduce_over_ranks(ms, iters, device):
     return float(t.item()), float(n.item())
 
 
-def alu_peak_g(dev, clocks):
-    """Nominal fp64 lane-ops/s (G) at the SM clock sampled under load."""
-    import torch
-    clk = clocks.summary() or {}
-    mhz = clk.get("sm_mhz") or 2070.0
-    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
-    return FP64_LANES_PER_SM_CLK * nsm * mhz * 1e6 / 1e9
+def host_cpu():
+    """(logical CPUs, CPU model name) of the host the oracle runs on."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        import platform
+        model = platform.processor() or platform.machine()
+    return os.cpu_count(), model
+
+
+def fp64_probe():
+    """The library's fp64-rate probe (8 independent FMA chains per thread, 32
+    warps per SM, the fastest of 3 launches of about 20 ms)."""
+    import matrix_free_pcg_gb300 as mf
+    return mf.pcg_measure_fp64_rate(32, 3)
 
 
 def sources_sha256(names):
@@ -318,9 +340,10 @@ def run_reference(args, w):
         tot_it += it
         tot_t += dt
     value = tot_it / tot_t
+    ncpu, model = host_cpu()
     sample = ("oracle_pcg on the full %dx%dx%d grid, %d fixed PCG iterations per step "
               "(initial residual and first preconditioner solve included), sequential C, "
-              "1 thread" % (w.nx, w.ny, w.nz, args.cpu_iters))
+              "1 thread of %d (%s)" % (w.nx, w.ny, w.nz, args.cpu_iters, ncpu, model))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -329,11 +352,40 @@ def run_reference(args, w):
         "config": {"workload": w.name, "grid": [w.nx, w.ny, w.nz], "iters_per_step":
                    args.cpu_iters, "l2": "inputs larger than L2"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "host_cpus": ncpu, "cpu_model": model, "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_cpu_all(args):
+    """The oracle as it stands, sequential C on 1 host thread, on all five
+    workloads with their own stopping rules (the CPU rows of the paper's
+    section 7 Tables 5 and 6): iterations, time to solution, iterations/s and
+    the bandwidth those iterations imply at the fused minimum of 88 B/cell."""
+    rank, _, _ = rank_info()
+    if rank != 0:
+        return 0
+    import oracle
+    ncpu, model = host_cpu()
+    for name in sorted(W.WORKLOADS, key=lambda k: W.WORKLOADS[k].n):
+        w = W.WORKLOADS[name]
+        h, ah, vec = workload_inputs(w)
+        b = oracle_rhs(w, h, ah, vec)
+        prob = oracle.Problem(w.nx, w.ny, w.nz, ah=ah, a_v=w.a_v, mass=w.mass, h=h)
+        t0 = time.perf_counter()
+        _, it, hist, st = oracle.pcg(prob, b, rtol=w.rtol, maxit=w.maxit)
+        dt = time.perf_counter() - t0
+        print(json.dumps({
+            "impl": "oracle", "workload": name, "grid": [w.nx, w.ny, w.nz], "cells": w.n,
+            "rtol": w.rtol, "maxit": w.maxit, "iters": it, "status": st,
+            "final_rel_residual": float(hist[-1]), "time_to_solution_s": dt,
+            "iters_per_s": it / dt, "fused_min_gbs": FUSED_MIN_BYTES * w.n * it / dt / 1e9,
+            "cores": 1, "host_cpus": ncpu, "cpu_model": model,
+            "what": "oracle_pcg from x0 = 0: initial residual, every iteration and the "
+                    "final update; sequential C, -O2 -ffp-contract=off"}), flush=True)
     return 0
 
 
@@ -379,6 +431,7 @@ def run_ours(args, w):
 
     for _ in range(max(args.warmup, 3)):
         step()
+    probe = fp64_probe()  # the measured fp64 rate, taken before the timed steps
 
     def barrier():
         if world > 1:
@@ -433,8 +486,11 @@ def run_ours(args, w):
         # and z (+ 2 factors)
         ops = {"apply_A": 8 if varying else 7, "precond": 3}
         byt = {"apply_A": 24 if varying else 16, "precond": 32 if varying else 16}
+        clk_s = clocks.summary() or {}
+        nsm_s = torch.cuda.get_device_properties(dev).multi_processor_count
+        peak_s = probe["lanes_per_sm_clk"] * nsm_s * (clk_s.get("sm_mhz") or probe["sm_mhz"]) / 1e3
         standalone = {k: {"ms": v, "fp64_gops": ops[k] * w.n / (v * 1e-3) / 1e9,
-                          "frac_fp64": ops[k] * w.n / (v * 1e-3) / 1e9 / alu_peak_g(dev, clocks),
+                          "frac_fp64": ops[k] * w.n / (v * 1e-3) / 1e9 / peak_s,
                           "gbs": byt[k] * w.n / (v * 1e-3) / 1e9,
                           "ops_per_cell": ops[k], "bytes_per_cell": byt[k]}
                       for k, v in out.items()}
@@ -469,20 +525,36 @@ def run_ours(args, w):
     ops_cell, bytes_cell = kinds[dom]
     sm_mhz = (clk or {}).get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
     nsm = torch.cuda.get_device_properties(dev).multi_processor_count
-    alu_peak = FP64_LANES_PER_SM_CLK * nsm * sm_mhz * 1e6 / 1e9  # G fp64 ops / s
+    # the measured fp64 rate: the probe's lane operations per SM per clock at
+    # the SM clock sampled during the timed steps (G fp64 ops / s)
+    alu_peak = probe["lanes_per_sm_clk"] * nsm * sm_mhz / 1e3
+    alu_nominal = FP64_LANES_PER_SM_CLK * nsm * sm_mhz * 1e6 / 1e9
     alu_ach = ops_cell * n / avg_s / 1e9
     hbm_ach = bytes_cell * n / avg_s / 1e9
     traffic = measured_traffic(dom, n, args.layout, args.factors, az_form)
+    # the same launch against HBM with the survey's algorithmic bytes (the
+    # paper's fused kernels without per-cell coefficients)
+    survey_cell = {"spmv_fused": SURVEY_BYTES_SPMV, "precond_fused": SURVEY_BYTES_PRECOND,
+                   "loop": FUSED_MIN_BYTES}[dom]
     roofline = {
         "bound": "alu", "kernel": "mg_vcycle" if (mgrid and dom == "precond_fused") else dom,
         "achieved": alu_ach, "peak": alu_peak,
         "unit": "G fp64 ops/s", "frac": alu_ach / alu_peak, "traffic": traffic,
-        "peak_source": "derived: %.0f fp64 lanes/SM/clk x %d SMs x %.0f MHz (median under load)"
-                       % (FP64_LANES_PER_SM_CLK, nsm, sm_mhz),
+        "peak_source": ("measured: fp64-rate probe %.3f lanes/SM/clk (8 independent FMA chains "
+                        "per thread, 32 warps/SM, %.0f MHz inside the probe) x %d SMs x %.0f MHz "
+                        "(median under load)" % (probe["lanes_per_sm_clk"], probe["sm_mhz"], nsm,
+                                                 sm_mhz)),
+        "peak_nominal": alu_nominal, "frac_nominal": alu_ach / alu_nominal,
+        "peak_nominal_source": "%.0f fp64 lanes/SM/clk x %d SMs x %.0f MHz"
+                               % (FP64_LANES_PER_SM_CLK, nsm, sm_mhz),
+        "fp64_probe": probe,
         "ops_per_cell": ops_cell, "bytes_per_cell": bytes_cell,
         "avg_launch_ms": avg_s * 1e3, "launches": dom_n,
         "hbm_achieved_gbs": hbm_ach, "hbm_peak_gbs": hbm_peak,
         "hbm_frac": hbm_ach / hbm_peak, "hbm_peak_source": peak_src,
+        "hbm_survey": {"bytes_per_cell": survey_cell,
+                       "achieved_gbs": survey_cell * n / avg_s / 1e9,
+                       "frac": survey_cell * n / avg_s / 1e9 / hbm_peak},
     }
     kernels = {k: {"ms": v[0], "launches": v[1]} for k, v in ktimes.items() if v[1]}
     # the iteration loop alone (both sweeps, or the persistent loop), per
@@ -497,7 +569,10 @@ def run_ours(args, w):
         "fused_min_gbs": FUSED_MIN_BYTES * n * iters_solve / (loop_ms * 1e-3) / 1e9,
     }
     loop_stats["algorithmic_frac"] = loop_stats["algorithmic_gbs"] / hbm_peak
+    loop_stats["fused_min_frac"] = loop_stats["fused_min_gbs"] / hbm_peak
     loop_stats["fused_min_frac_nominal_8tbs"] = loop_stats["fused_min_gbs"] / NOMINAL_HBM_GBS
+    loop_stats["fp64_gops"] = ops_iter * iters_solve / (loop_ms * 1e-3) / 1e9
+    loop_stats["fp64_frac"] = loop_stats["fp64_gops"] / alu_peak
     # DRAM bytes of one iteration (both sweeps, from the committed ncu captures)
     # against the fused minimum of 88 B/cell (u, p, z, q, r moved once, no
     # per-cell coefficients) and against this build's algorithmic bytes
@@ -523,35 +598,48 @@ def run_ours(args, w):
                                  **coeffs)  # warm-up
         barrier()
         torch.cuda.synchronize()
-        t0 = time.perf_counter()
+        t_e2e = 0.0
         e2e_it = 0
-        step_ms = []
+        step_ms, copy_ms = [], []
         for _ in range(nsteps):
             ts = time.perf_counter()
             it, _, st = solver.update_solve_host(bh, xh, rtol=w.rtol, maxit=w.maxit,
                                                  history=False, x0=None, **coeffs)
+            dt = time.perf_counter() - ts
+            t_e2e += dt
             e2e_it += it
-            step_ms.append(round(1e3 * (time.perf_counter() - ts), 3))
+            step_ms.append(round(1e3 * dt, 3))
+            # copy-only control, outside the timed total: the same bytes through
+            # the same page-locked buffers, one cudaMemcpyAsync each way, no solve
+            tc = time.perf_counter()
+            bd.copy_(bh, non_blocking=True)
+            xh.copy_(x, non_blocking=True)
+            torch.cuda.synchronize()
+            copy_ms.append(round(1e3 * (time.perf_counter() - tc), 3))
         torch.cuda.synchronize()
-        t_e2e = time.perf_counter() - t0
         t_e2e_ms, e2e_iters = reduce_over_ranks(1e3 * t_e2e, e2e_it, dev)
         e2e = {"value": e2e_iters / (1e-3 * t_e2e_ms), "unit": UNIT,
                # b, plus the coefficient arrays the step hands over (a_h field, dz)
                "h2d_bytes_per_step": 8 * n + (8 * w.nx * w.ny if varying else 0) + 8 * w.nz,
                "d2h_bytes_per_step": 8 * n,
-               "api": "pcg_update_solve_host (x0 = 0)", "steps": nsteps, "step_ms": step_ms}
+               "api": "pcg_update_solve_host (x0 = 0)", "steps": nsteps, "step_ms": step_ms,
+               "copy_only_ms": copy_ms,
+               "copy_only": "after each step, outside its time: the step's b in and x out "
+                            "through the same page-locked buffers, no solve"}
         del xh, bh
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         mgi = max(1, args.cpu_iters // 2) if mgrid else args.cpu_iters
         it_c, dt_c = cpu_oracle_sample(w, h, ah, oracle_rhs(w, h, ah, vec), mgi, mgrid)
+        ncpu, model = host_cpu()
         cpu = {"value": it_c / dt_c, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "host_cpus": ncpu, "cpu_model": model,
                "sample": "%s on the full %dx%dx%d grid, %d fixed PCG iterations "
                          "(initial residual and first preconditioner solve included), "
-                         "sequential C, 1 thread, %.1f s"
+                         "sequential C, 1 thread of %d (%s), %.1f s"
                          % ("oracle_mg_pcg" if mgrid else "oracle_pcg", w.nx, w.ny, w.nz, mgi,
-                            dt_c)}
+                            ncpu, model, dt_c)}
 
     if rank == 0:
         line = {
@@ -599,6 +687,8 @@ def main():
         nx, ny, nz = args.grid
         w = dataclasses.replace(w, name="%s_on_%dx%dx%d" % (w.name.rsplit("_", 1)[0], nx, ny, nz),
                                 nx=nx, ny=ny, nz=nz)
+    if args.cpu_all:
+        return run_cpu_all(args)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

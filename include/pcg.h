@@ -351,11 +351,12 @@ int pcg_update_solve_host(pcg_ctx* ctx, const pcg_coeffs* coeffs, const double* 
  * of 65,536 doubles (512 KB) compiled into the library, which every GPU that
  * loads the library holds until the process exits.
  *   r_dev, z_dev  device, N values each, must not overlap.
- *   rz_dev        device, 1 value: receives <r, z>.
+ *   rz_dev        device, 1 value: receives <r, z>; must not lie inside r or z.
  * Grids of more than 65,536 x 32 = 2,097,152 columns are rejected with
- * PCG_EINVAL.  The first call on a device looks up the device address of the
- * scratch array (cudaGetSymbolAddress); make that first call before any
- * stream capture.  All calls share the one array: calls that overlap on the
+ * PCG_EINVAL.  pcg_create looks up the device address of the scratch array
+ * (cudaGetSymbolAddress, which also loads the array's module on the device),
+ * so this call itself neither loads code nor allocates.  All calls share
+ * the one array: calls that overlap on the
  * GPU (from two streams or two host threads) race and give wrong results.
  * Asynchronous on the context's stream; calls no cudaMalloc, cudaFree or
  * other allocating routine. */
@@ -394,6 +395,23 @@ int pcg_kernel_times(pcg_ctx* ctx, double* ms_out /* PCG_K_COUNT */,
  * launched in its last call. */
 int pcg_launch_info(const pcg_ctx* ctx, int* grid_precond, int* grid_spmv,
                     long long* last_solve_launches);
+
+/* Measured fp64 rate of the current device's non-tensor pipe, the bound of
+ * the fused sweeps (their work is fp64 fused multiply-adds, products and sums;
+ * the paper reports measured rates per kernel, section 7 Table 7).  Runs one
+ * warm-up and `launches` timed launches (1..100, about 20 ms each) of a
+ * kernel whose threads each carry 8 independent chains of fp64 fused
+ * multiply-adds, warps_per_sm warps per SM (a multiple of 4 in [4, 64]), and
+ * reports the fastest launch:
+ *   *lane_ops_per_s    fp64 lane operations per second (an FMA counts one),
+ *   *sm_mhz            median SM clock inside that launch (clock64 against the
+ *                      global timer, per block),
+ *   *lanes_per_sm_clk  lane operations per SM per clock.
+ * Allocates and frees its own small buffers and stream; synchronous.  The
+ * error message of a failure is pcg_last_error(NULL).
+ * Errors: PCG_EINVAL, PCG_ENOMEM, PCG_ECUDA. */
+int pcg_measure_fp64_rate(int warps_per_sm, int launches, double* lane_ops_per_s,
+                          double* sm_mhz, double* lanes_per_sm_clk);
 
 #ifdef __cplusplus
 }

@@ -35,7 +35,8 @@ EXPORTED = ["pcg_create", "pcg_destroy", "pcg_update_coeffs", "pcg_set_stream", 
             "pcg_set_substructuring", "pcg_get_substructuring", "pcg_solve_host_x0",
             "pcg_set_loop", "pcg_get_loop", "pcg_test_barrier_absent", "pcg_set_az_form",
             "pcg_get_az_form", "pcg_set_preconditioner", "pcg_set_multigrid",
-            "pcg_get_multigrid", "pcg_mg_vcycle", "pcg_update_solve_host"]
+            "pcg_get_multigrid", "pcg_mg_vcycle", "pcg_update_solve_host",
+            "pcg_measure_fp64_rate"]
 PCG_LAYOUT_COLUMN, PCG_LAYOUT_TILED = 0, 1
 PCG_FACTORS_STORED, PCG_FACTORS_RECOMPUTE = 0, 1
 PCG_LOOP_AUTO, PCG_LOOP_BATCHED, PCG_LOOP_PERSISTENT, PCG_LOOP_CLUSTER = 0, 1, 2, 3
@@ -94,6 +95,7 @@ def _load(path=LIB_PATH):
         "pcg_mg_vcycle": (ctypes.c_int, [_vp, ctypes.c_void_p, ctypes.c_void_p]),
         "pcg_get_az_form": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int)]),
         "pcg_test_barrier_absent": (ctypes.c_int, [_vp, ctypes.c_int]),
+        "pcg_measure_fp64_rate": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _dp, _dp, _dp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -367,6 +369,18 @@ def pcg_launch_info(ctx):
     gm, ga, nl = ctypes.c_int(), ctypes.c_int(), ctypes.c_longlong()
     _check(_lib.pcg_launch_info(ctx, ctypes.byref(gm), ctypes.byref(ga), ctypes.byref(nl)), ctx)
     return {"grid_precond": gm.value, "grid_spmv": ga.value, "last_solve_launches": nl.value}
+
+
+def pcg_measure_fp64_rate(warps_per_sm=32, launches=3):
+    """Measured fp64 rate of the current device's non-tensor pipe: a dict with
+    lane operations per second (an FMA counts one), the SM clock measured
+    inside the fastest launch, and lane operations per SM per clock."""
+    rate, mhz, per_clk = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+    _check(_lib.pcg_measure_fp64_rate(int(warps_per_sm), int(launches), ctypes.byref(rate),
+                                      ctypes.byref(mhz), ctypes.byref(per_clk)))
+    return {"lane_ops_per_s": rate.value, "sm_mhz": mhz.value,
+            "lanes_per_sm_clk": per_clk.value, "warps_per_sm": int(warps_per_sm),
+            "launches": int(launches)}
 
 
 # ------------------------------------------------------------------- class

@@ -97,6 +97,9 @@ struct pcg_ctx {
   int hist_cap = 0;
   DevState* state = nullptr;
   double *b_host_api = nullptr, *x_host_api = nullptr;  // device copies for pcg_solve_host
+  // device address of the fixed scratch array of pcg_precond_dot_noalloc (not
+  // an allocation of the context: the array lives in the library's module)
+  double* noalloc_partials = nullptr;
   // second stream of pcg_update_solve_host: b and x0 go in while the set-up runs
   cudaStream_t copy_stream = nullptr;
   cudaEvent_t copy_done = nullptr;
@@ -1025,6 +1028,9 @@ int pcg_create(int nx, int ny, int nz, const pcg_coeffs* coeffs, pcg_ctx** out) 
     e = dalloc(&ctx->wscratch, (size_t)ctx->grid_m * pcg::kTile * nz);
   if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "workspace allocation"));
   op.wscratch = ctx->wscratch;
+  // device address of the allocation-free entry point's fixed scratch array
+  e = pcg::noalloc_scratch_address(&ctx->noalloc_partials);
+  if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "scratch address lookup"));
   st = load_coeffs(ctx, coeffs, varying);
   if (st) return bail(st);
   st = pcg_set_layout(ctx, PCG_LAYOUT_TILED);  // the default solver layout
@@ -1474,6 +1480,8 @@ int pcg_precond_dot_noalloc(pcg_ctx* ctx, const double* r_dev, double* z_dev, do
   if (!r_dev || !z_dev || !rz_dev)
     return fail(ctx, PCG_EINVAL, "r, z and rz must be non-NULL device pointers");
   if (overlap(r_dev, z_dev, ctx->op.n)) return fail(ctx, PCG_EINVAL, "r and z overlap");
+  if (overlap(rz_dev, r_dev, ctx->op.n) || overlap(rz_dev, z_dev, ctx->op.n))
+    return fail(ctx, PCG_EINVAL, "rz overlaps r or z");
   if (ctx->op.ntiles > pcg::kNoallocMaxTiles)
     return fail(ctx, PCG_EINVAL,
                 "grid has %lld columns; the no-allocation scratch holds at most %lld "
@@ -1481,9 +1489,73 @@ int pcg_precond_dot_noalloc(pcg_ctx* ctx, const double* r_dev, double* z_dev, do
                 ctx->op.ncols, pcg::kNoallocMaxTiles * pcg::kTile, pcg::kNoallocMaxTiles);
   DeviceGuard g(ctx->device);
   if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
-  cudaError_t e = pcg::launch_precond_dot_noalloc(ctx->op, r_dev, z_dev, rz_dev, ctx->num_sms,
+  cudaError_t e = pcg::launch_precond_dot_noalloc(ctx->op, r_dev, z_dev, rz_dev,
+                                                  ctx->noalloc_partials, ctx->num_sms,
                                                   ctx->stream);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "precond_dot_noalloc");
+  return PCG_OK;
+}
+
+int pcg_measure_fp64_rate(int warps_per_sm, int launches, double* lane_ops_per_s,
+                          double* sm_mhz, double* lanes_per_sm_clk) {
+  if (warps_per_sm < 4 || warps_per_sm > 64 || warps_per_sm % 4 != 0)
+    return fail(nullptr, PCG_EINVAL, "warps_per_sm must be a multiple of 4 in [4, 64]");
+  if (launches < 1 || launches > 100)
+    return fail(nullptr, PCG_EINVAL, "launches must be in [1, 100]");
+  if (!lane_ops_per_s || !sm_mhz || !lanes_per_sm_clk)
+    return fail(nullptr, PCG_EINVAL, "NULL output pointer");
+  int dev = 0, nsm = 0, clk_khz = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&clk_khz, cudaDevAttrClockRate, dev);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "device query");
+  const int threads = 128;  // four warps per block, one per sub-partition
+  const int blocks = nsm * warps_per_sm / 4;
+  // about 20 ms per launch at 2 lane operations per SM per clock
+  const double per_trip = (double)pcg::fp64_rate_lane_ops(blocks, threads, 1);
+  const int trips = std::max(1, (int)(0.02 * 2.0 * nsm * clk_khz * 1e3 / per_trip));
+  double* sink = nullptr;
+  unsigned long long* stamps = nullptr;
+  cudaStream_t s = nullptr;
+  cudaEvent_t ev[2] = {nullptr, nullptr};
+  e = cudaMalloc(&sink, sizeof(double) * blocks);
+  if (e == cudaSuccess) e = cudaMalloc(&stamps, sizeof(unsigned long long) * 2 * blocks);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreate(&ev[0]);
+  if (e == cudaSuccess) e = cudaEventCreate(&ev[1]);
+  std::vector<unsigned long long> st(2 * (size_t)blocks);
+  double best = 0.0, best_mhz = 0.0;
+  for (int l = -1; e == cudaSuccess && l < launches; ++l) {  // l = -1: warm-up
+    e = cudaEventRecord(ev[0], s);
+    if (e == cudaSuccess) e = pcg::launch_fp64_rate(blocks, threads, trips, sink, stamps, s);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[1], s);
+    if (e == cudaSuccess) e = cudaEventSynchronize(ev[1]);
+    float ms = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, ev[0], ev[1]);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(st.data(), stamps, sizeof(unsigned long long) * st.size(),
+                     cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess || l < 0 || ms <= 0.f) continue;
+    std::vector<double> mhz;
+    mhz.reserve(blocks);
+    for (int b = 0; b < blocks; ++b)
+      if (st[2 * b + 1] > 0) mhz.push_back(1e3 * (double)st[2 * b] / (double)st[2 * b + 1]);
+    std::sort(mhz.begin(), mhz.end());
+    const double rate = (double)pcg::fp64_rate_lane_ops(blocks, threads, trips) / (ms * 1e-3);
+    if (rate > best) {
+      best = rate;
+      best_mhz = mhz.empty() ? 0.0 : mhz[mhz.size() / 2];
+    }
+  }
+  if (ev[1]) cudaEventDestroy(ev[1]);
+  if (ev[0]) cudaEventDestroy(ev[0]);
+  if (s) cudaStreamDestroy(s);
+  if (stamps) cudaFree(stamps);
+  if (sink) cudaFree(sink);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "fp64 rate probe");
+  *lane_ops_per_s = best;
+  *sm_mhz = best_mhz;
+  *lanes_per_sm_clk = best_mhz > 0.0 ? best / (nsm * best_mhz * 1e6) : 0.0;
   return PCG_OK;
 }
 

@@ -139,9 +139,12 @@ cudaError_t launch_finalize(const Op& op, const DevState* st, double* x, const d
 
 // z = M^{-1} r and *rz = <r, z> with scratch from a fixed device array in
 // pcg_noalloc.cu (no allocation); at most kNoallocMaxTiles tiles of 32 columns.
+// partials: the array's device address on the current device, from
+// noalloc_scratch_address (called with that device current).
 constexpr long long kNoallocMaxTiles = 65536;
+cudaError_t noalloc_scratch_address(double** out);
 cudaError_t launch_precond_dot_noalloc(const Op& op, const double* r, double* z, double* rz,
-                                       int num_sms, cudaStream_t s);
+                                       double* partials, int num_sms, cudaStream_t s);
 
 // Row-tiled solver layout (pcg_tiled.cu): cell (c,k) at (c/32*nz + k)*32 + c%32.
 // Row-tiled vectors hold ntiles*32*nz values (the last tile padded to 32
@@ -238,6 +241,13 @@ cudaError_t launch_mg_coarse_ah(const Op& fine, const Op& coarse, const double* 
                                 int num_sms, cudaStream_t s);
 int grid_mg_first(const Op& op, int num_sms);
 int grid_mg_smooth(const Op& op, int num_sms);
+
+// fp64 rate probe (pcg_peak.cu): fp64 lane operations one launch of `blocks`
+// blocks of `threads` threads and `trips` loop trips performs, and the launch
+// (stamps: per block, SM cycles and global-timer nanoseconds).
+long long fp64_rate_lane_ops(int blocks, int threads, int trips);
+cudaError_t launch_fp64_rate(int blocks, int threads, int trips, double* sink,
+                             unsigned long long* stamps, cudaStream_t s);
 
 // Occupancy-derived grid sizes (blocks) for the persistent sweeps.  The
 // preconditioner's also fixes op.stream_smem (see pcg_kernels.cu).

@@ -13,29 +13,22 @@
 //
 // The scratch array lives in every GPU that loads this library until the
 // process exits.  In host code its name is only a stand-in for the device
-// copy, so the first call on each device looks up the real device address
-// with cudaGetSymbolAddress (with that device current) and caches it.
+// copy, so pcg_create looks up the real device address with
+// cudaGetSymbolAddress (with the context's device current) and keeps it in
+// the context; that lookup also loads this file's module on the device, so
+// the entry point itself neither loads code nor allocates.
 #include <cstdint>
-#include <mutex>
 
 #include "pcg_internal.h"
 
 namespace pcg {
 namespace {
 
-constexpr int kNoallocMaxDevices = 64;
-
 // Scratch: one partial sum of <r, z> per tile of 32 columns.  Every call
 // writes the partial of every tile of its grid before reading any of them,
 // so nothing has to be cleared between calls.  Calls that overlap on the GPU
 // (two streams, two host threads) race on this array.
 static __device__ __align__(256) double g_tile_partials[kNoallocMaxTiles];
-
-struct DeviceScratch {
-  double* partials = nullptr;  // device address of g_tile_partials on this device
-};
-DeviceScratch g_dev_scratch[kNoallocMaxDevices];
-std::mutex g_scratch_mutex;
 
 // One warp per tile of 32 columns, one column per lane, walking its column
 // in global memory: forward y_k = r_k + (T_{k-1/2}/D_{k-1}) y_{k-1} with
@@ -91,30 +84,18 @@ __global__ void k_sum_tiles(const double* __restrict__ partials, long long ntile
   if (threadIdx.x == 0) *out = sh[0];
 }
 
-// Device address of the scratch array on the current device, looked up once.
-cudaError_t scratch_address(double** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kNoallocMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (!g_dev_scratch[dev].partials) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_tile_partials);
-    if (e != cudaSuccess) return e;
-    g_dev_scratch[dev].partials = static_cast<double*>(p);
-  }
-  *out = g_dev_scratch[dev].partials;
-  return cudaSuccess;
-}
-
 }  // namespace
 
+cudaError_t noalloc_scratch_address(double** out) {
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_tile_partials);
+  if (e == cudaSuccess) *out = static_cast<double*>(p);
+  return e;
+}
+
 cudaError_t launch_precond_dot_noalloc(const Op& op, const double* r, double* z, double* rz,
-                                       int num_sms, cudaStream_t s) {
-  double* partials = nullptr;
-  cudaError_t e = scratch_address(&partials);
-  if (e != cudaSuccess) return e;
+                                       double* partials, int num_sms, cudaStream_t s) {
+  cudaError_t e = cudaSuccess;
   long long blocks = (op.ntiles + 7) / 8;  // 8 warps (tiles) per block of 256 threads
   const long long cap = 8LL * num_sms;
   if (blocks > cap) blocks = cap;

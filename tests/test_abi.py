@@ -133,3 +133,10 @@ def test_binding_constants_match_the_header(lib):
               "PCG_K_LOOP": "loop"}
     for v, k in kinds:
         assert lib.KERNEL_KINDS[v] == expect[k], (k, v)
+
+
+@pytest.mark.parametrize("warps,launches", [(0, 3), (3, 3), (68, 3), (32, 0), (32, 101)])
+def test_fp64_probe_rejects_bad_arguments(lib, warps, launches):
+    with pytest.raises(lib.PCGError) as e:
+        lib.pcg_measure_fp64_rate(warps, launches)
+    assert e.value.status == lib.PCG_EINVAL

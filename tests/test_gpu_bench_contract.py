@@ -53,7 +53,10 @@ def test_bench_line_has_the_contract_keys(workload):
     n = d["config"]["cells"]
     assert e2e["unit"] == "iters/s" and e2e["value"] > 0
     assert e2e["h2d_bytes_per_step"] >= 8 * n and e2e["d2h_bytes_per_step"] == 8 * n
-    assert len(e2e["step_ms"]) == 3
+    assert len(e2e["step_ms"]) == 3 and len(e2e["copy_only_ms"]) == 3
+    assert rl["peak_source"].startswith("measured") and rl["fp64_probe"]["lanes_per_sm_clk"] > 0
+    assert abs(rl["frac_nominal"] - rl["achieved"] / rl["peak_nominal"]) <= 1e-9
+    assert cpu["host_cpus"] >= 1 and cpu["cpu_model"]
     clk = d["clocks"]
     if clk is not None:
         assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(clk)
