@@ -13,7 +13,8 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libpcg.so")
 SOURCES = ["pcg_kernels.cu", "pcg_setup.cu", "pcg_tiled.cu", "pcg_persistent.cu", "pcg_split.cu",
-           "pcg_mg.cu", "pcg_cluster.cu", "pcg_api.cu", "pcg_noalloc.cu", "pcg_peak.cu"]
+           "pcg_mg.cu", "pcg_cluster.cu", "pcg_api.cu", "pcg_noalloc.cu", "pcg_peak.cu",
+           "pcg_tmem.cu"]
 HEADERS = [os.path.join(CSRC, "pcg_internal.h"), os.path.join(CSRC, "pcg_device.cuh"),
            os.path.join(CSRC, "pcg_sweeps.cuh"),
            os.path.join(ROOT, "include", "pcg.h")]

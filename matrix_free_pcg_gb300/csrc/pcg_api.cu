@@ -100,6 +100,8 @@ struct pcg_ctx {
   // device address of the fixed scratch array of pcg_precond_dot_noalloc (not
   // an allocation of the context: the array lives in the library's module)
   double* noalloc_partials = nullptr;
+  // the tensor-memory column solves (pcg_tmem.cu) can be launched
+  bool tmem_ok = false;
   // second stream of pcg_update_solve_host: b and x0 go in while the set-up runs
   cudaStream_t copy_stream = nullptr;
   cudaEvent_t copy_done = nullptr;
@@ -1014,6 +1016,10 @@ int pcg_create(int nx, int ny, int nz, const pcg_coeffs* coeffs, pcg_ctx** out) 
 
   e = pcg::prepare_kernels(op);
   if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "kernel attribute set-up"));
+  // the tensor-memory column solves need their shared-memory attribute; where
+  // it cannot be set the other column-solve kernels run instead
+  ctx->tmem_ok = pcg::prepare_precond_tmem() == cudaSuccess;
+  (void)cudaGetLastError();
   ctx->grid_m = pcg::grid_precond(op, ctx->num_sms);  // also sets op.stream_smem
   ctx->grid_a = pcg::grid_spmv(op, ctx->num_sms);
   ctx->grid_tm = pcg::grid_tiled_precond(op, ctx->num_sms);
@@ -1340,8 +1346,12 @@ int pcg_precond(pcg_ctx* ctx, const double* r_dev, double* z_dev) {
   if (overlap(r_dev, z_dev, ctx->op.n)) return fail(ctx, PCG_EINVAL, "r and z overlap");
   DeviceGuard g(ctx->device);
   if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
-  cudaError_t e = pcg::launch_precond(ctx->op, ctx->state, r_dev, z_dev, ctx->grid_m,
-                                      ctx->stream);
+  cudaError_t e =
+      (ctx->tmem_ok && pcg::precond_tmem_supported(ctx->op, r_dev, nullptr, z_dev))
+          ? pcg::launch_precond_tmem(ctx->op, ctx->state, const_cast<double*>(r_dev), nullptr,
+                                     z_dev, nullptr, nullptr, false,
+                                     pcg::grid_precond_tmem(ctx->num_sms), ctx->stream)
+          : pcg::launch_precond(ctx->op, ctx->state, r_dev, z_dev, ctx->grid_m, ctx->stream);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "precond launch");
   return PCG_OK;
 }

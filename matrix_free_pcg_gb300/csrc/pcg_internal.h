@@ -242,6 +242,21 @@ cudaError_t launch_mg_coarse_ah(const Op& fine, const Op& coarse, const double* 
 int grid_mg_first(const Op& op, int num_sms);
 int grid_mg_smooth(const Op& op, int num_sms);
 
+// Column solves with the forward result in tensor memory (pcg_tmem.cu), for
+// the caller's column-contiguous layout: nz in {32, 64, 128} and 16-byte
+// aligned vectors (precond_tmem_supported).  One block of 8 warps per SM
+// (grid_precond_tmem blocks), each block holding all of its SM's TMEM
+// columns.  fused: the Algorithm 3 sweep (r* = r - alpha q, reductions,
+// scalar step); otherwise z = M^{-1} r (q, partials and hist unused).
+// prepare_precond_tmem sets the kernels' shared-memory attributes (once per
+// device).
+bool precond_tmem_supported(const Op& op, const double* r, const double* q, const double* z);
+cudaError_t prepare_precond_tmem();
+int grid_precond_tmem(int num_sms);
+cudaError_t launch_precond_tmem(const Op& op, DevState* st, double* r, const double* q,
+                                double* z, double* partials, double* hist, bool fused, int grid,
+                                cudaStream_t s);
+
 // fp64 rate probe (pcg_peak.cu): fp64 lane operations one launch of `blocks`
 // blocks of `threads` threads and `trips` loop trips performs, and the launch
 // (stamps: per block, SM cycles and global-timer nanoseconds).

@@ -46,6 +46,12 @@ SHAPES = [
     (3, 1, 2, False, True),
     (2, 2, 4, True, False),
     (7, 5, 500, True, False),     # too tall for the staged tile: direct path
+    # nz = 32, 64, 128 with 16-byte aligned vectors: the standalone solve
+    # keeps its forward pass in tensor memory
+    (37, 29, 32, True, True),     # ragged last tile
+    (40, 9, 128, True, True),     # 360 columns: 11 full tiles + 8 columns
+    (20, 20, 64, False, False),
+    (256, 256, 32, True, True),   # 2048 tiles: more than one per warp of the grid
 ]
 
 
