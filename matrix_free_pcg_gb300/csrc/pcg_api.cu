@@ -861,10 +861,18 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
         if (split)
           return pcg::launch_precond_split(op, ctx->split_p, ctx->state, ctx->r, ctx->q, ctx->z,
                                            ctx->partials, ctx->hist, ctx->grid_sp, s);
-        return tiled ? pcg::launch_precond_tiled(op, ctx->state, ctx->r, ctx->q, ctx->z,
-                                                 ctx->partials, ctx->hist, ctx->grid_tm, s)
-                     : pcg::launch_precond_fused(op, ctx->state, ctx->r, ctx->q, ctx->z,
-                                                 ctx->partials, ctx->hist, ctx->grid_m, s);
+        if (tiled)
+          return pcg::launch_precond_tiled(op, ctx->state, ctx->r, ctx->q, ctx->z,
+                                           ctx->partials, ctx->hist, grid_pm, s);
+        // column layout: the tensor-memory sweep where it applies (nz = 32, 64,
+        // 128); its grid is smaller than grid_m, so the stencil sweep's
+        // partials after 2*grid_m stay clear of its own
+        if (ctx->tmem_ok && pcg::precond_tmem_supported(op, ctx->r, ctx->q, ctx->z))
+          return pcg::launch_precond_tmem(op, ctx->state, ctx->r, ctx->q, ctx->z, ctx->partials,
+                                          ctx->hist, true,
+                                          pcg::grid_precond_tmem(ctx->op, ctx->num_sms), s);
+        return pcg::launch_precond_fused(op, ctx->state, ctx->r, ctx->q, ctx->z, ctx->partials,
+                                         ctx->hist, ctx->grid_m, s);
       });
       if (e != cudaSuccess) return cuda_fail(ctx, e, "preconditioner sweep launch");
       if (enq + i < maxit) {
@@ -1020,6 +1028,7 @@ int pcg_create(int nx, int ny, int nz, const pcg_coeffs* coeffs, pcg_ctx** out) 
   // it cannot be set the other column-solve kernels run instead
   ctx->tmem_ok = pcg::prepare_precond_tmem() == cudaSuccess;
   (void)cudaGetLastError();
+  op.tmem = ctx->tmem_ok ? 1 : 0;
   ctx->grid_m = pcg::grid_precond(op, ctx->num_sms);  // also sets op.stream_smem
   ctx->grid_a = pcg::grid_spmv(op, ctx->num_sms);
   ctx->grid_tm = pcg::grid_tiled_precond(op, ctx->num_sms);
@@ -1350,7 +1359,7 @@ int pcg_precond(pcg_ctx* ctx, const double* r_dev, double* z_dev) {
       (ctx->tmem_ok && pcg::precond_tmem_supported(ctx->op, r_dev, nullptr, z_dev))
           ? pcg::launch_precond_tmem(ctx->op, ctx->state, const_cast<double*>(r_dev), nullptr,
                                      z_dev, nullptr, nullptr, false,
-                                     pcg::grid_precond_tmem(ctx->num_sms), ctx->stream)
+                                     pcg::grid_precond_tmem(ctx->op, ctx->num_sms), ctx->stream)
           : pcg::launch_precond(ctx->op, ctx->state, r_dev, z_dev, ctx->grid_m, ctx->stream);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "precond launch");
   return PCG_OK;

@@ -48,6 +48,7 @@ struct Op {
                        // per warp of the preconditioner grid
   int az_resid;        // row-tiled stencil sweep: A z = r + (A - M) z (M z = r from the
                        // preconditioner sweep) instead of the full 7-point stencil
+  int tmem;            // the tensor-memory column-solve kernels (pcg_tmem.cu) can be launched
   // substructured column solve (pcg_split.cu), row-tiled tables
   double* sp_nphi;     // per cell: T_{k+1/2}/D_k of the block's own LDL^T (0 at its top)
   double* sp_invd;     // per cell: 1/D_k of the block's LDL^T
@@ -245,14 +246,15 @@ int grid_mg_smooth(const Op& op, int num_sms);
 // Column solves with the forward result in tensor memory (pcg_tmem.cu), for
 // the caller's column-contiguous layout: nz in {32, 64, 128} and 16-byte
 // aligned vectors (precond_tmem_supported).  One block of 8 warps per SM
-// (grid_precond_tmem blocks), each block holding all of its SM's TMEM
+// (grid_precond_tmem blocks: at most one per SM and none without a tile,
+// never more than grid_precond's), each block holding all of its SM's TMEM
 // columns.  fused: the Algorithm 3 sweep (r* = r - alpha q, reductions,
 // scalar step); otherwise z = M^{-1} r (q, partials and hist unused).
 // prepare_precond_tmem sets the kernels' shared-memory attributes (once per
 // device).
 bool precond_tmem_supported(const Op& op, const double* r, const double* q, const double* z);
 cudaError_t prepare_precond_tmem();
-int grid_precond_tmem(int num_sms);
+int grid_precond_tmem(const Op& op, int num_sms);
 cudaError_t launch_precond_tmem(const Op& op, DevState* st, double* r, const double* q,
                                 double* z, double* partials, double* hist, bool fused, int grid,
                                 cudaStream_t s);

@@ -413,7 +413,11 @@ cudaError_t prepare_precond_tmem() {
   return e;
 }
 
-int grid_precond_tmem(int num_sms) { return num_sms; }
+int grid_precond_tmem(const Op& op, int num_sms) {
+  const long long work = (op.ntiles + kTwWarps - 1) / kTwWarps;  // blocks that get a tile
+  return (int)std::max(1LL, std::min((long long)num_sms, work));
+}
+
 
 cudaError_t launch_precond_tmem(const Op& op, DevState* st, double* r, const double* q, double* z,
                                 double* partials, double* hist, bool fused, int grid,
