@@ -268,7 +268,10 @@ cudaError_t launch_persistent(const Op& op, DevState* st, double* r, double* q, 
                               double* u, double* p, double* partials, double* hist, int grid,
                               unsigned int absent, cudaStream_t s) {
   Op o = op;
-  int seglen = tiled_spmv_seglen(op, grid);
+  // stencil units of 8 levels: measured against 2, 4 and 16 on 128x128x64 and
+  // 256x256x64 (45.96 against 46.69 us per iteration with 4, the batched
+  // sweep's choice for these grids; 123.5 against 125.4 us)
+  int seglen = std::min(8, op.nz);
   void* args[] = {&o, &st, &r, &q, &z, &u, &p, &partials, &hist, &seglen, &absent};
   const void* fn;
   if (op.varying)
