@@ -401,8 +401,9 @@ int pcg_launch_info(const pcg_ctx* ctx, int* grid_precond, int* grid_spmv,
  * the paper reports measured rates per kernel, section 7 Table 7).  Runs one
  * warm-up and `launches` timed launches (1..100, about 20 ms each) of a
  * kernel whose threads each carry 8 independent chains of fp64 fused
- * multiply-adds, warps_per_sm warps per SM (a multiple of 4 in [4, 64]), and
- * reports the fastest launch:
+ * multiply-adds, warps_per_sm warps per SM (1, 2, 3: one block per SM whose
+ * warps sit on that many of the SM's four sub-partitions; or a multiple of 4
+ * in [4, 64]: blocks of 4 warps), and reports the fastest launch:
  *   *lane_ops_per_s    fp64 lane operations per second (an FMA counts one),
  *   *sm_mhz            median SM clock inside that launch (clock64 against the
  *                      global timer, per block),

@@ -16,7 +16,7 @@ SOURCES = ["pcg_kernels.cu", "pcg_setup.cu", "pcg_tiled.cu", "pcg_persistent.cu"
            "pcg_mg.cu", "pcg_cluster.cu", "pcg_api.cu", "pcg_noalloc.cu", "pcg_peak.cu",
            "pcg_tmem.cu"]
 HEADERS = [os.path.join(CSRC, "pcg_internal.h"), os.path.join(CSRC, "pcg_device.cuh"),
-           os.path.join(CSRC, "pcg_sweeps.cuh"),
+           os.path.join(CSRC, "pcg_sweeps.cuh"), os.path.join(CSRC, "pcg_tmem.cuh"),
            os.path.join(ROOT, "include", "pcg.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # Host code (the per-level tables) is compiled without floating-point

@@ -1517,8 +1517,9 @@ int pcg_precond_dot_noalloc(pcg_ctx* ctx, const double* r_dev, double* z_dev, do
 
 int pcg_measure_fp64_rate(int warps_per_sm, int launches, double* lane_ops_per_s,
                           double* sm_mhz, double* lanes_per_sm_clk) {
-  if (warps_per_sm < 4 || warps_per_sm > 64 || warps_per_sm % 4 != 0)
-    return fail(nullptr, PCG_EINVAL, "warps_per_sm must be a multiple of 4 in [4, 64]");
+  if (warps_per_sm < 1 || warps_per_sm > 64 || (warps_per_sm > 4 && warps_per_sm % 4 != 0))
+    return fail(nullptr, PCG_EINVAL,
+                "warps_per_sm must be 1, 2, 3 or a multiple of 4 in [4, 64]");
   if (launches < 1 || launches > 100)
     return fail(nullptr, PCG_EINVAL, "launches must be in [1, 100]");
   if (!lane_ops_per_s || !sm_mhz || !lanes_per_sm_clk)
@@ -1528,8 +1529,10 @@ int pcg_measure_fp64_rate(int warps_per_sm, int launches, double* lane_ops_per_s
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&clk_khz, cudaDevAttrClockRate, dev);
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "device query");
-  const int threads = 128;  // four warps per block, one per sub-partition
-  const int blocks = nsm * warps_per_sm / 4;
+  // four warps per block, one per sub-partition; below four warps per SM, one
+  // block per SM with warps on sub-partitions 0 .. warps_per_sm-1
+  const int threads = 32 * std::min(warps_per_sm, 4);
+  const int blocks = nsm * std::max(warps_per_sm / 4, 1);
   // about 20 ms per launch at 2 lane operations per SM per clock
   const double per_trip = (double)pcg::fp64_rate_lane_ops(blocks, threads, 1);
   const int trips = std::max(1, (int)(0.02 * 2.0 * nsm * clk_khz * 1e3 / per_trip));

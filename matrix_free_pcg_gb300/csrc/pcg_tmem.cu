@@ -28,6 +28,7 @@
 #include <algorithm>
 
 #include "pcg_device.cuh"
+#include "pcg_tmem.cuh"
 
 namespace pcg {
 namespace {
@@ -44,64 +45,6 @@ constexpr uint32_t kTwColsPerWarp = 256;     // per warp: 128 doubles per TMEM l
 template <bool FUSED>
 __host__ __device__ constexpr int kTwWarpDoubles() {
   return ((FUSED ? 2 : 1) * kTwStages + 1) * kTile * kTwCS;
-}
-
-// ---- tensor memory (tcgen05) wrappers; every one is warp-wide (.sync.aligned)
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   smem_addr(dst)),
-               "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_fence_before_sync() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_fence_after_sync() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// 8 doubles of this thread into 16 consecutive columns of its TMEM lane.
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const double (&v)[8]) {
-  uint32_t u[16];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    u[2 * j] = (uint32_t)__double2loint(v[j]);
-    u[2 * j + 1] = (uint32_t)__double2hiint(v[j]);
-  }
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-      "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]), "r"(u[7]),
-      "r"(u[8]), "r"(u[9]), "r"(u[10]), "r"(u[11]), "r"(u[12]), "r"(u[13]), "r"(u[14]),
-      "r"(u[15])
-      : "memory");
-}
-
-// The 8 doubles stored by tmem_st8 at taddr, back into this thread's
-// registers; the load is complete (tcgen05.wait::ld) when this returns.
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, double (&v)[8]) {
-  uint32_t u[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15}, [%16];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]),
-        "=r"(u[7]), "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]),
-        "=r"(u[14]), "=r"(u[15])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int j = 0; j < 8; ++j) v[j] = __hiloint2double((int)u[2 * j + 1], (int)u[2 * j]);
 }
 
 // Algorithm 3 sweep (FUSED: r* = r - alpha q written back, ||r*||^2 and

@@ -135,7 +135,7 @@ def test_binding_constants_match_the_header(lib):
         assert lib.KERNEL_KINDS[v] == expect[k], (k, v)
 
 
-@pytest.mark.parametrize("warps,launches", [(0, 3), (3, 3), (68, 3), (32, 0), (32, 101)])
+@pytest.mark.parametrize("warps,launches", [(0, 3), (6, 3), (68, 3), (32, 0), (32, 101)])
 def test_fp64_probe_rejects_bad_arguments(lib, warps, launches):
     with pytest.raises(lib.PCGError) as e:
         lib.pcg_measure_fp64_rate(warps, launches)

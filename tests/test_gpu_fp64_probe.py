@@ -23,3 +23,7 @@ def test_fp64_probe_measures_a_plausible_rate():
         assert abs(rel - 1.0) < 1e-9, r
     a, b = (r["lanes_per_sm_clk"] for r in runs)
     assert abs(a - b) <= 0.05 * max(a, b), runs
+    # one warp per SM: one sub-partition's pipe, at most its nominal half lane per clock
+    one = mf.pcg_measure_fp64_rate(1, 2)
+    assert 0.3 < one["lanes_per_sm_clk"] <= 0.51, one
+    assert one["lanes_per_sm_clk"] * 4 >= a * 0.99, (one, runs)
