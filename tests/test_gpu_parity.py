@@ -94,6 +94,7 @@ SOLVE_CASES = [
     (40, 36, 64, False, True, 1e4),
     (17, 19, 130, True, True, 1e5),
     (6, 5, 500, False, False, 1e3),
+    (45, 26, 32, True, True, 1e4),   # the column layout's tensor-memory sweep at nz = 32
 ]
 
 
