@@ -271,6 +271,15 @@ int pcg_mg_vcycle(pcg_ctx* ctx, const double* r_dev, double* z_dev);
  * Errors: PCG_EINVAL (NULL, absent < 0). */
 int pcg_test_barrier_absent(pcg_ctx* ctx, int absent);
 
+/* Test hook for the column solves on column-contiguous vectors (pcg_precond
+ * and the column layout's preconditioner sweep): enable = 0 makes them take
+ * the kernels that keep the forward pass's w in global memory instead of in
+ * the SM's tensor memory, so that both can be checked and timed; 1 (default)
+ * takes the tensor-memory kernels wherever they apply (nz = 32, 64, 128,
+ * 16-byte aligned vectors) and the device allows them.
+ * Errors: PCG_EINVAL (NULL). */
+int pcg_test_tensor_memory(pcg_ctx* ctx, int enable);
+
 /* Blocks per column the row-tiled preconditioner sweep currently uses
  * (1: Thomas), after the automatic choice.  Errors: PCG_EINVAL (NULL). */
 int pcg_get_substructuring(const pcg_ctx* ctx, int* nblocks_out);

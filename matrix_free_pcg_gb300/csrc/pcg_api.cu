@@ -100,8 +100,9 @@ struct pcg_ctx {
   // device address of the fixed scratch array of pcg_precond_dot_noalloc (not
   // an allocation of the context: the array lives in the library's module)
   double* noalloc_partials = nullptr;
-  // the tensor-memory column solves (pcg_tmem.cu) can be launched
-  bool tmem_ok = false;
+  // the tensor-memory column solves (pcg_tmem.cu) can be launched; tmem_off:
+  // switched off by the test hook pcg_test_tensor_memory
+  bool tmem_ok = false, tmem_off = false;
   // second stream of pcg_update_solve_host: b and x0 go in while the set-up runs
   cudaStream_t copy_stream = nullptr;
   cudaEvent_t copy_done = nullptr;
@@ -867,7 +868,7 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
         // column layout: the tensor-memory sweep where it applies (nz = 32, 64,
         // 128); its grid is smaller than grid_m, so the stencil sweep's
         // partials after 2*grid_m stay clear of its own
-        if (ctx->tmem_ok && pcg::precond_tmem_supported(op, ctx->r, ctx->q, ctx->z))
+        if (ctx->tmem_ok && !ctx->tmem_off && pcg::precond_tmem_supported(op, ctx->r, ctx->q, ctx->z))
           return pcg::launch_precond_tmem(op, ctx->state, ctx->r, ctx->q, ctx->z, ctx->partials,
                                           ctx->hist, true,
                                           pcg::grid_precond_tmem(ctx->op, ctx->num_sms), s);
@@ -1313,6 +1314,12 @@ int pcg_get_az_form(const pcg_ctx* ctx, int* form_out) {
   return PCG_OK;
 }
 
+int pcg_test_tensor_memory(pcg_ctx* ctx, int enable) {
+  if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
+  ctx->tmem_off = enable == 0;
+  return PCG_OK;
+}
+
 int pcg_test_barrier_absent(pcg_ctx* ctx, int absent) {
   if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
   if (absent < 0) return fail(ctx, PCG_EINVAL, "absent must be >= 0");
@@ -1356,7 +1363,7 @@ int pcg_precond(pcg_ctx* ctx, const double* r_dev, double* z_dev) {
   DeviceGuard g(ctx->device);
   if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
   cudaError_t e =
-      (ctx->tmem_ok && pcg::precond_tmem_supported(ctx->op, r_dev, nullptr, z_dev))
+      (ctx->tmem_ok && !ctx->tmem_off && pcg::precond_tmem_supported(ctx->op, r_dev, nullptr, z_dev))
           ? pcg::launch_precond_tmem(ctx->op, ctx->state, const_cast<double*>(r_dev), nullptr,
                                      z_dev, nullptr, nullptr, false,
                                      pcg::grid_precond_tmem(ctx->op, ctx->num_sms), ctx->stream)

@@ -64,11 +64,15 @@ def test_apply_A_matches_oracle(shape):
     assert rel_maxdiff(y, oracle.apply_A(prob, x)) <= OP_TOL
 
 
+@pytest.mark.parametrize("tmem", [True, False], ids=["tmem", "global_w"])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s[:3])) +
                          ("v" if s[3] else "c") + ("g" if s[4] else "u"))
-def test_precond_matches_oracle(shape):
+def test_precond_matches_oracle(shape, tmem):
+    # both column-solve kernel families: w in tensor memory (where it
+    # applies) and w in global memory
     prob, kw, r = case(*shape)
     with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        mf.pcg_test_tensor_memory(s.ctx, tmem)
         z = s.precond(torch.from_numpy(r).to(DEV)).cpu().numpy()
     assert rel_maxdiff(z, oracle.precond(prob, r)) <= OP_TOL
 
@@ -102,11 +106,16 @@ def configure(s, mode):
     """mode: "column"; "tiled" (Thomas column solves, stored factors, batched
     loop); "tiled_recompute" (Thomas, factors rebuilt per sweep);
     "tiled_split" (substructured column solves, blocks chosen automatically);
-    "tiled_persistent" (Thomas, stored factors, one cooperative kernel).
+    "tiled_persistent" (Thomas, stored factors, one cooperative kernel);
+    "column_global_w" (the column layout without tensor memory).
     The row-tiled modes form A z as r + (A - M) z wherever that applies (the
     default); a "_stencil" suffix selects the full 7-point stencil."""
     stencil = mode.endswith("_stencil")
     mode = mode[: -len("_stencil")] if stencil else mode
+    # "column_global_w": the column layout with its preconditioner sweep on the
+    # kernels that keep w in global memory instead of tensor memory
+    mf.pcg_test_tensor_memory(s.ctx, mode != "column_global_w")
+    mode = "column" if mode == "column_global_w" else mode
     s.set_layout("column" if mode == "column" else "tiled")
     s.set_factors("recompute" if mode == "tiled_recompute" else "stored")
     s.set_loop("persistent" if mode == "tiled_persistent" else "batched")
@@ -119,8 +128,8 @@ def configure(s, mode):
     assert s.az_form == ("residual" if thomas and not stencil else "stencil")
 
 
-MODES = ["column", "column_stencil", "tiled", "tiled_stencil", "tiled_recompute", "tiled_split",
-         "tiled_persistent", "tiled_persistent_stencil"]
+MODES = ["column", "column_stencil", "column_global_w", "tiled", "tiled_stencil",
+         "tiled_recompute", "tiled_split", "tiled_persistent", "tiled_persistent_stencil"]
 
 
 @pytest.mark.parametrize("layout", MODES)
