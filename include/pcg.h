@@ -349,6 +349,27 @@ int pcg_update_solve_host(pcg_ctx* ctx, const pcg_coeffs* coeffs, const double* 
                           const double* x0_host, double* x_host, double rtol, int maxit,
                           int* iters_out, double* res_hist);
 
+/* As pcg_update_solve_host, but the solution's copy to x_host is left
+ * running when the call returns, so that it overlaps the next call's
+ * set-up and solve (a caller solving a sequence of systems hides the
+ * device-to-host copy of each solution behind the next solve).  The
+ * iteration count, the history and the status are final on return; x_host
+ * is written by a copy on a stream of the context and must be neither read
+ * nor freed before pcg_host_wait (or any synchronous host-buffer call on the
+ * context, which waits first) returns.  Consecutive calls alternate between
+ * two device copies of x, so the copy of one call's solution and the next
+ * call's solve do not touch the same memory; the first call allocates the
+ * second copy and the stream.  Errors: as pcg_update_solve_host; an error of
+ * a copy left running is reported by pcg_host_wait. */
+int pcg_update_solve_host_async(pcg_ctx* ctx, const pcg_coeffs* coeffs, const double* b_host,
+                                const double* x0_host, double* x_host, double rtol, int maxit,
+                                int* iters_out, double* res_hist);
+
+/* Waits until the solution copies left running by pcg_update_solve_host_async
+ * have reached their host buffers.  Errors: PCG_EINVAL (NULL), PCG_ECUDA (a
+ * copy failed). */
+int pcg_host_wait(pcg_ctx* ctx);
+
 /* z = M^{-1} r and *rz_dev = <r, z>, without allocating anything.
  * The paper has no counterpart: this entry point exists for callers that
  * must not allocate device memory while they run -- for instance code that

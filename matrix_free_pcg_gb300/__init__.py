@@ -36,7 +36,8 @@ EXPORTED = ["pcg_create", "pcg_destroy", "pcg_update_coeffs", "pcg_set_stream", 
             "pcg_set_loop", "pcg_get_loop", "pcg_test_barrier_absent", "pcg_set_az_form",
             "pcg_get_az_form", "pcg_set_preconditioner", "pcg_set_multigrid",
             "pcg_get_multigrid", "pcg_mg_vcycle", "pcg_update_solve_host",
-            "pcg_measure_fp64_rate", "pcg_test_tensor_memory"]
+            "pcg_measure_fp64_rate", "pcg_test_tensor_memory", "pcg_update_solve_host_async",
+            "pcg_host_wait"]
 PCG_LAYOUT_COLUMN, PCG_LAYOUT_TILED = 0, 1
 PCG_FACTORS_STORED, PCG_FACTORS_RECOMPUTE = 0, 1
 PCG_LOOP_AUTO, PCG_LOOP_BATCHED, PCG_LOOP_PERSISTENT, PCG_LOOP_CLUSTER = 0, 1, 2, 3
@@ -75,6 +76,10 @@ def _load(path=LIB_PATH):
         "pcg_update_solve_host": (ctypes.c_int, [_vp, ctypes.POINTER(pcg_coeffs), _vp, _vp, _vp,
                                                  ctypes.c_double, ctypes.c_int,
                                                  ctypes.POINTER(ctypes.c_int), _vp]),
+        "pcg_update_solve_host_async": (ctypes.c_int, [_vp, ctypes.POINTER(pcg_coeffs), _vp, _vp,
+                                                       _vp, ctypes.c_double, ctypes.c_int,
+                                                       ctypes.POINTER(ctypes.c_int), _vp]),
+        "pcg_host_wait": (ctypes.c_int, [_vp]),
         "pcg_last_error": (ctypes.c_char_p, [_vp]),
         "pcg_enable_timing": (ctypes.c_int, [_vp, ctypes.c_int]),
         "pcg_kernel_times": (ctypes.c_int, [_vp, _vp, _vp]),
@@ -347,6 +352,30 @@ def pcg_update_solve_host(ctx, nx, ny, nz, b, x0, x, rtol, maxit, history=True, 
     return it.value, (hist[: it.value + 1] if history else None), st
 
 
+def pcg_update_solve_host_async(ctx, nx, ny, nz, b, x0, x, rtol, maxit, history=True, a_h=1.0,
+                                a_h_field=None, a_v=1.0, mass=1.0, dz=None):
+    """As pcg_update_solve_host, with x's copy to the host left running (it
+    overlaps the next call); read x only after pcg_host_wait."""
+    n = int(nx) * int(ny) * int(nz)
+    c, keep = make_coeffs(nx, ny, nz, a_h, a_h_field, a_v, mass, dz)
+    it = ctypes.c_int(-1)
+    hist = np.full(int(maxit) + 1, np.nan) if history else None
+    x0p = None if x0 is None else _host_ptr(x0, n, "x0")
+    st = _lib.pcg_update_solve_host_async(ctx, ctypes.byref(c), _host_ptr(b, n, "b"), x0p,
+                                          _host_ptr(x, n, "x", writable=True), float(rtol),
+                                          int(maxit), ctypes.byref(it),
+                                          hist.ctypes.data_as(_vp) if history else None)
+    del keep
+    if st not in (PCG_OK, PCG_ENOTCONV, PCG_EBREAKDOWN):
+        _check(st, ctx)
+    return it.value, (hist[: it.value + 1] if history else None), st
+
+
+def pcg_host_wait(ctx):
+    """Wait for the solution copies left running by pcg_update_solve_host_async."""
+    return _check(_lib.pcg_host_wait(ctx), ctx)
+
+
 def pcg_precond_dot_noalloc(ctx, n, r, z, rz):
     """z = M^{-1} r and rz[0] = <r, z>, with no device allocation.
 
@@ -532,6 +561,16 @@ class Solver:
         arrays (b and x0 copied in while the set-up runs)."""
         return pcg_update_solve_host(self.ctx, self.nx, self.ny, self.nz, b, x0, x, rtol, maxit,
                                      history, a_h, a_h_field, a_v, mass, dz)
+
+    def update_solve_host_async(self, b, x, rtol=1e-10, maxit=500, history=True, x0=None,
+                                a_h=1.0, a_h_field=None, a_v=1.0, mass=1.0, dz=None):
+        """pcg_update_solve_host_async: as update_solve_host, x's copy left
+        running; call host_wait before reading x."""
+        return pcg_update_solve_host_async(self.ctx, self.nx, self.ny, self.nz, b, x0, x, rtol,
+                                           maxit, history, a_h, a_h_field, a_v, mass, dz)
+
+    def host_wait(self):
+        pcg_host_wait(self.ctx)
 
     def enable_timing(self, enable=True):
         pcg_enable_timing(self.ctx, enable)

@@ -106,6 +106,14 @@ struct pcg_ctx {
   // second stream of pcg_update_solve_host: b and x0 go in while the set-up runs
   cudaStream_t copy_stream = nullptr;
   cudaEvent_t copy_done = nullptr;
+  // pcg_update_solve_host_async: x of consecutive calls alternates between two
+  // device copies (x_host_api and x_async2); its copy-out runs on out_stream
+  // and out_done[k] marks the end of the last one that read copy k
+  double* x_async2 = nullptr;
+  cudaStream_t out_stream = nullptr;
+  cudaEvent_t out_done[2] = {nullptr, nullptr}, solved = nullptr;
+  bool out_pending[2] = {false, false};
+  int out_slot = 0;
   // set by the host-buffer entry points right before their solve (and taken
   // back at its start): the initial guess is zero and its device copy was not
   // written, so the row-tiled start reads no x
@@ -237,6 +245,7 @@ void free_all(pcg_ctx* ctx) {
   double* bufs[] = {ctx->r,     ctx->z,     ctx->p,     ctx->q,        ctx->lev,
                     ctx->ah,    ctx->faceE, ctx->faceN, ctx->cdiag,    ctx->tnphi,
                     ctx->tinvd, ctx->partials, ctx->hist, ctx->b_host_api, ctx->x_host_api,
+                    ctx->x_async2,
                     ctx->wscratch, ctx->u_t, ctx->cdiag_t, ctx->cwE_t, ctx->cwN_t,
                     ctx->nscratch,
                     ctx->op.sp_nphi, ctx->op.sp_invd, ctx->op.sp_ta, ctx->op.sp_tb,
@@ -259,6 +268,14 @@ void free_all(pcg_ctx* ctx) {
   ctx->copy_done = nullptr;
   if (ctx->copy_stream) cudaStreamDestroy(ctx->copy_stream);
   ctx->copy_stream = nullptr;
+  for (cudaEvent_t& ev : ctx->out_done) {
+    if (ev) cudaEventDestroy(ev);
+    ev = nullptr;
+  }
+  if (ctx->solved) cudaEventDestroy(ctx->solved);
+  ctx->solved = nullptr;
+  if (ctx->out_stream) cudaStreamDestroy(ctx->out_stream);
+  ctx->out_stream = nullptr;
   mg_release(ctx);
 }
 
@@ -1061,6 +1078,8 @@ void pcg_destroy(pcg_ctx* ctx) {
   if (!ctx) return;
   DeviceGuard g(ctx->device);
   cudaStreamSynchronize(ctx->stream);
+  if (ctx->copy_stream) cudaStreamSynchronize(ctx->copy_stream);
+  if (ctx->out_stream) cudaStreamSynchronize(ctx->out_stream);
   free_all(ctx);
   delete ctx;
 }
@@ -1399,6 +1418,14 @@ static cudaError_t host_api_buffers(pcg_ctx* ctx) {
   return e;
 }
 
+// The copy-outs of earlier asynchronous calls, finished (host side).
+static cudaError_t wait_copy_outs(pcg_ctx* ctx) {
+  if (!ctx->out_stream) return cudaSuccess;
+  cudaError_t e = cudaStreamSynchronize(ctx->out_stream);
+  if (e == cudaSuccess) ctx->out_pending[0] = ctx->out_pending[1] = false;
+  return e;
+}
+
 static int check_host_x0(pcg_ctx* ctx, const double* b_host, const double* x0_host,
                          const double* x_host) {
   if (x0_host && x0_host != x_host && overlap(b_host, x0_host, ctx->op.n))
@@ -1435,7 +1462,8 @@ int pcg_solve_host_x0(pcg_ctx* ctx, const double* b_host, const double* x0_host,
   if (st) return st;
   DeviceGuard g(ctx->device);
   if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
-  cudaError_t e = host_api_buffers(ctx);
+  cudaError_t e = wait_copy_outs(ctx);  // an asynchronous call's copy-out may read x_host_api
+  if (e == cudaSuccess) e = host_api_buffers(ctx);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "device buffers for b and x");
   const size_t bytes = sizeof(double) * (size_t)ctx->op.n;
   const bool x0_zero = zero_x0_skips_copy(ctx, x0_host);
@@ -1448,9 +1476,10 @@ int pcg_solve_host_x0(pcg_ctx* ctx, const double* b_host, const double* x0_host,
   return solve_copy_out(ctx, x0_zero, x_host, rtol, maxit, iters_out, res_hist);
 }
 
-int pcg_update_solve_host(pcg_ctx* ctx, const pcg_coeffs* coeffs, const double* b_host,
-                          const double* x0_host, double* x_host, double rtol, int maxit,
-                          int* iters_out, double* res_hist) {
+// pcg_update_solve_host (async false) and pcg_update_solve_host_async.
+static int update_solve_host(pcg_ctx* ctx, const pcg_coeffs* coeffs, const double* b_host,
+                             const double* x0_host, double* x_host, double rtol, int maxit,
+                             int* iters_out, double* res_hist, bool async) {
   if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
   int st = validate_coeffs(ctx, ctx->op.nx, ctx->op.ny, ctx->op.nz, coeffs);
   if (st) return st;
@@ -1463,14 +1492,33 @@ int pcg_update_solve_host(pcg_ctx* ctx, const pcg_coeffs* coeffs, const double* 
   if (st) return st;
   DeviceGuard g(ctx->device);
   if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
-  cudaError_t e = host_api_buffers(ctx);
+  cudaError_t e = async ? cudaSuccess : wait_copy_outs(ctx);
+  if (e == cudaSuccess) e = host_api_buffers(ctx);
   if (e == cudaSuccess && !ctx->copy_stream)
     e = cudaStreamCreateWithFlags(&ctx->copy_stream, cudaStreamNonBlocking);
   if (e == cudaSuccess && !ctx->copy_done)
     e = cudaEventCreateWithFlags(&ctx->copy_done, cudaEventDisableTiming);
+  if (async) {
+    if (e == cudaSuccess && !ctx->x_async2) e = dalloc(&ctx->x_async2, ctx->op.n);
+    if (e == cudaSuccess && !ctx->out_stream)
+      e = cudaStreamCreateWithFlags(&ctx->out_stream, cudaStreamNonBlocking);
+    for (cudaEvent_t* ev : {&ctx->out_done[0], &ctx->out_done[1], &ctx->solved})
+      if (e == cudaSuccess && !*ev) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+  }
   // no earlier work on the context's stream may still use the device copies
   if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "device buffers for b and x");
+  // the device copy of x: the asynchronous calls alternate between two, so
+  // that one call's copy-out overlaps the next call's solve; a copy-out still
+  // reading the one used now is waited for on the device, by both streams
+  // that write it (x0 in, the solve)
+  const int slot = async ? ctx->out_slot : 0;
+  double* xs = slot ? ctx->x_async2 : ctx->x_host_api;
+  if (async && ctx->out_pending[slot]) {
+    e = cudaStreamWaitEvent(ctx->copy_stream, ctx->out_done[slot], 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->stream, ctx->out_done[slot], 0);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "device-to-host copy order");
+  }
   const size_t bytes = sizeof(double) * (size_t)ctx->op.n;
   const bool x0_zero = zero_x0_skips_copy(ctx, x0_host);
   bool copies_enqueued = false;
@@ -1479,10 +1527,9 @@ int pcg_update_solve_host(pcg_ctx* ctx, const pcg_coeffs* coeffs, const double* 
     cudaError_t ce = cudaMemcpyAsync(ctx->b_host_api, b_host, bytes, cudaMemcpyHostToDevice,
                                      ctx->copy_stream);
     if (ce == cudaSuccess && x0_host)
-      ce = cudaMemcpyAsync(ctx->x_host_api, x0_host, bytes, cudaMemcpyHostToDevice,
-                           ctx->copy_stream);
+      ce = cudaMemcpyAsync(xs, x0_host, bytes, cudaMemcpyHostToDevice, ctx->copy_stream);
     if (ce == cudaSuccess && !x0_host && !x0_zero)
-      ce = cudaMemsetAsync(ctx->x_host_api, 0, bytes, ctx->copy_stream);  // x0 = +0.0
+      ce = cudaMemsetAsync(xs, 0, bytes, ctx->copy_stream);  // x0 = +0.0
     if (ce == cudaSuccess) ce = cudaEventRecord(ctx->copy_done, ctx->copy_stream);
     return ce;
   };
@@ -1493,7 +1540,43 @@ int pcg_update_solve_host(pcg_ctx* ctx, const pcg_coeffs* coeffs, const double* 
   }
   e = cudaStreamWaitEvent(ctx->stream, ctx->copy_done, 0);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "host-to-device copy");
-  return solve_copy_out(ctx, x0_zero, x_host, rtol, maxit, iters_out, res_hist);
+  if (!async) return solve_copy_out(ctx, x0_zero, x_host, rtol, maxit, iters_out, res_hist);
+  // asynchronous: the solve, then x out on out_stream, not waited for
+  ctx->x0_zero = x0_zero;
+  st = solve_device(ctx, ctx->b_host_api, xs, rtol, maxit, iters_out, res_hist);
+  if (st != PCG_OK && st != PCG_ENOTCONV && st != PCG_EBREAKDOWN) return st;
+  e = cudaEventRecord(ctx->solved, ctx->stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->out_stream, ctx->solved, 0);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(x_host, xs, bytes, cudaMemcpyDeviceToHost, ctx->out_stream);
+  if (e == cudaSuccess) e = cudaEventRecord(ctx->out_done[slot], ctx->out_stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "device-to-host copy");
+  ctx->out_pending[slot] = true;
+  ctx->out_slot = slot ^ 1;
+  return st;
+}
+
+int pcg_update_solve_host(pcg_ctx* ctx, const pcg_coeffs* coeffs, const double* b_host,
+                          const double* x0_host, double* x_host, double rtol, int maxit,
+                          int* iters_out, double* res_hist) {
+  return update_solve_host(ctx, coeffs, b_host, x0_host, x_host, rtol, maxit, iters_out,
+                           res_hist, false);
+}
+
+int pcg_update_solve_host_async(pcg_ctx* ctx, const pcg_coeffs* coeffs, const double* b_host,
+                                const double* x0_host, double* x_host, double rtol, int maxit,
+                                int* iters_out, double* res_hist) {
+  return update_solve_host(ctx, coeffs, b_host, x0_host, x_host, rtol, maxit, iters_out,
+                           res_hist, true);
+}
+
+int pcg_host_wait(pcg_ctx* ctx) {
+  if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
+  const cudaError_t e = wait_copy_outs(ctx);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "device-to-host copy");
+  return PCG_OK;
 }
 
 int pcg_solve_host(pcg_ctx* ctx, const double* b_host, double* x_host, double rtol, int maxit,

@@ -53,7 +53,8 @@ def test_bench_line_has_the_contract_keys(workload):
     n = d["config"]["cells"]
     assert e2e["unit"] == "iters/s" and e2e["value"] > 0
     assert e2e["h2d_bytes_per_step"] >= 8 * n and e2e["d2h_bytes_per_step"] == 8 * n
-    assert len(e2e["step_ms"]) == 3 and len(e2e["copy_only_ms"]) == 3
+    assert len(e2e["step_ms"]) == 3 and len(e2e["sync"]["copy_only_ms"]) == 3
+    assert e2e["sync"]["value"] > 0 and "async" in e2e["api"]
     assert rl["peak_source"].startswith("measured") and rl["fp64_probe"]["lanes_per_sm_clk"] > 0
     assert abs(rl["frac_nominal"] - rl["achieved"] / rl["peak_nominal"]) <= 1e-9
     assert cpu["host_cpus"] >= 1 and cpu["cpu_model"]

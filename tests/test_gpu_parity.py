@@ -227,6 +227,52 @@ def test_update_solve_host_equals_update_then_solve(cfg):
     assert np.linalg.norm(x4 - x_ref) <= SOL_TOL * np.linalg.norm(x_ref)
 
 
+@pytest.mark.parametrize("layout", ["tiled", "column"])
+def test_update_solve_host_async_matches_the_synchronous_call(layout):
+    # a sequence of solves whose solution copies run behind the next solve:
+    # every solution, count and history bit for bit the synchronous call's,
+    # with separate output buffers, with one shared buffer (the last solution
+    # after the wait) and with initial guesses copied in on the second stream
+    nx, ny, nz = 37, 29, 32
+    prob, kw, _ = case(nx, ny, nz, True, True, a_v=1e4, seed=40)
+    n = prob.n
+    rng = np.random.default_rng(41)
+    steps = []
+    for i in range(5):
+        coef = dict(kw, a_h_field=prob.ah * (1.0 + 0.1 * i), a_v=1e4 * (1 + i), mass=1.0)
+        x0 = rng.standard_normal(n) if i % 2 else None
+        steps.append((torch.from_numpy(rng.uniform(-1, 1, n)).pin_memory(), x0, coef))
+    ref = []
+    with mf.Solver(nx, ny, nz, **kw) as s:
+        s.set_layout(layout)
+        for bh, x0, coef in steps:
+            x = torch.empty(n, dtype=torch.float64).pin_memory()
+            it, h, st = s.update_solve_host(bh, x, rtol=1e-10, x0=x0, **coef)
+            ref.append((it, h, st, x.numpy().copy()))
+    with mf.Solver(nx, ny, nz, **kw) as s:
+        s.set_layout(layout)
+        outs = [torch.full((n,), float("nan"), dtype=torch.float64).pin_memory() for _ in steps]
+        got = [s.update_solve_host_async(bh, x, rtol=1e-10, x0=x0, **coef)
+               for (bh, x0, coef), x in zip(steps, outs)]
+        s.host_wait()
+        for (it, h, st), x, (it_r, h_r, st_r, x_r) in zip(got, outs, ref):
+            assert (it, st) == (it_r, st_r) and np.array_equal(h, h_r)
+            assert np.array_equal(x.numpy(), x_r)
+        # one shared output buffer: after the wait it holds the last solution
+        shared = torch.full((n,), float("nan"), dtype=torch.float64).pin_memory()
+        for bh, x0, coef in steps:
+            s.update_solve_host_async(bh, shared, rtol=1e-10, x0=x0, **coef)
+        s.host_wait()
+        assert np.array_equal(shared.numpy(), ref[-1][3])
+        # a synchronous call right after asynchronous ones waits for their copies
+        bh, x0, coef = steps[0]
+        s.update_solve_host_async(steps[1][0], outs[1], rtol=1e-10, x0=steps[1][1], **steps[1][2])
+        x = torch.empty(n, dtype=torch.float64).pin_memory()
+        s.update_solve_host(bh, x, rtol=1e-10, x0=x0, **coef)
+        assert np.array_equal(x.numpy(), ref[0][3])
+        assert np.array_equal(outs[1].numpy(), ref[1][3])
+
+
 def test_update_solve_host_initial_guess_and_errors():
     prob, kw, b = case(30, 26, 24, True, True, a_v=1e3, seed=32)
     x0 = np.random.default_rng(33).standard_normal(prob.n)
