@@ -590,9 +590,14 @@ def run_ours(args, w):
     t_m = measured_traffic("precond_fused", n, args.layout, args.factors, az_form)
     t_a = measured_traffic("spmv_fused", n, args.layout, args.factors, az_form)
     if t_m and t_a:
+        # the ncu DRAM bytes of one iteration over the loop's live time per
+        # iteration: the bandwidth the fused iteration sustains in DRAM terms
+        dram_gbs = (t_m + t_a) / (loop_stats["ms_per_iter"] * 1e-3) / 1e9
         dram_iter = {"bytes": t_m + t_a, "per_cell": (t_m + t_a) / n,
                      "vs_fused_min_88": (t_m + t_a) / (88.0 * n),
-                     "vs_algorithmic": (t_m + t_a) / bytes_iter}
+                     "vs_algorithmic": (t_m + t_a) / bytes_iter,
+                     "gbs": dram_gbs, "frac": dram_gbs / hbm_peak,
+                     "frac_nominal_8tbs": dram_gbs / NOMINAL_HBM_GBS}
 
     # end to end through the host-buffer entry point that takes the step's
     # coefficients and right-hand side together (pcg_update_solve_host with
