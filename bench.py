@@ -137,6 +137,8 @@ def parse():
                          "multigrid with it as smoother")
     ap.add_argument("--mg-levels", type=int, default=0,
                     help="multigrid levels at most (0: coarsen while nx and ny are even)")
+    ap.add_argument("--loop", choices=["auto", "batched", "persistent", "cluster"],
+                    default="auto", help="solve loop (row-tiled layout)")
     ap.add_argument("--grid", type=int, nargs=3, metavar=("NX", "NY", "NZ"),
                     help="same coefficients on another grid size (profiling captures)")
     ap.add_argument("--cpu-all", action="store_true",
@@ -419,6 +421,7 @@ def run_ours(args, w):
     solver.set_factors(args.factors)
     solver.set_substructuring(args.substructuring)
     solver.set_az_form(args.az_form)
+    solver.set_loop(args.loop)
     mgrid = args.preconditioner == "multigrid"
     if mgrid:
         solver.set_multigrid(1, 0.8, args.mg_levels)
@@ -693,6 +696,7 @@ def run_ours(args, w):
                               % (8e-6 * n)),
                        "layout": args.layout, "factors": args.factors,
                        "substructuring": solver.substructuring, "az_form": az_form,
+                       "loop": solver.loop,
                        "preconditioner": args.preconditioner,
                        "multigrid": ({"levels": solver.multigrid_levels, "nu": 1, "omega": 0.8}
                                      if mgrid else None),
