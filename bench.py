@@ -144,6 +144,12 @@ def parse():
     ap.add_argument("--cpu-all", action="store_true",
                     help="time the CPU oracle (1 thread) on every workload with its own "
                          "stopping rule, one JSON line per workload (no GPU work)")
+    ap.add_argument("--cpu-openmp", action="store_true",
+                    help="with --cpu-all: the same oracle source built with -fopenmp, on every "
+                         "host thread")
+    ap.add_argument("--no-cpu-openmp", action="store_true",
+                    help="leave out the cpu_baseline_openmp line")
+    ap.add_argument("--cpu-omp-sample", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -333,6 +339,59 @@ def cpu_oracle_sample(w, h, ah, b, iters, multigrid=False):
     return it, dt
 
 
+def openmp_threads():
+    """Threads the OpenMP build of the oracle uses in this process (its
+    runtime is loaded with the library)."""
+    import ctypes
+    try:
+        return int(ctypes.CDLL("libgomp.so.1").omp_get_max_threads())
+    except (OSError, AttributeError):
+        return None
+
+
+def run_cpu_omp_sample(args, w):
+    """Child process of cpu_openmp_sample: the OpenMP build (ORACLE_LIB) on the
+    full grid, args.cpu_iters fixed iterations; one JSON line."""
+    h, ah, vec = workload_inputs(w)
+    b = oracle_rhs(w, h, ah, vec)
+    it, dt = cpu_oracle_sample(w, h, ah, b, args.cpu_iters)
+    print(json.dumps({"iters": it, "seconds": dt, "threads": openmp_threads()}), flush=True)
+    return 0
+
+
+def cpu_openmp_sample(args, w, iters):
+    """The same oracle source built with -fopenmp (loops over cells and columns
+    on every host thread, dot products in per-thread parts), timed like the
+    sequential sample in a child process on the same workload.  Returns the
+    cpu_baseline_openmp object, or one that says why there is none."""
+    try:
+        from oracle import build as obuild
+        lib = obuild.build(openmp=True)
+    except (OSError, subprocess.SubprocessError) as e:
+        return {"unavailable": "the OpenMP build of the oracle failed: %s" % e}
+    ncpu, model = host_cpu()
+    env = dict(os.environ, ORACLE_LIB=lib)
+    env.setdefault("OMP_NUM_THREADS", str(ncpu))
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-omp-sample", "--workload",
+           args.workload, "--cpu-iters", str(iters)]
+    if args.grid:
+        cmd += ["--grid"] + [str(v) for v in args.grid]
+    try:
+        out = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=900,
+                             check=True).stdout
+        res = json.loads(out.strip().splitlines()[-1])
+    except (OSError, subprocess.SubprocessError, ValueError, IndexError) as e:
+        return {"unavailable": "the OpenMP sample failed: %s" % e}
+    return {"value": res["iters"] / res["seconds"], "unit": UNIT, "cores": res["threads"],
+            "kind": "oracle_openmp", "host_cpus": ncpu, "cpu_model": model,
+            "sample": "oracle_pcg built with -fopenmp from the same source (cells and columns "
+                      "on every thread, per-thread partial dot products), the full %dx%dx%d "
+                      "grid, %d fixed PCG iterations (initial residual and first preconditioner "
+                      "solve included), %s threads of %d (%s), %.1f s"
+                      % (w.nx, w.ny, w.nz, res["iters"], res["threads"], ncpu, model,
+                         res["seconds"])}
+
+
 def run_reference(args, w):
     rank, world, _ = rank_info()
     if rank != 0:
@@ -375,8 +434,13 @@ def run_cpu_all(args):
     rank, _, _ = rank_info()
     if rank != 0:
         return 0
-    import oracle
     ncpu, model = host_cpu()
+    if args.cpu_openmp:
+        from oracle import build as obuild
+        os.environ["ORACLE_LIB"] = obuild.build(openmp=True)
+        os.environ.setdefault("OMP_NUM_THREADS", str(ncpu))
+    import oracle
+    threads = (openmp_threads() if args.cpu_openmp else 1)
     for name in sorted(W.WORKLOADS, key=lambda k: W.WORKLOADS[k].n):
         w = W.WORKLOADS[name]
         h, ah, vec = workload_inputs(w)
@@ -386,13 +450,16 @@ def run_cpu_all(args):
         _, it, hist, st = oracle.pcg(prob, b, rtol=w.rtol, maxit=w.maxit)
         dt = time.perf_counter() - t0
         print(json.dumps({
-            "impl": "oracle", "workload": name, "grid": [w.nx, w.ny, w.nz], "cells": w.n,
+            "impl": "oracle_openmp" if args.cpu_openmp else "oracle", "workload": name,
+            "grid": [w.nx, w.ny, w.nz], "cells": w.n,
             "rtol": w.rtol, "maxit": w.maxit, "iters": it, "status": st,
             "final_rel_residual": float(hist[-1]), "time_to_solution_s": dt,
             "iters_per_s": it / dt, "fused_min_gbs": FUSED_MIN_BYTES * w.n * it / dt / 1e9,
-            "cores": 1, "host_cpus": ncpu, "cpu_model": model,
+            "cores": threads, "host_cpus": ncpu, "cpu_model": model,
             "what": "oracle_pcg from x0 = 0: initial residual, every iteration and the "
-                    "final update; sequential C, -O2 -ffp-contract=off"}), flush=True)
+                    "final update; " + ("the same source built with -fopenmp"
+                                        if args.cpu_openmp else
+                                        "sequential C, -O2 -ffp-contract=off")}), flush=True)
     return 0
 
 
@@ -680,6 +747,11 @@ def run_ours(args, w):
                          "sequential C, 1 thread of %d (%s), %.1f s"
                          % ("oracle_mg_pcg" if mgrid else "oracle_pcg", w.nx, w.ny, w.nz, mgi,
                             ncpu, model, dt_c)}
+    cpu_omp = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.no_cpu_openmp:
+        cpu_omp = ({"unavailable": "the OpenMP build parallelises the line-preconditioned "
+                                   "PCG only"} if mgrid else
+                   cpu_openmp_sample(args, w, args.cpu_iters))
 
     if rank == 0:
         line = {
@@ -707,7 +779,7 @@ def run_ours(args, w):
             "bytes_per_cell_iter": bytes_iter / n, "fp64_ops_per_cell_iter": ops_iter / n,
             "dram_per_iter": dram_iter, "standalone": standalone,
             "roofline": roofline, "kernels": kernels, "clocks": clk, "e2e": e2e,
-            "cpu_baseline": cpu, "gpu_launches": launches,
+            "cpu_baseline": cpu, "cpu_baseline_openmp": cpu_omp, "gpu_launches": launches,
             "time_to_solution_ms": ms_max / args.steps,
         }
         print(json.dumps(line), flush=True)
@@ -730,6 +802,8 @@ def main():
                                 nx=nx, ny=ny, nz=nz)
     if args.cpu_all:
         return run_cpu_all(args)
+    if args.cpu_omp_sample:
+        return run_cpu_omp_sample(args, w)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

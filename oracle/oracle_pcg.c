@@ -41,6 +41,14 @@
  * Solver (section 4, left-preconditioned conjugate gradients, Hestenes and
  * Stiefel).  Textbook PCG; the stopping test ||r_k|| / ||r_0|| < rtol of
  * Algorithm 1 (tau = 0).
+ *
+ * OpenMP.  The benchmark's second, labelled CPU line builds this same file
+ * with -fopenmp (liboracle_pcg_omp.so): the loops over cells and columns of
+ * the line-preconditioned PCG then run on all host cores, and the dot
+ * products add per-thread partial sums.  That build is a timing baseline
+ * only.  The sequential build, which the tests and every comparison with the
+ * GPU use, does not see the OpenMP lines: its arithmetic and its order are
+ * the ones written.
  */
 #include <math.h>
 #include <stdint.h>
@@ -52,6 +60,15 @@
 #define ORACLE_ENOMEM    2
 #define ORACLE_ENOTCONV  4
 #define ORACLE_EBREAKDOWN 5
+
+#ifdef _OPENMP
+#define OMP_PRAGMA(x) _Pragma(#x)
+#define OMP_FOR OMP_PRAGMA(omp parallel for schedule(static))
+#define OMP_FOR_SUM(v) OMP_PRAGMA(omp parallel for schedule(static) reduction(+ : v))
+#else
+#define OMP_FOR
+#define OMP_FOR_SUM(v)
+#endif
 
 typedef struct {
   int nx, ny, nz;
@@ -123,6 +140,7 @@ static double apply_row(const grid_t* g, int i, int j, int k, const double* x) {
 }
 
 static void apply_A(const grid_t* g, const double* x, double* y) {
+  OMP_FOR
   for (int j = 0; j < g->ny; ++j)
     for (int i = 0; i < g->nx; ++i)
       for (int k = 0; k < g->nz; ++k)
@@ -154,6 +172,31 @@ static int thomas_column(const grid_t* g, int i, int j, const double* r, double*
 }
 
 static int precond(const grid_t* g, const double* r, double* z, double* phi, double* y) {
+#ifdef _OPENMP
+  /* OpenMP build: the columns in parallel, each thread with its own scratch;
+   * the status is that of any column that fails */
+  int st = ORACLE_OK;
+  const int64_t ncols = (int64_t)g->nx * g->ny;
+  (void)phi;
+  (void)y;
+#pragma omp parallel reduction(max : st)
+  {
+    /* the thread's copy of st (a max reduction's starts at INT_MIN) */
+    double* tphi = (double*)malloc(sizeof(double) * g->nz);
+    double* ty = (double*)malloc(sizeof(double) * g->nz);
+    st = (tphi && ty) ? ORACLE_OK : ORACLE_ENOMEM;
+#pragma omp for schedule(static)
+    for (int64_t c = 0; c < ncols; ++c) {
+      if (st == ORACLE_OK) {
+        int64_t off = c * g->nz;
+        st = thomas_column(g, (int)(c % g->nx), (int)(c / g->nx), r + off, z + off, tphi, ty);
+      }
+    }
+    free(tphi);
+    free(ty);
+  }
+  return st;
+#else
   for (int j = 0; j < g->ny; ++j)
     for (int i = 0; i < g->nx; ++i) {
       int64_t off = ((int64_t)j * g->nx + i) * g->nz;
@@ -161,10 +204,12 @@ static int precond(const grid_t* g, const double* r, double* z, double* phi, dou
       if (st) return st;
     }
   return ORACLE_OK;
+#endif
 }
 
 static double dot(int64_t n, const double* a, const double* b) {
   double s = 0.0;
+  OMP_FOR_SUM(s)
   for (int64_t l = 0; l < n; ++l) s += a[l] * b[l];
   return s;
 }
@@ -257,6 +302,7 @@ static int pcg_loop(const grid_t* g, prec_fn prec, void* pctx, const double* b, 
 
   /* r_0 = b - A x_0,  z_0 = B r_0,  p_0 = z_0 */
   apply_A(g, x, q);
+  OMP_FOR
   for (int64_t l = 0; l < n; ++l) r[l] = b[l] - q[l];
   double rho0 = sqrt(dot(n, r, r));
   *iters = 0;
@@ -275,7 +321,9 @@ static int pcg_loop(const grid_t* g, prec_fn prec, void* pctx, const double* b, 
     double sigma = dot(n, p, q);
     if (!(sigma > 0.0)) { st = ORACLE_EBREAKDOWN; goto done; }
     double alpha = kappa / sigma;
+    OMP_FOR
     for (int64_t l = 0; l < n; ++l) x[l] += alpha * p[l];
+    OMP_FOR
     for (int64_t l = 0; l < n; ++l) r[l] -= alpha * q[l];
     double rnorm = sqrt(dot(n, r, r));
     double res = rnorm / rho0;
@@ -290,6 +338,7 @@ static int pcg_loop(const grid_t* g, prec_fn prec, void* pctx, const double* b, 
     if (!(kappa_new > 0.0)) { st = ORACLE_EBREAKDOWN; goto done; }
     double beta = kappa_new / kappa;
     kappa = kappa_new;
+    OMP_FOR
     for (int64_t l = 0; l < n; ++l) p[l] = z[l] + beta * p[l];
   }
   if (rtol > 0.0) st = ORACLE_ENOTCONV;
