@@ -26,7 +26,8 @@ _i64p = ctypes.POINTER(ctypes.c_int64)
 def _load():
     global _lib
     if _lib is None:
-        # ORACLE_LIB lets the mutation test load a deliberately broken copy.
+        # ORACLE_LIB selects another build: a mutation test's deliberately
+        # broken copy, or the benchmark's OpenMP build (oracle/build.py).
         path = os.environ.get("ORACLE_LIB") or _build.build()
         lib = ctypes.CDLL(path)
         common = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _dp, ctypes.c_double,
