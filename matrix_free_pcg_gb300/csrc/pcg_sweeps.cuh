@@ -55,7 +55,12 @@ __device__ __forceinline__ void precond_tile(const Op& op, long long t, int lane
   double* __restrict__ zt = z + base;
   const double* __restrict__ fi = VARY ? op.tinvd + base : op.lev + LV_INVD * nz;
   const double* __restrict__ fn = VARY ? op.tnphi + base : op.lev + LV_NPHI * nz;
-  // ---- forward: level k uses nphi_{k-1} (0 at k = 0) and 1/D_k
+  // ---- forward: level k uses nphi_{k-1} (0 at k = 0) and 1/D_k.  Only the w
+  // scratch is marked to stay in L2 (evict-last) for the backward pass; the
+  // factors' first read streams like the rest, though the backward pass reads
+  // nphi again.  Kept as well, they crowded w out of L2: on 512x512x128 with
+  // an a_h field ncu measured 55.2 B per cell and 0.385 ms per sweep, against
+  // 53.9 B and 0.377 ms with nphi streamed.
   constexpr int CF = COHERENT ? kTmChunkP : kTmChunk;
   double cr[CF], cq[CF], ci[CF], cn[CF];
 #pragma unroll
@@ -65,7 +70,7 @@ __device__ __forceinline__ void precond_tile(const Op& op, long long t, int lane
     cq[j] = (FUSED && in) ? (COHERENT ? __ldcg(qt + j * kTile) : ld_hint(qt + j * kTile, stream))
                           : 0.0;
     ci[j] = in ? (VARY ? ld_hint(fi + j * fs, stream) : __ldg(fi + j)) : 0.0;
-    cn[j] = in ? (VARY ? ld_hint(fn + j * fs, keep) : __ldg(fn + j)) : 0.0;
+    cn[j] = in ? (VARY ? ld_hint(fn + j * fs, stream) : __ldg(fn + j)) : 0.0;
   }
   double y = 0.0, nprev = 0.0, w = 0.0;
 #pragma unroll 1
@@ -79,7 +84,7 @@ __device__ __forceinline__ void precond_tile(const Op& op, long long t, int lane
       nq[j] = (FUSED && in) ? (COHERENT ? __ldcg(qt + k * kTile) : ld_hint(qt + k * kTile, stream))
                             : 0.0;
       ni[j] = in ? (VARY ? ld_hint(fi + k * fs, stream) : __ldg(fi + k)) : 0.0;
-      nn[j] = in ? (VARY ? ld_hint(fn + k * fs, keep) : __ldg(fn + k)) : 0.0;
+      nn[j] = in ? (VARY ? ld_hint(fn + k * fs, stream) : __ldg(fn + k)) : 0.0;
     }
 #pragma unroll
     for (int j = 0; j < CF; ++j) {
