@@ -656,7 +656,7 @@ def run_ours(args, w):
     loop_stats["fp64_frac"] = loop_stats["fp64_gops"] / alu_peak
     # DRAM bytes of one iteration (both sweeps, from the committed ncu captures)
     # against the fused minimum of 88 B/cell (u, p, z, q, r moved once, no
-    # per-cell coefficients) and against this build's algorithmic bytes
+    # per-cell coefficients) and against the sweeps' own algorithmic bytes (with the per-cell coefficients)
     dram_iter = None
     t_m = measured_traffic("precond_fused", n, args.layout, args.factors, az_form)
     t_a = measured_traffic("spmv_fused", n, args.layout, args.factors, az_form)
