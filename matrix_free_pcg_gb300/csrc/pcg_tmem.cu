@@ -16,7 +16,8 @@
 // 32(w mod 4) .. 32(w mod 4)+31, one per column of its tile, and columns
 // 256 floor(w/4) .. +255, i.e. 128 doubles per grid column (nz <= 128).  The
 // w round trip then costs neither L2 traffic nor global load latency, and
-// two warps per sub-partition hide each other's fp64 latency.
+// two warps per sub-partition overlap each other's loads and stores with
+// their fp64 work (a warp alone adds its operand moves to its fp64 issue).
 //
 // r (and q) stream through per-warp rings of 8-level chunks in shared
 // memory, filled two chunks ahead by 16-byte asynchronous copies in a
@@ -60,7 +61,8 @@ __host__ __device__ constexpr int kTwWarpDoubles() {
 // A warp runs the forward pass of its next tile in step with the back
 // substitution of its previous one, chunk by chunk (8 levels): two
 // independent dependency chains per lane instead of one, so that two warps
-// per sub-partition keep the fp64 pipe fed.  Both passes share one tile's
+// per sub-partition keep the fp64 pipe fed (measured: one chain per warp,
+// 0.902 ms, against 0.789 ms on 1024x1024x128).  Both passes share one tile's
 // worth of TMEM: step s of the back substitution reads the region that step s
 // of the forward pass then overwrites.  For that, the i-th tile of a warp
 // keeps its chunk m in region m (i even) or NCH-1-m (i odd): the back
