@@ -373,9 +373,9 @@ int pcg_host_wait(pcg_ctx* ctx);
 /* z = M^{-1} r and *rz_dev = <r, z>, without allocating anything.
  * The paper has no counterpart: this entry point exists for callers that
  * must not allocate device memory while they run -- for instance code that
- * must not synchronise the device (cudaFree does, cudaMalloc may), code
- * running while a stream is captured into a CUDA graph, or applications
- * that hand all device memory to their own pool at start-up.  The context
+ * must not synchronise the device (cudaFree does, cudaMalloc may), or
+ * applications that hand all device memory to their own pool at start-up
+ * and leave none for a library to take.  The context
  * (made earlier with pcg_create) supplies the operator tables; the only
  * scratch, one partial sum per tile of 32 columns, comes from a fixed array
  * of 65,536 doubles (512 KB) compiled into the library, which every GPU that

@@ -6,9 +6,9 @@
 // one partial sum per 32-column tile -- from a fixed array compiled into
 // this library instead of from an allocation.  Some callers must not call
 // cudaMalloc/cudaFree while they run: code that must not synchronise the
-// device (cudaFree does, and cudaMalloc may), code running while a stream is
-// being captured into a CUDA graph, or applications that reserve all device
-// memory for their own pool at start-up.  The operator tables still come from
+// device (cudaFree does, and cudaMalloc may), or applications that reserve
+// all device memory for their own pool at start-up.  The operator tables
+// still come from
 // a context made beforehand with pcg_create.
 //
 // The scratch array lives in every GPU that loads this library until the

@@ -3,8 +3,8 @@ and against the CPU oracle.
 
 pcg_precond_dot_noalloc is for callers that must not allocate device memory
 while they run -- code that must not synchronise the device (as cudaFree
-does), code running during a CUDA-graph stream capture, applications that
-reserve all device memory for their own pool.  It returns z = M^{-1} r and
+does), applications that reserve all device memory for their own pool.  It
+returns z = M^{-1} r and
 <r, z>, taking its scratch from a fixed array inside the library that every
 call reuses.  So it must agree with pcg_precond, and with the oracle's
 column solve (eq. (19)) and <r, z> formed from it, on every call, not only
