@@ -8,8 +8,7 @@
 // cudaMalloc/cudaFree while they run: code that must not synchronise the
 // device (cudaFree does, and cudaMalloc may), or applications that reserve
 // all device memory for their own pool at start-up.  The operator tables
-// still come from
-// a context made beforehand with pcg_create.
+// still come from a context made beforehand with pcg_create.
 //
 // The scratch array lives in every GPU that loads this library until the
 // process exits.  In host code its name is only a stand-in for the device
