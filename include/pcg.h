@@ -38,7 +38,11 @@
  *
  * Errors.  Every function returns a status code (pcg_status) and never
  * aborts, exits or prints.  On failure, pcg_last_error() gives a message.
- * Argument errors are detected on the host before any work is enqueued.
+ * Argument errors are detected on the host before any work is enqueued,
+ * except the values of an a_h field passed to pcg_update_coeffs or
+ * pcg_update_solve_host(_async): those are copied to a staging buffer and
+ * checked there on the device; a rejected field leaves the context as it
+ * was.
  */
 #ifndef PCG_H
 #define PCG_H

@@ -90,6 +90,7 @@ struct DevState {
   double mg_R;       // multigrid preconditioner: ||r||^2 of the current iteration, from the
                      // fine level's first smoothing sweep, for the stopping test
   int setup_error;   // a non-positive Thomas pivot was met in the setup kernel
+  int field_error;   // a value of an uploaded a_h field is negative, infinite or NaN
   int dev_error;     // a bounded device wait ran out (pcg_status PCG_ETIMEOUT)
   unsigned int bar_count;  // arrivals at the grid barriers of the persistent solve loop
 };
@@ -98,6 +99,9 @@ struct DevState {
 // update: pcg_kernels.cu); all enqueue on `s` and return the launch error
 
 cudaError_t launch_face_coeffs(const Op& op, double* faceE, double* faceN, cudaStream_t s);
+// *err = 1 if some f[i], i < n, is negative, infinite or NaN (err untouched
+// otherwise: the caller zeroes it first).
+cudaError_t launch_check_field(const double* f, long long n, int* err, cudaStream_t s);
 // Per-cell diagonal (column-contiguous, and row-tiled when cdiag_t is not
 // NULL), horizontal weights (row-tiled, when cwE_t is not NULL) and Thomas
 // factors (row-tiled) of an a_h field, after the face values.

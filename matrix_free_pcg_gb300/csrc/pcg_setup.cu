@@ -6,6 +6,8 @@
 // and section 4.2 eq. (18); the Thomas factors of the column blocks of the
 // preconditioner, section 4.1 eq. (19).  Run once per operator (pcg_create,
 // pcg_update_coeffs).
+#include <algorithm>
+#include <cfloat>
 #include <cstdint>
 
 #include "pcg_device.cuh"
@@ -20,6 +22,17 @@ __global__ void k_face_coeffs(Op op, double* __restrict__ faceE, double* __restr
     const Nbr nb = neighbours(op, c);
     faceE[c] = 0.5 * (op.ah[c] + op.ah[nb.e]);
     faceN[c] = 0.5 * (op.ah[c] + op.ah[nb.n]);
+  }
+}
+
+// The admissibility check of an uploaded a_h field (finite and >= 0, as the
+// operator of eqs. (5)-(8) needs), on its staging copy: every offending
+// thread stores the same 1.
+__global__ void k_check_field(const double* __restrict__ f, long long n, int* err) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const double v = f[i];
+    if (!(v >= 0.0 && v <= DBL_MAX)) *err = 1;
   }
 }
 
@@ -98,6 +111,13 @@ cudaError_t launch_face_coeffs(const Op& op, double* faceE, double* faceN, cudaS
   long long g = (op.ncols + 255) / 256;
   if (g > 65536) g = 65536;
   k_face_coeffs<<<(int)g, 256, 0, s>>>(op, faceE, faceN);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_check_field(const double* f, long long n, int* err, cudaStream_t s) {
+  long long g = (n + 255) / 256;
+  if (g > 4096) g = 4096;
+  k_check_field<<<(int)std::max<long long>(g, 1), 256, 0, s>>>(f, n, err);
   return cudaGetLastError();
 }
 

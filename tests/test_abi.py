@@ -59,7 +59,11 @@ def test_create_rejects_bad_sizes(lib, dims):
 @pytest.mark.parametrize("kw,msg", [({"mass": 0.0}, "mass"), ({"mass": float("nan")}, "mass"),
                                     ({"a_v": -1.0}, "a_v"), ({"a_h": -0.5}, "a_h"),
                                     ({"dz": [1.0, 0.0, 1.0]}, "dz[1]"),
-                                    ({"a_h_field": [1.0] * 3 + [float("inf")]}, "a_h_field[3]")])
+                                    ({"a_h_field": [1.0] * 3 + [float("inf")]}, "a_h_field[3]"),
+                                    ({"a_h_field": [1.0, float("nan"), 1.0, 1.0]}, "a_h_field[1]"),
+                                    ({"a_h_field": [1.0, 1.0, -0.1, 1.0]}, "a_h_field[2]"),
+                                    ({"a_h_field": [1.0, 1.0, 1.0, -float("inf")]},
+                                     "a_h_field[3]")])
 def test_create_rejects_bad_coefficients(lib, kw, msg):
     args = dict(a_h=1.0, a_v=10.0, mass=1.0)
     args.update(kw)

@@ -973,3 +973,39 @@ def test_cluster_loop_status_semantics_and_timing():
         s.set_substructuring(1)
         s.set_loop("cluster")
         assert s.loop == "persistent"
+
+
+@pytest.mark.parametrize("bad", [float("nan"), -0.25, float("inf")], ids=["nan", "negative", "inf"])
+@pytest.mark.parametrize("api", ["update_coeffs", "update_solve_host", "update_solve_host_async"])
+def test_rejected_field_leaves_the_context_as_it_was(bad, api):
+    # the field of an update is checked on the device in a staging copy:
+    # a bad value is named by its index, and the context keeps its old
+    # coefficients (a solve gives the same bits as before the attempt)
+    prob, kw, b = case(37, 29, 16, True, True, a_v=1e3, seed=41)
+    with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        bd = torch.from_numpy(b).to(DEV)
+        x1 = torch.zeros_like(bd)
+        i1, h1, _ = s.solve(bd, x1, rtol=1e-10)
+        field = np.array(kw["a_h_field"], dtype=np.float64).ravel().copy() * 2.0
+        where = 517
+        field[where] = bad
+        new = dict(kw, a_h_field=field.reshape(prob.ny, prob.nx))
+        with pytest.raises(mf.PCGError) as e:
+            if api == "update_coeffs":
+                s.update_coeffs(**new)
+            else:
+                xh = np.zeros(prob.n)
+                getattr(s, api)(b, xh, **new)
+        assert e.value.status == mf.PCG_EINVAL
+        assert "a_h_field[%d]" % where in mf.pcg_last_error(s.ctx)
+        s.host_wait()
+        x2 = torch.zeros_like(bd)
+        i2, h2, _ = s.solve(bd, x2, rtol=1e-10)
+        assert i1 == i2 and np.array_equal(h1, h2) and torch.equal(x1, x2)
+        # and a good field after the rejected one is taken
+        field[where] = 1.0
+        s.update_coeffs(**dict(kw, a_h_field=field.reshape(prob.ny, prob.nx)))
+        prob2 = oracle.Problem(prob.nx, prob.ny, prob.nz, ah=field.reshape(prob.ny, prob.nx),
+                               a_v=prob.a_v, mass=prob.mass, h=prob.h)
+        y = s.apply_A(bd).cpu().numpy()
+    assert rel_maxdiff(y, oracle.apply_A(prob2, b)) <= OP_TOL
