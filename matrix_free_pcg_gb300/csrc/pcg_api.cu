@@ -86,15 +86,16 @@ struct pcg_ctx {
   int cl_ctas = 0;                   // CTAs of the cluster loop (0: does not fit)
   unsigned int test_absent = 0;      // test hook: arrivals the persistent barriers miss
   size_t partials_cap = 0;           // doubles in `partials`
-  // CUDA graphs of the row-tiled loop: two instances, launched alternately so
-  // that one can be read back (timing) while the other runs.  They are
-  // captured again whenever config_gen, the batch size or timing changed.
-  BatchGraph graphs[2];
+  // CUDA graphs of the row-tiled loop, one set without and one with timing
+  // events ([timing]); each set has two instances, launched alternately so
+  // that one can be read back (timing) while the other runs.  A set is
+  // captured again when config_gen or the batch size changed since its last
+  // capture, so switching timing on and off costs no capture once both exist.
+  BatchGraph graphs[2][2];
   cudaStream_t cap_stream = nullptr;  // private stream for the captures
   unsigned long long config_gen = 1;  // bumped by every change a graph depends on
-  unsigned long long graph_gen = 0;
-  int graph_batch = 0;
-  bool graph_timing = false;
+  unsigned long long graph_gen[2] = {0, 0};
+  int graph_batch[2] = {0, 0};
   bool graphs_off = false;            // a capture failed: direct launches from then on
   int hist_cap = 0;
   DevState* state = nullptr;
@@ -121,6 +122,12 @@ struct pcg_ctx {
   // written, so the row-tiled start reads no x
   bool x0_zero = false;
   DevState* pinned = nullptr;                           // 3 host slots
+  // flags the set-up kernels write straight into host memory (mapped, page-
+  // locked): [0] the a_h field check, [1] the pivots of the Thomas factors.
+  // A device-to-host copy would queue behind an asynchronous call's copy-out
+  // of x on the same copy engine (1 GB, 5.6 ms); a kernel's store does not.
+  int* hflags = nullptr;
+  int* dflags = nullptr;  // the device's address of hflags
   int grid_m = 1, grid_a = 1;
   long long last_launches = 0;
   // timing
@@ -266,14 +273,16 @@ void free_all(pcg_ctx* ctx) {
     if (b) cudaFree(b);
   if (ctx->state) cudaFree(ctx->state);
   if (ctx->pinned) cudaFreeHost(ctx->pinned);
+  if (ctx->hflags) cudaFreeHost(ctx->hflags);
   for (cudaEvent_t e : ctx->event_pool) cudaEventDestroy(e);
   ctx->event_pool.clear();
-  for (BatchGraph& g : ctx->graphs) {
-    if (g.exec) cudaGraphExecDestroy(g.exec);
-    g.exec = nullptr;
-    for (cudaEvent_t e : g.ev) cudaEventDestroy(e);
-    g.ev.clear();
-  }
+  for (auto& set : ctx->graphs)
+    for (BatchGraph& g : set) {
+      if (g.exec) cudaGraphExecDestroy(g.exec);
+      g.exec = nullptr;
+      for (cudaEvent_t e : g.ev) cudaEventDestroy(e);
+      g.ev.clear();
+    }
   if (ctx->cap_stream) cudaStreamDestroy(ctx->cap_stream);
   ctx->cap_stream = nullptr;
   if (ctx->copy_done) cudaEventDestroy(ctx->copy_done);
@@ -545,20 +554,15 @@ int load_coeffs(pcg_ctx* ctx, const pcg_coeffs* c, bool varying,
     // update, with the GPU idle); only a field that passes replaces the
     // context's, so a rejected one leaves the context as it was.
     const size_t bytes = ctx->op.ncols * sizeof(double);
-    cudaError_t e = cudaMemsetAsync(&ctx->state->field_error, 0, sizeof(int), ctx->stream);
+    volatile int* hf = ctx->hflags;
+    hf[0] = 0;
+    cudaError_t e = cudaMemcpyAsync(ctx->ah_stage, c->a_h_field, bytes, cudaMemcpyHostToDevice,
+                                    ctx->stream);
     if (e == cudaSuccess)
-      e = cudaMemcpyAsync(ctx->ah_stage, c->a_h_field, bytes, cudaMemcpyHostToDevice,
-                          ctx->stream);
-    if (e == cudaSuccess)
-      e = pcg::launch_check_field(ctx->ah_stage, ctx->op.ncols, &ctx->state->field_error,
-                                  ctx->stream);
-    int bad = 0;
-    if (e == cudaSuccess)
-      e = cudaMemcpyAsync(&bad, &ctx->state->field_error, sizeof(int), cudaMemcpyDeviceToHost,
-                          ctx->stream);
+      e = pcg::launch_check_field(ctx->ah_stage, ctx->op.ncols, ctx->dflags, ctx->stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "upload of a_h_field");
-    if (bad) {
+    if (hf[0]) {
       const int st = first_bad_field_value(ctx, c->a_h_field, ctx->op.ncols);
       return st ? st : fail(ctx, PCG_EINVAL, "a_h_field changed while it was read");
     }
@@ -600,10 +604,11 @@ int load_coeffs(pcg_ctx* ctx, const pcg_coeffs* c, bool varying,
       e = meanwhile();
       if (e != cudaSuccess) return cuda_fail(ctx, e, "host-to-device copy");
     }
-    int bad = 0;
-    e = cudaMemcpyAsync(&bad, &ctx->state->setup_error, sizeof(int), cudaMemcpyDeviceToHost,
-                        ctx->stream);
+    volatile int* hf = ctx->hflags;
+    hf[1] = 0;
+    e = pcg::launch_flag_to_host(&ctx->state->setup_error, ctx->dflags + 1, ctx->stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+    const int bad = hf[1];
     if (t0 && t1) {
       float ms = 0.0f;
       if (e == cudaSuccess && cudaEventElapsedTime(&ms, t0, t1) == cudaSuccess) {
@@ -868,22 +873,22 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
   // operands are the context's own buffers).  Sweeps past the last
   // iteration see `done` and return at once, so every batch is a full one.
   bool use_graphs = tiled && !ctx->graphs_off && !persistent;
-  if (use_graphs && (ctx->graph_gen != ctx->config_gen || ctx->graph_batch != batch ||
-                     ctx->graph_timing != ctx->timing)) {
-    for (BatchGraph& g : ctx->graphs) {
-      if (capture_batch(ctx, op, split, grid_pm, batch, ctx->timing, g) != cudaSuccess) {
+  const int tv = ctx->timing ? 1 : 0;
+  BatchGraph* graphs = ctx->graphs[tv];
+  if (use_graphs && (ctx->graph_gen[tv] != ctx->config_gen || ctx->graph_batch[tv] != batch)) {
+    for (BatchGraph* g = graphs; g != graphs + 2; ++g) {
+      if (capture_batch(ctx, op, split, grid_pm, batch, ctx->timing, *g) != cudaSuccess) {
         use_graphs = false;
         ctx->graphs_off = true;  // this driver or device refuses: launch directly from now on
         break;
       }
     }
-    ctx->graph_gen = ctx->config_gen;
-    ctx->graph_batch = batch;
-    ctx->graph_timing = ctx->timing;
+    ctx->graph_gen[tv] = ctx->config_gen;
+    ctx->graph_batch[tv] = batch;
   }
   std::vector<float> tm_m, tm_a;  // graph sweep times in launch order (timing)
   while (use_graphs && enq <= maxit && !stop) {
-    e = cudaGraphLaunch(ctx->graphs[slot].exec, s);
+    e = cudaGraphLaunch(graphs[slot].exec, s);
     ctx->last_launches += (long long)(mgrid ? ctx->mg_launches + 1 : 2) * batch;
     enq += batch;
     if (e == cudaSuccess)
@@ -894,7 +899,7 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
     if (pending >= 0) {
       e = cudaEventSynchronize(ev[pending]);
       if (e != cudaSuccess) return cuda_fail(ctx, e, "solve loop");
-      if (ctx->timing) read_batch_times(ctx->graphs[pending], batch, tm_m, tm_a);
+      if (ctx->timing) read_batch_times(graphs[pending], batch, tm_m, tm_a);
       if (ctx->pinned[pending].done) stop = true;
     }
     pending = slot;
@@ -971,7 +976,7 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
   }
   if (ctx->timing) {
     collect_events(ctx, fin.it, fin.it > 0 ? fin.it - 1 : 0);
-    if (last_graph >= 0) read_batch_times(ctx->graphs[last_graph], batch, tm_m, tm_a);
+    if (last_graph >= 0) read_batch_times(graphs[last_graph], batch, tm_m, tm_a);
     // only the sweeps that did work: the first `it` preconditioner and
     // `it - 1` stencil sweeps in launch order
     const size_t wm = std::min<size_t>(tm_m.size(), fin.it > 0 ? (size_t)fin.it : 0);
@@ -1065,6 +1070,10 @@ int pcg_create(int nx, int ny, int nz, const pcg_coeffs* coeffs, pcg_ctx** out) 
   if (e == cudaSuccess)
     e = cudaHostAlloc(reinterpret_cast<void**>(&ctx->pinned), 3 * sizeof(DevState),
                       cudaHostAllocDefault);
+  if (e == cudaSuccess)
+    e = cudaHostAlloc(reinterpret_cast<void**>(&ctx->hflags), 4 * sizeof(int), cudaHostAllocMapped);
+  if (e == cudaSuccess)
+    e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&ctx->dflags), ctx->hflags, 0);
   if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "workspace allocation"));
   memset(ctx->pinned, 0, 3 * sizeof(DevState));
   op.lev = ctx->lev;

@@ -90,7 +90,6 @@ struct DevState {
   double mg_R;       // multigrid preconditioner: ||r||^2 of the current iteration, from the
                      // fine level's first smoothing sweep, for the stopping test
   int setup_error;   // a non-positive Thomas pivot was met in the setup kernel
-  int field_error;   // a value of an uploaded a_h field is negative, infinite or NaN
   int dev_error;     // a bounded device wait ran out (pcg_status PCG_ETIMEOUT)
   unsigned int bar_count;  // arrivals at the grid barriers of the persistent solve loop
 };
@@ -102,6 +101,9 @@ cudaError_t launch_face_coeffs(const Op& op, double* faceE, double* faceN, cudaS
 // *err = 1 if some f[i], i < n, is negative, infinite or NaN (err untouched
 // otherwise: the caller zeroes it first).
 cudaError_t launch_check_field(const double* f, long long n, int* err, cudaStream_t s);
+// *dst = *src by one thread (dst: mapped host memory, read after the stream
+// synchronises, without a copy engine).
+cudaError_t launch_flag_to_host(const int* src, int* dst, cudaStream_t s);
 // Per-cell diagonal (column-contiguous, and row-tiled when cdiag_t is not
 // NULL), horizontal weights (row-tiled, when cwE_t is not NULL) and Thomas
 // factors (row-tiled) of an a_h field, after the face values.

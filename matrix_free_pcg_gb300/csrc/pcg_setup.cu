@@ -114,6 +114,13 @@ cudaError_t launch_face_coeffs(const Op& op, double* faceE, double* faceN, cudaS
   return cudaGetLastError();
 }
 
+__global__ void k_flag_to_host(const int* src, int* dst) { *dst = *src; }
+
+cudaError_t launch_flag_to_host(const int* src, int* dst, cudaStream_t s) {
+  k_flag_to_host<<<1, 1, 0, s>>>(src, dst);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_check_field(const double* f, long long n, int* err, cudaStream_t s) {
   long long g = (n + 255) / 256;
   if (g > 4096) g = 4096;
