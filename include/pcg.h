@@ -90,11 +90,15 @@ void pcg_destroy(pcg_ctx* ctx);
 /* Replace the coefficients of an existing context without any allocation
  * (same grid).  A context created with a constant a_h cannot switch to a
  * field (PCG_EINVAL); the reverse is allowed.  Enqueued on the context's
- * stream. */
+ * stream: with a constant a_h the call returns without waiting for the
+ * device; with an a_h field it returns after the set-up kernels, whose
+ * checks it reports (PCG_EINVAL for a bad field value, PCG_EBREAKDOWN for a
+ * non-positive Thomas pivot). */
 int pcg_update_coeffs(pcg_ctx* ctx, const pcg_coeffs* coeffs);
 
 /* Use `stream` (a cudaStream_t, or NULL for the legacy default stream) for
- * all later work of this context. */
+ * all later work of this context.  Work already queued on the previous
+ * stream comes first: the new stream waits for it on the device. */
 int pcg_set_stream(pcg_ctx* ctx, void* stream);
 
 /* Layout of the solver's internal vectors (r, z, p, q and a copy of the

@@ -128,6 +128,10 @@ struct pcg_ctx {
   // of x on the same copy engine (1 GB, 5.6 ms); a kernel's store does not.
   int* hflags = nullptr;
   int* dflags = nullptr;  // the device's address of hflags
+  // page-locked copy of the per-level table being uploaded, and the end of
+  // that upload (the next update waits for it before it writes the copy)
+  double* lev_pinned = nullptr;
+  cudaEvent_t lev_done = nullptr;
   int grid_m = 1, grid_a = 1;
   long long last_launches = 0;
   // timing
@@ -274,6 +278,9 @@ void free_all(pcg_ctx* ctx) {
   if (ctx->state) cudaFree(ctx->state);
   if (ctx->pinned) cudaFreeHost(ctx->pinned);
   if (ctx->hflags) cudaFreeHost(ctx->hflags);
+  if (ctx->lev_pinned) cudaFreeHost(ctx->lev_pinned);
+  if (ctx->lev_done) cudaEventDestroy(ctx->lev_done);
+  ctx->lev_done = nullptr;
   for (cudaEvent_t e : ctx->event_pool) cudaEventDestroy(e);
   ctx->event_pool.clear();
   for (auto& set : ctx->graphs)
@@ -579,8 +586,16 @@ int load_coeffs(pcg_ctx* ctx, const pcg_coeffs* c, bool varying,
   ctx->mass_host = c->mass;
   ctx->dz_host.assign((size_t)ctx->op.nz, 1.0);
   if (c->dz) ctx->dz_host.assign(c->dz, c->dz + ctx->op.nz);
-  cudaError_t e = cudaMemcpyAsync(ctx->lev, lev.data(), lev.size() * sizeof(double),
-                                  cudaMemcpyHostToDevice, ctx->stream);
+  // the table goes up from a page-locked copy, so the upload is queued on the
+  // stream without a wait for the host (a pageable source would make the copy
+  // wait for the stream's earlier work first)
+  cudaError_t e = cudaEventSynchronize(ctx->lev_done);  // the previous upload has read the copy
+  if (e == cudaSuccess) {
+    std::memcpy(ctx->lev_pinned, lev.data(), lev.size() * sizeof(double));
+    e = cudaMemcpyAsync(ctx->lev, ctx->lev_pinned, lev.size() * sizeof(double),
+                        cudaMemcpyHostToDevice, ctx->stream);
+  }
+  if (e == cudaSuccess) e = cudaEventRecord(ctx->lev_done, ctx->stream);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "upload of the level table");
   if (ctx->op.varying != (varying ? 1 : 0)) {
     ctx->op.varying = varying ? 1 : 0;
@@ -620,13 +635,10 @@ int load_coeffs(pcg_ctx* ctx, const pcg_coeffs* c, bool varying,
     if (t1) cudaEventDestroy(t1);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "coefficient set-up");
     if (bad) return fail(ctx, PCG_EBREAKDOWN, "a Thomas pivot of some column is not positive");
-  } else {
-    if (meanwhile) {
-      e = meanwhile();
-      if (e != cudaSuccess) return cuda_fail(ctx, e, "host-to-device copy");
-    }
-    e = cudaStreamSynchronize(ctx->stream);
-    if (e != cudaSuccess) return cuda_fail(ctx, e, "coefficient upload");
+  } else if (meanwhile) {
+    // a constant a_h: the level table is all there is, queued on the stream
+    e = meanwhile();
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "host-to-device copy");
   }
   if (ctx->split_p > 1) {
     st = run_split_setup(ctx);
@@ -1074,6 +1086,10 @@ int pcg_create(int nx, int ny, int nz, const pcg_coeffs* coeffs, pcg_ctx** out) 
     e = cudaHostAlloc(reinterpret_cast<void**>(&ctx->hflags), 4 * sizeof(int), cudaHostAllocMapped);
   if (e == cudaSuccess)
     e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&ctx->dflags), ctx->hflags, 0);
+  if (e == cudaSuccess)
+    e = cudaHostAlloc(reinterpret_cast<void**>(&ctx->lev_pinned),
+                      (size_t)pcg::kLevCount * nz * sizeof(double), cudaHostAllocDefault);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->lev_done, cudaEventDisableTiming);
   if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "workspace allocation"));
   memset(ctx->pinned, 0, 3 * sizeof(DevState));
   op.lev = ctx->lev;
@@ -1405,7 +1421,20 @@ int pcg_get_substructuring(const pcg_ctx* ctx, int* nblocks_out) {
 
 int pcg_set_stream(pcg_ctx* ctx, void* stream) {
   if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
-  ctx->stream = static_cast<cudaStream_t>(stream);
+  cudaStream_t next = static_cast<cudaStream_t>(stream);
+  if (next != ctx->stream) {
+    // work queued on the old stream (a coefficient upload, a standalone
+    // operator) comes before the new stream's
+    DeviceGuard g(ctx->device);
+    if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
+    cudaEvent_t ev = nullptr;
+    cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventRecord(ev, ctx->stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(next, ev, 0);
+    if (ev) cudaEventDestroy(ev);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "stream switch");
+  }
+  ctx->stream = next;
   return PCG_OK;
 }
 
