@@ -307,8 +307,6 @@ void free_all(pcg_ctx* ctx) {
   mg_release(ctx);
 }
 
-// Upload coefficients and (for a field) rebuild the per-column and per-cell
-// tables on the device.  Synchronous.
 // Tables of the substructured column solve for the current coefficients.
 // Synchronous.
 int run_split_setup(pcg_ctx* ctx) {
@@ -550,9 +548,12 @@ cudaError_t mg_enqueue(pcg_ctx* ctx, const Op& op0, double* b0, double* out, boo
   return e;
 }
 
-// `meanwhile`, when given, is called once the set-up work is enqueued and
-// before the host waits for it: work it enqueues on another stream runs
-// alongside the set-up.
+// Upload coefficients and (for a field) rebuild the per-column and per-cell
+// tables on the device.  With a field the call waits twice: for the field's
+// check before anything changes, and for the set-up kernels' pivot check;
+// with a constant a_h it only queues the level table.  `meanwhile`, when
+// given, is called once the set-up work is enqueued and before the host
+// waits for it: work it enqueues on another stream runs alongside the set-up.
 int load_coeffs(pcg_ctx* ctx, const pcg_coeffs* c, bool varying,
                 const std::function<cudaError_t()>& meanwhile = {}) {
   if (varying) {
