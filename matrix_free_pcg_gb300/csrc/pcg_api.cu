@@ -307,6 +307,18 @@ void free_all(pcg_ctx* ctx) {
   mg_release(ctx);
 }
 
+// The set-up kernels' pivot flag (DevState::setup_error) on the host, after
+// the stream's work so far: a kernel stores it into mapped host memory
+// (hflags[1]), so the wait involves no copy engine (see pcg_ctx::hflags).
+cudaError_t read_setup_error(pcg_ctx* ctx, int* bad) {
+  volatile int* hf = ctx->hflags;
+  hf[1] = 0;
+  cudaError_t e = pcg::launch_flag_to_host(&ctx->state->setup_error, ctx->dflags + 1, ctx->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+  *bad = hf[1];
+  return e;
+}
+
 // Tables of the substructured column solve for the current coefficients.
 // Synchronous.
 int run_split_setup(pcg_ctx* ctx) {
@@ -320,10 +332,7 @@ int run_split_setup(pcg_ctx* ctx) {
   if (e == cudaSuccess) e = pcg::launch_split_setup(ctx->op, ctx->split_p, ctx->state, ctx->stream);
   if (t1) cudaEventRecord(t1, ctx->stream);
   int bad = 0;
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(&bad, &ctx->state->setup_error, sizeof(int), cudaMemcpyDeviceToHost,
-                        ctx->stream);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+  if (e == cudaSuccess) e = read_setup_error(ctx, &bad);
   if (t0 && t1) {
     float ms = 0.0f;
     if (e == cudaSuccess && cudaEventElapsedTime(&ms, t0, t1) == cudaSuccess) {
@@ -465,10 +474,7 @@ int mg_setup(pcg_ctx* ctx) {
   ctx->mg_grid_first = pcg::grid_mg_first(f, ctx->num_sms);
   ctx->mg_grid_smooth = pcg::grid_mg_smooth(f, ctx->num_sms);
   int bad = 0;
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(&bad, &ctx->state->setup_error, sizeof(int), cudaMemcpyDeviceToHost,
-                        ctx->stream);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+  if (e == cudaSuccess) e = read_setup_error(ctx, &bad);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "multigrid level set-up");
   if (bad) return fail(ctx, PCG_EBREAKDOWN, "a Thomas pivot on a multigrid level is not positive");
   // reduction partials for the finest level's fused sweeps
@@ -620,11 +626,8 @@ int load_coeffs(pcg_ctx* ctx, const pcg_coeffs* c, bool varying,
       e = meanwhile();
       if (e != cudaSuccess) return cuda_fail(ctx, e, "host-to-device copy");
     }
-    volatile int* hf = ctx->hflags;
-    hf[1] = 0;
-    e = pcg::launch_flag_to_host(&ctx->state->setup_error, ctx->dflags + 1, ctx->stream);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
-    const int bad = hf[1];
+    int bad = 0;
+    if (e == cudaSuccess) e = read_setup_error(ctx, &bad);
     if (t0 && t1) {
       float ms = 0.0f;
       if (e == cudaSuccess && cudaEventElapsedTime(&ms, t0, t1) == cudaSuccess) {
