@@ -500,8 +500,8 @@ def run_ours(args, w):
 
     def step():
         solver.update_coeffs(**coeffs)
-        x.zero_()
-        it, _, st = solver.solve(bd, x, rtol=w.rtol, maxit=w.maxit, history=False)
+        # from x0 = 0: the library neither reads x nor needs it filled
+        it, _, st = solver.solve_from_zero(bd, x, rtol=w.rtol, maxit=w.maxit, history=False)
         if st not in (mf.PCG_OK,):
             raise RuntimeError("solve status %d: %s" % (st, mf.pcg_last_error(solver.ctx)))
         return it

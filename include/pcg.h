@@ -320,6 +320,12 @@ int pcg_precond(pcg_ctx* ctx, const double* r_dev, double* z_dev);
 int pcg_solve(pcg_ctx* ctx, const double* b_dev, double* x_dev, double rtol, int maxit,
               int* iters_out, double* res_hist);
 
+/* As pcg_solve from the initial guess x0 = 0: x_dev receives the solution
+ * and is never read, so neither the caller nor the library fills or scans it
+ * first.  Same arguments, stream semantics and errors as pcg_solve. */
+int pcg_solve_from_zero(pcg_ctx* ctx, const double* b_dev, double* x_dev, double rtol,
+                        int maxit, int* iters_out, double* res_hist);
+
 /* As pcg_solve, with b and x in HOST memory: copies b and x in, solves,
  * copies x out (section 6: the host copies the initial solution and the
  * right-hand side in and the solution out).  The device copies of b and x

@@ -37,7 +37,7 @@ EXPORTED = ["pcg_create", "pcg_destroy", "pcg_update_coeffs", "pcg_set_stream", 
             "pcg_get_az_form", "pcg_set_preconditioner", "pcg_set_multigrid",
             "pcg_get_multigrid", "pcg_mg_vcycle", "pcg_update_solve_host",
             "pcg_measure_fp64_rate", "pcg_test_tensor_memory", "pcg_update_solve_host_async",
-            "pcg_host_wait"]
+            "pcg_host_wait", "pcg_solve_from_zero"]
 PCG_LAYOUT_COLUMN, PCG_LAYOUT_TILED = 0, 1
 PCG_FACTORS_STORED, PCG_FACTORS_RECOMPUTE = 0, 1
 PCG_LOOP_AUTO, PCG_LOOP_BATCHED, PCG_LOOP_PERSISTENT, PCG_LOOP_CLUSTER = 0, 1, 2, 3
@@ -69,6 +69,8 @@ def _load(path=LIB_PATH):
         "pcg_precond": (ctypes.c_int, [_vp, _vp, _vp]),
         "pcg_solve": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_double, ctypes.c_int,
                                      ctypes.POINTER(ctypes.c_int), _vp]),
+        "pcg_solve_from_zero": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_double, ctypes.c_int,
+                                               ctypes.POINTER(ctypes.c_int), _vp]),
         "pcg_solve_host": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_double, ctypes.c_int,
                                           ctypes.POINTER(ctypes.c_int), _vp]),
         "pcg_solve_host_x0": (ctypes.c_int, [_vp, _vp, _vp, _vp, ctypes.c_double, ctypes.c_int,
@@ -296,12 +298,14 @@ def pcg_precond(ctx, n, r, z):
     return _check(_lib.pcg_precond(ctx, _dev_ptr(r, n, "r"), _dev_ptr(z, n, "z")), ctx)
 
 
-def pcg_solve(ctx, n, b, x, rtol, maxit, history=True):
-    """Returns (iters, hist or None, status); raises on EINVAL/ENOMEM/ECUDA."""
+def pcg_solve(ctx, n, b, x, rtol, maxit, history=True, from_zero=False):
+    """Returns (iters, hist or None, status); raises on EINVAL/ENOMEM/ECUDA.
+    from_zero: pcg_solve_from_zero (x0 = 0; x is written, never read)."""
     it = ctypes.c_int(-1)
     hist = np.full(int(maxit) + 1, np.nan) if history else None
-    st = _lib.pcg_solve(ctx, _dev_ptr(b, n, "b"), _dev_ptr(x, n, "x"), float(rtol), int(maxit),
-                        ctypes.byref(it), hist.ctypes.data_as(_vp) if history else None)
+    fn = _lib.pcg_solve_from_zero if from_zero else _lib.pcg_solve
+    st = fn(ctx, _dev_ptr(b, n, "b"), _dev_ptr(x, n, "x"), float(rtol), int(maxit),
+            ctypes.byref(it), hist.ctypes.data_as(_vp) if history else None)
     if st not in (PCG_OK, PCG_ENOTCONV, PCG_EBREAKDOWN):
         _check(st, ctx)
     return it.value, (hist[: it.value + 1] if history else None), st
@@ -547,6 +551,11 @@ class Solver:
         """x (device tensor): initial guess in, solution out.
         Returns (iters, residual history, status)."""
         return pcg_solve(self.ctx, self.n, b, x, rtol, maxit, history)
+
+    def solve_from_zero(self, b, x, rtol=1e-10, maxit=500, history=True):
+        """pcg_solve_from_zero: x0 = 0; x (device tensor) receives the
+        solution and is never read."""
+        return pcg_solve(self.ctx, self.n, b, x, rtol, maxit, history, from_zero=True)
 
     def solve_host(self, b, x, rtol=1e-10, maxit=500, history=True, x0="x"):
         """x0="x": x holds the initial guess (pcg_solve_host); None: zero initial

@@ -1488,6 +1488,23 @@ int pcg_solve(pcg_ctx* ctx, const double* b_dev, double* x_dev, double rtol, int
   return solve_device(ctx, b_dev, x_dev, rtol, maxit, iters_out, res_hist);
 }
 
+int pcg_solve_from_zero(pcg_ctx* ctx, const double* b_dev, double* x_dev, double rtol,
+                        int maxit, int* iters_out, double* res_hist) {
+  if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
+  int st = check_solve_args(ctx, b_dev, x_dev, rtol, maxit);
+  if (st) return st;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
+  if (ctx->layout == PCG_LAYOUT_TILED) {
+    ctx->x0_zero = true;  // the row-tiled start is told; x is written, never read
+  } else {
+    const cudaError_t e =
+        cudaMemsetAsync(x_dev, 0, sizeof(double) * (size_t)ctx->op.n, ctx->stream);  // +0.0
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "initial guess");
+  }
+  return solve_device(ctx, b_dev, x_dev, rtol, maxit, iters_out, res_hist);
+}
+
 // Device copies of b and x for the host-buffer entry points (made on first use).
 static cudaError_t host_api_buffers(pcg_ctx* ctx) {
   cudaError_t e = cudaSuccess;

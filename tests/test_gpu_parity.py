@@ -1009,3 +1009,19 @@ def test_rejected_field_leaves_the_context_as_it_was(bad, api):
                                a_v=prob.a_v, mass=prob.mass, h=prob.h)
         y = s.apply_A(bd).cpu().numpy()
     assert rel_maxdiff(y, oracle.apply_A(prob2, b)) <= OP_TOL
+
+
+@pytest.mark.parametrize("mode", ["tiled", "column", "tiled_persistent"])
+def test_solve_from_zero_never_reads_x(mode):
+    # pcg_solve_from_zero: the same bits as pcg_solve from an x filled with
+    # +0.0, whatever x held before (here NaN)
+    prob, kw, b = case(37, 29, 16, True, True, a_v=1e3, seed=43)
+    with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        configure(s, mode)
+        bd = torch.from_numpy(b).to(DEV)
+        x1 = torch.zeros_like(bd)
+        i1, h1, st1 = s.solve(bd, x1, rtol=1e-10)
+        x2 = torch.full_like(bd, float("nan"))
+        i2, h2, st2 = s.solve_from_zero(bd, x2, rtol=1e-10)
+    assert st1 == st2 == mf.PCG_OK and i1 == i2
+    assert np.array_equal(h1, h2) and torch.equal(x1, x2)
