@@ -701,6 +701,10 @@ void collect_events(pcg_ctx* ctx, long long work_m, long long work_a) {
 bool overlap(const double* a, const double* b, long long n) {
   return (a < b + n) && (b < a + n);
 }
+// [a, a+na) and [b, b+nb) share an element
+bool overlap(const double* a, long long na, const double* b, long long nb) {
+  return (a < b + nb) && (b < a + na);
+}
 
 // Grids that the automatic loop choice runs persistent (and the layout the
 // automatic choices assume: row-tiled): fewer than 4 tiles of 32 columns per
@@ -1684,7 +1688,8 @@ int pcg_precond_dot_noalloc(pcg_ctx* ctx, const double* r_dev, double* z_dev, do
   if (!r_dev || !z_dev || !rz_dev)
     return fail(ctx, PCG_EINVAL, "r, z and rz must be non-NULL device pointers");
   if (overlap(r_dev, z_dev, ctx->op.n)) return fail(ctx, PCG_EINVAL, "r and z overlap");
-  if (overlap(rz_dev, r_dev, ctx->op.n) || overlap(rz_dev, z_dev, ctx->op.n))
+  // rz is one value: only an rz inside r or z overlaps them
+  if (overlap(rz_dev, 1, r_dev, ctx->op.n) || overlap(rz_dev, 1, z_dev, ctx->op.n))
     return fail(ctx, PCG_EINVAL, "rz overlaps r or z");
   if (ctx->op.ntiles > pcg::kNoallocMaxTiles)
     return fail(ctx, PCG_EINVAL,

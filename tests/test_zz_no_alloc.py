@@ -120,4 +120,7 @@ def test_noalloc_rejects_overlapping_arguments():
         with pytest.raises(mf.PCGError):
             mf.pcg_precond_dot_noalloc(s.ctx, n, r, buf[1:n + 1], buf[2 * n:])  # r and z overlap
         mf.pcg_precond_dot_noalloc(s.ctx, n, r, z, buf[2 * n:])  # disjoint: accepted
+        # rz just before r, and just before z: one value, not n, so disjoint
+        mf.pcg_precond_dot_noalloc(s.ctx, n, buf[1:n + 1], buf[n + 1:], buf[0:1])
+        mf.pcg_precond_dot_noalloc(s.ctx, n, buf[n + 1:], buf[1:n + 1], buf[0:1])
         torch.cuda.synchronize()
