@@ -427,7 +427,11 @@ typedef enum {
   PCG_K_SETUP = 6,         /* coefficient set-up kernels of pcg_update_coeffs (face values,
                               per-cell diagonal and Thomas factors), timed together */
   PCG_K_LOOP = 7,          /* persistent solve loop: all iterations of both sweeps */
-  PCG_K_COUNT = 8
+  PCG_K_PRECOND_FIRST = 8, /* the first Algorithm 3 sweep of a batched row-tiled solve
+                              (alpha = 0: r* = r, q not read) */
+  PCG_K_SPMV_FIRST = 9,    /* the first Algorithm 2 sweep of a batched row-tiled solve
+                              (alpha = beta = 0: p = z, q = Az, u not updated) */
+  PCG_K_COUNT = 10
 } pcg_kernel_kind;
 
 int pcg_enable_timing(pcg_ctx* ctx, int enable);

@@ -25,7 +25,7 @@ PCG_OK, PCG_EINVAL, PCG_ENOMEM, PCG_ECUDA, PCG_ENOTCONV, PCG_EBREAKDOWN, PCG_ETI
 STATUS_NAMES = {0: "PCG_OK", 1: "PCG_EINVAL", 2: "PCG_ENOMEM", 3: "PCG_ECUDA",
                 4: "PCG_ENOTCONV", 5: "PCG_EBREAKDOWN", 6: "PCG_ETIMEOUT"}
 KERNEL_KINDS = ["precond_fused", "spmv_fused", "residual", "finalize", "apply_A", "precond",
-                "setup", "loop"]
+                "setup", "loop", "precond_first", "spmv_first"]
 PCG_K_COUNT = len(KERNEL_KINDS)
 
 EXPORTED = ["pcg_create", "pcg_destroy", "pcg_update_coeffs", "pcg_set_stream", "pcg_apply_A",

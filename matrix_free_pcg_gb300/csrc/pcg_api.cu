@@ -686,8 +686,12 @@ cudaError_t timed(pcg_ctx* ctx, int kind, F&& launch) {
 void collect_events(pcg_ctx* ctx, long long work_m, long long work_a) {
   long long seen_m = 0, seen_a = 0;
   for (const KernelEvent& ke : ctx->events) {
-    if (ke.kind == PCG_K_PRECOND_FUSED && seen_m++ >= work_m) continue;
-    if (ke.kind == PCG_K_SPMV_FUSED && seen_a++ >= work_a) continue;
+    // the first-iteration sweeps come first in launch order, counted with
+    // the rest of their kind's work
+    const bool sweep_m = ke.kind == PCG_K_PRECOND_FUSED || ke.kind == PCG_K_PRECOND_FIRST;
+    const bool sweep_a = ke.kind == PCG_K_SPMV_FUSED || ke.kind == PCG_K_SPMV_FIRST;
+    if (sweep_m && seen_m++ >= work_m) continue;
+    if (sweep_a && seen_a++ >= work_a) continue;
     float ms = 0.0f;
     if (cudaEventElapsedTime(&ms, ke.start, ke.stop) == cudaSuccess) {
       ctx->ms[ke.kind] += ms;
@@ -855,18 +859,22 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
               [&] { return pcg::launch_x0_nonzero(x, op.n, ctx->state, ctx->num_sms, s); });
     if (e != cudaSuccess) return cuda_fail(ctx, e, "initial guess check launch");
   }
+  // Persistent loop: every iteration in one cooperative kernel; cluster loop:
+  // every iteration in one cluster, the vectors in its shared memory.
+  const int loop = resolved_loop(ctx);
+  const bool persistent = loop == PCG_LOOP_PERSISTENT || loop == PCG_LOOP_CLUSTER;
+  // The batched row-tiled loop with stored factors and Thomas column solves
+  // runs its first iteration with the first-iteration sweeps (alpha = beta =
+  // 0, p = q = 0 never read), so the start writes neither p nor q.
+  const bool first_direct = tiled && !persistent && !mgrid && !split && !op.recompute;
   e = timed(ctx, PCG_K_RESIDUAL, [&] {
     return tiled ? pcg::launch_residual_tiled(op, ctx->state, b, x, ctx->r, ctx->u_t, ctx->p,
-                                              ctx->q, rtol, maxit, x0_check, s)
+                                              ctx->q, rtol, maxit, x0_check, s, !first_direct)
                  : pcg::launch_residual(op, ctx->state, b, x, ctx->r, ctx->p, ctx->q, rtol,
                                         maxit, ctx->grid_a, s);
   });
   if (e != cudaSuccess) return cuda_fail(ctx, e, "residual kernel launch");
 
-  // Persistent loop: every iteration in one cooperative kernel; cluster loop:
-  // every iteration in one cluster, the vectors in its shared memory.
-  const int loop = resolved_loop(ctx);
-  const bool persistent = loop == PCG_LOOP_PERSISTENT || loop == PCG_LOOP_CLUSTER;
   if (loop == PCG_LOOP_CLUSTER) {
     e = timed(ctx, PCG_K_LOOP, [&] {
       return pcg::launch_cluster_loop(op, ctx->state, ctx->r, ctx->u_t, ctx->p, ctx->hist,
@@ -888,6 +896,19 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
   int enq = 0, slot = 0, pending = -1;
   cudaEvent_t ev[2] = {pool_event(ctx), pool_event(ctx)};
   if (!ev[0] || !ev[1]) return fail(ctx, PCG_ECUDA, "event creation failed");
+  if (first_direct) {  // iteration 0, outside the graphs
+    e = timed(ctx, PCG_K_PRECOND_FIRST, [&] {
+      return pcg::launch_precond_tiled(op, ctx->state, ctx->r, ctx->q, ctx->z, ctx->partials,
+                                       ctx->hist, grid_pm, s, true);
+    });
+    if (e == cudaSuccess && maxit > 0)
+      e = timed(ctx, PCG_K_SPMV_FIRST, [&] {
+        return pcg::launch_spmv_tiled(op, ctx->state, ctx->z, ctx->r, ctx->u_t, ctx->p, ctx->q,
+                                      ctx->partials + 2 * grid_pm, ctx->grid_ta, s, true);
+      });
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "first iteration launch");
+    enq = 1;
+  }
   bool stop = false;
   // Row-tiled layout: every batch is one launch of a CUDA graph (all its
   // operands are the context's own buffers).  Sweeps past the last
@@ -998,9 +1019,12 @@ int solve_device(pcg_ctx* ctx, const double* b, double* x, double rtol, int maxi
     collect_events(ctx, fin.it, fin.it > 0 ? fin.it - 1 : 0);
     if (last_graph >= 0) read_batch_times(graphs[last_graph], batch, tm_m, tm_a);
     // only the sweeps that did work: the first `it` preconditioner and
-    // `it - 1` stencil sweeps in launch order
-    const size_t wm = std::min<size_t>(tm_m.size(), fin.it > 0 ? (size_t)fin.it : 0);
-    const size_t wa = std::min<size_t>(tm_a.size(), fin.it > 1 ? (size_t)fin.it - 1 : 0);
+    // `it - 1` stencil sweeps in launch order (the graphs' after the directly
+    // launched first iteration, which collect_events counted)
+    const long long f = (first_direct && last_graph >= 0) ? 1 : 0;
+    const size_t wm = std::min<size_t>(tm_m.size(), fin.it > f ? (size_t)(fin.it - f) : 0);
+    const size_t wa =
+        std::min<size_t>(tm_a.size(), fin.it > 1 + f ? (size_t)(fin.it - 1 - f) : 0);
     for (size_t i = 0; i < wm; ++i) ctx->ms[PCG_K_PRECOND_FUSED] += tm_m[i];
     for (size_t i = 0; i < wa; ++i) ctx->ms[PCG_K_SPMV_FUSED] += tm_a[i];
     ctx->launches[PCG_K_PRECOND_FUSED] += (long long)wm;

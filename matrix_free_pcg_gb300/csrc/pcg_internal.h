@@ -119,9 +119,12 @@ cudaError_t launch_residual(const Op& op, DevState* st, const double* b, const d
 // u_t = x0 and p_t = q_t = 0 at the row-tiled positions (b and x0 in the
 // caller's column-contiguous layout).  With x0_checked, st->x0_nonzero (from
 // launch_x0_nonzero) tells whether x0 may be skipped entirely.
+// zero_pq: also write p = q = 0 (not needed when the first sweeps of the
+// solve are the first-iteration variants, which read neither)
 cudaError_t launch_residual_tiled(const Op& op, DevState* st, const double* b, const double* x,
                                   double* r_t, double* u_t, double* p_t, double* q_t, double rtol,
-                                  int maxit, bool x0_checked, cudaStream_t s);
+                                  int maxit, bool x0_checked, cudaStream_t s,
+                                  bool zero_pq = true);
 // st->x0_nonzero = whether any of the n values of x has a bit set (all +0.0:
 // the zero initial guess).  Clears the flag first.
 cudaError_t launch_x0_nonzero(const double* x, long long n, DevState* st, int num_sms,
@@ -163,14 +166,18 @@ cudaError_t launch_from_tiled(const Op& op, const DevState* st, const double* sr
 // Algorithm 3 / Algorithm 2 sweeps on row-tiled vectors; with op.recompute the
 // per-cell diagonal and Thomas factors are rebuilt on the fly (op.nscratch must
 // then hold kTmWarpsPerBlock*32*nz doubles per block of grid_tiled_precond).
+// first: the first sweep of a solve (alpha = 0, q never written; stored
+// factors only)
 cudaError_t launch_precond_tiled(const Op& op, DevState* st, double* r, const double* q,
                                  double* z, double* partials, double* hist, int grid,
-                                 cudaStream_t s);
+                                 cudaStream_t s, bool first = false);
 // With op.az_resid the stencil sweep reads r (the residual that the
 // preconditioner sweep's z solves M z = r for) instead of the diagonal.
+// first: the first sweep of a solve (alpha = beta = 0, p and q never written,
+// u holding x0; stored factors only)
 cudaError_t launch_spmv_tiled(const Op& op, DevState* st, const double* z, const double* r,
                               double* u, double* p, double* q, double* partials, int grid,
-                              cudaStream_t s);
+                              cudaStream_t s, bool first = false);
 // Warps per block of the row-tiled preconditioner sweep, and its resident
 // warps per SM (each warp keeps the w of its tile and the factors the
 // backward pass reads again live in L2; 12 per SM keep this within L2 at

@@ -973,7 +973,7 @@ __global__ void __launch_bounds__(256) k_residual_tiled(Op op, DevState* st,
                                                         double* __restrict__ u_t,
                                                         double* __restrict__ p_t,
                                                         double* __restrict__ q_t, double rtol,
-                                                        int maxit) {
+                                                        int maxit, bool zero_pq) {
   const bool x_zero = CHECKED && st->x0_nonzero == 0;  // (the reset below leaves the flag)
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
     st->alpha = 0.0;
@@ -1026,8 +1026,10 @@ __global__ void __launch_bounds__(256) k_residual_tiled(Op op, DevState* st,
       const long long o = (t * nz + k) * kTile + lane;
       r_t[o] = sr[kk][lane];
       u_t[o] = sx[kk][lane];
-      p_t[o] = 0.0;
-      q_t[o] = 0.0;
+      if (zero_pq) {
+        p_t[o] = 0.0;
+        q_t[o] = 0.0;
+      }
     }
   }
 }
@@ -1256,10 +1258,11 @@ cudaError_t launch_residual(const Op& op, DevState* st, const double* b, const d
 
 cudaError_t launch_residual_tiled(const Op& op, DevState* st, const double* b, const double* x,
                                   double* r_t, double* u_t, double* p_t, double* q_t, double rtol,
-                                  int maxit, bool x0_checked, cudaStream_t s) {
+                                  int maxit, bool x0_checked, cudaStream_t s, bool zero_pq) {
   const dim3 g((unsigned)op.ntiles, (unsigned)((op.nz + kTile - 1) / kTile));
 #define PCG_RES(VY, CK) \
-  k_residual_tiled<VY, CK><<<g, 256, 0, s>>>(op, st, x, b, r_t, u_t, p_t, q_t, rtol, maxit)
+  k_residual_tiled<VY, CK><<<g, 256, 0, s>>>(op, st, x, b, r_t, u_t, p_t, q_t, rtol, maxit, \
+                                             zero_pq)
   if (op.varying) {
     if (x0_checked) PCG_RES(true, true); else PCG_RES(true, false);
   } else {

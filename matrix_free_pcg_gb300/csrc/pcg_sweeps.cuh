@@ -40,7 +40,10 @@ __device__ __forceinline__ long long tiled_base(long long col, int nz) {
 // it is read from L2, past the SM's non-coherent L1.  SCALE: z is stored as
 // zscale * M^{-1} r (the damped line relaxation of the multigrid smoother),
 // and <r*, z> is not accumulated (the smoother's caller reduces its own).
-template <bool VARY, bool FUSED, bool COHERENT = false, bool SCALE = false>
+// FIRST (FUSED): the first sweep of a solve, where alpha = 0 and q was never
+// written: r* = r, so q is not read and r not written back (fma(-0, q, r)
+// with q = 0 is r, bit for bit).
+template <bool VARY, bool FUSED, bool COHERENT = false, bool SCALE = false, bool FIRST = false>
 __device__ __forceinline__ void precond_tile(const Op& op, long long t, int lane,
                                              double* __restrict__ r, const double* __restrict__ q,
                                              double* __restrict__ z, double nalpha, uint64_t keep,
@@ -67,8 +70,9 @@ __device__ __forceinline__ void precond_tile(const Op& op, long long t, int lane
   for (int j = 0; j < CF; ++j) {
     const bool in = j < nz;
     cr[j] = in ? ld_hint(rt + j * kTile, stream) : 0.0;
-    cq[j] = (FUSED && in) ? (COHERENT ? __ldcg(qt + j * kTile) : ld_hint(qt + j * kTile, stream))
-                          : 0.0;
+    cq[j] = (FUSED && !FIRST && in)
+                ? (COHERENT ? __ldcg(qt + j * kTile) : ld_hint(qt + j * kTile, stream))
+                : 0.0;
     ci[j] = in ? (VARY ? ld_hint(fi + j * fs, stream) : __ldg(fi + j)) : 0.0;
     cn[j] = in ? (VARY ? ld_hint(fn + j * fs, stream) : __ldg(fn + j)) : 0.0;
   }
@@ -81,8 +85,9 @@ __device__ __forceinline__ void precond_tile(const Op& op, long long t, int lane
       const int k = k0 + CF + j;
       const bool in = k < nz;
       nr[j] = in ? ld_hint(rt + k * kTile, stream) : 0.0;
-      nq[j] = (FUSED && in) ? (COHERENT ? __ldcg(qt + k * kTile) : ld_hint(qt + k * kTile, stream))
-                            : 0.0;
+      nq[j] = (FUSED && !FIRST && in)
+                  ? (COHERENT ? __ldcg(qt + k * kTile) : ld_hint(qt + k * kTile, stream))
+                  : 0.0;
       ni[j] = in ? (VARY ? ld_hint(fi + k * fs, stream) : __ldg(fi + k)) : 0.0;
       nn[j] = in ? (VARY ? ld_hint(fn + k * fs, stream) : __ldg(fn + k)) : 0.0;
     }
@@ -92,9 +97,9 @@ __device__ __forceinline__ void precond_tile(const Op& op, long long t, int lane
       if (k < nz) {
         double rk = cr[j];
         if (FUSED) {
-          rk = fma(nalpha, cq[j], rk);
+          if (!FIRST) rk = fma(nalpha, cq[j], rk);
           accR = fma(rk, rk, accR);
-          st_hint(rt + k * kTile, rk, stream);
+          if (!FIRST) st_hint(rt + k * kTile, rk, stream);
         }
         y = fma(nprev, y, rk);
         w = y * ci[j];
@@ -163,7 +168,14 @@ __device__ __forceinline__ void precond_tile(const Op& op, long long t, int lane
 //
 // COHERENT: z and r were written by other blocks of the same launch (the
 // persistent loop), so they are read from L2, past the SM's non-coherent L1.
-template <bool VARY, bool RECOMP, bool RESID, bool COHERENT = false>
+//
+// FIRST: the first sweep of a solve, where alpha = beta = 0 and p = q = 0 were
+// never written: u keeps x0 (not read, not written), p = z and q = A z
+// start from r (RESID) or the diagonal term alone, so neither u, p nor q is
+// read -- 3 fp64 operations and 32 bytes per cell fewer.  The values are
+// those of the general sweep with those zeros (fma(0, 0, v) = v), up to the
+// sign of an exact zero.
+template <bool VARY, bool RECOMP, bool RESID, bool COHERENT = false, bool FIRST = false>
 __device__ __forceinline__ void spmv_unit(const Op& op, long long unit, int lane,
                                           const double* __restrict__ z,
                                           const double* __restrict__ r, double* __restrict__ u,
@@ -200,11 +212,11 @@ __device__ __forceinline__ void spmv_unit(const Op& op, long long unit, int lane
     const double zu = (!RESID && k + 1 < nz) ? ldz(o + kTile) : 0.0;
     if (RESID) zc = ldz(o);
     const double zE = ldz(bE + ko), zW = ldz(bW + ko), zN = ldz(bN + ko), zS = ldz(bS + ko);
-    double uc = __ldcs(u + o);
-    double pc = __ldcs(p + o);
-    const double qc = __ldcs(q + o);
-    uc = fma(alpha, pc, uc);
-    pc = fma(beta, pc, zc);
+    double uc = FIRST ? 0.0 : __ldcs(u + o);
+    double pc = FIRST ? 0.0 : __ldcs(p + o);
+    const double qc = FIRST ? 0.0 : __ldcs(q + o);
+    if (!FIRST) uc = fma(alpha, pc, uc);
+    pc = FIRST ? zc : fma(beta, pc, zc);
     double a;
     if (VARY) {
       // per-cell horizontal weights -h_k a_f (west and south: the
@@ -227,9 +239,10 @@ __device__ __forceinline__ void spmv_unit(const Op& op, long long unit, int lane
         cS = __ldg(op.cwN_t + bS + ko);
       }
       if (RESID) {
-        a = fma(beta, qc, COHERENT ? __ldcg(r + o) : __ldcs(r + o));
+        const double rc = COHERENT ? __ldcg(r + o) : __ldcs(r + o);
+        a = FIRST ? rc : fma(beta, qc, rc);
       } else {
-        a = fma(d, zc, beta * qc);
+        a = FIRST ? d * zc : fma(d, zc, beta * qc);
         a = fma(__ldg(lev + LV_UP * nz + k), zu, a);
         a = fma(__ldg(lev + LV_DN * nz + k), zd, a);
       }
@@ -240,16 +253,18 @@ __device__ __forceinline__ void spmv_unit(const Op& op, long long unit, int lane
     } else {
       const double hs = (zE + zW) + (zN + zS);
       if (RESID) {
-        a = fma(beta, qc, COHERENT ? __ldcg(r + o) : __ldcs(r + o));
+        const double rc = COHERENT ? __ldcg(r + o) : __ldcs(r + o);
+        a = FIRST ? rc : fma(beta, qc, rc);
       } else {
-        a = fma(__ldg(lev + LV_DIAG * nz + k), zc, beta * qc);
+        a = FIRST ? __ldg(lev + LV_DIAG * nz + k) * zc
+                  : fma(__ldg(lev + LV_DIAG * nz + k), zc, beta * qc);
         a = fma(__ldg(lev + LV_UP * nz + k), zu, a);
         a = fma(__ldg(lev + LV_DN * nz + k), zd, a);
       }
       a = fma(__ldg(lev + LV_HW * nz + k), hs, a);
     }
     sig = fma(pc, a, sig);
-    __stcs(u + o, uc);
+    if (!FIRST) __stcs(u + o, uc);
     __stcs(p + o, pc);
     __stcs(q + o, a);
     if (!RESID) {

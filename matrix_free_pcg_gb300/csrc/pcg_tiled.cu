@@ -74,8 +74,8 @@ __global__ void __launch_bounds__(256) k_retile(Op op, const DevState* st,
 // nphi backward) one chunk ahead into registers: the loads of chunk c+1 are
 // in flight while chunk c computes.  w is written into z on the way up with
 // the L2 evict-last hint and replaced by z on the way down; streamed data
-// carries evict-first.
-template <bool VARY, bool FUSED>
+// carries evict-first.  FIRST: the first sweep of a solve (see precond_tile).
+template <bool VARY, bool FUSED, bool FIRST = false>
 __global__ void __launch_bounds__(kTmThreads) k_precond_tiled(Op op, DevState* st,
                                                               double* __restrict__ r,
                                                               const double* __restrict__ q,
@@ -90,7 +90,8 @@ __global__ void __launch_bounds__(kTmThreads) k_precond_tiled(Op op, DevState* s
   const uint64_t keep = l2_keep(), stream = l2_stream();
   double accR = 0.0, accK = 0.0;
   for (long long t = warp0; t < op.ntiles; t += nwarps)
-    precond_tile<VARY, FUSED>(op, t, lane, r, q, z, nalpha, keep, stream, accR, accK);
+    precond_tile<VARY, FUSED, false, false, FIRST>(op, t, lane, r, q, z, nalpha, keep, stream,
+                                                   accR, accK);
   if (FUSED) {
     double R, K;
     if (grid_sum2<kTmThreads>(accR, accK, partials, &st->ticket_m, R, K))
@@ -230,8 +231,8 @@ __global__ void __launch_bounds__(kTmThreads) k_precond_tiled_rc(Op op, DevState
 // seglen levels of one tile (the stencil has no recurrence along k), so that
 // grids with few tiles still give every warp several units; units are
 // assigned statically (segment-major), which keeps the sum bitwise
-// repeatable.
-template <bool VARY, bool RECOMP, bool RESID>
+// repeatable.  FIRST: the first sweep of a solve (see spmv_unit).
+template <bool VARY, bool RECOMP, bool RESID, bool FIRST = false>
 __global__ void __launch_bounds__(256) k_spmv_tiled(Op op, DevState* st,
                                                     const double* __restrict__ z,
                                                     const double* __restrict__ r,
@@ -248,7 +249,8 @@ __global__ void __launch_bounds__(256) k_spmv_tiled(Op op, DevState* st,
   double sig = 0.0;
   const long long nunits = op.ntiles * ((op.nz + seglen - 1) / seglen);
   for (long long unit = warp0; unit < nunits; unit += nwarps)
-    spmv_unit<VARY, RECOMP, RESID>(op, unit, lane, z, r, u, p, q, alpha, beta, seglen, sig);
+    spmv_unit<VARY, RECOMP, RESID, false, FIRST>(op, unit, lane, z, r, u, p, q, alpha, beta,
+                                                 seglen, sig);
   double S, unused;
   if (grid_sum2<256>(sig, 0.0, partials, &st->ticket_a, S, unused)) {
     st->last_sigma = S;
@@ -284,7 +286,15 @@ cudaError_t launch_from_tiled(const Op& op, const DevState* st, const double* sr
 
 cudaError_t launch_precond_tiled(const Op& op, DevState* st, double* r, const double* q,
                                  double* z, double* partials, double* hist, int grid,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, bool first) {
+  if (first && !op.recompute) {
+    if (op.varying)
+      k_precond_tiled<true, true, true><<<grid, kTmThreads, 0, s>>>(op, st, r, q, z, partials, hist);
+    else
+      k_precond_tiled<false, true, true><<<grid, kTmThreads, 0, s>>>(op, st, r, q, z, partials,
+                                                                      hist);
+    return cudaGetLastError();
+  }
   if (op.varying && op.recompute)
     k_precond_tiled_rc<true><<<grid, kTmThreads, 0, s>>>(op, st, r, q, z, partials, hist);
   else if (op.varying)
@@ -296,9 +306,27 @@ cudaError_t launch_precond_tiled(const Op& op, DevState* st, double* r, const do
 
 cudaError_t launch_spmv_tiled(const Op& op, DevState* st, const double* z, const double* r,
                               double* u, double* p, double* q, double* partials, int grid,
-                              cudaStream_t s) {
+                              cudaStream_t s, bool first) {
   const int seglen = tiled_spmv_seglen(op, grid);
   const bool rs = op.az_resid != 0;
+  if (first && !op.recompute) {
+    if (op.varying) {
+      if (rs)
+        k_spmv_tiled<true, false, true, true><<<grid, 256, 0, s>>>(op, st, z, r, u, p, q, partials,
+                                                                   seglen);
+      else
+        k_spmv_tiled<true, false, false, true><<<grid, 256, 0, s>>>(op, st, z, r, u, p, q, partials,
+                                                                    seglen);
+    } else {
+      if (rs)
+        k_spmv_tiled<false, false, true, true><<<grid, 256, 0, s>>>(op, st, z, r, u, p, q, partials,
+                                                                    seglen);
+      else
+        k_spmv_tiled<false, false, false, true><<<grid, 256, 0, s>>>(op, st, z, r, u, p, q,
+                                                                     partials, seglen);
+    }
+    return cudaGetLastError();
+  }
   if (op.varying && op.recompute) {
     if (rs)
       k_spmv_tiled<true, true, true><<<grid, 256, 0, s>>>(op, st, z, r, u, p, q, partials, seglen);

@@ -134,7 +134,8 @@ def test_binding_constants_match_the_header(lib):
     expect = {"PCG_K_PRECOND_FUSED": "precond_fused", "PCG_K_SPMV_FUSED": "spmv_fused",
               "PCG_K_RESIDUAL": "residual", "PCG_K_FINALIZE": "finalize",
               "PCG_K_APPLY_A": "apply_A", "PCG_K_PRECOND": "precond", "PCG_K_SETUP": "setup",
-              "PCG_K_LOOP": "loop"}
+              "PCG_K_LOOP": "loop", "PCG_K_PRECOND_FIRST": "precond_first",
+              "PCG_K_SPMV_FIRST": "spmv_first"}
     for v, k in kinds:
         assert lib.KERNEL_KINDS[v] == expect[k], (k, v)
 
