@@ -279,6 +279,14 @@ int pcg_mg_vcycle(pcg_ctx* ctx, const double* r_dev, double* z_dev);
  * Errors: PCG_EINVAL (NULL, absent < 0). */
 int pcg_test_barrier_absent(pcg_ctx* ctx, int absent);
 
+/* Test hook: fills the solver's own work vectors (r, z, p, q and the row-tiled
+ * iterate, padding included) with NaN, as memory that an earlier user left
+ * behind may hold.  A solve writes each of them before it reads it, so its
+ * results do not depend on what they held.  Asynchronous, on the context's
+ * stream; the caller's vectors are not touched.
+ * Errors: PCG_EINVAL (NULL), PCG_ECUDA. */
+int pcg_test_poison_work(pcg_ctx* ctx);
+
 /* Test hook for the column solves on column-contiguous vectors (pcg_precond
  * and the column layout's preconditioner sweep): enable = 0 makes them take
  * the kernels that keep the forward pass's w in global memory instead of in

@@ -37,7 +37,7 @@ EXPORTED = ["pcg_create", "pcg_destroy", "pcg_update_coeffs", "pcg_set_stream", 
             "pcg_get_az_form", "pcg_set_preconditioner", "pcg_set_multigrid",
             "pcg_get_multigrid", "pcg_mg_vcycle", "pcg_update_solve_host",
             "pcg_measure_fp64_rate", "pcg_test_tensor_memory", "pcg_update_solve_host_async",
-            "pcg_host_wait", "pcg_solve_from_zero"]
+            "pcg_host_wait", "pcg_solve_from_zero", "pcg_test_poison_work"]
 PCG_LAYOUT_COLUMN, PCG_LAYOUT_TILED = 0, 1
 PCG_FACTORS_STORED, PCG_FACTORS_RECOMPUTE = 0, 1
 PCG_LOOP_AUTO, PCG_LOOP_BATCHED, PCG_LOOP_PERSISTENT, PCG_LOOP_CLUSTER = 0, 1, 2, 3
@@ -103,6 +103,7 @@ def _load(path=LIB_PATH):
         "pcg_get_az_form": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int)]),
         "pcg_test_barrier_absent": (ctypes.c_int, [_vp, ctypes.c_int]),
         "pcg_test_tensor_memory": (ctypes.c_int, [_vp, ctypes.c_int]),
+        "pcg_test_poison_work": (ctypes.c_int, [_vp]),
         "pcg_measure_fp64_rate": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _dp, _dp, _dp]),
     }
     for name, (res, args) in sig.items():
@@ -282,6 +283,12 @@ def pcg_test_barrier_absent(ctx, absent):
     """Test hook: the persistent loop's barriers miss `absent` arrivals, so the
     next persistent solve's first barrier wait runs out (PCG_ETIMEOUT)."""
     return _check(_lib.pcg_test_barrier_absent(ctx, int(absent)), ctx)
+
+
+def pcg_test_poison_work(ctx):
+    """Test hook: fills the context's work vectors with NaN (as memory left by
+    an earlier user may hold); a solve must not depend on what they held."""
+    return _check(_lib.pcg_test_poison_work(ctx), ctx)
 
 
 def pcg_test_tensor_memory(ctx, enable):

@@ -1432,6 +1432,19 @@ int pcg_test_tensor_memory(pcg_ctx* ctx, int enable) {
   return PCG_OK;
 }
 
+int pcg_test_poison_work(pcg_ctx* ctx) {
+  if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return fail(ctx, PCG_ECUDA, "cannot make device %d current", ctx->device);
+  // every byte 0xFF: each double is a NaN, padding included
+  const size_t bytes = sizeof(double) * (size_t)(ctx->op.ntiles * pcg::kTile * ctx->op.nz);
+  cudaError_t e = cudaSuccess;
+  for (double* v : {ctx->r, ctx->z, ctx->p, ctx->q, ctx->u_t})
+    if (v && e == cudaSuccess) e = cudaMemsetAsync(v, 0xFF, bytes, ctx->stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "work vector fill");
+  return PCG_OK;
+}
+
 int pcg_test_barrier_absent(pcg_ctx* ctx, int absent) {
   if (!ctx) return fail(nullptr, PCG_EINVAL, "ctx is NULL");
   if (absent < 0) return fail(ctx, PCG_EINVAL, "absent must be >= 0");

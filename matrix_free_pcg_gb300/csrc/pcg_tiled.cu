@@ -30,7 +30,10 @@ namespace {
 // block through a padded shared tile (coalesced on both sides).
 // TO_TILED: dst_t = src_k.  Otherwise dst_k = src_t + alpha * p_t (AXPY,
 // alpha from the device state: the deferred x += alpha p of Algorithm 1), or
-// a plain copy.
+// a plain copy.  With alpha = 0 -- a solve that stopped before its first
+// direction, or a breakdown that keeps the iterate before the current one --
+// dst_k = src_t and p_t is not read: the batched row-tiled start leaves p
+// unwritten, so it may hold anything (a NaN would survive 0 * p).
 template <bool TO_TILED, bool AXPY>
 __global__ void __launch_bounds__(256) k_retile(Op op, const DevState* st,
                                                 const double* __restrict__ src,
@@ -45,6 +48,7 @@ __global__ void __launch_bounds__(256) k_retile(Op op, const DevState* st,
   const int nc = (int)min((long long)kTile, op.ncols - col0);
   const int nk = min(kTile, nz - k0);
   const double alpha = AXPY ? st->alpha : 0.0;
+  const bool axpy = AXPY && alpha != 0.0;
   if (TO_TILED) {
     for (int c = ty; c < nc; c += 8)
       if (tx < nk) tile[c][tx] = src[(col0 + c) * nz + k0 + tx];
@@ -57,7 +61,7 @@ __global__ void __launch_bounds__(256) k_retile(Op op, const DevState* st,
     for (int k = ty; k < nk; k += 8)
       if (tx < nc) {
         const long long o = (t * nz + k0 + k) * kTile + tx;
-        tile[tx][k] = AXPY ? fma(alpha, pt[o], src[o]) : src[o];
+        tile[tx][k] = axpy ? fma(alpha, pt[o], src[o]) : src[o];
       }
     __syncthreads();
     for (int c = ty; c < nc; c += 8)

@@ -91,6 +91,7 @@ def test_null_context_calls_fail_cleanly(lib):
     assert lib._lib.pcg_get_substructuring(None, None) == lib.PCG_EINVAL
     assert lib._lib.pcg_get_loop(None, None) == lib.PCG_EINVAL
     assert lib._lib.pcg_test_barrier_absent(None, 0) == lib.PCG_EINVAL
+    assert lib._lib.pcg_test_poison_work(None) == lib.PCG_EINVAL
     assert lib._lib.pcg_set_az_form(None, lib.PCG_AZ_AUTO) == lib.PCG_EINVAL
     assert lib._lib.pcg_get_az_form(None, None) == lib.PCG_EINVAL
     assert lib._lib.pcg_set_preconditioner(None, lib.PCG_PREC_LINE) == lib.PCG_EINVAL

@@ -1029,3 +1029,44 @@ def test_solve_from_zero_never_reads_x(mode):
         i2, h2, st2 = s.solve_from_zero(bd, x2, rtol=1e-10)
     assert st1 == st2 == mf.PCG_OK and i1 == i2
     assert np.array_equal(h1, h2) and torch.equal(x1, x2)
+
+
+@pytest.mark.parametrize("mode", MODES + ["tiled_cluster", "tiled_multigrid"])
+def test_solves_write_work_vectors_before_reading_them(mode):
+    # The context's work vectors filled with NaN, as memory that an earlier
+    # user left behind may hold: a solve from x0 = 0 with b = 0, a solve
+    # allowed no iteration (x = x0) and a full solve give the same bits as
+    # without the fill.  The batched row-tiled start leaves p unwritten, so a
+    # solve that stops before its first direction must not read it.
+    prob, kw, b = case(20, 18, 16, True, True, a_v=1e3, seed=53)
+    x0 = np.random.default_rng(54).standard_normal(prob.n)
+    with mf.Solver(prob.nx, prob.ny, prob.nz, **kw) as s:
+        if mode == "tiled_cluster":
+            configure(s, "tiled")
+            s.set_loop("cluster")
+            assert s.loop == "cluster"
+        elif mode == "tiled_multigrid":
+            configure(s, "tiled")
+            s.set_preconditioner("multigrid")
+        else:
+            configure(s, mode)
+        bd = torch.from_numpy(b).to(DEV)
+        x0d = torch.from_numpy(x0).to(DEV)
+        runs = []
+        for poison in (False, True):
+            out = []
+            for rhs, guess, maxit in ((torch.zeros_like(bd), None, 500), (bd, x0d, 0),
+                                      (bd, None, 500)):
+                if poison:
+                    mf.pcg_test_poison_work(s.ctx)
+                x = torch.zeros_like(bd) if guess is None else guess.clone()
+                it, hist, st = s.solve(rhs, x, rtol=1e-10, maxit=maxit)
+                out.append((it, st, hist, x.cpu().numpy()))
+            runs.append(out)
+    (z_it, z_st, _, z_x), (m_it, m_st, _, m_x), (f_it, f_st, _, _) = runs[1]
+    assert (z_it, z_st) == (0, mf.PCG_OK) and np.array_equal(z_x, np.zeros(prob.n))
+    assert (m_it, m_st) == (0, mf.PCG_ENOTCONV) and np.array_equal(m_x, x0)
+    assert f_st == mf.PCG_OK and f_it > 1
+    for a, c in zip(runs[0], runs[1]):
+        assert a[:2] == c[:2]
+        assert np.array_equal(a[2], c[2]) and np.array_equal(a[3], c[3])
