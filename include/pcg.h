@@ -381,8 +381,11 @@ int pcg_update_solve_host(pcg_ctx* ctx, const pcg_coeffs* coeffs, const double* 
  * context, which waits first) returns.  Consecutive calls alternate between
  * two device copies of x, so the copy of one call's solution and the next
  * call's solve do not touch the same memory; the first call allocates the
- * second copy and the stream.  Errors: as pcg_update_solve_host; an error of
- * a copy left running is reported by pcg_host_wait. */
+ * second copy and the stream.  b_host and x0_host may be the x_host of an
+ * earlier call whose copy is still running (a sequence in which each solve
+ * starts from the last solution): the copy-in then waits for that copy on the
+ * device.  Errors: as pcg_update_solve_host; an error of a copy left running
+ * is reported by pcg_host_wait. */
 int pcg_update_solve_host_async(pcg_ctx* ctx, const pcg_coeffs* coeffs, const double* b_host,
                                 const double* x0_host, double* x_host, double rtol, int maxit,
                                 int* iters_out, double* res_hist);

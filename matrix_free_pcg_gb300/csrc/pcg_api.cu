@@ -116,6 +116,7 @@ struct pcg_ctx {
   cudaStream_t out_stream = nullptr;
   cudaEvent_t out_done[2] = {nullptr, nullptr}, solved = nullptr;
   bool out_pending[2] = {false, false};
+  const double* out_host[2] = {nullptr, nullptr};  // the host buffer each copy-out writes
   int out_slot = 0;
   // set by the host-buffer entry points right before their solve (and taken
   // back at its start): the initial guess is zero and its device copy was not
@@ -1655,6 +1656,17 @@ static int update_solve_host(pcg_ctx* ctx, const pcg_coeffs* coeffs, const doubl
     if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->stream, ctx->out_done[slot], 0);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "device-to-host copy order");
   }
+  // b or x0 in a host buffer that an earlier call's copy-out may still be
+  // writing (a sequence of solves each started from the last solution): the
+  // copy-in waits for that copy-out on the device
+  for (int k = 0; k < 2 && async; ++k) {
+    const long long n = ctx->op.n;
+    if (ctx->out_pending[k] && (overlap(b_host, n, ctx->out_host[k], n) ||
+                                (x0_host && overlap(x0_host, n, ctx->out_host[k], n)))) {
+      e = cudaStreamWaitEvent(ctx->copy_stream, ctx->out_done[k], 0);
+      if (e != cudaSuccess) return cuda_fail(ctx, e, "host-to-device copy order");
+    }
+  }
   const size_t bytes = sizeof(double) * (size_t)ctx->op.n;
   const bool x0_zero = zero_x0_skips_copy(ctx, x0_host);
   bool copies_enqueued = false;
@@ -1688,6 +1700,7 @@ static int update_solve_host(pcg_ctx* ctx, const pcg_coeffs* coeffs, const doubl
   if (e == cudaSuccess) e = cudaEventRecord(ctx->out_done[slot], ctx->out_stream);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "device-to-host copy");
   ctx->out_pending[slot] = true;
+  ctx->out_host[slot] = x_host;
   ctx->out_slot = slot ^ 1;
   return st;
 }

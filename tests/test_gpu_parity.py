@@ -273,6 +273,43 @@ def test_update_solve_host_async_matches_the_synchronous_call(layout):
         assert np.array_equal(outs[1].numpy(), ref[1][3])
 
 
+@pytest.mark.parametrize("layout", ["tiled", "column"])
+def test_update_solve_host_async_chain_from_the_last_solution(layout):
+    # each solve of a sequence starts from the previous solution, passed as x0
+    # while that solution's copy to the host (16 MB, page-locked) may still be
+    # running: the copy-in waits for it.  A constant a_h, whose update does not
+    # wait for the device, starts the copy-in at once; the outputs start as
+    # NaN, so a copy-in that overtook the copy-out would show.
+    nx, ny, nz = 128, 128, 128
+    h = W.layer_thickness(nz, True)
+    n = nx * ny * nz
+    rng = np.random.default_rng(46)
+    steps = [(torch.from_numpy(rng.uniform(-1, 1, n)).pin_memory(),
+              dict(a_h=1.0 + 0.25 * i, a_v=1e3 * (1 + i), mass=1.0, dz=h)) for i in range(4)]
+    kw = dict(a_h=1.0, a_v=1e3, mass=1.0, dz=h)
+
+    def chain(solve):
+        with mf.Solver(nx, ny, nz, **kw) as s:
+            s.set_layout(layout)
+            prev = torch.zeros(n, dtype=torch.float64).pin_memory()
+            outs, res = [], []
+            for bh, coef in steps:
+                x = torch.full((n,), float("nan"), dtype=torch.float64).pin_memory()
+                res.append(solve(s, bh, x, prev, coef))
+                outs.append(x)
+                prev = x
+            s.host_wait()
+        return res, [x.numpy() for x in outs]
+
+    ref, x_ref = chain(lambda s, bh, x, x0, coef: s.update_solve_host(bh, x, rtol=1e-8, x0=x0,
+                                                                      **coef))
+    got, x_got = chain(lambda s, bh, x, x0, coef: s.update_solve_host_async(bh, x, rtol=1e-8,
+                                                                            x0=x0, **coef))
+    for (it, h_, st), (it_r, h_r, st_r), x, x_r in zip(got, ref, x_got, x_ref):
+        assert st_r == mf.PCG_OK and (it, st) == (it_r, st_r) and np.array_equal(h_, h_r)
+        assert np.array_equal(x, x_r)
+
+
 def test_update_solve_host_initial_guess_and_errors():
     prob, kw, b = case(30, 26, 24, True, True, a_v=1e3, seed=32)
     x0 = np.random.default_rng(33).standard_normal(prob.n)
