@@ -36,6 +36,8 @@ MUTANTS = {
     "direction_unpreconditioned": ("p[l] = z[l] + beta * p[l];", "p[l] = r[l] + beta * p[l];"),
     "residual_sign": ("r[l] -= alpha * q[l];", "r[l] += alpha * q[l];"),
     "solution_uses_q": ("x[l] += alpha * p[l];", "x[l] += alpha * q[l];"),
+    "stopping_ratio_squared": ("double res = rnorm / rho0;",
+                               "double res = (rnorm * rnorm) / (rho0 * rho0);"),
 }
 
 # Mistakes in the multigrid part, checked against its own pins.

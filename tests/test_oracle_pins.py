@@ -198,6 +198,35 @@ def test_pcg_iterates_match_scipy_cg(k):
     assert np.linalg.norm(x - x_ref) <= 1e-11 * np.linalg.norm(x_ref)
 
 
+@pytest.mark.parametrize("cfg", [
+    # nx, ny, nz, seed, graded, varying, a_v, rtol
+    (6, 5, 12, 70, True, True, 1e3, 1e-8),
+    (8, 8, 6, 71, False, True, 50.0, 1e-10),
+    (5, 7, 9, 72, True, False, 1e4, 1e-6),
+    (9, 4, 16, 73, True, True, 1e5, 1e-10),
+])
+def test_pcg_iteration_count_and_history_match_scipy_cg(cfg):
+    """The iteration at which ||r_k|| < rtol ||r_0|| first holds (x0 = 0, so
+    ||r_0|| = ||b||), and ||r_k|| / ||r_0|| on the way there, against scipy's
+    CG -- its own loop and the same stopping rule -- with the same matrix and
+    M; scipy's iterates give the true residuals."""
+    nx, ny, nz, seed, graded, varying, a_v, rtol = cfg
+    prob, ah, h = random_problem(nx, ny, nz, seed, graded=graded, varying=varying, a_v=a_v)
+    A = tp.assemble_A(ah, h, prob.a_v, prob.mass).tocsr()
+    M = tp.assemble_M(ah, h, prob.a_v, prob.mass).tocsc()
+    Mop = spla.LinearOperator(A.shape, matvec=spla.factorized(M))
+    b = np.random.default_rng(seed + 1).standard_normal(prob.n)
+    xs = []
+    _, info = spla.cg(A, b, x0=np.zeros(prob.n), rtol=rtol, atol=0.0, maxiter=500, M=Mop,
+                      callback=lambda xk: xs.append(xk.copy()))
+    assert info == 0
+    x, iters, hist, st = oracle.pcg(prob, b, rtol=rtol, maxit=500)
+    assert st == oracle.OK and iters == len(xs) > 1
+    true = np.array([np.linalg.norm(b - A @ xk) for xk in xs]) / np.linalg.norm(b)
+    np.testing.assert_allclose(hist[1:], true, rtol=1e-6, atol=1e-12)
+    assert hist[iters] < rtol <= hist[iters - 1]
+
+
 def test_pcg_zero_horizontal_coupling_converges_in_one_iteration():
     prob = oracle.Problem(6, 5, 8, ah=0.0, a_v=1e3, mass=1.0,
                           h=W.layer_thickness(8, graded=True))
