@@ -1,6 +1,6 @@
-// Tensor-memory (TMEM) wrappers shared by the kernels that keep the Thomas
-// forward pass's w in the SM's tensor memory (pcg_tmem.cu, and the row-tiled
-// preconditioner sweep in pcg_sweeps.cuh / pcg_tiled.cu).  TMEM is the 256 KB
+// Tensor-memory (TMEM) wrappers of the column-layout kernels that keep the
+// Thomas forward pass's w in the SM's tensor memory (pcg_tmem.cu; the
+// row-tiled sweep keeps w in L2 instead).  TMEM is the 256 KB
 // per SM that the tensor cores use for accumulators: 128 lanes of 512 32-bit
 // columns; a warp reaches the 32 lanes of its sub-partition (warp w of a
 // block: lanes 32 (w mod 4) .. +31).  Internal; internal linkage.
