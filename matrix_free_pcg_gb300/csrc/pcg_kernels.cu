@@ -957,7 +957,9 @@ __global__ void __launch_bounds__(256) k_x0_nonzero(const double* __restrict__ x
 
 // Start of a solve in the row-tiled layout, one kernel: r = b - A x0 from the
 // caller's column-contiguous b and x0, written row-tiled together with u = x0
-// and p = q = 0, and the scalar state of a new solve (as k_stencil MODE 1).
+// (and p = q = 0 with zero_pq: a solve whose first sweeps are the
+// first-iteration variants reads neither), and the scalar state of a new
+// solve (as k_stencil MODE 1).
 // A block takes one tile of 32 columns and 32 levels: it reads along k
 // (coalesced in the caller's layout), turns the 32 x 32 patch around in
 // shared memory, and writes along the columns (coalesced in the solver's).
