@@ -248,6 +248,32 @@ def test_pcg_eigenmode_rhs_converges_in_one_iteration():
     assert np.max(np.abs(x - v / lam)) <= 1e-13 * np.max(np.abs(v / lam))
 
 
+def test_pcg_stops_after_as_many_iterations_as_distinct_eigenvalues():
+    """b in the span of m eigenvectors of M^-1 A with distinct eigenvalues: the
+    Krylov space holds the solution after m steps, so PCG stops at exactly m
+    (the residual at rounding level there and not before), with x the sum of
+    each mode over its eigenvalue of A.  With a constant a_h and uniform
+    layers the Fourier x cosine modes are eigenvectors of A and of M alike."""
+    nx, ny, nz, a_h, a_v, mass = 8, 6, 5, 1.0, 100.0, 1.0
+    prob = oracle.Problem(nx, ny, nz, ah=a_h, a_v=a_v, mass=mass)
+    modes = [(1, 2, 3), (2, 0, 1), (4, 3, 0)]
+
+    def eig(p, q, m):  # of A, and of M^-1 A
+        lh = 4 * np.sin(np.pi * p / nx) ** 2 + 4 * np.sin(np.pi * q / ny) ** 2
+        lv = 4 * np.sin(np.pi * m / (2 * nz)) ** 2
+        lam = mass + a_h * lh + a_v * lv
+        return lam, lam / (mass + 4 * a_h + a_v * lv)
+
+    assert np.min(np.diff(sorted(eig(*t)[1] for t in modes))) > 1e-2
+    for count in (1, 2, 3):
+        b = sum(tp.fourier_mode(nx, ny, nz, *t) for t in modes[:count])
+        x_ref = sum(tp.fourier_mode(nx, ny, nz, *t) / eig(*t)[0] for t in modes[:count])
+        x, iters, hist, st = oracle.pcg(prob, b, rtol=1e-10)
+        assert (iters, st) == (count, oracle.OK)
+        assert hist[count] < 1e-12 and np.all(hist[:count] > 1e-3)
+        assert np.max(np.abs(x - x_ref)) <= 1e-12 * np.max(np.abs(x_ref))
+
+
 def test_pcg_error_decreases_monotonically_in_A_norm():
     prob, ah, h = random_problem(5, 5, 6, seed=50)
     A = tp.assemble_A(ah, h, prob.a_v, prob.mass).toarray()
