@@ -1203,10 +1203,15 @@ int pcg_set_layout(pcg_ctx* ctx, int layout) {
   cudaError_t e = cudaStreamSynchronize(ctx->stream);
   const long long npad = ctx->op.ntiles * pcg::kTile * ctx->op.nz;
   if (e == cudaSuccess && layout == PCG_LAYOUT_TILED && !ctx->u_t) e = dalloc(&ctx->u_t, npad);
-  if (e == cudaSuccess && layout == PCG_LAYOUT_TILED && ctx->has_field_buffers && !ctx->cdiag_t) {
-    e = dalloc(&ctx->cdiag_t, npad);
-    if (e == cudaSuccess) e = dalloc(&ctx->cwE_t, npad);
-    if (e == cudaSuccess) e = dalloc(&ctx->cwN_t, npad);
+  if (e == cudaSuccess && layout == PCG_LAYOUT_TILED && ctx->has_field_buffers &&
+      !(ctx->cdiag_t && ctx->cwE_t && ctx->cwN_t)) {
+    // each table where it is missing: an earlier attempt that ran out of
+    // memory may have made some of them
+    for (double** t : {&ctx->cdiag_t, &ctx->cwE_t, &ctx->cwN_t})
+      if (e == cudaSuccess && !*t) {
+        e = dalloc(t, npad);
+        if (e != cudaSuccess) *t = nullptr;
+      }
     ctx->op.cdiag_t = ctx->cdiag_t;
     ctx->op.cwE_t = ctx->cwE_t;
     ctx->op.cwN_t = ctx->cwN_t;
@@ -1285,6 +1290,7 @@ int pcg_set_substructuring(pcg_ctx* ctx, int nblocks) {
       *t = nullptr;
     }
     ctx->split_p = 1;
+    ctx->config_gen++;  // no captured sweep may keep the freed tables, even if what follows fails
     if (P > 1) {
       const size_t npad = (size_t)op.ntiles * pcg::kTile * nz;
       const size_t per_col = (size_t)op.ntiles * pcg::kTile;
